@@ -1,0 +1,33 @@
+"""Plain, slow, float64 CPU oracle for the per-cycle verify step of MTP speculative decoding.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, links or calls this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of ``bench.py`` may use
+it. The CUDA library and its Python binding share no code with it (no kernels, headers, tables
+or helpers); the only thing both sides consume is the seeded input generator in ``synth/``,
+which holds none of the method's arithmetic. Random numbers the method draws are passed in as
+callables or arrays, or generated here from the published Philox definition.
+
+What it follows (sources are the pages' titles and sections):
+
+* lucebox-hub PR #15 "feat(qwen4exp): MTP speculative decoding", sections *What* and
+  *Exactness*: draft head over the first 64,000 vocabulary rows with an on-GPU argmax; one
+  batched verify of k drafts over k+1 rows; greedy acceptance byte-identical to MTP off;
+  bit-exact rollback of KV and recurrent state.
+* DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", sections
+  *Implementation* and the closing comment: probability-ratio acceptance ``u*q <= p``,
+  ``max(0, p - q)`` residual correction, zero/non-finite probability handling, EOS inside a
+  proposal block, verification-row snapshots, rejected-row trimming, replay fallback.
+* llama.cpp PR #28104 "qwen4exp : port NextN/MTP speculative decoding to master", commits
+  "full checkpoints for MTP rollback", the replay-livelock fix and "keep speculative
+  checkpoints on device": restore-and-replay without re-verification, state kept on device.
+* Philox4x32-10: Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+  SC'11, section 3 (the Philox S-box) and Table 2 (round constants).
+
+Modules: ``philox`` (uniforms), ``lmhead`` (logits and row statistics), ``accept`` (drafting,
+acceptance, residual and bonus sampling, EOS), ``state`` (KV trim, snapshot commit, replay on
+the synthetic recurrent step). Every function is pinned by a ``-m "not gpu"`` test against
+closed forms, brute force, library routines or published test vectors; the one exception is
+recorded as "parity unpinned" in its docstring.
+"""
+
+from . import philox, lmhead, accept, state  # noqa: F401

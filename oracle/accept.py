@@ -1,0 +1,213 @@
+"""Drafting and acceptance for one request and one verify cycle (oracle; test infrastructure only).
+
+Sources (page titles and sections):
+
+* lucebox-hub PR #15 "MTP speculative decoding", *What*: the draft head picks its token by
+  argmax over the first 64,000 vocabulary rows; the trunk verifies k drafts in one pass of
+  k+1 rows. *Exactness*: a greedy draft is accepted only if it equals the trunk's token, so the
+  output is byte-identical to MTP off. *Speed*: 7.74 tokens per cycle at seven drafts implies
+  k+1 tokens when every draft passes -- the bonus token from the last verify row.
+* DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", *Implementation* and the
+  closing comment: probability-ratio acceptance ``u*q <= p``, residual correction from
+  ``max(0, p - q)``, zero/non-finite probability handling, EOS inside a proposal block without
+  retaining tokens or state beyond EOS.
+
+The algorithm, per request (row r of the verify logits predicts the token after input r; draft
+d_i is checked against verify row i-1; ``pos_base`` is the absolute position of the first
+token this cycle emits):
+
+T == 0 (greedy):
+    for i = 1..k: t = argmax z[i-1]; if d_i == t: emit d_i (stop if EOS) else emit t, stop.
+    all k accepted: emit argmax z[k] (bonus).
+T > 0 (ratio rule), p_r = softmax(z[r]/T) over V, q_i = softmax(y[i]/T) over the draft rows and
+0 beyond them (q_i = one-hot at d_i when no draft logits are given):
+    for i = 1..k: u = U(pos_base+i-1, ACCEPT)
+        if p_{i-1}(d_i) > 0 and u * q_i(d_i) <= p_{i-1}(d_i): emit d_i (stop if EOS)
+        else: r = max(0, p_{i-1} - q_i); if sum r <= 0: r = p_{i-1}
+              emit the inverse-CDF draw of r with U(pos_base+i-1, RESIDUAL); stop.
+    all k accepted: emit the inverse-CDF draw of p_k with U(pos_base+k, BONUS).
+
+Inverse CDF: the smallest j (ascending token id) with cumsum(w)[j] > u * sum(w); if rounding
+leaves none, the last j with w[j] > 0. Readings where the pages are silent are listed in the
+design notes (draft rows checked against row i-1, lowest-index argmax ties, ``<=`` in the ratio
+test, rejection when p(d) == 0 even at u == 0, fall back to p when the residual is empty, an
+emitted EOS from a correction or bonus also ends the block).
+
+Status codes (no decision is taken and nothing is emitted when status != 0):
+    1 non-finite verify logits (NaN or +Inf anywhere in a row used, or a row of all -Inf),
+      or non-finite draft logits at T > 0; 2 k outside [0, k_max]; 5 a draft id outside [0, V).
+
+Every decision records a margin so the GPU comparison can set aside near-ties: ('gap', top-2
+logit gap) for argmax decisions, ('ratio', |u*q - p|) for ratio tests and ('cdf', distance from
+u*sum(w) to the nearest cumulative boundary) for inverse-CDF draws, both in probability units.
+
+Pinned by: brute-force enumeration of the emitted-sequence law at V=8 (exact against the
+chained target law within the 24-bit grid error), a chi-square test at V=4096, the T=0 identity
+with sequential greedy decoding, and the special cases p == q (all accepted) and q one-hot on a
+token with p == 0 (always rejected, residual == p).
+"""
+
+import numpy as np
+
+from . import lmhead
+from .philox import PURPOSE_ACCEPT, PURPOSE_BONUS, PURPOSE_DRAFT, PURPOSE_RESIDUAL
+
+STATUS_OK = 0
+STATUS_NONFINITE = 1
+STATUS_BAD_K = 2
+STATUS_BAD_TOKEN = 5
+
+
+def inverse_cdf(w, u):
+    """Inverse-CDF draw from non-negative weights ``w`` with uniform ``u`` in [0, 1).
+
+    Returns (j, margin): j = the smallest index with cumsum(w)[j] > u * S where S = sum(w)
+    (taken as the last cumulative value); if none (rounding), the last index with w[j] > 0.
+    margin = distance from u*S to the nearer edge of bin j, in the units of w.
+    """
+    w = np.asarray(w, dtype=np.float64)
+    c = np.cumsum(w)
+    S = c[-1]
+    t = u * S
+    idx = np.flatnonzero(c > t)
+    if idx.size:
+        j = int(idx[0])
+    else:
+        j = int(np.flatnonzero(w > 0)[-1])
+    lo = c[j - 1] if j > 0 else 0.0
+    margin = min(abs(c[j] - t), abs(t - lo))
+    return j, float(margin)
+
+
+def draft_token(y, T, u=None):
+    """The draft head's token from its logits row ``y`` (float64 [Vd]).
+
+    T == 0: argmax (lowest index on ties) -- lucebox-hub PR #15, *What*: the draft head "picks
+    its token on the GPU". T > 0: inverse-CDF draw of softmax(y/T) with ``u`` =
+    U(pos, DRAFT) (the reading that makes the ratio rule exact: drafts distributed as q).
+    Returns (token, margin) with margin as in ``inverse_cdf`` (or the top-2 gap at T == 0).
+    """
+    st = lmhead.row_stats(y, T)
+    if st["nonfinite"]:
+        return -1, 0.0
+    if T == 0:
+        return st["argmax"], st["gap"]
+    return inverse_cdf(lmhead.probs(y, T), u)
+
+
+def _q_at(y, x, T):
+    """q_i(x) for draft logits row y over the draft rows (0 beyond them)."""
+    if x >= y.shape[0]:
+        return 0.0
+    return float(lmhead.probs(y, T)[x])
+
+
+def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
+    """Acceptance for one request and one cycle.
+
+    z:       float64 [>= k+1, V] verify logits; row r predicts position pos_base + r.
+    y:       float64 [>= k, Vd] draft logits (row i-1 belongs to draft i) or None (one-hot q).
+    drafts:  ints, drafts[i-1] = d_i.
+    uniform: callable (pos, purpose) -> u in [0, 1) (the request's seeded Philox stream).
+    Returns dict(status, n_accept, tokens, n_emit, eos_hit, sample_kind, sample_row, margins)
+    with sample_kind 0 none, 1 residual, 2 bonus draw.
+    """
+    res = dict(status=STATUS_OK, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
+               sample_kind=0, sample_row=-1, margins=[])
+
+    def fail(code):
+        res.update(status=code, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
+                   sample_kind=0, sample_row=-1)
+        return res
+
+    if k < 0 or k > k_max:
+        return fail(STATUS_BAD_K)
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[1]
+    d = [int(x) for x in drafts[:k]]
+    if any(x < 0 or x >= V for x in d):
+        return fail(STATUS_BAD_TOKEN)
+    zst = [lmhead.row_stats(z[r], T) for r in range(k + 1)]
+    if any(s["nonfinite"] for s in zst):
+        return fail(STATUS_NONFINITE)
+    if T > 0 and y is not None:
+        y = np.asarray(y, dtype=np.float64)
+        if any(lmhead.row_stats(y[i], T)["nonfinite"] for i in range(k)):
+            return fail(STATUS_NONFINITE)
+
+    tokens = res["tokens"]
+    margins = res["margins"]
+
+    def emit(tok):
+        tokens.append(int(tok))
+        if eos_id >= 0 and tok == eos_id:
+            res["eos_hit"] = True
+            return True
+        return False
+
+    if T == 0:
+        for i in range(1, k + 1):
+            t = zst[i - 1]["argmax"]
+            margins.append(("gap", zst[i - 1]["gap"]))
+            if d[i - 1] == t:
+                res["n_accept"] += 1
+                if emit(t):
+                    break
+            else:
+                emit(t)
+                break
+        else:
+            margins.append(("gap", zst[k]["gap"]))
+            emit(zst[k]["argmax"])
+    else:
+        for i in range(1, k + 1):
+            x = d[i - 1]
+            p = lmhead.probs(z[i - 1], T)
+            if y is None:
+                q = np.zeros(V)
+                q[x] = 1.0
+            else:
+                qd = lmhead.probs(y[i - 1], T)
+                q = np.zeros(V)
+                q[: qd.shape[0]] = qd
+            px, qx = float(p[x]), float(q[x])
+            u = uniform(pos_base + i - 1, PURPOSE_ACCEPT)
+            margins.append(("ratio", abs(u * qx - px)))
+            if px > 0.0 and u * qx <= px:
+                res["n_accept"] += 1
+                if emit(x):
+                    break
+            else:
+                r = np.maximum(0.0, p - q)
+                if not np.sum(r) > 0.0:
+                    r = p
+                u2 = uniform(pos_base + i - 1, PURPOSE_RESIDUAL)
+                j, m = inverse_cdf(r, u2)
+                margins.append(("cdf", m))
+                res.update(sample_kind=1, sample_row=i - 1)
+                emit(j)
+                break
+        else:
+            p = lmhead.probs(z[k], T)
+            u3 = uniform(pos_base + k, PURPOSE_BONUS)
+            j, m = inverse_cdf(p, u3)
+            margins.append(("cdf", m))
+            res.update(sample_kind=2, sample_row=k)
+            emit(j)
+    res["n_emit"] = len(tokens)
+    return res
+
+
+def draft_chain_tokens(y_rows, T, uniform, pos_base):
+    """Draft tokens for one request from precomputed draft logits rows (row i-1 -> draft i).
+
+    Each draft is an independent call of ``draft_token`` with U(pos_base+i-1, DRAFT). Returns
+    (tokens, margins).
+    """
+    toks, margins = [], []
+    for i in range(1, len(y_rows) + 1):
+        u = uniform(pos_base + i - 1, PURPOSE_DRAFT) if T > 0 else None
+        t, m = draft_token(y_rows[i - 1], T, u)
+        toks.append(t)
+        margins.append(("gap" if T == 0 else "cdf", m))
+    return toks, margins
