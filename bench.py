@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the verify step of MTP speculative decoding on GB300.
+
+Headline workload (greedy k=1): hidden 2560, bf16 LM head of 151,936 rows, draft head over the
+first 64,000 rows, 2 verify rows, batch 1. One STEP is one verify cycle -- the verify LM-head
+GEMV over the k+1 rows plus acceptance -- on device-resident inputs (drafts produced by the
+draft head before the timed region). Printed as one JSON line (rank 0):
+
+  value        verify cycles/s over all ranks (replicas: every rank runs the same workload)
+  roofline     the verify GEMV: algorithmic bytes per launch / its mean CUDA-event duration,
+               against the measured HBM copy bandwidth
+  full_cycle   k draft-head steps + verify + acceptance: cycles/s and emitted tokens/s
+  sweep        k = 1..7 at temperature 0 and 1 (verify rows k+1)
+  commit       snapshot commit and replay of the 64K-context state
+  e2e          the same verify cycle through SpecVerifyEngine with host buffers (pinned H2D of the
+               step's hidden rows and drafts, D2H of the 64-byte result) inside the timed region
+  cpu_baseline the float64 oracle on the host cores, on a bounded sample
+
+``--impl reference`` times the float64 oracle instead (the only other implementation of this
+method here), on the same workload, metric and unit.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import configs, gen  # noqa: E402
+
+METRIC = "verify cycles/s & emitted tok/s at k=1..7; LM-head HBM GB/s vs 8 TB/s"
+# DRAM traffic of one verify GEMV launch on the headline workload, read from the ncu capture
+# summarised in profiles/ (None until a capture of the current kernel exists).
+GEMV_TRAFFIC_BYTES = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="few launches, no sweep/baseline: for ncu launch lists")
+    return ap.parse_args()
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def workload_config(cfg, extra=None):
+    c = {"workload": f"{cfg.name}: d={cfg.d}, V={cfg.V} {cfg.wdtype} LM head, draft rows "
+                     f"{cfg.Vd}, k={cfg.k}, {cfg.k + 1} verify rows, batch {cfg.batch}",
+         "hidden": cfg.d, "vocab": cfg.V, "draft_rows": cfg.Vd, "k": cfg.k,
+         "verify_rows": cfg.k + 1, "batch": cfg.batch, "temperature": cfg.temps[0],
+         "l2": "inputs larger than L2 (778 MB of weights streamed per step); no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            w = [x.strip() for x in line.split(",")]
+            if len(w) < 9:
+                continue
+            try:
+                sm.append(float(w[1]))
+                smax.append(float(w[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, w[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------- GPU arm
+def build_inputs(cfg, W, n_pool, k, T, rng_seed):
+    """Pool of cycle inputs: verify rows [n, k+1, d] and draft rows [n, k, d] (bf16 bits)."""
+    H = np.empty((n_pool, k + 1, cfg.d), dtype=np.uint16)
+    Hd = np.empty((n_pool, max(k, 1), cfg.d), dtype=np.uint16)
+    for c in range(n_pool):
+        inp = gen.cycle_inputs(cfg, W, c, seed=rng_seed, k=k)
+        H[c] = inp["H"]
+        if k:
+            Hd[c, :k] = inp["Hd"]
+    return H, Hd
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    from mtp_speculative_decoding_spec_gb300 import build as _build
+    from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
+
+    _build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    cfg = configs.get(1)
+    W = gen.lm_weights(cfg)
+    Wd = torch.from_numpy(W.view(np.int16)).to(dev)
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    n_pool = 64 if args.profile else 512
+    k = cfg.k
+    Hp, Hdp = build_inputs(cfg, W, n_pool, k, cfg.temps[0], rng_seed=100 + rank)
+    Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+    Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+
+    eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k, cfg.eos_id,
+                           device=dev, want_q_logits=False)
+    eng.set_requests(temps=[0.0], seeds=[0], pos=[0], k=[k])
+    # drafts of every pool entry, produced by the draft head on the GPU before timing
+    drafts_pool = torch.zeros((n_pool, 1, k), dtype=torch.int32, device=dev)
+    for c in range(n_pool):
+        for i in range(1, k + 1):
+            eng.draft_step(i, Hdp_d[c, i - 1:i])
+        drafts_pool[c].copy_(eng.drafts[:, :k])
+    torch.cuda.synchronize()
+
+    def step(c):
+        eng.verify(Hp_d[c])
+        spec.spec_accept(1, k, eng.k, drafts_pool[c], eng.logits, eng.stats, cfg.V, k + 1,
+                         None, None, cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id, eng.seeds, eng.pos,
+                         eng.out, eng.counters, eng.ws)
+
+    K, Wm = args.steps, args.warmup
+    for c in range(Wm):
+        step(c % n_pool)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    with clocks:
+        t_start.record(stream)
+        for c in range(K):
+            ev[c][0].record(stream)
+            eng.verify(Hp_d[c % n_pool])
+            ev[c][1].record(stream)
+            spec.spec_accept(1, k, eng.k, drafts_pool[c % n_pool], eng.logits, eng.stats, cfg.V,
+                             k + 1, None, None, cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id,
+                             eng.seeds, eng.pos, eng.out, eng.counters, eng.ws)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    gemv_ms = [a.elapsed_time(b) for a, b in ev]
+    gemv_mean_s = statistics.mean(gemv_ms) / 1e3
+    err = int(eng.ws[4:8].cpu().numpy().view(np.uint32)[0])
+    cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+    elapsed_max = max_over_ranks(elapsed)
+    value = world * K / elapsed_max
+    algo_bytes = cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16
+    achieved = algo_bytes / gemv_mean_s / 1e9
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "verify cycles/s",
+        "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": round(elapsed_max / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(cfg, {"parallelism": f"replicas x{world}",
+                                        "step": "verify GEMV (2 rows) + acceptance"}),
+        "roofline": {"bound": "hbm", "kernel": "gemv_rows_kernel (verify, 2 rows)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "mean_launch_us": round(gemv_mean_s * 1e6, 2),
+                     "traffic": GEMV_TRAFFIC_BYTES},
+        "acceptance": round(float(cnt["accepted"]) / max(1.0, float(cnt["drafted"])), 4),
+        "gpu_launches": 2 * K,
+        "workspace_error": err,
+    }
+    cs = clocks.summary()
+    res["clocks"] = cs
+
+    if not args.profile:
+        res["full_cycle"] = full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, min(K, 2000), dev)
+        res["e2e"] = e2e(eng, cfg, Hp, drafts_pool, n_pool, k, min(K, 2000), dev, world,
+                         max_over_ranks)
+        if not args.no_sweep:
+            res["sweep"] = sweep(dev, W, Wd, hbm_peak)
+            res["commit"] = commit_bench(dev, hbm_peak)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
+        res["cpu_baseline"] = cpu_baseline(cfg, W, args.cpu_seconds)
+    if world > 1:
+        res["value_check"] = sum_over_ranks(K / elapsed)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
+    import torch
+    for c in range(10):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k)
+    eng.counters.zero_()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for c in range(K):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k)
+    b.record()
+    torch.cuda.synchronize()
+    s = a.elapsed_time(b) / 1e3
+    import mtp_speculative_decoding_spec_gb300 as spec
+    cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+    return {"cycles_s": round(K / s, 2), "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
+            "tokens_per_cycle": round(float(cnt["emitted"]) / K, 4), "steps": K,
+            "step": f"{k} draft-head step(s) + verify + acceptance"}
+
+
+def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    H_host = torch.from_numpy(Hp.view(np.int16)).pin_memory()
+    D_host = drafts_pool.cpu().pin_memory()
+    out_host = torch.empty((K, spec.ACCEPT_OUT_BYTES), dtype=torch.uint8).pin_memory()
+    H_dev = torch.empty_like(H_host[0], device=dev)
+    D_dev = torch.empty_like(D_host[0], device=dev)
+
+    def one(c, j):
+        H_dev.copy_(H_host[c], non_blocking=True)
+        D_dev.copy_(D_host[c], non_blocking=True)
+        eng.verify(H_dev)
+        spec.spec_accept(1, k, eng.k, D_dev, eng.logits, eng.stats, cfg.V, k + 1, None, None,
+                         cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id, eng.seeds, eng.pos, eng.out,
+                         eng.counters, eng.ws)
+        out_host[j].copy_(eng.out, non_blocking=True)
+
+    for c in range(10):
+        one(c % n_pool, 0)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for c in range(K):
+        one(c % n_pool, c)
+    torch.cuda.synchronize()
+    s = max_over_ranks(time.perf_counter() - t0)
+    h2d = H_host[0].numel() * 2 + D_host[0].numel() * 4
+    return {"value": round(world * K / s, 2), "unit": "verify cycles/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": spec.ACCEPT_OUT_BYTES,
+            "steps": K, "api": "SpecVerifyEngine.verify + spec_accept, pinned host buffers"}
+
+
+def sweep(dev, W, Wd, hbm_peak):
+    """k = 1..7 at temperature 0 (greedy) and 1 (ratio rule with q rows)."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
+    out = {}
+    base = configs.get(2)
+    n_pool, K = 32, 200
+    for T in (0.0, 1.0):
+        for k in range(1, 8):
+            cfg = configs.Config(**{**base.__dict__, "k": k, "temps": (T,)})
+            Hp, Hdp = build_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
+            Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+            Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+            eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
+                                   cfg.eos_id, device=dev, want_q_logits=True)
+            eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k])
+            for c in range(5):
+                eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
+            torch.cuda.synchronize()
+            eng.counters.zero_()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                   torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for c in range(K):
+                cc = c % n_pool
+                for i in range(1, k + 1):
+                    eng.draft_step(i, Hdp_d[cc, i - 1:i])
+                ev[c][0].record()
+                eng.verify(Hp_d[cc])
+                ev[c][1].record()
+                eng.accept()
+                ev[c][2].record()
+            b.record()
+            torch.cuda.synchronize()
+            s = a.elapsed_time(b) / 1e3
+            verify_s = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
+            gemv_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+            cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+            gbs = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 +
+                   (k + 1) * cfg.V * 4 * (T > 0)) / gemv_s / 1e9
+            out[f"T{T:g}_k{k}"] = {
+                "verify_cycles_s": round(K / verify_s, 1),
+                "full_cycles_s": round(K / s, 1),
+                "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
+                "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
+                "acceptance": round(float(cnt["accepted"]) / max(1, float(cnt["drafted"])), 3),
+                "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4)}
+            del eng, Hp_d, Hdp_d
+    return out
+
+
+def commit_bench(dev, hbm_peak):
+    """Snapshot commit and replay of the 64K-context state (36 x [16,128,128] + conv rows)."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    cfg = configs.get(3)
+    ns = 9
+    L, H, dk, dv = cfg.rec_layers, cfg.rec_heads, cfg.rec_dk, cfg.rec_dv
+    rec_elems, conv_elems = L * H * dk * dv, L * cfg.conv_rows * cfg.conv_width
+    kvb = cfg.kv_layers * 2 * cfg.kv_capacity * cfg.kv_row_bytes
+    kv = torch.zeros(kvb, dtype=torch.uint8, device=dev)
+    kv_len = torch.tensor([cfg.context], dtype=torch.int64, device=dev)
+    live = torch.zeros(rec_elems, device=dev)
+    slots = torch.randn(ns * rec_elems, device=dev)
+    clive = torch.zeros(conv_elems, device=dev)
+    cslots = torch.randn(ns * conv_elems, device=dev)
+    a = torch.rand((ns - 1) * L * H, device=dev)
+    b = torch.randn((ns - 1) * L * H * dk, device=dev)
+    c = torch.randn((ns - 1) * L * H * dv, device=dev)
+    x = torch.randn((ns - 1) * L * cfg.conv_width, device=dev)
+    d = spec.spec_state_desc()
+    d.kv, d.kv_request_stride, d.kv_layers = kv.data_ptr(), kvb, cfg.kv_layers
+    d.kv_capacity, d.kv_row_bytes, d.kv_len = cfg.kv_capacity, cfg.kv_row_bytes, kv_len.data_ptr()
+    d.rec_layers, d.rec_heads, d.rec_dk, d.rec_dv = L, H, dk, dv
+    d.rec_live, d.rec_slots = live.data_ptr(), slots.data_ptr()
+    d.conv_rows, d.conv_width = cfg.conv_rows, cfg.conv_width
+    d.conv_live, d.conv_slots, d.n_slots = clive.data_ptr(), cslots.data_ptr(), ns
+    d.step_a, d.step_b, d.step_c, d.conv_in = a.data_ptr(), b.data_ptr(), c.data_ptr(), x.data_ptr()
+    out = {}
+    acc = np.zeros(1, dtype=spec.ACCEPT_OUT_DTYPE)
+    acc["n_emit"] = 4
+    acc_d = torch.from_numpy(acc.view(np.uint8)).to(dev)
+    k_d = torch.tensor([7], dtype=torch.int32, device=dev)
+    moved = 2 * 4 * (rec_elems + conv_elems) + 4 * cfg.kv_row_bytes * 2
+    for mode, name in ((spec.SPEC_COMMIT_SNAPSHOT, "snapshot"), (spec.SPEC_COMMIT_REPLAY, "replay")):
+        for _ in range(3):
+            kv_len.fill_(cfg.context)
+            spec.spec_commit_rollback(1, d, acc_d, k_d, mode)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(20):
+            kv_len.fill_(cfg.context)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            spec.spec_commit_rollback(1, d, acc_d, k_d, mode)
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        t = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ts) / 1e3
+        out[name] = {"us": round(t * 1e6, 2), "bytes": moved,
+                     "gbs": round(moved / t / 1e9, 1), "frac": round(moved / t / 1e9 / hbm_peak, 4)}
+    return out
+
+
+def cpu_baseline(cfg, W, seconds):
+    """The float64 oracle as it stands: verify cycles on the host cores until `seconds`."""
+    from oracle import accept as o_accept
+    from oracle import lmhead as o_lm
+    n, t0 = 0, time.perf_counter()
+    while n < 2 or time.perf_counter() - t0 < seconds:
+        inp = gen.cycle_inputs(cfg, W, n, seed=999, k=cfg.k)
+        z = o_lm.logits(W, inp["H"])
+        y = o_lm.logits(W, inp["Hd"], rows=cfg.Vd)
+        d, _ = o_accept.draft_chain_tokens(y, 0.0, None, 0)
+        o_accept.accept_request(z, None, d, cfg.k, 0.0, cfg.eos_id, None, 0)
+        n += 1
+    s = time.perf_counter() - t0
+    return {"value": round(n / s, 4), "unit": "verify cycles/s", "kind": "oracle",
+            "cores": len(os.sched_getaffinity(0)),
+            "sample": f"{n} full cycles (draft-head logits over {cfg.Vd} rows, verify logits "
+                      f"over {cfg.V} rows x {cfg.k + 1}, greedy acceptance) in float64 numpy",
+            "seconds": round(s, 2)}
+
+
+# ------------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import accept as o_accept
+    from oracle import lmhead as o_lm
+    cfg = configs.get(1)
+    W = gen.lm_weights(cfg)
+    K, Wm = args.steps, args.warmup
+
+    def one_step(c, rows):
+        inp = gen.cycle_inputs(cfg, W, c, seed=999, k=cfg.k)
+        z = o_lm.logits(W[:rows], inp["H"])
+        o_accept.accept_request(z, None, [0] * cfg.k, cfg.k, 0.0, cfg.eos_id, None, 0)
+
+    t0 = time.perf_counter()
+    one_step(0, 2048)
+    probe = time.perf_counter() - t0
+    budget = 90.0
+    rows = int(max(256, min(cfg.V, 2048 * budget / max(1, K + Wm) / max(probe, 1e-6))))
+    for c in range(Wm):
+        one_step(c, rows)
+    t0 = time.perf_counter()
+    for c in range(K):
+        one_step(c, rows)
+    s = time.perf_counter() - t0
+    per_cycle = s / K * cfg.V / rows
+    value = 1.0 / per_cycle
+    sample = (f"each step: float64 oracle verify cycle over {rows} of {cfg.V} LM-head rows "
+              f"(2 verify rows) + greedy acceptance; time scaled by {cfg.V}/{rows}")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4),
+           "unit": "verify cycles/s", "n_gpus": world, "steps": K, "warmup": Wm,
+           "ms_per_step": round(per_cycle * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(cfg, {"parallelism": "host cores"}),
+           "cpu_baseline": {"value": round(value, 4), "unit": "verify cycles/s",
+                            "kind": "oracle", "cores": len(os.sched_getaffinity(0)),
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "verify cycles/s",
+                   "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = rank_info()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,263 @@
+/*
+ * spec.h -- C ABI of libspec.so: the per-cycle verify step of MTP speculative decoding on one
+ * GB300 (sm_103a).
+ *
+ * One decode cycle (lucebox-hub PR #15 "MTP speculative decoding", section "What"): the MTP
+ * head proposes up to seven drafts, each picked on the GPU over the first 64,000 vocabulary
+ * rows and fed to the next draft from device memory; the trunk verifies the k drafts in one
+ * batched pass of k+1 rows through the shared LM head; the accepted prefix is committed and
+ * the rest rolled back bit-exactly (section "Exactness"). DS4Server issue #98 ("Add Qwen3.8
+ * Flash Next native MTP speculation", section "Implementation") adds the sampled variant:
+ * probability-ratio acceptance u*q(x) <= p(x), residual correction from max(0, p - q), EOS
+ * inside a proposal block, verification-row snapshots and rejected-row trimming. llama.cpp PR
+ * #28104 (commit "keep speculative checkpoints on device") is why every call here stays on the
+ * device: no call reads a result back to the host.
+ *
+ * Conventions for every call
+ *   - All array arguments are DEVICE pointers unless stated; the caller owns and allocates
+ *     every buffer (weights, activations, outputs, state, workspace). The library allocates
+ *     no memory and keeps no state beyond cached device attributes.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Nothing synchronises with the host.
+ *   - Host-detectable errors (null required pointer, sizes out of range, misalignment) return
+ *     SPEC_ERR_INVALID or SPEC_ERR_UNSUPPORTED before anything is enqueued. A failed launch
+ *     returns SPEC_ERR_CUDA. Data-dependent problems never trap: they are written to the
+ *     per-request status (spec_accept_out.status) and that request commits nothing.
+ *   - Workspace: calls that reduce across thread blocks take a caller-allocated workspace of
+ *     at least spec_workspace_bytes() bytes, 256-byte aligned, ZERO-FILLED ONCE before its
+ *     first use. Every call leaves it reusable (its counters back at zero). Calls that may run
+ *     concurrently (different streams) need separate workspaces. Byte offset 4 of the
+ *     workspace holds a 32-bit error word that kernels set (never clear) if an internal
+ *     bounded wait gives up; 0 means no error.
+ *   - Limits: 1..8 verify rows per request (k = 0..7 drafts), at most 8 rows in total per
+ *     spec_lmhead_verify / spec_draft_argmax call on the GEMV path; hidden size d with
+ *     d * element_size a multiple of 16 bytes and d <= 3072 (bf16) / 1536 (fp32); V < 2^24.
+ */
+#ifndef SPEC_H
+#define SPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *spec_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID = 1,     /* bad argument: nothing enqueued */
+  SPEC_ERR_UNSUPPORTED = 2, /* valid but outside what this build implements */
+  SPEC_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
+} spec_status;
+
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+
+/* Per-request status written by spec_accept / spec_commit_rollback. */
+enum {
+  SPEC_REQ_OK = 0,
+  SPEC_REQ_NONFINITE = 1,   /* NaN or +Inf in a logit row the decision needs (or a row of -Inf) */
+  SPEC_REQ_BAD_K = 2,       /* k outside [0, k_max] or k + 1 > verify rows */
+  SPEC_REQ_KV_OVERFLOW = 3, /* commit: P + k + 1 exceeds the KV capacity (trim clipped) */
+  SPEC_REQ_NO_LOGITS = 4,   /* temperature > 0 but the needed logits/q_logits were not given */
+  SPEC_REQ_BAD_TOKEN = 5    /* a draft id outside [0, V) */
+};
+
+/* Statistics of one logit row z[0..V) at the row's temperature T (T <= 0 means greedy and the
+ * normaliser is taken at T = 1):
+ *   max      = max_v z[v]                              (NaN if any z[v] is NaN or +Inf)
+ *   log_norm = log sum_v exp((z[v] - max) / T)
+ *   gap      = max - (largest z[v] over v != argmax)   (top-2 gap; +Inf when V == 1)
+ *   argmax   = lowest v with z[v] == max
+ * The temperature-T distribution is p[v] = exp((z[v] - max) / T - log_norm). */
+typedef struct {
+  float max;
+  float log_norm;
+  float gap;
+  int32_t argmax;
+} spec_rowstats;
+
+/* Result of one cycle for one request (64 bytes). tokens[0..n_emit) are the emitted tokens
+ * t_1..t_m; unused entries are -1. sample_kind: 0 no draw, 1 residual draw, 2 bonus draw;
+ * sample_row = the verify row the draw used (-1 if none). */
+typedef struct {
+  int32_t status;
+  int32_t n_accept; /* drafts accepted */
+  int32_t n_emit;   /* m = tokens emitted; the state keeps exactly m rows */
+  int32_t eos_hit;  /* 1 if the last emitted token is the EOS id */
+  int32_t tokens[8];
+  int32_t sample_kind;
+  int32_t sample_row;
+  int32_t reserved[2];
+} spec_accept_out;
+
+/* Per-request telemetry accumulated by spec_accept (DS4Server issue #98, "Implementation":
+ * report drafted tokens, accepted tokens, verifier passes and acceptance depth). */
+typedef struct {
+  uint64_t cycles;   /* verifier passes */
+  uint64_t drafted;  /* sum of k */
+  uint64_t accepted; /* sum of n_accept */
+  uint64_t emitted;  /* sum of n_emit */
+  uint64_t eos;      /* cycles that ended on EOS */
+  uint64_t errors;   /* cycles with status != 0 */
+  uint64_t depth[8]; /* histogram of n_accept = 0..7 */
+} spec_counters;
+
+/* Where the state to commit lives (a HOST struct holding DEVICE pointers). Any part may be
+ * absent: kv_layers = 0, rec_layers = 0 or conv_rows = 0 disables it.
+ *
+ *   KV cache: request b owns the bytes kv + b*kv_request_stride, laid out
+ *             [kv_layers][2 (K, V)][kv_capacity][kv_row_bytes]; kv_len[b] = P, the number of
+ *             valid positions before this cycle's k+1 verify rows (written at P..P+k).
+ *   recurrent:rec_live  [B][rec_layers][rec_heads][rec_dk][rec_dv] float32
+ *             rec_slots [B][n_slots][rec_layers][rec_heads][rec_dk][rec_dv] float32;
+ *             slot 0 = the state before the cycle, slot r+1 = after verify row r.
+ *   conv rows:conv_live [B][rec_layers][conv_rows][conv_width] float32, oldest row first;
+ *             conv_slots[B][n_slots][rec_layers][conv_rows][conv_width] float32.
+ *   replay inputs (mode SPEC_COMMIT_REPLAY only), per verify row r < n_slots-1:
+ *             step_a [B][n_slots-1][rec_layers][rec_heads]         decay
+ *             step_b [B][n_slots-1][rec_layers][rec_heads][rec_dk]
+ *             step_c [B][n_slots-1][rec_layers][rec_heads][rec_dv]
+ *             conv_in[B][n_slots-1][rec_layers][conv_width]         conv input of row r
+ * n_slots >= k_max + 2. All float arrays 16-byte aligned; rec_dv, conv_width multiples of 4;
+ * kv_row_bytes and kv_request_stride multiples of 16. */
+typedef struct {
+  void *kv;
+  int64_t kv_request_stride;
+  int32_t kv_layers;
+  int64_t kv_capacity;
+  int64_t kv_row_bytes;
+  int64_t *kv_len;
+  int32_t rec_layers, rec_heads, rec_dk, rec_dv;
+  float *rec_live;
+  const float *rec_slots;
+  int32_t conv_rows, conv_width;
+  float *conv_live;
+  const float *conv_slots;
+  int32_t n_slots;
+  const float *step_a;
+  const float *step_b;
+  const float *step_c;
+  const float *conv_in;
+} spec_state_desc;
+
+enum { SPEC_COMMIT_SNAPSHOT = 0, SPEC_COMMIT_REPLAY = 1 };
+
+/* Workspace bytes needed by any call of this library on the current device for vocabularies
+ * up to V rows and up to max_batch requests per call. */
+size_t spec_workspace_bytes(int64_t V, int32_t max_batch);
+
+/* Human-readable name of a spec_status. */
+const char *spec_status_str(spec_status s);
+
+/*
+ * spec_lmhead_verify -- the shared LM head over the verify rows (lucebox-hub PR #15, "What":
+ * the trunk verifies the drafts in one batched forward; "Exactness": verify stays
+ * batch-invariant up to eight rows).
+ *
+ *   W           [V, d] LM-head weights, row-major (vocabulary-major), bf16 or fp32 (`wdt`).
+ *   H           [B*R, d] verify hidden rows, same dtype as W; row b*R + r is request b's row r.
+ *   temperature [B] float; <= 0 means greedy for that request.
+ *   logits      [B*R, V] float32 or NULL. Rows of requests with temperature > 0 receive
+ *               z = H W^T; rows of greedy requests are left untouched. NULL = statistics only.
+ *   stats       [B*R] spec_rowstats of each row at its request's temperature.
+ * Each row's logits and statistics are bitwise independent of how many rows share the call
+ * (batch invariance). B*R <= 8 runs the streaming GEMV. Returns SPEC_ERR_UNSUPPORTED for
+ * larger batches until the batched path is present in this build (spec_batched_supported()).
+ */
+spec_status spec_lmhead_verify(const void *W, spec_dtype wdt, int64_t V, int64_t d,
+                               const void *H, int32_t B, int32_t R, const float *temperature,
+                               float *logits, spec_rowstats *stats, void *workspace,
+                               size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_draft_argmax -- draft-head projection over the first V_draft rows of the same LM head
+ * with the token choice fused in; the token stays in device memory for the next draft
+ * (lucebox-hub PR #15, "What": "the draft head covers 64,000 vocabulary rows ... picks its
+ * token on the GPU and feeds the next draft from device memory").
+ *
+ *   W, wdt, d   as for spec_lmhead_verify; only rows [0, V_draft) are read.
+ *   h           [B, d] draft hidden rows (one per request), B <= 8.
+ *   temperature [B]: <= 0 -> token = argmax (lowest index on ties); > 0 -> token drawn from
+ *               softmax(y / T) by inverse CDF with the uniform U(seed[b], pos[b]+pos_offset,
+ *               DRAFT) (Philox4x32-10; see spec_accept for the uniform's definition).
+ *   seed [B] uint64, pos [B] int64: the request's Philox key and the absolute position the
+ *               draft predicts is pos[b] + pos_offset.
+ *   token_out   written at token_out[b * token_stride] (int32).
+ *   q_logits    [B, q_stride] float32 (row b at q_logits + b*q_stride, first V_draft used) or
+ *               NULL; required when any temperature > 0 (a request with T > 0 and no q_logits
+ *               gets token -1). q_stats [B] or NULL.
+ */
+spec_status spec_draft_argmax(const void *W, spec_dtype wdt, int64_t V_draft, int64_t d,
+                              const void *h, int32_t B, const float *temperature,
+                              const uint64_t *seed, const int64_t *pos, int32_t pos_offset,
+                              int32_t *token_out, int32_t token_stride, float *q_logits,
+                              int64_t q_stride, spec_rowstats *q_stats, void *workspace,
+                              size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_accept -- acceptance, residual correction, bonus token and EOS truncation for B
+ * requests (greedy rule: lucebox-hub PR #15, "Exactness"; ratio rule, residual, zero and
+ * non-finite handling, EOS: DS4Server issue #98, "Implementation" and closing comment).
+ *
+ * For request b with k = k[b] drafts d_i = drafts[b*k_max + i-1] (i = 1..k), verify row r at
+ * logits/stats row b*R + r (row r predicts position pos_base[b] + r):
+ *   T <= 0: accept d_i while d_i == argmax z_{i-1}; the first mismatch emits argmax z_{i-1};
+ *           all k accepted emits the bonus argmax z_k.
+ *   T  > 0: p_r = softmax(z_r / T); q_i = softmax(y_i / T) over the draft rows, 0 beyond them,
+ *           or one-hot at d_i when q_logits is NULL. Accept d_i while p_{i-1}(d_i) > 0 and
+ *           u*q_i(d_i) <= p_{i-1}(d_i), u = U(pos_base+i-1, ACCEPT); at the first rejection
+ *           emit an inverse-CDF draw from r = max(0, p_{i-1} - q_i) (from p_{i-1} if r sums to
+ *           zero) with U(pos_base+i-1, RESIDUAL); all k accepted emits a draw from p_k with
+ *           U(pos_base+k, BONUS).
+ *   An emitted EOS (eos_id >= 0) ends the block; nothing after it is emitted.
+ * Uniforms: U(pos, purpose) = (w0 >> 8) * 2^-24 where w0 is the first word of
+ * Philox4x32-10(counter = (pos mod 2^32, pos >> 32, 0, purpose), key = (seed mod 2^32,
+ * seed >> 32)) (Salmon et al., SC'11); purposes DRAFT = 1, ACCEPT = 2, RESIDUAL = 3, BONUS = 4.
+ * Inverse CDF: the smallest token id whose cumulative weight exceeds u * total, with weights
+ * quantised to multiples of 2^-40 and summed exactly in 64-bit integers.
+ *
+ *   logits [B*R, V] float32: needed for requests with T > 0 (status SPEC_REQ_NO_LOGITS if
+ *          NULL); stats [B*R] from spec_lmhead_verify.
+ *   q_logits [k_max*B, q_stride] float32, draft-major: draft i of request b at row
+ *          (i-1)*B + b (what spec_draft_argmax writes for draft i when given q_logits + (i-1)*B
+ *          rows), or NULL; q_stats [k_max*B] alongside it (required when q_logits is given).
+ *   out [B]: results. counters [B] or NULL: accumulated telemetry.
+ */
+spec_status spec_accept(int32_t B, int32_t k_max, const int32_t *k, const int32_t *drafts,
+                        const float *logits, const spec_rowstats *stats, int64_t V, int32_t R,
+                        const float *q_logits, const spec_rowstats *q_stats, int64_t V_draft,
+                        int64_t q_stride, const float *temperature, int32_t eos_id,
+                        const uint64_t *seed, const int64_t *pos_base, spec_accept_out *out,
+                        spec_counters *counters, void *workspace, size_t workspace_bytes,
+                        spec_stream_t stream);
+
+/*
+ * spec_commit_rollback -- keep the accepted prefix, drop the rest, on the device (DS4Server
+ * issue #98, "Implementation": trim rejected rows, commit or replay only accepted recurrent
+ * rows; llama.cpp PR #28104: full-checkpoint restore and replay without re-verification,
+ * checkpoints kept on device).
+ *
+ * With m = out[b].n_emit (m = 0 if out[b].status != 0) and P = kv_len[b] read on the device:
+ *   KV rows [P+m, P+k[b]+1) are zero-filled (clipped to capacity), kv_len[b] = P + m;
+ *   SPEC_COMMIT_SNAPSHOT: rec_live <- rec_slots[m], conv_live <- conv_slots[m];
+ *   SPEC_COMMIT_REPLAY:   rec_live <- slot 0 advanced over rows 0..m-1 by
+ *                         S = fl32(fl32(a*S) + fl32(b_i*c_j)) per layer and head, each
+ *                         operation rounded separately; conv_live <- the last conv_rows rows
+ *                         of (conv_slots[0] rows, conv_in rows 0..m-1).
+ * Both modes produce identical bytes when the slots were captured with the same step.
+ *   k [B] the cycle's draft counts; commit_status [B] int32 or NULL (SPEC_REQ_KV_OVERFLOW).
+ */
+spec_status spec_commit_rollback(int32_t B, const spec_state_desc *st,
+                                 const spec_accept_out *acc, const int32_t *k, int32_t mode,
+                                 int32_t *commit_status, spec_stream_t stream);
+
+/* 1 if this build has the batched tensor-core path for more than 8 verify rows per call. */
+int32_t spec_batched_supported(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_H */

@@ -1,0 +1,89 @@
+"""Python binding of libspec.so: the per-cycle verify step of MTP speculative decoding on a
+GB300 (sm_103a).
+
+Each function has the name and argument order of the C call in include/spec.h and only
+marshals arguments: torch tensors (device memory) become raw pointers, the stream defaults to
+torch's current stream, and a non-zero spec_status raises SpecError. Every step of the path
+runs in the library's CUDA kernels; nothing here computes, and nothing falls back to the CPU.
+"""
+
+from . import _abi
+from ._abi import (ACCEPT_OUT_DTYPE, COUNTERS_DTYPE, REQ_BAD_K, REQ_BAD_TOKEN,  # noqa: F401
+                   REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_NONFINITE, REQ_OK, ROWSTATS_DTYPE,
+                   SPEC_BF16, SPEC_COMMIT_REPLAY, SPEC_COMMIT_SNAPSHOT, SPEC_F32,
+                   spec_state_desc)
+
+ROWSTATS_BYTES = ROWSTATS_DTYPE.itemsize
+ACCEPT_OUT_BYTES = ACCEPT_OUT_DTYPE.itemsize
+COUNTERS_BYTES = COUNTERS_DTYPE.itemsize
+
+
+class SpecError(RuntimeError):
+    def __init__(self, name, status):
+        self.status = status
+        msg = _abi.lib().spec_status_str(status).decode()
+        super().__init__(f"{name} returned {msg} ({status})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name, st):
+    if st != 0:
+        raise SpecError(name, st)
+
+
+def spec_workspace_bytes(V, max_batch):
+    return int(_abi.lib().spec_workspace_bytes(int(V), int(max_batch)))
+
+
+def spec_batched_supported():
+    return bool(_abi.lib().spec_batched_supported())
+
+
+def spec_lmhead_verify(W, wdt, V, d, H, B, R, temperature, logits, stats, workspace,
+                       stream=None):
+    _check("spec_lmhead_verify", _abi.lib().spec_lmhead_verify(
+        _ptr(W), wdt, V, d, _ptr(H), B, R, _ptr(temperature), _ptr(logits), _ptr(stats),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def spec_draft_argmax(W, wdt, V_draft, d, h, B, temperature, seed, pos, pos_offset, token_out,
+                      token_stride, q_logits, q_stride, q_stats, workspace, stream=None):
+    _check("spec_draft_argmax", _abi.lib().spec_draft_argmax(
+        _ptr(W), wdt, V_draft, d, _ptr(h), B, _ptr(temperature), _ptr(seed), _ptr(pos),
+        pos_offset, _ptr(token_out), token_stride, _ptr(q_logits), q_stride, _ptr(q_stats),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_draft, q_stride,
+                temperature, eos_id, seed, pos_base, out, counters, workspace, stream=None):
+    _check("spec_accept", _abi.lib().spec_accept(
+        B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(q_logits),
+        _ptr(q_stats), V_draft, q_stride, _ptr(temperature), eos_id, _ptr(seed), _ptr(pos_base),
+        _ptr(out), _ptr(counters), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def spec_commit_rollback(B, st, acc, k, mode, commit_status=None, stream=None):
+    """``st`` is a ``spec_state_desc`` (host struct of device pointers)."""
+    import ctypes
+    _check("spec_commit_rollback", _abi.lib().spec_commit_rollback(
+        B, ctypes.byref(st), _ptr(acc), _ptr(k), mode, _ptr(commit_status), _stream(stream)))

@@ -1,0 +1,298 @@
+// extern "C" entry points of libspec.so: argument validation, workspace layout, launch
+// configuration. Every call validates on the host, then enqueues on the caller's stream; no
+// call allocates memory or synchronises.
+#include <stdint.h>
+#include <string.h>
+
+#include "params.cuh"
+
+
+namespace spec {
+namespace {
+
+constexpr int kMaxTileRows = 2048;  // per-block tile of the GEMV (logits kept in smem)
+constexpr int kMaxWarpsPerRow = 12;
+
+struct DevAttr {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+DevAttr dev_attr() {
+  static DevAttr cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevAttr{};
+  if (cache[dev].sms == 0) {
+    DevAttr a;
+    cudaDeviceGetAttribute(&a.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&a.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cache[dev] = a;
+  }
+  return cache[dev];
+}
+
+int gemv_grid(int64_t V, int sms) {
+  int64_t g = sms;
+  const int64_t need = (V + kMaxTileRows - 1) / kMaxTileRows;
+  if (need > g) g = need;
+  return static_cast<int>(g);
+}
+
+int accept_slices(int64_t V) { return static_cast<int>((V + kAcceptSlice - 1) / kAcceptSlice); }
+
+// Workspace layout. Offsets that depend on the batch would let calls with different batches
+// overlap one another's zero-initialised counters, so only the accept tickets depend on B and
+// they sit at the END of the caller's buffer:
+//   [0, 256)                    header (GEMV ticket, error word)
+//   [256, part_end)             GEMV per-block partials (grid of the vocabulary size)
+//   [part_end, sums_end)        accept per-slice sums (B * slices * 16 bytes)
+//   [ws_bytes - tickets, end)   accept tickets, one per request
+struct WsLayout {
+  size_t part, sums, tickets_bytes, total;
+};
+
+WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
+  WsLayout w;
+  w.part = sizeof(WsHeader);
+  w.sums = w.part + align_up(sizeof(GemvPartial) * kMaxRows * gemv_grid(V, sms), 256);
+  w.tickets_bytes = align_up(sizeof(uint32_t) * static_cast<size_t>(max_batch), 256);
+  w.total = w.sums +
+            align_up(sizeof(unsigned long long) * 2 * static_cast<size_t>(max_batch) *
+                         accept_slices(V),
+                     256) +
+            w.tickets_bytes;
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int next_pow2_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
+
+// Configure and launch the GEMV for `nrows` rows over the first V rows of W.
+spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const void* H,
+                     int nrows, int rows_per_req, const float* temperature, float* logits,
+                     int64_t logits_stride, spec_rowstats* stats, int draft,
+                     const uint64_t* seed, const int64_t* pos, int pos_offset,
+                     int32_t* token_out, int token_stride, void* workspace,
+                     size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream) {
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  const int elt = (wdt == SPEC_BF16) ? 2 : 4;
+  const int64_t row_bytes = d * elt;
+  if (row_bytes % 16 != 0) return SPEC_ERR_INVALID;
+  const int cpr = static_cast<int>(row_bytes / 16);
+  const int wpr = (cpr + 31) / 32;
+  if (wpr > kMaxWarpsPerRow) return SPEC_ERR_UNSUPPORTED;
+  const WsLayout wl = ws_layout(V, batch_for_ws, a.sms);
+  if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
+
+  GemvLaunch L;
+  memset(&L, 0, sizeof(L));
+  GemvParams& p = L.p;
+  const int grid = gemv_grid(V, a.sms);
+  const int rp = next_pow2_rows(nrows);
+  const int ng = (kMaxWarpsPerRow / wpr) > 0 ? (kMaxWarpsPerRow / wpr) : 1;
+  const int nw = wpr * ng;
+  const int stage_rows = 4 * ng;
+  const int stage_bytes = static_cast<int>(align_up(static_cast<size_t>(stage_rows) * row_bytes, 128));
+  const int tile_cap = static_cast<int>(align_up(static_cast<size_t>((V + grid - 1) / grid), 4));
+  const size_t fixed = static_cast<size_t>(rp) * tile_cap * 4 + 64;
+  const size_t per_stage = static_cast<size_t>(stage_bytes) + static_cast<size_t>(nw) * 32 * 4 +
+                           (2 + static_cast<size_t>(ng)) * 8;
+  const size_t budget = static_cast<size_t>(a.smem_optin);
+  if (budget <= fixed + 2 * per_stage) return SPEC_ERR_UNSUPPORTED;
+  int stages = static_cast<int>((budget - fixed) / per_stage);
+  if (stages > 8) stages = 8;
+  // the last block reuses the stage ring for two doubles per block per warp
+  const size_t scratch = static_cast<size_t>(nw + 1) * 2 * grid * sizeof(double);
+  if (static_cast<size_t>(stages) * stage_bytes < scratch) return SPEC_ERR_UNSUPPORTED;
+
+  p.W = static_cast<const uint8_t*>(W);
+  p.V = V;
+  p.row_bytes = static_cast<int>(row_bytes);
+  p.cpr = cpr;
+  p.wpr = wpr;
+  p.ng = ng;
+  p.nw = nw;
+  p.stages = stages;
+  p.stage_rows = stage_rows;
+  p.stage_bytes = stage_bytes;
+  p.tile_cap = tile_cap;
+  p.H = static_cast<const uint8_t*>(H);
+  p.h_row_bytes = static_cast<int>(row_bytes);
+  p.nrows = nrows;
+  p.rows_per_req = rows_per_req;
+  p.temperature = temperature;
+  p.logits = logits;
+  p.logits_stride = logits_stride;
+  p.stats = stats;
+  p.draft = draft;
+  p.seed = seed;
+  p.pos = pos;
+  p.pos_offset = pos_offset;
+  p.token_out = token_out;
+  p.token_stride = token_stride;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  L.grid = grid;
+  L.threads = (nw + 1) * 32;
+  L.smem = static_cast<int>(fixed + static_cast<size_t>(stages) * per_stage);
+  const cudaError_t e = gemv_dispatch(L, wdt == SPEC_BF16, rp, stream);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" {
+
+size_t spec_workspace_bytes(int64_t V, int32_t max_batch) {
+  if (V < 1 || max_batch < 1) return 0;
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return 0;
+  return ws_layout(V, max_batch, a.sms).total;
+}
+
+const char* spec_status_str(spec_status s) {
+  switch (s) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_INVALID: return "SPEC_ERR_INVALID";
+    case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+  }
+  return "SPEC_ERR_UNKNOWN";
+}
+
+int32_t spec_batched_supported(void) { return 0; }
+
+spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t d,
+                               const void* H, int32_t B, int32_t R, const float* temperature,
+                               float* logits, spec_rowstats* stats, void* workspace,
+                               size_t workspace_bytes, spec_stream_t stream) {
+  if (!W || !H || !temperature || !stats || !workspace) return SPEC_ERR_INVALID;
+  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(H) || !aligned16(workspace)) return SPEC_ERR_INVALID;
+  if (static_cast<int64_t>(B) * R > kMaxRows) return SPEC_ERR_UNSUPPORTED;
+  return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
+                  nullptr, 0, nullptr, 0, workspace, workspace_bytes, B,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, int64_t d,
+                              const void* h, int32_t B, const float* temperature,
+                              const uint64_t* seed, const int64_t* pos, int32_t pos_offset,
+                              int32_t* token_out, int32_t token_stride, float* q_logits,
+                              int64_t q_stride, spec_rowstats* q_stats, void* workspace,
+                              size_t workspace_bytes, spec_stream_t stream) {
+  if (!W || !h || !temperature || !seed || !pos || !token_out || !workspace)
+    return SPEC_ERR_INVALID;
+  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (V_draft < 1 || V_draft >= (int64_t(1) << 24) || d < 1 || B < 1 || B > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (token_stride < 1 || (q_logits && q_stride < V_draft)) return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(h) || !aligned16(workspace)) return SPEC_ERR_INVALID;
+  return run_gemv(W, wdt, V_draft, d, h, B, 1, temperature, q_logits, q_stride, q_stats, 1,
+                  seed, pos, pos_offset, token_out, token_stride, workspace, workspace_bytes,
+                  B, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
+                        const float* logits, const spec_rowstats* stats, int64_t V, int32_t R,
+                        const float* q_logits, const spec_rowstats* q_stats, int64_t V_draft,
+                        int64_t q_stride, const float* temperature, int32_t eos_id,
+                        const uint64_t* seed, const int64_t* pos_base, spec_accept_out* out,
+                        spec_counters* counters, void* workspace, size_t workspace_bytes,
+                        spec_stream_t stream) {
+  if (B < 1 || k_max < 0 || k_max > kMaxRows - 1 || R < 1 || R > kMaxRows) return SPEC_ERR_INVALID;
+  if (!k || (k_max > 0 && !drafts) || !stats || !temperature || !seed || !pos_base || !out ||
+      !workspace)
+    return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24)) return SPEC_ERR_INVALID;
+  if (q_logits && (!q_stats || V_draft < 1 || V_draft > V || q_stride < V_draft))
+    return SPEC_ERR_INVALID;
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  const WsLayout wl = ws_layout(V, B, a.sms);
+  if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
+  AcceptParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.k_max = k_max;
+  p.R = R;
+  p.NS = accept_slices(V);
+  p.k = k;
+  p.drafts = drafts;
+  p.logits = logits;
+  p.stats = stats;
+  p.V = V;
+  p.q_logits = q_logits;
+  p.q_stats = q_stats;
+  p.Vd = q_logits ? V_draft : 0;
+  p.q_stride = q_stride;
+  p.temperature = temperature;
+  p.eos = eos_id;
+  p.seed = seed;
+  p.pos_base = pos_base;
+  p.out = out;
+  p.counters = counters;
+  // tickets: the last 4*B bytes of the buffer, its end rounded down to 4 bytes (see WsLayout)
+  const size_t end4 = workspace_bytes & ~static_cast<size_t>(3);
+  p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + end4 -
+                                          sizeof(uint32_t) * static_cast<size_t>(B));
+  p.sums = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + wl.sums);
+  const cudaError_t e = accept_launch(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
+                                 const spec_accept_out* acc, const int32_t* k, int32_t mode,
+                                 int32_t* commit_status, spec_stream_t stream) {
+  if (B < 1 || !st || !acc || !k) return SPEC_ERR_INVALID;
+  if (mode != SPEC_COMMIT_SNAPSHOT && mode != SPEC_COMMIT_REPLAY) return SPEC_ERR_INVALID;
+  if (st->n_slots < 2) return SPEC_ERR_INVALID;
+  if (st->kv_layers < 0 || st->rec_layers < 0 || st->conv_rows < 0) return SPEC_ERR_INVALID;
+  if (st->kv_layers > 0) {
+    if (!st->kv || !st->kv_len || st->kv_capacity < 1 || st->kv_row_bytes < 16 ||
+        st->kv_row_bytes % 16 != 0 || st->kv_request_stride % 16 != 0 || !aligned16(st->kv))
+      return SPEC_ERR_INVALID;
+    if (st->kv_request_stride < 2 * st->kv_layers * st->kv_capacity * st->kv_row_bytes &&
+        B > 1)
+      return SPEC_ERR_INVALID;
+  }
+  if (st->rec_layers > 0) {
+    if (st->rec_heads < 1 || st->rec_dk < 1 || st->rec_dv < 4 || st->rec_dv % 4 != 0)
+      return SPEC_ERR_INVALID;
+    if (!st->rec_live || !st->rec_slots || !aligned16(st->rec_live) || !aligned16(st->rec_slots))
+      return SPEC_ERR_INVALID;
+    if (mode == SPEC_COMMIT_REPLAY &&
+        (!st->step_a || !st->step_b || !st->step_c || !aligned16(st->step_c)))
+      return SPEC_ERR_INVALID;
+    if (st->conv_rows > 0) {
+      if (st->conv_width < 4 || st->conv_width % 4 != 0 || !st->conv_live || !st->conv_slots ||
+          !aligned16(st->conv_live) || !aligned16(st->conv_slots))
+        return SPEC_ERR_INVALID;
+      if (mode == SPEC_COMMIT_REPLAY && (!st->conv_in || !aligned16(st->conv_in)))
+        return SPEC_ERR_INVALID;
+    }
+  }
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  CommitParams p;
+  memset(&p, 0, sizeof(p));
+  p.st = *st;
+  p.acc = acc;
+  p.k = k;
+  p.mode = mode;
+  p.commit_status = commit_status;
+  int per_req = (4 * a.sms + B - 1) / B;
+  if (st->rec_layers == 0) per_req = 1;
+  if (per_req < 1) per_req = 1;
+  const cudaError_t e = commit_launch(p, B, per_req, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,360 @@
+// Acceptance, residual correction, bonus token and EOS truncation for B requests.
+//
+// Rules (lucebox-hub PR #15 "MTP speculative decoding", section "Exactness": a greedy draft
+// is accepted only if it equals the trunk's token; DS4Server issue #98 "Add Qwen3.8 Flash Next
+// native MTP speculation", section "Implementation" and closing comment: probability-ratio
+// acceptance u*q <= p, max(0, p - q) residual correction, zero / non-finite probability
+// handling, EOS inside a proposal block) -- see spec_accept in spec.h for the exact statement.
+//
+// Work layout: grid (slices, B), one block per 1,024-entry slice of the vocabulary of one
+// request. Every block first takes the O(k) decision for its request (identical in every
+// block); when the decision needs a draw over the whole vocabulary (residual at the first
+// rejection, or the bonus at temperature > 0) each block sums its slice's weights, quantised
+// to 2^-40 units, in exact 64-bit integers; the last block of the request (a per-request
+// ticket, no inter-block waiting) picks the slice holding the target and rescans it. Integer
+// sums make the drawn token independent of block scheduling and summation order.
+#include <math.h>
+
+#include "params.cuh"
+
+namespace spec {
+
+
+struct Decision {
+  int status, n_accept, ntok, eos_hit;
+  int tokens[8];
+  int need;  // 0 none, 1 residual draw, 2 bonus draw
+  int srow;  // verify row of the draw
+  int xrej;  // the rejected draft (one-hot q)
+  int pad;
+};
+
+// p(v) = exp((z - max)/T) * exp(-log_norm), every operation rounded on its own.
+__device__ __forceinline__ float prob_of(float z, float mx, float invT, float inv_norm) {
+  return __fmul_rn(expf(__fmul_rn(__fsub_rn(z, mx), invT)), inv_norm);
+}
+
+struct DrawCtx {
+  const float* prow;  // verify logits row of the draw
+  float pmax, pinvT, pinv_norm;
+  const float* qrow;  // draft logits row (residual with q_logits), else null
+  float qmax, qinv_norm;
+  int64_t Vd;
+  int xrej;        // one-hot q position (residual without q_logits), else -1
+  bool residual;
+};
+
+// The two integer weights of vocabulary entry j: residual max(0, p - q) and p itself.
+__device__ __forceinline__ void entry_weights(const DrawCtx& c, int64_t j,
+                                              unsigned long long& wr,
+                                              unsigned long long& wp) {
+  const float pj = prob_of(__ldcg(c.prow + j), c.pmax, c.pinvT, c.pinv_norm);
+  wp = quantise(pj);
+  if (!c.residual) {
+    wr = wp;
+    return;
+  }
+  float qj = 0.f;
+  if (c.qrow) {
+    if (j < c.Vd) qj = prob_of(__ldcg(c.qrow + j), c.qmax, c.pinvT, c.qinv_norm);
+  } else {
+    qj = (j == c.xrej) ? 1.f : 0.f;
+  }
+  wr = quantise(fmaxf(0.f, __fsub_rn(pj, qj)));
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
+                                                            unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_u64(v);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0ull;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += sh[w];
+  return t;
+}
+
+__device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
+  spec_accept_out o;
+  o.status = D.status;
+  o.n_accept = D.n_accept;
+  o.n_emit = D.ntok;
+  o.eos_hit = D.eos_hit;
+  for (int i = 0; i < 8; ++i) o.tokens[i] = i < D.ntok ? D.tokens[i] : -1;
+  o.sample_kind = D.need;
+  o.sample_row = D.need ? D.srow : -1;
+  o.reserved[0] = 0;
+  o.reserved[1] = 0;
+  p.out[b] = o;
+  if (p.counters) {
+    spec_counters* c = p.counters + b;
+    c->cycles += 1ull;
+    if (D.status == SPEC_REQ_OK) {
+      c->drafted += static_cast<unsigned long long>(k);
+      c->accepted += static_cast<unsigned long long>(D.n_accept);
+      c->emitted += static_cast<unsigned long long>(D.ntok);
+      c->eos += static_cast<unsigned long long>(D.eos_hit);
+      c->depth[D.n_accept & 7] += 1ull;
+    } else {
+      c->errors += 1ull;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptParams p) {
+  __shared__ Decision D;
+  __shared__ int sx[8], sam[8];
+  __shared__ unsigned long long sh[kAcceptThreads / 32];
+  __shared__ int s_last, s_slice, s_tok;
+  __shared__ unsigned long long s_before;
+
+  const int b = blockIdx.y, sl = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = p.k[b];
+  const float T = p.temperature[b];
+
+  // ---------------- the O(k) decision (same in every block of the request) ----------------
+  if (warp == 0) {
+    int status = SPEC_REQ_OK;
+    const bool kbad = (k < 0 || k > p.k_max || k + 1 > p.R);
+    if (kbad) status = SPEC_REQ_BAD_K;
+    int x = -1;
+    bool xbad = false;
+    if (!kbad && lane < k) {
+      x = p.drafts[static_cast<size_t>(b) * p.k_max + lane];
+      xbad = (x < 0 || static_cast<int64_t>(x) >= p.V);
+    }
+    if (status == SPEC_REQ_OK && __any_sync(0xffffffffu, xbad)) status = SPEC_REQ_BAD_TOKEN;
+    if (status == SPEC_REQ_OK && T > 0.f &&
+        (p.logits == nullptr || (p.q_logits != nullptr && p.q_stats == nullptr)))
+      status = SPEC_REQ_NO_LOGITS;
+    spec_rowstats st{0.f, 0.f, 0.f, -1};
+    bool nf = false;
+    if (status == SPEC_REQ_OK) {
+      if (lane <= k) {
+        st = p.stats[static_cast<size_t>(b) * p.R + lane];
+        nf = isnan(st.max);
+      }
+      if (T > 0.f && p.q_logits && lane < k)
+        nf = nf || isnan(p.q_stats[static_cast<size_t>(lane) * p.B + b].max);
+      if (__any_sync(0xffffffffu, nf)) status = SPEC_REQ_NONFINITE;
+    }
+    bool acc = false;
+    if (status == SPEC_REQ_OK && lane < k) {
+      if (!(T > 0.f)) {
+        acc = (x == st.argmax);
+      } else {
+        const float invT = __fdiv_rn(1.f, T);
+        const size_t row = static_cast<size_t>(b) * p.R + lane;
+        const float px = prob_of(__ldcg(p.logits + row * p.V + x), st.max, invT,
+                                 expf(-st.log_norm));
+        float qx = 1.f;
+        if (p.q_logits) {
+          qx = 0.f;
+          if (static_cast<int64_t>(x) < p.Vd) {
+            const size_t qr = static_cast<size_t>(lane) * p.B + b;
+            const spec_rowstats qs = p.q_stats[qr];
+            qx = prob_of(__ldcg(p.q_logits + qr * p.q_stride + x), qs.max, invT,
+                         expf(-qs.log_norm));
+          }
+        }
+        const float u = u24_to_float(uniform_u24(p.seed[b], p.pos_base[b] + lane, PURPOSE_ACCEPT));
+        acc = (px > 0.f) && (__fmul_rn(u, qx) <= px);
+      }
+    }
+    const unsigned accmask = __ballot_sync(0xffffffffu, acc);
+    if (lane < 8) {
+      sx[lane] = x;
+      sam[lane] = st.argmax;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      Decision d;
+      d.status = status;
+      d.n_accept = 0;
+      d.ntok = 0;
+      d.eos_hit = 0;
+      d.need = 0;
+      d.srow = -1;
+      d.xrej = -1;
+      d.pad = 0;
+      if (status == SPEC_REQ_OK) {
+        bool stop = false;
+        for (int i = 0; i < k && !stop; ++i) {
+          if ((accmask >> i) & 1u) {
+            d.tokens[d.ntok++] = sx[i];
+            d.n_accept++;
+            if (p.eos >= 0 && sx[i] == p.eos) {
+              d.eos_hit = 1;
+              stop = true;
+            }
+          } else {
+            if (!(T > 0.f)) {
+              d.tokens[d.ntok++] = sam[i];
+              if (p.eos >= 0 && sam[i] == p.eos) d.eos_hit = 1;
+            } else {
+              d.need = 1;
+              d.srow = i;
+              d.xrej = sx[i];
+            }
+            stop = true;
+          }
+        }
+        if (!stop) {
+          if (!(T > 0.f)) {
+            d.tokens[d.ntok++] = sam[k];
+            if (p.eos >= 0 && sam[k] == p.eos) d.eos_hit = 1;
+          } else {
+            d.need = 2;
+            d.srow = k;
+          }
+        }
+      }
+      D = d;
+    }
+  }
+  __syncthreads();
+
+  if (D.need == 0) {
+    if (sl == 0 && tid == 0) finalize(p, b, D, k);
+    return;
+  }
+
+  // ---------------- slice sums of the draw's integer weights ----------------
+  DrawCtx c;
+  {
+    const size_t prow = static_cast<size_t>(b) * p.R + D.srow;
+    const spec_rowstats ps = p.stats[prow];
+    c.prow = p.logits + prow * p.V;
+    c.pmax = ps.max;
+    c.pinvT = __fdiv_rn(1.f, T);
+    c.pinv_norm = expf(-ps.log_norm);
+    c.residual = (D.need == 1);
+    c.qrow = nullptr;
+    c.qmax = 0.f;
+    c.qinv_norm = 0.f;
+    c.Vd = p.Vd;
+    c.xrej = -1;
+    if (c.residual) {
+      if (p.q_logits) {
+        const size_t qr = static_cast<size_t>(D.srow) * p.B + b;
+        const spec_rowstats qs = p.q_stats[qr];
+        c.qrow = p.q_logits + qr * p.q_stride;
+        c.qmax = qs.max;
+        c.qinv_norm = expf(-qs.log_norm);
+      } else {
+        c.xrej = D.xrej;
+      }
+    }
+  }
+  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
+  unsigned long long sr = 0ull, sp = 0ull;
+  for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
+    const int64_t j = j0 + e * kAcceptThreads + tid;
+    if (j < p.V) {
+      unsigned long long wr, wp;
+      entry_weights(c, j, wr, wp);
+      sr += wr;
+      sp += wp;
+    }
+  }
+  sr = block_sum_u64(sr, sh);
+  sp = block_sum_u64(sp, sh);
+  unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * 2;
+  if (tid == 0) {
+    mysum[0] = sr;
+    mysum[1] = sp;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(p.tickets + b, 1u);
+    s_last = (t == static_cast<unsigned>(p.NS) - 1u) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---------------- last block of the request: locate and rescan the slice ----------------
+  const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * 2;
+  unsigned long long tr = 0ull, tp = 0ull;
+  for (int i = tid; i < p.NS; i += kAcceptThreads) {
+    tr += __ldcg(rs + 2 * i);
+    tp += __ldcg(rs + 2 * i + 1);
+  }
+  tr = block_sum_u64(tr, sh);
+  tp = block_sum_u64(tp, sh);
+  const bool use_p = (D.need == 2) || (tr == 0ull);
+  const unsigned long long total = use_p ? tp : tr;
+  const uint32_t purpose = (D.need == 1) ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
+  const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + D.srow, purpose);
+  const unsigned long long target = cdf_target(u24, total);
+  if (tid == 0) {
+    unsigned long long cum = 0ull;
+    int slice = -1;
+    for (int i = 0; i < p.NS; ++i) {
+      const unsigned long long w = __ldcg(rs + 2 * i + (use_p ? 1 : 0));
+      if (w > 0ull && cum + w > target) {
+        slice = i;
+        break;
+      }
+      cum += w;
+    }
+    s_slice = slice;
+    s_before = cum;
+    s_tok = -1;
+  }
+  __syncthreads();
+  int tok = -1;
+  if (s_slice >= 0) {
+    const int64_t base = static_cast<int64_t>(s_slice) * kAcceptSlice;
+    unsigned long long carry = s_before;
+    for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
+      const int64_t j = base + e * kAcceptThreads + tid;
+      unsigned long long w = 0ull;
+      if (j < p.V) {
+        unsigned long long wr, wp;
+        entry_weights(c, j, wr, wp);
+        w = use_p ? wp : wr;
+      }
+      // block inclusive scan of w in ascending j
+      unsigned long long incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long up = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += up;
+      }
+      __syncthreads();
+      if (lane == 31) sh[warp] = incl;
+      __syncthreads();
+      unsigned long long wbefore = 0ull, round_total = 0ull;
+      for (int w2 = 0; w2 < kAcceptThreads / 32; ++w2) {
+        if (w2 < warp) wbefore += sh[w2];
+        round_total += sh[w2];
+      }
+      const unsigned long long cum_incl = carry + wbefore + incl;
+      if (w > 0ull && cum_incl > target && cum_incl - w <= target) s_tok = static_cast<int>(j);
+      carry += round_total;
+      __syncthreads();
+      if (s_tok >= 0) break;
+    }
+    tok = s_tok;
+  }
+  if (tid == 0) {
+    Decision d = D;
+    if (tok < 0) tok = p.stats[static_cast<size_t>(b) * p.R + D.srow].argmax;  // unreachable
+    d.tokens[d.ntok++] = tok;
+    if (p.eos >= 0 && tok == p.eos) d.eos_hit = 1;
+    finalize(p, b, d, k);
+    p.tickets[b] = 0u;
+  }
+}
+
+cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream) {
+  dim3 grid(prm.NS, prm.B);
+  accept_kernel<<<grid, kAcceptThreads, 0, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace spec

@@ -1,0 +1,77 @@
+// Launch parameter blocks of the kernels (passed by value to each kernel).
+#pragma once
+
+#include "common.cuh"
+
+namespace spec {
+
+struct GemvParams {
+  const uint8_t* W;
+  int64_t V;
+  int row_bytes;
+  int cpr;  // 16-byte chunks per weight row
+  int wpr;  // warps per weight row
+  int ng;   // row groups per block
+  int nw;   // compute warps = wpr * ng
+  int stages;
+  int stage_rows;  // = 4 * ng
+  int stage_bytes;
+  int tile_cap;  // max rows per block tile
+  const uint8_t* H;
+  int h_row_bytes;
+  int nrows;
+  int rows_per_req;
+  const float* temperature;
+  float* logits;  // nullable
+  int64_t logits_stride;
+  spec_rowstats* stats;  // nullable
+  int draft;
+  const uint64_t* seed;
+  const int64_t* pos;
+  int pos_offset;
+  int32_t* token_out;
+  int token_stride;
+  WsHeader* hdr;
+  GemvPartial* part;
+};
+
+struct GemvLaunch {
+  int grid, threads, smem;
+  GemvParams p;
+};
+
+struct AcceptParams {
+  int B, k_max, R, NS;
+  const int32_t* k;
+  const int32_t* drafts;
+  const float* logits;
+  const spec_rowstats* stats;
+  int64_t V;
+  const float* q_logits;
+  const spec_rowstats* q_stats;
+  int64_t Vd;
+  int64_t q_stride;
+  const float* temperature;
+  int eos;
+  const uint64_t* seed;
+  const int64_t* pos_base;
+  spec_accept_out* out;
+  spec_counters* counters;
+  uint32_t* tickets;         // [B]
+  unsigned long long* sums;  // [B][NS][2]: residual weight, p weight
+};
+
+struct CommitParams {
+  spec_state_desc st;
+  const spec_accept_out* acc;
+  const int32_t* k;
+  int mode;
+  int32_t* commit_status;
+};
+
+cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
+cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
+cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
+                          cudaStream_t stream);
+
+}  // namespace spec

@@ -1,0 +1,95 @@
+"""SpecVerifyEngine: owns the device buffers of one verify-step configuration and enqueues the
+cycle -- k draft-head steps, the verify LM head, acceptance, commit -- on one CUDA stream.
+
+PyTorch provides device memory and the stream; every step runs in libspec.so's kernels. No call
+here reads a result back to the host except ``cycle_from_host``, which is the end-to-end path:
+it copies one cycle's inputs from pinned host memory, runs the cycle and copies the 64-byte
+results back, all asynchronously on the stream.
+"""
+
+import torch
+
+from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_BF16, spec_accept,
+               spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify, spec_workspace_bytes)
+
+
+class SpecVerifyEngine:
+    def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
+                 want_q_logits=True):
+        self.W, self.wdt, self.V, self.d, self.Vd = W, wdt, V, d, Vd
+        self.B, self.R, self.k_max, self.eos_id = B, R, k_max, eos_id
+        dev = torch.device(device)
+        self.device = dev
+        n = spec_workspace_bytes(V, B)
+        self.ws = torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device=dev)
+        self.logits = torch.empty((B * R, V), dtype=torch.float32, device=dev)
+        self.stats = torch.zeros(B * R * ROWSTATS_BYTES, dtype=torch.uint8, device=dev)
+        kq = max(k_max, 1)
+        self.q = torch.empty((kq * B, Vd), dtype=torch.float32, device=dev) if want_q_logits \
+            else None
+        self.qs = torch.zeros(kq * B * ROWSTATS_BYTES, dtype=torch.uint8, device=dev)
+        self.drafts = torch.zeros((B, kq), dtype=torch.int32, device=dev)
+        self.out = torch.zeros(B * ACCEPT_OUT_BYTES, dtype=torch.uint8, device=dev)
+        self.counters = torch.zeros(B * COUNTERS_BYTES, dtype=torch.uint8, device=dev)
+        self.temps = torch.zeros(B, dtype=torch.float32, device=dev)
+        self.seeds = torch.zeros(B, dtype=torch.int64, device=dev)
+        self.pos = torch.zeros(B, dtype=torch.int64, device=dev)
+        self.k = torch.full((B,), k_max, dtype=torch.int32, device=dev)
+        self.commit_status = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.state = None
+        self.dtype_bytes = 2 if wdt == SPEC_BF16 else 4
+
+    # ---------------------------------------------------------------- configuration
+    def set_requests(self, temps=None, seeds=None, pos=None, k=None):
+        for dst, src in ((self.temps, temps), (self.seeds, seeds), (self.pos, pos),
+                         (self.k, k)):
+            if src is not None:
+                dst.copy_(torch.as_tensor(src, dtype=dst.dtype), non_blocking=True)
+
+    def attach_state(self, desc, mode):
+        """A spec_state_desc (device pointers) committed after every acceptance."""
+        self.state, self.state_mode = desc, mode
+
+    # ---------------------------------------------------------------- the cycle
+    def draft_step(self, i, h):
+        """Draft i (1-based) for every request from draft-head hidden rows h [B, d]."""
+        B = self.B
+        spec_draft_argmax(self.W, self.wdt, self.Vd, self.d, h, B, self.temps, self.seeds,
+                          self.pos, i - 1, self.drafts[:, i - 1:], self.drafts.shape[1],
+                          None if self.q is None else self.q[(i - 1) * B:], self.Vd,
+                          self.qs[(i - 1) * B * ROWSTATS_BYTES:], self.ws)
+
+    def verify(self, H):
+        spec_lmhead_verify(self.W, self.wdt, self.V, self.d, H, self.B, self.R, self.temps,
+                           self.logits, self.stats, self.ws)
+
+    def accept(self, use_q=True):
+        q = self.q if (use_q and self.q is not None) else None
+        spec_accept(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats, self.V,
+                    self.R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
+                    self.eos_id, self.seeds, self.pos, self.out, self.counters, self.ws)
+
+    def commit(self):
+        if self.state is not None:
+            spec_commit_rollback(self.B, self.state, self.out, self.k, self.state_mode,
+                                 self.commit_status)
+
+    def verify_cycle(self, H):
+        """Verify + accept (+ commit): one verify cycle on device-resident inputs."""
+        self.verify(H)
+        self.accept()
+        self.commit()
+
+    def cycle(self, H, Hd, k):
+        """Full cycle: k draft steps (Hd [k, B, d]), verify, accept, commit."""
+        for i in range(1, k + 1):
+            self.draft_step(i, Hd[i - 1])
+        self.verify_cycle(H)
+
+    def cycle_from_host(self, H_host, Hd_host, k, out_host, H_dev, Hd_dev):
+        """End-to-end cycle: pinned host inputs -> device, the cycle, results -> pinned host."""
+        H_dev.copy_(H_host, non_blocking=True)
+        if k > 0:
+            Hd_dev[:k].copy_(Hd_host[:k], non_blocking=True)
+        self.cycle(H_dev, Hd_dev, k)
+        out_host.copy_(self.out, non_blocking=True)

@@ -1,0 +1,118 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every symbol include/spec.h
+declares, and rejects bad arguments on the host before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mtp_speculative_decoding_spec_gb300 import build
+    build.build()
+    import mtp_speculative_decoding_spec_gb300 as spec
+    return spec._abi.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "spec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "spec_lmhead_verify" in names and "spec_commit_rollback" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    import mtp_speculative_decoding_spec_gb300 as spec
+    assert set(spec._abi.EXPORTS) == set(names)
+
+
+def test_status_strings(lib):
+    assert lib.spec_status_str(0) == b"SPEC_OK"
+    assert lib.spec_status_str(1) == b"SPEC_ERR_INVALID"
+    assert lib.spec_status_str(3) == b"SPEC_ERR_CUDA"
+
+
+def test_struct_layouts_match_the_c_compiler(tmp_path):
+    """Sizes and field offsets of the binding's structs equal what a C compiler gives for
+    include/spec.h."""
+    import shutil
+    import subprocess
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in spec.spec_state_desc._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec.h"', "int main(void){",
+            'printf("%zu %zu %zu %zu\\n", sizeof(spec_rowstats), sizeof(spec_accept_out), '
+            "sizeof(spec_counters), sizeof(spec_state_desc));"]
+    for f in fields:
+        prog.append(f'printf("%zu\\n", offsetof(spec_state_desc, {f}));')
+    prog.append("return 0;}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    sizes = [int(x) for x in out[:4]]
+    assert sizes == [spec.ROWSTATS_BYTES, spec.ACCEPT_OUT_BYTES, spec.COUNTERS_BYTES,
+                     ctypes.sizeof(spec.spec_state_desc)]
+    offs = [int(x) for x in out[4:]]
+    assert offs == [getattr(spec.spec_state_desc, f).offset for f in fields]
+
+
+def test_host_validation_without_gpu(lib):
+    """Null pointers and out-of-range sizes are rejected before any CUDA call."""
+    null = None
+    fake = 256  # a 16-byte aligned non-null pointer value; never dereferenced on these paths
+    assert lib.spec_lmhead_verify(null, 0, 10, 64, fake, 1, 1, fake, null, fake, fake, 1 << 20,
+                                  null) == 1
+    assert lib.spec_lmhead_verify(fake, 0, 10, 64, fake, 1, 9, fake, null, fake, fake, 1 << 20,
+                                  null) == 1
+    assert lib.spec_lmhead_verify(fake, 7, 10, 64, fake, 1, 1, fake, null, fake, fake, 1 << 20,
+                                  null) == 1
+    assert lib.spec_lmhead_verify(fake + 8, 0, 10, 64, fake, 1, 1, fake, null, fake, fake,
+                                  1 << 20, null) == 1
+    assert lib.spec_lmhead_verify(fake, 0, 1 << 24, 64, fake, 1, 1, fake, null, fake, fake,
+                                  1 << 20, null) == 1
+    assert lib.spec_draft_argmax(fake, 0, 10, 64, fake, 9, fake, fake, fake, 0, fake, 1, null,
+                                 0, null, fake, 1 << 20, null) == 1
+    assert lib.spec_accept(0, 3, fake, fake, fake, fake, 10, 4, null, null, 10, 10, fake, 2,
+                           fake, fake, fake, null, fake, 1 << 20, null) == 1
+    assert lib.spec_accept(1, 8, fake, fake, fake, fake, 10, 4, null, null, 10, 10, fake, 2,
+                           fake, fake, fake, null, fake, 1 << 20, null) == 1
+    assert lib.spec_accept(1, 3, fake, fake, fake, fake, 10, 4, fake, null, 10, 10, fake, 2,
+                           fake, fake, fake, null, fake, 1 << 20, null) == 1
+    import mtp_speculative_decoding_spec_gb300 as spec
+    d = spec.spec_state_desc()
+    d.n_slots = 9
+    d.kv_layers = 1
+    assert lib.spec_commit_rollback(1, ctypes.byref(d), fake, fake, 0, null, null) == 1
+    d.kv_layers = 0
+    assert lib.spec_commit_rollback(1, ctypes.byref(d), fake, fake, 5, null, null) == 1
+    assert lib.spec_commit_rollback(1, None, fake, fake, 0, null, null) == 1
+
+
+def test_binding_raises_on_error(lib):
+    import mtp_speculative_decoding_spec_gb300 as spec
+    with pytest.raises(spec.SpecError) as e:
+        spec._check("spec_accept", 1)
+    assert e.value.status == 1 and "SPEC_ERR_INVALID" in str(e.value)
+
+
+def test_no_cpu_fallback_in_product_package():
+    """The product package never imports the oracle or computes on the host."""
+    pkg = os.path.join(ROOT, "mtp_speculative_decoding_spec_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "oracle" not in src, f
+            assert "import numpy" not in src or f == "_abi.py", f
