@@ -189,7 +189,7 @@ def run_ours(args, rank, local_rank, world):
     W = gen.lm_weights(cfg)
     Wd = torch.from_numpy(W.view(np.int16)).to(dev)
     hbm_peak, tf_peak, peak_src = measured_peaks()
-    n_pool = 64 if args.profile else 512
+    n_pool = 16 if args.profile else 512
     k = cfg.k
     Hp, Hdp = build_inputs(cfg, W, n_pool, k, cfg.temps[0], rng_seed=100 + rank)
     Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
@@ -267,6 +267,8 @@ def run_ours(args, rank, local_rank, world):
     cs = clocks.summary()
     res["clocks"] = cs
 
+    if args.profile:
+        profile_extras(dev, W, Wd)
     if not args.profile:
         res["full_cycle"] = full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, min(K, 2000), dev)
         res["e2e"] = e2e(eng, cfg, Hp, drafts_pool, n_pool, k, min(K, 2000), dev, world,
@@ -283,6 +285,28 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def profile_extras(dev, W, Wd):
+    """Launches for ncu captures after the greedy section: 5 sampled k=7 cycles (7 draft
+    steps, an 8-row verify, acceptance with residual/bonus draws), then 3 snapshot commits and
+    3 replay commits of the 64K-context state."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
+    cfg = configs.get(2)
+    k = cfg.k
+    Hp, Hdp = build_inputs(cfg, W, 5, k, 1.0, rng_seed=5)
+    Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+    Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+    eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k, cfg.eos_id,
+                           device=dev, want_q_logits=True)
+    eng.set_requests(temps=[1.0], seeds=[3], pos=[0], k=[k])
+    for c in range(5):
+        eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
+    torch.cuda.synchronize()
+    commit_bench(dev, 6736.5, reps=3, warm=0)
 
 
 def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
@@ -392,7 +416,7 @@ def sweep(dev, W, Wd, hbm_peak):
     return out
 
 
-def commit_bench(dev, hbm_peak):
+def commit_bench(dev, hbm_peak, reps=20, warm=3):
     """Snapshot commit and replay of the 64K-context state (36 x [16,128,128] + conv rows)."""
     import torch
 
@@ -427,12 +451,12 @@ def commit_bench(dev, hbm_peak):
     k_d = torch.tensor([7], dtype=torch.int32, device=dev)
     moved = 2 * 4 * (rec_elems + conv_elems) + 4 * cfg.kv_row_bytes * 2
     for mode, name in ((spec.SPEC_COMMIT_SNAPSHOT, "snapshot"), (spec.SPEC_COMMIT_REPLAY, "replay")):
-        for _ in range(3):
+        for _ in range(warm):
             kv_len.fill_(cfg.context)
             spec.spec_commit_rollback(1, d, acc_d, k_d, mode)
         torch.cuda.synchronize()
         ts = []
-        for _ in range(20):
+        for _ in range(reps):
             kv_len.fill_(cfg.context)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()

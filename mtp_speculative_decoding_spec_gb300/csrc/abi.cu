@@ -93,19 +93,24 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const int rp = next_pow2_rows(nrows);
   const int ng = (kMaxWarpsPerRow / wpr) > 0 ? (kMaxWarpsPerRow / wpr) : 1;
   const int nw = wpr * ng;
-  const int stage_rows = 4 * ng;
+  const int rows_per_group = (rp >= 8) ? 4 : 8;  // must match RowsPerStage<RP> in gemv.cu
+  const int stage_rows = rows_per_group * ng;
   const int stage_bytes = static_cast<int>(align_up(static_cast<size_t>(stage_rows) * row_bytes, 128));
   const int tile_cap = static_cast<int>(align_up(static_cast<size_t>((V + grid - 1) / grid), 4));
-  const size_t fixed = static_cast<size_t>(rp) * tile_cap * 4 + 64;
-  const size_t per_stage = static_cast<size_t>(stage_bytes) + static_cast<size_t>(nw) * 32 * 4 +
-                           (2 + static_cast<size_t>(ng)) * 8;
-  const size_t budget = static_cast<size_t>(a.smem_optin);
-  if (budget <= fixed + 2 * per_stage) return SPEC_ERR_UNSUPPORTED;
-  int stages = static_cast<int>((budget - fixed) / per_stage);
-  if (stages > 8) stages = 8;
   // the last block reuses the stage ring for two doubles per block per warp
-  const size_t scratch = static_cast<size_t>(nw + 1) * 2 * grid * sizeof(double);
-  if (static_cast<size_t>(stages) * stage_bytes < scratch) return SPEC_ERR_UNSUPPORTED;
+  const size_t scratch = static_cast<size_t>(nw + 2) * 2 * grid * sizeof(double);
+  const size_t fixed = static_cast<size_t>(rp) * tile_cap * 4 + 64;
+  const size_t misc_per_stage = static_cast<size_t>(nw) * 32 * 4 + (2 + static_cast<size_t>(ng)) * 8;
+  const size_t budget = static_cast<size_t>(a.smem_optin);
+  int stages = 8;
+  size_t ring = 0, smem_total = 0;
+  for (; stages >= 2; --stages) {
+    ring = static_cast<size_t>(stages) * stage_bytes;
+    if (ring < scratch) ring = align_up(scratch, 128);
+    smem_total = fixed + static_cast<size_t>(stages) * misc_per_stage + ring;
+    if (smem_total <= budget) break;
+  }
+  if (stages < 2) return SPEC_ERR_UNSUPPORTED;
 
   p.W = static_cast<const uint8_t*>(W);
   p.V = V;
@@ -117,6 +122,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.stages = stages;
   p.stage_rows = stage_rows;
   p.stage_bytes = stage_bytes;
+  p.ring_bytes = static_cast<int>(ring);
   p.tile_cap = tile_cap;
   p.H = static_cast<const uint8_t*>(H);
   p.h_row_bytes = static_cast<int>(row_bytes);
@@ -135,8 +141,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
-  L.threads = (nw + 1) * 32;
-  L.smem = static_cast<int>(fixed + static_cast<size_t>(stages) * per_stage);
+  L.threads = (nw + 2) * 32;  // consumers, producer, reducer
+  L.smem = static_cast<int>(smem_total);
   const cudaError_t e = gemv_dispatch(L, wdt == SPEC_BF16, rp, stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -75,6 +75,30 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   return t;
 }
 
+// Inclusive scan of one value per thread across the block (ascending thread order); returns
+// the thread's inclusive prefix and, through *total, the block total.
+__device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long long w,
+                                                                  unsigned long long* sh,
+                                                                  unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long up = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += up;
+  }
+  __syncthreads();
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  unsigned long long before = 0ull, t = 0ull;
+  for (int w2 = 0; w2 < static_cast<int>(blockDim.x >> 5); ++w2) {
+    if (w2 < warp) before += sh[w2];
+    t += sh[w2];
+  }
+  *total = t;
+  return before + incl;
+}
+
 __device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
   spec_accept_out o;
   o.status = D.status;
@@ -290,22 +314,27 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   const uint32_t purpose = (D.need == 1) ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
   const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + D.srow, purpose);
   const unsigned long long target = cdf_target(u24, total);
+  // locate the slice holding the target: block-parallel scan over the slice sums
   if (tid == 0) {
-    unsigned long long cum = 0ull;
-    int slice = -1;
-    for (int i = 0; i < p.NS; ++i) {
-      const unsigned long long w = __ldcg(rs + 2 * i + (use_p ? 1 : 0));
-      if (w > 0ull && cum + w > target) {
-        slice = i;
-        break;
-      }
-      cum += w;
-    }
-    s_slice = slice;
-    s_before = cum;
+    s_slice = -1;
     s_tok = -1;
   }
-  __syncthreads();
+  {
+    unsigned long long carry = 0ull;
+    for (int base = 0; base < p.NS; base += kAcceptThreads) {
+      const int i = base + tid;
+      const unsigned long long w = (i < p.NS) ? __ldcg(rs + 2 * i + (use_p ? 1 : 0)) : 0ull;
+      unsigned long long round_total;
+      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
+      if (w > 0ull && cum > target && cum - w <= target) {
+        s_slice = i;
+        s_before = cum - w;
+      }
+      carry += round_total;
+      __syncthreads();
+      if (s_slice >= 0) break;
+    }
+  }
   int tok = -1;
   if (s_slice >= 0) {
     const int64_t base = static_cast<int64_t>(s_slice) * kAcceptSlice;
@@ -318,23 +347,9 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
         entry_weights(c, j, wr, wp);
         w = use_p ? wp : wr;
       }
-      // block inclusive scan of w in ascending j
-      unsigned long long incl = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long up = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += up;
-      }
-      __syncthreads();
-      if (lane == 31) sh[warp] = incl;
-      __syncthreads();
-      unsigned long long wbefore = 0ull, round_total = 0ull;
-      for (int w2 = 0; w2 < kAcceptThreads / 32; ++w2) {
-        if (w2 < warp) wbefore += sh[w2];
-        round_total += sh[w2];
-      }
-      const unsigned long long cum_incl = carry + wbefore + incl;
-      if (w > 0ull && cum_incl > target && cum_incl - w <= target) s_tok = static_cast<int>(j);
+      unsigned long long round_total;
+      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
+      if (w > 0ull && cum > target && cum - w <= target) s_tok = static_cast<int>(j);
       carry += round_total;
       __syncthreads();
       if (s_tok >= 0) break;

@@ -18,6 +18,21 @@
 namespace spec {
 
 
+// Grid-stride copy of n 16-byte vectors with four loads in flight per thread.
+__device__ __forceinline__ void copy_vec4(float4* __restrict__ dst, const float4* __restrict__ src,
+                                          int64_t n, int64_t gt, int64_t gs) {
+  int64_t i = gt;
+  for (; i + 3 * gs < n; i += 4 * gs) {
+    const float4 a = __ldcs(src + i), b = __ldcs(src + i + gs), c = __ldcs(src + i + 2 * gs),
+                 d = __ldcs(src + i + 3 * gs);
+    __stcs(dst + i, a);
+    __stcs(dst + i + gs, b);
+    __stcs(dst + i + 2 * gs, c);
+    __stcs(dst + i + 3 * gs, d);
+  }
+  for (; i < n; i += gs) __stcs(dst + i, __ldcs(src + i));
+}
+
 __global__ void __launch_bounds__(256) commit_kernel(const CommitParams p) {
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
@@ -59,63 +74,66 @@ __global__ void __launch_bounds__(256) commit_kernel(const CommitParams p) {
 
   // ---------------- recurrent state ----------------
   if (st.rec_layers > 0) {
-    const int64_t L = st.rec_layers, H = st.rec_heads, dk = st.rec_dk, dv = st.rec_dv;
-    const int64_t elems = L * H * dk * dv;
+    const int dv = st.rec_dv, dk = st.rec_dk;
+    const int64_t elems = static_cast<int64_t>(st.rec_layers) * st.rec_heads * dk * dv;
     float* live = st.rec_live + static_cast<size_t>(b) * elems;
     if (p.mode == SPEC_COMMIT_SNAPSHOT) {
-      const float4* src =
-          reinterpret_cast<const float4*>(st.rec_slots + (static_cast<size_t>(b) * ns + m) * elems);
-      float4* dst = reinterpret_cast<float4*>(live);
-      for (int64_t i = gt; i < elems / 4; i += gs) dst[i] = __ldcs(src + i);
+      copy_vec4(reinterpret_cast<float4*>(live),
+                reinterpret_cast<const float4*>(st.rec_slots + (static_cast<size_t>(b) * ns + m) * elems),
+                elems / 4, gt, gs);
     } else {
       const float* slot0 = st.rec_slots + static_cast<size_t>(b) * ns * elems;
       const int64_t rows = ns - 1;
+      const int64_t LH = static_cast<int64_t>(st.rec_layers) * st.rec_heads;
+      const float* A = st.step_a + static_cast<size_t>(b) * rows * LH;
+      const float* Bv = st.step_b + static_cast<size_t>(b) * rows * LH * dk;
+      const float* Cv = st.step_c + static_cast<size_t>(b) * rows * LH * dv;
+      const int per_head = dk * dv;  // < 2^31 for any supported shape
       for (int64_t i = gt; i < elems / 4; i += gs) {
         const int64_t e = i * 4;
-        const int64_t j = e % dv;
-        const int64_t ii = (e / dv) % dk;
-        const int64_t lh = e / (dv * dk);  // layer * H + head
-        float4 s = __ldcs(reinterpret_cast<const float4*>(slot0 + e));
+        const int64_t lh = e / per_head;  // layer * heads + head
+        const int rem = static_cast<int>(e - lh * per_head);
+        const int ii = rem / dv, j = rem - ii * dv;
+        float4 sv = __ldcs(reinterpret_cast<const float4*>(slot0 + e));
         for (int t = 0; t < m; ++t) {
-          const int64_t rl = (static_cast<int64_t>(b) * rows + t) * L * H + lh;
-          const float a = __ldg(st.step_a + rl);
-          const float bb = __ldg(st.step_b + rl * dk + ii);
-          const float4 c = __ldg(reinterpret_cast<const float4*>(st.step_c + rl * dv + j));
-          s.x = __fadd_rn(__fmul_rn(a, s.x), __fmul_rn(bb, c.x));
-          s.y = __fadd_rn(__fmul_rn(a, s.y), __fmul_rn(bb, c.y));
-          s.z = __fadd_rn(__fmul_rn(a, s.z), __fmul_rn(bb, c.z));
-          s.w = __fadd_rn(__fmul_rn(a, s.w), __fmul_rn(bb, c.w));
+          const int64_t rl = static_cast<int64_t>(t) * LH + lh;
+          const float a = __ldg(A + rl);
+          const float bb = __ldg(Bv + rl * dk + ii);
+          const float4 c = __ldg(reinterpret_cast<const float4*>(Cv + rl * dv + j));
+          sv.x = __fadd_rn(__fmul_rn(a, sv.x), __fmul_rn(bb, c.x));
+          sv.y = __fadd_rn(__fmul_rn(a, sv.y), __fmul_rn(bb, c.y));
+          sv.z = __fadd_rn(__fmul_rn(a, sv.z), __fmul_rn(bb, c.z));
+          sv.w = __fadd_rn(__fmul_rn(a, sv.w), __fmul_rn(bb, c.w));
         }
-        *reinterpret_cast<float4*>(live + e) = s;
+        __stcs(reinterpret_cast<float4*>(live + e), sv);
       }
     }
   }
 
   // ---------------- conv rows ----------------
   if (st.rec_layers > 0 && st.conv_rows > 0) {
-    const int64_t L = st.rec_layers, C = st.conv_rows, W = st.conv_width;
-    const int64_t elems = L * C * W;
+    const int C = st.conv_rows, W = st.conv_width;
+    const int64_t elems = static_cast<int64_t>(st.rec_layers) * C * W;
     float* live = st.conv_live + static_cast<size_t>(b) * elems;
     if (p.mode == SPEC_COMMIT_SNAPSHOT) {
-      const float4* src = reinterpret_cast<const float4*>(
-          st.conv_slots + (static_cast<size_t>(b) * ns + m) * elems);
-      float4* dst = reinterpret_cast<float4*>(live);
-      for (int64_t i = gt; i < elems / 4; i += gs) dst[i] = __ldcs(src + i);
+      copy_vec4(reinterpret_cast<float4*>(live),
+                reinterpret_cast<const float4*>(st.conv_slots + (static_cast<size_t>(b) * ns + m) * elems),
+                elems / 4, gt, gs);
     } else {
       const float* slot0 = st.conv_slots + static_cast<size_t>(b) * ns * elems;
       const int64_t rows = ns - 1;
+      const int64_t L = st.rec_layers;
+      const float* X = st.conv_in + static_cast<size_t>(b) * rows * L * W;
+      const int per_layer = C * W;
       for (int64_t i = gt; i < elems / 4; i += gs) {
         const int64_t e = i * 4;
-        const int64_t w = e % W;
-        const int64_t cr = (e / W) % C;
-        const int64_t l = e / (W * C);
-        const int64_t srcrow = m + cr;  // row index into (conv rows of slot 0, conv_in rows)
-        const float* src;
-        if (srcrow < C)
-          src = slot0 + (l * C + srcrow) * W + w;
-        else
-          src = st.conv_in + ((static_cast<int64_t>(b) * rows + (srcrow - C)) * L + l) * W + w;
-        *reinterpret_cast<float4*>(live + e) = __ldcs(reinterpret_cast<const float4*>(src));
+        const int64_t l = e / per_layer;
+        const int rem = static_cast<int>(e - l * per_layer);
+        const int cr = rem / W, w = rem - cr * W;
+        const int srcrow = m + cr;  // row of (conv rows of slot 0, then conv_in rows)
+        const float* src = (srcrow < C) ? slot0 + (l * C + srcrow) * W + w
+                                        : X + (static_cast<int64_t>(srcrow - C) * L + l) * W + w;
+        __stcs(reinterpret_cast<float4*>(live + e), __ldcs(reinterpret_cast<const float4*>(src)));
       }
     }
   }

@@ -78,33 +78,29 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps (up to ~hint ns, or until the
+// phase completes) instead of spinning on issue slots other warps need.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~limit_ns of wall time (checked every
-// 256 polls) and returns false; the caller records an error and stops waiting.
+// Bounded wait on an mbarrier phase: gives up after ~limit_ns of wall time and returns false;
+// the caller records an error and stops waiting.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 1;; ++it) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      const uint64_t t = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = t;
-      } else if (t - t0 > limit_ns) {
-        return false;
-      }
-    }
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -83,33 +83,43 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
   return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
 }
 
+// Rows of the weight matrix each row group handles per stage: the reduction of G*RP partial
+// sums per lane costs about the same for any G*RP <= 32, so G shrinks as the rows grow.
+template <int RP>
+struct RowsPerStage {
+  static constexpr int G = (RP >= 8) ? 4 : 8;
+};
+
 template <int RP, bool BF16>
-__global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
-  constexpr int EPC = BF16 ? 8 : 4;  // elements per 16-byte chunk
-  constexpr int NV = 4 * RP;          // partial sums per lane per stage (4 weight rows)
-  constexpr int SPREAD = 32 / NV;     // lanes holding the same value after the reduction
+__global__ void __launch_bounds__(448, 1) gemv_rows_kernel(const GemvParams p) {
+  constexpr int EPC = BF16 ? 8 : 4;       // elements per 16-byte chunk
+  constexpr int G = RowsPerStage<RP>::G;  // weight rows per row group per stage
+  constexpr int NV = G * RP;              // partial sums per lane per stage
+  constexpr int SPREAD = 32 / NV;         // lanes holding the same value after the reduction
+  static_assert(NV <= 32 && 32 % NV == 0, "reduction layout");
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages, NW = p.nw;
+  const int PRODUCER = NW, REDUCER = NW + 1;
   uint8_t* stage_base = smem;
-  float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  float* red = reinterpret_cast<float*>(smem + p.ring_bytes);  // [S][NW][32]
   float* ztile = red + static_cast<size_t>(S) * NW * 32;
   uint64_t* full = reinterpret_cast<uint64_t*>(ztile + static_cast<size_t>(RP) * p.tile_cap);
   uint64_t* empty = full + S;
   uint64_t* redbar = empty + S;  // [S][ng]
   int* flags = reinterpret_cast<int*>(redbar + S * p.ng);  // [0] abort, [1] last block
 
-  const int G = gridDim.x, blk = blockIdx.x;
-  const int64_t v0 = static_cast<int64_t>(blk) * p.V / G;
-  const int64_t v1 = static_cast<int64_t>(blk + 1) * p.V / G;
+  const int GR = gridDim.x, blk = blockIdx.x;
+  const int64_t v0 = static_cast<int64_t>(blk) * p.V / GR;
+  const int64_t v1 = static_cast<int64_t>(blk + 1) * p.V / GR;
   const int nt = static_cast<int>(v1 - v0);
   const int nst = (nt + p.stage_rows - 1) / p.stage_rows;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NW);
+      mbar_init(&empty[s], NW + 1);  // every consumer warp and the reducer
     }
     for (int s = 0; s < S * p.ng; ++s) mbar_init(&redbar[s], p.wpr);
     flags[0] = 0;
@@ -118,8 +128,8 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
   }
   __syncthreads();
 
-  if (warp == NW) {
-    // ---------------- producer: stream weight rows into the stage ring ----------------
+  if (warp == PRODUCER) {
+    // ---------------- producer: stream whole weight rows into the stage ring ----------------
     if (lane == 0) {
       int issued = 0;
       for (int it = 0; it < nst; ++it) {
@@ -146,6 +156,45 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
         }
       }
     }
+  } else if (warp == REDUCER) {
+    // ---------------- reducer: sum each row's per-warp partials in ascending warp order -------
+    float tq[RP];
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+      tq[r] = (r < p.nrows && p.logits) ? p.temperature[r / p.rows_per_req] : 0.f;
+    for (int it = 0; it < nst; ++it) {
+      const int s = it % S;
+      const uint32_t ph = (it / S) & 1;
+      const int rows = min(p.stage_rows, nt - it * p.stage_rows);
+      bool ok = true;
+      for (int gi = 0; gi < p.ng; ++gi) {
+        if (!mbar_wait_bounded(&redbar[s * p.ng + gi], ph)) {
+          atomicOr(&p.hdr->error, ERR_GEMV_WAIT_RED);
+          atomicExch(&flags[0], 1);
+          ok = false;
+          break;
+        }
+        if (lane < NV) {
+          const int g = lane / RP, r = lane % RP;
+          const int lr = gi * G + g;
+          if (r < p.nrows && lr < rows) {
+            const float* src = red + (static_cast<size_t>(s) * NW + gi * p.wpr) * 32 + lane;
+            float z = 0.f;
+            for (int w2 = 0; w2 < p.wpr; ++w2) z += src[w2 * 32];
+            const int local = it * p.stage_rows + lr;
+            ztile[static_cast<size_t>(r) * p.tile_cap + local] = z;
+            float tr = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < RP; ++rr)
+              if (rr == r) tr = tq[rr];
+            if (tr > 0.f) p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = z;
+          }
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage's partial sums are consumed
+    }
   } else {
     // ---------------- consumers: dot products against register-resident H ----------------
     const int gi = warp / p.wpr, wi = warp - gi * p.wpr;
@@ -160,10 +209,6 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
                                              static_cast<size_t>(chunk) * 16);
       unpack16<BF16>(hv, h[r]);
     }
-    float tq[RP];
-#pragma unroll
-    for (int r = 0; r < RP; ++r)
-      tq[r] = (r < p.nrows && p.logits) ? p.temperature[r / p.rows_per_req] : 0.f;
 
     for (int it = 0; it < nst; ++it) {
       const int s = it % S;
@@ -179,66 +224,42 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
       for (int i = 0; i < NV; ++i) v[i] = 0.f;
       if (active) {
         const uint8_t* sp = stage_base + static_cast<size_t>(s) * p.stage_bytes +
-                            static_cast<size_t>(gi * 4) * p.row_bytes +
+                            static_cast<size_t>(gi * G) * p.row_bytes +
                             static_cast<size_t>(chunk) * 16;
-        uint4 w[4];
+        uint4 w[G];
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          w[g] = (gi * 4 + g < rows) ? lds128(sp + static_cast<size_t>(g) * p.row_bytes)
+        for (int g = 0; g < G; ++g)
+          w[g] = (gi * G + g < rows) ? lds128(sp + static_cast<size_t>(g) * p.row_bytes)
                                      : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < G; ++g) {
           float wf[EPC];
           unpack16<BF16>(w[g], wf);
 #pragma unroll
           for (int r = 0; r < RP; ++r) {
-            float a = 0.f;
+            // packed fp32x2 FMAs: even and odd elements accumulate separately, then add
+            float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) a = fmaf(wf[e], h[r][e], a);
-            v[g * RP + r] = a;
+            for (int e = 0; e < EPC; e += 2)
+              a = __ffma2_rn(make_float2(wf[e], wf[e + 1]), make_float2(h[r][e], h[r][e + 1]), a);
+            v[g * RP + r] = a.x + a.y;
           }
         }
       }
-      __syncwarp();
-      if (wi != 0 && lane == 0) mbar_arrive(&empty[s]);
-
       ReduceScatter<NV, 16>::run(v, lane);
       float* rb = red + (static_cast<size_t>(s) * NW + warp) * 32;
       if ((lane % SPREAD) == 0) rb[lane / SPREAD] = v[0];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&redbar[s * p.ng + gi]);
-
-      if (wi == 0) {
-        if (!mbar_wait_bounded(&redbar[s * p.ng + gi], ph)) {
-          atomicOr(&p.hdr->error, ERR_GEMV_WAIT_RED);
-          atomicExch(&flags[0], 1);
-          break;
-        }
-        if (lane < NV) {
-          const int g = lane / RP, r = lane % RP;
-          const int lr = gi * 4 + g;
-          if (r < p.nrows && lr < rows) {
-            float z = 0.f;
-            for (int w2 = 0; w2 < p.wpr; ++w2)
-              z += red[(static_cast<size_t>(s) * NW + gi * p.wpr + w2) * 32 + lane];
-            const int local = it * p.stage_rows + lr;
-            ztile[static_cast<size_t>(r) * p.tile_cap + local] = z;
-            float tr = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < RP; ++rr)
-              if (rr == r) tr = tq[rr];
-            if (tr > 0.f) p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = z;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        mbar_arrive(&redbar[s * p.ng + gi]);
+        mbar_arrive(&empty[s]);
       }
     }
   }
   __syncthreads();
 
   // ---------------- per-block partial statistics of each row ----------------
-  const int NWALL = NW + 1;
+  const int NWALL = NW + 2;
   for (int q = warp; q < p.nrows; q += NWALL) {
     const float T = p.temperature[q / p.rows_per_req];
     const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
@@ -277,7 +298,7 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
   __syncthreads();
   if (tid == 0) {
     const unsigned ticket = atomicAdd(&p.hdr->gemv_ticket, 1u);
-    flags[1] = (ticket == static_cast<unsigned>(G) - 1u) ? 1 : 0;
+    flags[1] = (ticket == static_cast<unsigned>(GR) - 1u) ? 1 : 0;
   }
   __syncthreads();
   if (!flags[1]) return;
@@ -285,15 +306,15 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
 
   // ---------------- last block: combine the partials of every block ----------------
   // The stage ring is free now; it holds per-block weights and scale factors.
-  double* blk_w = reinterpret_cast<double*>(stage_base) + static_cast<size_t>(warp) * 2 * G;
-  double* blk_f = blk_w + G;
+  double* blk_w = reinterpret_cast<double*>(stage_base) + static_cast<size_t>(warp) * 2 * GR;
+  double* blk_f = blk_w + GR;
   for (int q = warp; q < p.nrows; q += NWALL) {
     const float T = p.temperature[q / p.rows_per_req];
     const float Te = T > 0.f ? T : 1.f;
     const float invT = __fdiv_rn(1.f, Te);
     Top2 t = top2_empty();
     int bad = 0;
-    for (int cc = lane; cc < G; cc += 32) {
+    for (int cc = lane; cc < GR; cc += 32) {
       const GemvPartial* pp = p.part + static_cast<size_t>(cc) * kMaxRows + q;
       bad |= __ldcg(&pp->flags);
       const int32_t idx = __ldcg(&pp->idx);
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
     const bool nonfinite = bad || t.idx == kNoIndex || t.best == -INFINITY;
     const float M = t.best;
     double S = 0.0;
-    for (int cc = lane; cc < G; cc += 32) {
+    for (int cc = lane; cc < GR; cc += 32) {
       const GemvPartial* pp = p.part + static_cast<size_t>(cc) * kMaxRows + q;
       const float mc = __ldcg(&pp->m);
       const unsigned long long sc = __ldcg(&pp->s);
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
         if (lane == 0) {
           double cum = 0.0;
           int last_nz = -1;
-          for (int cc = 0; cc < G; ++cc) {
+          for (int cc = 0; cc < GR; ++cc) {
             const double w = blk_w[cc];
             if (w > 0.0) last_nz = cc;
             if (w > 0.0 && cum + w > target) {
@@ -372,8 +393,8 @@ __global__ void __launch_bounds__(416, 1) gemv_rows_kernel(const GemvParams p) {
         cstar = __shfl_sync(0xffffffffu, cstar, 0);
         tt = __shfl_sync(0xffffffffu, tt, 0);
         if (cstar >= 0) {
-          const int64_t c0 = static_cast<int64_t>(cstar) * p.V / G;
-          const int64_t c1 = static_cast<int64_t>(cstar + 1) * p.V / G;
+          const int64_t c0 = static_cast<int64_t>(cstar) * p.V / GR;
+          const int64_t c1 = static_cast<int64_t>(cstar + 1) * p.V / GR;
           const float mc = __ldcg(&(p.part + static_cast<size_t>(cstar) * kMaxRows + q)->m);
           const float* yrow = p.logits + static_cast<size_t>(q) * p.logits_stride;
           unsigned long long carry = 0ull;

@@ -16,6 +16,7 @@ struct GemvParams {
   int stages;
   int stage_rows;  // = 4 * ng
   int stage_bytes;
+  int ring_bytes;  // >= stages * stage_bytes; the last block reuses it as scratch
   int tile_cap;  // max rows per block tile
   const uint8_t* H;
   int h_row_bytes;
