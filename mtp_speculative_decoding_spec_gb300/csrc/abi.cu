@@ -4,14 +4,38 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cuda.h>
+
 #include "params.cuh"
 
 
 namespace spec {
 namespace {
 
-constexpr int kMaxTileRows = 2048;  // per-block tile of the GEMV (logits kept in smem)
-constexpr int kMaxWarpsPerRow = 12;
+constexpr int kBandRows = 48;         // GEMV band: 12 consumer warps x 4 rows
+constexpr int kMaxBandsPerBlock = 42;  // per-block tile of the GEMV (logits kept in smem)
+constexpr int kGemvThreads = 13 * 32;  // 12 consumer warps + 1 producer
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime (no -lcuda).
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
 
 struct DevAttr {
   int sms = 0;
@@ -31,9 +55,11 @@ DevAttr dev_attr() {
   return cache[dev];
 }
 
+int64_t gemv_bands(int64_t V) { return (V + kBandRows - 1) / kBandRows; }
+
 int gemv_grid(int64_t V, int sms) {
   int64_t g = sms;
-  const int64_t need = (V + kMaxTileRows - 1) / kMaxTileRows;
+  const int64_t need = (gemv_bands(V) + kMaxBandsPerBlock - 1) / kMaxBandsPerBlock;
   if (need > g) g = need;
   return static_cast<int>(g);
 }
@@ -80,49 +106,58 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const int elt = (wdt == SPEC_BF16) ? 2 : 4;
   const int64_t row_bytes = d * elt;
   if (row_bytes % 16 != 0) return SPEC_ERR_INVALID;
-  const int cpr = static_cast<int>(row_bytes / 16);
-  const int wpr = (cpr + 31) / 32;
-  if (wpr > kMaxWarpsPerRow) return SPEC_ERR_UNSUPPORTED;
+  if (d > (wdt == SPEC_BF16 ? 3072 : 1536)) return SPEC_ERR_UNSUPPORTED;
   const WsLayout wl = ws_layout(V, batch_for_ws, a.sms);
   if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
+  EncodeTiledFn encode = encode_tiled();
+  if (!encode) return SPEC_ERR_CUDA;
 
   GemvLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
   const int grid = gemv_grid(V, a.sms);
   const int rp = next_pow2_rows(nrows);
-  const int ng = (kMaxWarpsPerRow / wpr) > 0 ? (kMaxWarpsPerRow / wpr) : 1;
-  const int nw = wpr * ng;
-  const int rows_per_group = (rp >= 8) ? 4 : 8;  // must match RowsPerStage<RP> in gemv.cu
-  const int stage_rows = rows_per_group * ng;
-  const int stage_bytes = static_cast<int>(align_up(static_cast<size_t>(stage_rows) * row_bytes, 128));
-  const int tile_cap = static_cast<int>(align_up(static_cast<size_t>((V + grid - 1) / grid), 4));
+  const int slab_elems = 512 / elt;
+  const int nslab = static_cast<int>((d + slab_elems - 1) / slab_elems);
+  const int64_t nbands = gemv_bands(V);
+  const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * kBandRows);
+  const int stage_bytes = kBandRows * 512;
+  const int pairs = (elt == 2) ? 4 : 2;
+  const int row_pairs = rp >= 2 ? rp / 2 : 1;
+  const size_t hs_bytes = static_cast<size_t>(nslab) * pairs * row_pairs * 32 * 16;
   // the last block reuses the stage ring for two doubles per block per warp
-  const size_t scratch = static_cast<size_t>(nw + 2) * 2 * grid * sizeof(double);
-  const size_t fixed = static_cast<size_t>(rp) * tile_cap * 4 + 64;
-  const size_t misc_per_stage = static_cast<size_t>(nw) * 32 * 4 + (2 + static_cast<size_t>(ng)) * 8;
+  const size_t scratch = static_cast<size_t>(kGemvThreads / 32) * 2 * grid * sizeof(double);
+  const size_t fixed = hs_bytes + static_cast<size_t>(rp) * tile_cap * 4 + 128;  // + flags, temps
   const size_t budget = static_cast<size_t>(a.smem_optin);
   int stages = 8;
   size_t ring = 0, smem_total = 0;
   for (; stages >= 2; --stages) {
     ring = static_cast<size_t>(stages) * stage_bytes;
     if (ring < scratch) ring = align_up(scratch, 128);
-    smem_total = fixed + static_cast<size_t>(stages) * misc_per_stage + ring;
+    smem_total = ring + fixed + static_cast<size_t>(stages) * 16;
     if (smem_total <= budget) break;
   }
   if (stages < 2) return SPEC_ERR_UNSUPPORTED;
 
-  p.W = static_cast<const uint8_t*>(W);
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(V)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(slab_elems), static_cast<cuuint32_t>(kBandRows)};
+  const cuuint32_t estride[2] = {1, 1};
+  if (encode(&L.wmap, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             2, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPEC_ERR_CUDA;
+
   p.V = V;
-  p.row_bytes = static_cast<int>(row_bytes);
-  p.cpr = cpr;
-  p.wpr = wpr;
-  p.ng = ng;
-  p.nw = nw;
+  p.d = static_cast<int>(d);
+  p.nslab = nslab;
+  p.slab_elems = slab_elems;
+  p.nbands = nbands;
   p.stages = stages;
-  p.stage_rows = stage_rows;
   p.stage_bytes = stage_bytes;
   p.ring_bytes = static_cast<int>(ring);
+  p.hs_bytes = static_cast<int>(hs_bytes);
   p.tile_cap = tile_cap;
   p.H = static_cast<const uint8_t*>(H);
   p.h_row_bytes = static_cast<int>(row_bytes);
@@ -141,7 +176,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
-  L.threads = (nw + 2) * 32;  // consumers, producer, reducer
+  L.threads = kGemvThreads;
   L.smem = static_cast<int>(smem_total);
   const cudaError_t e = gemv_dispatch(L, wdt == SPEC_BF16, rp, stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -5,17 +5,20 @@
 // verifies k drafts in one batched forward of k+1 rows through the shared LM head; the draft
 // head covers the first 64,000 vocabulary rows and picks its token on the GPU): z = H W^T with
 // W [V, d] bf16 (or fp32) streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming
-// GEMV: the weight bytes bound it, so the design is about keeping HBM busy:
-//   * one persistent block per SM; block c owns the contiguous rows [c*V/G, (c+1)*V/G)
-//     (balanced to one row, no wave tail);
-//   * a producer warp streams groups of whole weight rows (contiguous bytes) into a ring of
-//     shared-memory stages with 1-D bulk (TMA) copies completed on mbarriers;
-//   * each consumer thread owns one 16-byte chunk of the hidden dimension and holds the
-//     matching slice of every H row in registers, so a weight byte is read from shared memory
-//     once and used for all rows; partial dot products are combined by a fixed butterfly
-//     (xor 16, 8, 4, 2, 1) and then across the warps of a row in ascending order. That order
-//     does not depend on how many rows share the call, so every row's logits are bitwise
-//     batch-invariant (section "Exactness": verify stays batch-invariant up to eight rows);
+// GEMV: the weight bytes bound it, so the design is about keeping HBM busy with few
+// instructions per weight byte:
+//   * one persistent block per SM; the vocabulary is cut into 48-row bands and block c owns a
+//     contiguous run of bands (balanced to one band, no wave tail, the same cut for any number
+//     of rows);
+//   * a producer warp streams each band as k-slabs of [48 rows x 512 bytes] with 2-D TMA
+//     tensor copies into a ring of shared-memory stages completed on mbarriers;
+//   * twelve consumer warps each own 4 rows of the band and compute their full dot products:
+//     lane l takes bytes [16 l, 16 l + 16) of every slab row, and the H rows sit in shared
+//     memory as fp32 pairs laid out so that one conflict-free 128-bit load feeds packed
+//     fp32x2 FMAs for two H rows; one butterfly (xor 16, 8, 4, 2, 1) per band finishes each
+//     dot product. Every step of a row's sum is fixed by k alone, so every row's logits are
+//     bitwise batch-invariant (section "Exactness": verify stays batch-invariant up to eight
+//     rows);
 //   * the block keeps its tile of logits in shared memory, reduces max / argmax / top-2 and a
 //     sum of exp((z - m)/T) quantised to 2^-40 units in 64-bit integers (exact, so the sum
 //     does not depend on order either), and the last block to finish combines the per-block
@@ -83,69 +86,115 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
   return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
 }
 
-// Rows of the weight matrix each row group handles per stage: the reduction of G*RP partial
-// sums per lane costs about the same for any G*RP <= 32, so G shrinks as the rows grow.
-template <int RP>
-struct RowsPerStage {
-  static constexpr int G = (RP >= 8) ? 4 : 8;
-};
+constexpr int kBandWarps = 12;                     // consumer warps per block
+constexpr int kRowsPerWarp = 4;                    // weight rows per consumer warp per band
+constexpr int kBandRows = kBandWarps * kRowsPerWarp;  // 48
+constexpr int kSlabBytes = 512;                    // bytes of one weight row per k-slab
+
+// Rows [v0, v1) of block `blk`: a contiguous run of 48-row bands.
+__device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, int64_t V,
+                                          int64_t& v0, int64_t& v1) {
+  const int64_t b0 = static_cast<int64_t>(blk) * nbands / nblk;
+  const int64_t b1 = static_cast<int64_t>(blk + 1) * nbands / nblk;
+  v0 = b0 * kBandRows;
+  v1 = min(b1 * kBandRows, V);
+  if (v1 < v0) v1 = v0;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar))
+      : "memory");
+}
 
 template <int RP, bool BF16>
-__global__ void __launch_bounds__(448, 1) gemv_rows_kernel(const GemvParams p) {
-  constexpr int EPC = BF16 ? 8 : 4;       // elements per 16-byte chunk
-  constexpr int G = RowsPerStage<RP>::G;  // weight rows per row group per stage
-  constexpr int NV = G * RP;              // partial sums per lane per stage
-  constexpr int SPREAD = 32 / NV;         // lanes holding the same value after the reduction
+__global__ void __maxnreg__(152)
+    gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
+  constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
+  constexpr int PP = EPC / 2;               // element pairs per chunk
+  constexpr int RH = RP >= 2 ? RP / 2 : 1;  // H row pairs held per 128-bit load
+  constexpr int G = kRowsPerWarp;
+  constexpr int NV = G * RP;                // dot products finished per warp per band
+  constexpr int SPREAD = 32 / NV;           // lanes holding the same value after the reduction
   static_assert(NV <= 32 && 32 % NV == 0, "reduction layout");
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = p.stages, NW = p.nw;
-  const int PRODUCER = NW, REDUCER = NW + 1;
-  uint8_t* stage_base = smem;
-  float* red = reinterpret_cast<float*>(smem + p.ring_bytes);  // [S][NW][32]
-  float* ztile = red + static_cast<size_t>(S) * NW * 32;
+  const int S = p.stages, NW = kBandWarps, PRODUCER = kBandWarps;
+  uint8_t* stage_base = smem;                                     // ring, [S][48 rows][512 B]
+  float4* hs = reinterpret_cast<float4*>(smem + p.ring_bytes);   // H pairs
+  float* ztile = reinterpret_cast<float*>(smem + p.ring_bytes + p.hs_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(ztile + static_cast<size_t>(RP) * p.tile_cap);
   uint64_t* empty = full + S;
-  uint64_t* redbar = empty + S;  // [S][ng]
-  int* flags = reinterpret_cast<int*>(redbar + S * p.ng);  // [0] abort, [1] last block
+  int* flags = reinterpret_cast<int*>(empty + S);  // [0] abort, [1] last block
+  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] temperature of each row
 
   const int GR = gridDim.x, blk = blockIdx.x;
-  const int64_t v0 = static_cast<int64_t>(blk) * p.V / GR;
-  const int64_t v1 = static_cast<int64_t>(blk + 1) * p.V / GR;
+  int64_t v0, v1;
+  block_rows(blk, GR, p.nbands, p.V, v0, v1);
   const int nt = static_cast<int>(v1 - v0);
-  const int nst = (nt + p.stage_rows - 1) / p.stage_rows;
+  const int nb = (nt + kBandRows - 1) / kBandRows;  // bands of this block
+  const int niter = nb * p.nslab;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NW + 1);  // every consumer warp and the reducer
+      mbar_init(&empty[s], NW);
     }
-    for (int s = 0; s < S * p.ng; ++s) mbar_init(&redbar[s], p.wpr);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
   }
+  if (tid < kMaxRows)
+    s_temp[tid] = (tid < p.nrows && p.logits) ? p.temperature[tid / p.rows_per_req] : 0.f;
+  // H rows -> shared memory as fp32 pairs: entry ((s*PP + q)*RH + rr)*32 + l holds
+  // (h[2rr][k], h[2rr][k+1], h[2rr+1][k], h[2rr+1][k+1]) with k = s*slab_elems + l*EPC + 2q.
+  {
+    const int total = p.nslab * PP * RH * 32;
+    for (int i = tid; i < total; i += blockDim.x) {
+      const int l = i & 31, rr = (i >> 5) % RH, q = (i / (32 * RH)) % PP, s = i / (32 * RH * PP);
+      const int k = s * p.slab_elems + l * EPC + 2 * q;
+      float h4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = 2 * rr + (u >> 1), kk = k + (u & 1);
+        float hv = 0.f;
+        if (r < p.nrows && kk < p.d) {
+          if constexpr (BF16) {
+            const uint16_t bits =
+                reinterpret_cast<const uint16_t*>(p.H + static_cast<size_t>(r) * p.h_row_bytes)[kk];
+            hv = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+          } else {
+            hv = reinterpret_cast<const float*>(p.H + static_cast<size_t>(r) * p.h_row_bytes)[kk];
+          }
+        }
+        h4[u] = hv;
+      }
+      hs[i] = make_float4(h4[0], h4[1], h4[2], h4[3]);
+    }
+  }
   __syncthreads();
 
   if (warp == PRODUCER) {
-    // ---------------- producer: stream whole weight rows into the stage ring ----------------
+    // ---------------- producer: stream k-slabs of 48-row bands into the stage ring ---------
     if (lane == 0) {
       int issued = 0;
-      for (int it = 0; it < nst; ++it) {
+      const int y0 = static_cast<int>(v0);
+      for (int it = 0; it < niter; ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1)) {
           atomicOr(&p.hdr->error, ERR_GEMV_WAIT_EMPTY);
           atomicExch(&flags[0], 1);
           break;
         }
-        const int rows = min(p.stage_rows, nt - it * p.stage_rows);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(p.row_bytes);
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(stage_base + static_cast<size_t>(s) * p.stage_bytes,
-                 p.W + static_cast<size_t>(v0 + static_cast<int64_t>(it) * p.stage_rows) *
-                           p.row_bytes,
-                 bytes, &full[s]);
+        const int band = it / p.nslab, slab = it - band * p.nslab;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(p.stage_bytes));
+        tma_load_2d(stage_base + static_cast<size_t>(s) * p.stage_bytes, &wmap,
+                    slab * p.slab_elems, y0 + band * kBandRows, &full[s]);
         issued = it + 1;
       }
       // every issued copy must have landed before this block may exit
@@ -156,110 +205,83 @@ __global__ void __launch_bounds__(448, 1) gemv_rows_kernel(const GemvParams p) {
         }
       }
     }
-  } else if (warp == REDUCER) {
-    // ---------------- reducer: sum each row's per-warp partials in ascending warp order -------
-    float tq[RP];
-#pragma unroll
-    for (int r = 0; r < RP; ++r)
-      tq[r] = (r < p.nrows && p.logits) ? p.temperature[r / p.rows_per_req] : 0.f;
-    for (int it = 0; it < nst; ++it) {
-      const int s = it % S;
-      const uint32_t ph = (it / S) & 1;
-      const int rows = min(p.stage_rows, nt - it * p.stage_rows);
-      bool ok = true;
-      for (int gi = 0; gi < p.ng; ++gi) {
-        if (!mbar_wait_bounded(&redbar[s * p.ng + gi], ph)) {
-          atomicOr(&p.hdr->error, ERR_GEMV_WAIT_RED);
-          atomicExch(&flags[0], 1);
-          ok = false;
-          break;
-        }
-        if (lane < NV) {
-          const int g = lane / RP, r = lane % RP;
-          const int lr = gi * G + g;
-          if (r < p.nrows && lr < rows) {
-            const float* src = red + (static_cast<size_t>(s) * NW + gi * p.wpr) * 32 + lane;
-            float z = 0.f;
-            for (int w2 = 0; w2 < p.wpr; ++w2) z += src[w2 * 32];
-            const int local = it * p.stage_rows + lr;
-            ztile[static_cast<size_t>(r) * p.tile_cap + local] = z;
-            float tr = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < RP; ++rr)
-              if (rr == r) tr = tq[rr];
-            if (tr > 0.f) p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = z;
-          }
-        }
-      }
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // the stage's partial sums are consumed
-    }
   } else {
-    // ---------------- consumers: dot products against register-resident H ----------------
-    const int gi = warp / p.wpr, wi = warp - gi * p.wpr;
-    const int chunk = wi * 32 + lane;
-    const bool active = chunk < p.cpr;
-    float h[RP][EPC];
-#pragma unroll
-    for (int r = 0; r < RP; ++r) {
-      uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-      if (active && r < p.nrows)
-        hv = *reinterpret_cast<const uint4*>(p.H + static_cast<size_t>(r) * p.h_row_bytes +
-                                             static_cast<size_t>(chunk) * 16);
-      unpack16<BF16>(hv, h[r]);
-    }
-
-    for (int it = 0; it < nst; ++it) {
+    // ---------------- consumers: 4 rows per warp, full dot products ----------------
+    const int wrow = warp * G;  // first row of this warp within a band
+    float2 acc[G][RP];
+    for (int it = 0; it < niter; ++it) {
       const int s = it % S;
       const uint32_t ph = (it / S) & 1;
+      const int band = it / p.nslab, slab = it - band * p.nslab;
+      if (slab == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int r = 0; r < RP; ++r) acc[g][r] = make_float2(0.f, 0.f);
+      }
       if (!mbar_wait_bounded(&full[s], ph)) {
         atomicOr(&p.hdr->error, ERR_GEMV_WAIT_FULL);
         atomicExch(&flags[0], 1);
         break;
       }
-      const int rows = min(p.stage_rows, nt - it * p.stage_rows);
-      float v[NV];
+      uint4 w[G];
+      const uint8_t* sp = stage_base + static_cast<size_t>(s) * p.stage_bytes +
+                          static_cast<size_t>(wrow) * kSlabBytes + lane * 16;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) v[i] = 0.f;
-      if (active) {
-        const uint8_t* sp = stage_base + static_cast<size_t>(s) * p.stage_bytes +
-                            static_cast<size_t>(gi * G) * p.row_bytes +
-                            static_cast<size_t>(chunk) * 16;
-        uint4 w[G];
+      for (int g = 0; g < G; ++g) w[g] = lds128(sp + g * kSlabBytes);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // release orders the loads above before reuse
+
+      const float4* hp = hs + static_cast<size_t>(slab) * PP * RH * 32 + lane;
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          w[g] = (gi * G + g < rows) ? lds128(sp + static_cast<size_t>(g) * p.row_bytes)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+      for (int q = 0; q < PP; ++q) {
+        float4 hq[RH];
+#pragma unroll
+        for (int rr = 0; rr < RH; ++rr) hq[rr] = hp[(q * RH + rr) * 32];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float wf[EPC];
-          unpack16<BF16>(w[g], wf);
+          float2 wp;
+          if constexpr (BF16) {
+            const uint32_t u = (q == 0) ? w[g].x : (q == 1) ? w[g].y : (q == 2) ? w[g].z : w[g].w;
+            wp = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+          } else {
+            wp = (q == 0) ? make_float2(__uint_as_float(w[g].x), __uint_as_float(w[g].y))
+                          : make_float2(__uint_as_float(w[g].z), __uint_as_float(w[g].w));
+          }
 #pragma unroll
-          for (int r = 0; r < RP; ++r) {
-            // packed fp32x2 FMAs: even and odd elements accumulate separately, then add
-            float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < EPC; e += 2)
-              a = __ffma2_rn(make_float2(wf[e], wf[e + 1]), make_float2(h[r][e], h[r][e + 1]), a);
-            v[g * RP + r] = a.x + a.y;
+          for (int rr = 0; rr < RH; ++rr) {
+            acc[g][2 * rr] = __ffma2_rn(wp, make_float2(hq[rr].x, hq[rr].y), acc[g][2 * rr]);
+            if (2 * rr + 1 < RP)
+              acc[g][2 * rr + 1] =
+                  __ffma2_rn(wp, make_float2(hq[rr].z, hq[rr].w), acc[g][2 * rr + 1]);
           }
         }
       }
-      ReduceScatter<NV, 16>::run(v, lane);
-      float* rb = red + (static_cast<size_t>(s) * NW + warp) * 32;
-      if ((lane % SPREAD) == 0) rb[lane / SPREAD] = v[0];
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&redbar[s * p.ng + gi]);
-        mbar_arrive(&empty[s]);
+
+      if (slab == p.nslab - 1) {
+        // the band's dot products are complete in each lane's k-range: sum across the warp
+        float v[NV];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int r = 0; r < RP; ++r) v[g * RP + r] = acc[g][r].x + acc[g][r].y;
+        ReduceScatter<NV, 16>::run(v, lane);
+        if ((lane % SPREAD) == 0) {
+          const int i = lane / SPREAD, g = i / RP, r = i % RP;
+          const int local = band * kBandRows + wrow + g;
+          if (r < p.nrows && local < nt) {
+            ztile[static_cast<size_t>(r) * p.tile_cap + local] = v[0];
+            if (s_temp[r] > 0.f)
+              p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = v[0];
+          }
+        }
       }
     }
   }
   __syncthreads();
 
   // ---------------- per-block partial statistics of each row ----------------
-  const int NWALL = NW + 2;
+  const int NWALL = NW + 1;
   for (int q = warp; q < p.nrows; q += NWALL) {
     const float T = p.temperature[q / p.rows_per_req];
     const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
@@ -393,8 +415,8 @@ __global__ void __launch_bounds__(448, 1) gemv_rows_kernel(const GemvParams p) {
         cstar = __shfl_sync(0xffffffffu, cstar, 0);
         tt = __shfl_sync(0xffffffffu, tt, 0);
         if (cstar >= 0) {
-          const int64_t c0 = static_cast<int64_t>(cstar) * p.V / GR;
-          const int64_t c1 = static_cast<int64_t>(cstar + 1) * p.V / GR;
+          int64_t c0, c1;
+          block_rows(cstar, GR, p.nbands, p.V, c0, c1);
           const float mc = __ldcg(&(p.part + static_cast<size_t>(cstar) * kMaxRows + q)->m);
           const float* yrow = p.logits + static_cast<size_t>(q) * p.logits_stride;
           unsigned long long carry = 0ull;
@@ -438,7 +460,7 @@ static cudaError_t launch_variant(const GemvLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_smem = L.smem;
   }
-  kern<<<L.grid, L.threads, L.smem, stream>>>(L.p);
+  kern<<<L.grid, L.threads, L.smem, stream>>>(L.wmap, L.p);
   return cudaGetLastError();
 }
 

@@ -1,23 +1,23 @@
 // Launch parameter blocks of the kernels (passed by value to each kernel).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace spec {
 
 struct GemvParams {
-  const uint8_t* W;
-  int64_t V;
-  int row_bytes;
-  int cpr;  // 16-byte chunks per weight row
-  int wpr;  // warps per weight row
-  int ng;   // row groups per block
-  int nw;   // compute warps = wpr * ng
+  int64_t V;        // rows projected (the verify vocabulary, or the draft rows)
+  int d;            // hidden size
+  int nslab;        // 512-byte k-slabs per weight row
+  int slab_elems;   // elements per slab
+  int64_t nbands;   // 48-row bands over V
   int stages;
-  int stage_rows;  // = 4 * ng
-  int stage_bytes;
-  int ring_bytes;  // >= stages * stage_bytes; the last block reuses it as scratch
-  int tile_cap;  // max rows per block tile
+  int stage_bytes;  // one slab of one band: 48 rows x 512 bytes
+  int ring_bytes;   // >= stages * stage_bytes; the last block reuses it as scratch
+  int hs_bytes;     // shared-memory copy of H as fp32 pairs
+  int tile_cap;     // max rows per block tile
   const uint8_t* H;
   int h_row_bytes;
   int nrows;
@@ -38,6 +38,7 @@ struct GemvParams {
 
 struct GemvLaunch {
   int grid, threads, smem;
+  CUtensorMap wmap;  // W as a 2-D tensor [V rows][d], box [48 rows][512 bytes]
   GemvParams p;
 };
 
