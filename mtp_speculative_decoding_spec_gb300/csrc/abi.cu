@@ -12,9 +12,9 @@
 namespace spec {
 namespace {
 
-constexpr int kBandRows = 48;         // GEMV band: 12 consumer warps x 4 rows
-constexpr int kMaxBandsPerBlock = 42;  // per-block tile of the GEMV (logits kept in smem)
-constexpr int kGemvThreads = 13 * 32;  // 12 consumer warps + 1 producer
+constexpr int kBandRows = 44;         // GEMV band: 11 consumer warps x 4 rows
+constexpr int kMaxBandsPerBlock = 46;  // per-block tile of the GEMV (logits kept in smem)
+constexpr int kGemvThreads = 12 * 32;  // 11 consumer warps + 1 producer
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

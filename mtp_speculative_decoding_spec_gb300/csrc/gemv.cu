@@ -7,12 +7,12 @@
 // W [V, d] bf16 (or fp32) streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming
 // GEMV: the weight bytes bound it, so the design is about keeping HBM busy with few
 // instructions per weight byte:
-//   * one persistent block per SM; the vocabulary is cut into 48-row bands and block c owns a
+//   * one persistent block per SM; the vocabulary is cut into 44-row bands and block c owns a
 //     contiguous run of bands (balanced to one band, no wave tail, the same cut for any number
 //     of rows);
-//   * a producer warp streams each band as k-slabs of [48 rows x 512 bytes] with 2-D TMA
+//   * a producer warp streams each band as k-slabs of [44 rows x 512 bytes] with 2-D TMA
 //     tensor copies into a ring of shared-memory stages completed on mbarriers;
-//   * twelve consumer warps each own 4 rows of the band and compute their full dot products:
+//   * eleven consumer warps each own 4 rows of the band and compute their full dot products:
 //     lane l takes bytes [16 l, 16 l + 16) of every slab row, and the H rows sit in shared
 //     memory as fp32 pairs laid out so that one conflict-free 128-bit load feeds packed
 //     fp32x2 FMAs for two H rows; one butterfly (xor 16, 8, 4, 2, 1) per band finishes each
@@ -86,12 +86,14 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
   return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
 }
 
-constexpr int kBandWarps = 12;                     // consumer warps per block
+// 11 consumer warps + 1 producer: 12 warps put 3 on each SM sub-partition, whose 16K
+// registers then allow up to 168 per thread (the 8-row variant needs ~150).
+constexpr int kBandWarps = 11;                     // consumer warps per block
 constexpr int kRowsPerWarp = 4;                    // weight rows per consumer warp per band
-constexpr int kBandRows = kBandWarps * kRowsPerWarp;  // 48
+constexpr int kBandRows = kBandWarps * kRowsPerWarp;  // 44
 constexpr int kSlabBytes = 512;                    // bytes of one weight row per k-slab
 
-// Rows [v0, v1) of block `blk`: a contiguous run of 48-row bands.
+// Rows [v0, v1) of block `blk`: a contiguous run of 44-row bands.
 __device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, int64_t V,
                                           int64_t& v0, int64_t& v1) {
   const int64_t b0 = static_cast<int64_t>(blk) * nbands / nblk;
@@ -112,7 +114,7 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 }
 
 template <int RP, bool BF16>
-__global__ void __maxnreg__(152)
+__global__ void __maxnreg__(168)
     gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
   constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
   constexpr int PP = EPC / 2;               // element pairs per chunk
@@ -125,7 +127,7 @@ __global__ void __maxnreg__(152)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages, NW = kBandWarps, PRODUCER = kBandWarps;
-  uint8_t* stage_base = smem;                                     // ring, [S][48 rows][512 B]
+  uint8_t* stage_base = smem;                                     // ring, [S][44 rows][512 B]
   float4* hs = reinterpret_cast<float4*>(smem + p.ring_bytes);   // H pairs
   float* ztile = reinterpret_cast<float*>(smem + p.ring_bytes + p.hs_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(ztile + static_cast<size_t>(RP) * p.tile_cap);
@@ -180,7 +182,7 @@ __global__ void __maxnreg__(152)
   __syncthreads();
 
   if (warp == PRODUCER) {
-    // ---------------- producer: stream k-slabs of 48-row bands into the stage ring ---------
+    // ---------------- producer: stream k-slabs of 44-row bands into the stage ring ---------
     if (lane == 0) {
       int issued = 0;
       const int y0 = static_cast<int>(v0);
@@ -460,6 +462,10 @@ static cudaError_t launch_variant(const GemvLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_smem = L.smem;
   }
+  int fit = 0;  // registers and shared memory must admit one block per SM
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, L.threads, L.smem);
+  if (e != cudaSuccess) return e;
+  if (fit < 1) return cudaErrorLaunchOutOfResources;
   kern<<<L.grid, L.threads, L.smem, stream>>>(L.wmap, L.p);
   return cudaGetLastError();
 }
