@@ -37,6 +37,9 @@ def _compile(src, verbose):
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{res.stdout}\n{res.stderr}")
+    # keep ptxas's resource report (registers, spills, shared memory) next to the object
+    with open(os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".ptxas.log"), "w") as f:
+        f.write(res.stderr)
     return obj, res.stderr if verbose else ""
 
 

@@ -116,3 +116,37 @@ def test_no_cpu_fallback_in_product_package():
             src = open(os.path.join(pkg, f)).read()
             assert "oracle" not in src, f
             assert "import numpy" not in src or f == "_abi.py", f
+
+
+# threads per block of each kernel, as launched by abi.cu / gemv.cu
+_BLOCK_THREADS = {"gemv_rows_kernel": 12 * 32, "accept_kernel": 256, "commit_kernel": 256}
+
+
+def test_register_budget_per_sub_partition(lib):
+    """Each SM has four sub-partitions with 16K registers each and a block's warps are spread
+    round-robin over them, so regs/thread (allocated in multiples of 8) times 32 times the warps
+    on the fullest sub-partition must fit in 16,384 -- or the launch fails. Also: no spills."""
+    import glob
+    logs = glob.glob(os.path.join(ROOT, "mtp_speculative_decoding_spec_gb300", "_build",
+                                  "*.ptxas.log"))
+    assert logs, "build did not record ptxas output"
+    seen = 0
+    for path in logs:
+        name = None
+        for line in open(path):
+            m = re.search(r"Compiling entry function '(\w+)'", line)
+            if m:
+                name = m.group(1)
+            m = re.search(r"(\d+) bytes spill stores", line)
+            if m and name:
+                assert int(m.group(1)) == 0, f"{name} spills"
+            m = re.search(r"Used (\d+) registers", line)
+            if m and name:
+                regs = int(m.group(1))
+                base = next(k for k in _BLOCK_THREADS if k in name)
+                warps = _BLOCK_THREADS[base] // 32
+                per_sp = -(-warps // 4)
+                alloc = -(-regs // 8) * 8
+                assert alloc * 32 * per_sp <= 16384, (name, regs, warps)
+                seen += 1
+    assert seen >= 10
