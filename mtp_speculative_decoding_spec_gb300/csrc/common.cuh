@@ -92,16 +92,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~limit_ns of wall time and returns false;
-// the caller records an error and stops waiting.
+// Bounded wait on an mbarrier phase: gives up after ~limit_ns of wall time (the timer is read
+// every 64 polls) and returns false; the caller records an error and stops waiting.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if ((n & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Packed fp32x2 arithmetic on 64-bit registers (two fp32 lanes: low word = x, high = y).
+__device__ __forceinline__ void ffma2_acc(unsigned long long& acc, unsigned long long a,
+                                          unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return __uint_as_float(lo) + __uint_as_float(hi);
+}
+__device__ __forceinline__ void lds128_b64(const void* p, unsigned long long& a,
+                                           unsigned long long& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(smem_u32(p)));
 }
 
 // One-dimensional bulk copy global -> shared completed on an mbarrier (size and both

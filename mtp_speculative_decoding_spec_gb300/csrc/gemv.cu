@@ -186,18 +186,26 @@ __global__ void __maxnreg__(168)
     if (lane == 0) {
       int issued = 0;
       const int y0 = static_cast<int>(v0);
+      int s = 0, band = 0, slab = 0;
+      uint32_t eph = 0;  // parity of the empty-barrier phase to wait for (second lap onwards)
       for (int it = 0; it < niter; ++it) {
-        const int s = it % S;
-        if (it >= S && !mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1)) {
+        if (it >= S && !mbar_wait_bounded(&empty[s], eph)) {
           atomicOr(&p.hdr->error, ERR_GEMV_WAIT_EMPTY);
           atomicExch(&flags[0], 1);
           break;
         }
-        const int band = it / p.nslab, slab = it - band * p.nslab;
         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(p.stage_bytes));
         tma_load_2d(stage_base + static_cast<size_t>(s) * p.stage_bytes, &wmap,
                     slab * p.slab_elems, y0 + band * kBandRows, &full[s]);
         issued = it + 1;
+        if (++slab == p.nslab) {
+          slab = 0;
+          ++band;
+        }
+        if (++s == S) {
+          s = 0;
+          if (it + 1 > S) eph ^= 1u;  // laps 2, 3, ... wait on phases 0, 1, 0, ...
+        }
       }
       // every issued copy must have landed before this block may exit
       for (int it = max(0, issued - S); it < issued; ++it) {
@@ -210,16 +218,16 @@ __global__ void __maxnreg__(168)
   } else {
     // ---------------- consumers: 4 rows per warp, full dot products ----------------
     const int wrow = warp * G;  // first row of this warp within a band
-    float2 acc[G][RP];
+    // acc[g][r]: packed (even-element, odd-element) partial sums of row g against H row r
+    unsigned long long acc[G][RP];
+    int s = 0, band = 0, slab = 0;
+    uint32_t ph = 0;
     for (int it = 0; it < niter; ++it) {
-      const int s = it % S;
-      const uint32_t ph = (it / S) & 1;
-      const int band = it / p.nslab, slab = it - band * p.nslab;
       if (slab == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int r = 0; r < RP; ++r) acc[g][r] = make_float2(0.f, 0.f);
+          for (int r = 0; r < RP; ++r) acc[g][r] = 0ull;
       }
       if (!mbar_wait_bounded(&full[s], ph)) {
         atomicOr(&p.hdr->error, ERR_GEMV_WAIT_FULL);
@@ -237,25 +245,22 @@ __global__ void __maxnreg__(168)
       const float4* hp = hs + static_cast<size_t>(slab) * PP * RH * 32 + lane;
 #pragma unroll
       for (int q = 0; q < PP; ++q) {
-        float4 hq[RH];
+        unsigned long long h0[RH], h1[RH];  // (h[2rr][k], h[2rr][k+1]), (h[2rr+1][k], ...)
 #pragma unroll
-        for (int rr = 0; rr < RH; ++rr) hq[rr] = hp[(q * RH + rr) * 32];
+        for (int rr = 0; rr < RH; ++rr) lds128_b64(hp + (q * RH + rr) * 32, h0[rr], h1[rr]);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float2 wp;
+          unsigned long long wp;
           if constexpr (BF16) {
             const uint32_t u = (q == 0) ? w[g].x : (q == 1) ? w[g].y : (q == 2) ? w[g].z : w[g].w;
-            wp = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+            wp = pack2(u << 16, u & 0xffff0000u);
           } else {
-            wp = (q == 0) ? make_float2(__uint_as_float(w[g].x), __uint_as_float(w[g].y))
-                          : make_float2(__uint_as_float(w[g].z), __uint_as_float(w[g].w));
+            wp = (q == 0) ? pack2(w[g].x, w[g].y) : pack2(w[g].z, w[g].w);
           }
 #pragma unroll
           for (int rr = 0; rr < RH; ++rr) {
-            acc[g][2 * rr] = __ffma2_rn(wp, make_float2(hq[rr].x, hq[rr].y), acc[g][2 * rr]);
-            if (2 * rr + 1 < RP)
-              acc[g][2 * rr + 1] =
-                  __ffma2_rn(wp, make_float2(hq[rr].z, hq[rr].w), acc[g][2 * rr + 1]);
+            ffma2_acc(acc[g][2 * rr], wp, h0[rr]);
+            if (2 * rr + 1 < RP) ffma2_acc(acc[g][2 * rr + 1], wp, h1[rr]);
           }
         }
       }
@@ -266,7 +271,7 @@ __global__ void __maxnreg__(168)
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int r = 0; r < RP; ++r) v[g * RP + r] = acc[g][r].x + acc[g][r].y;
+          for (int r = 0; r < RP; ++r) v[g * RP + r] = sum2(acc[g][r]);
         ReduceScatter<NV, 16>::run(v, lane);
         if ((lane % SPREAD) == 0) {
           const int i = lane / SPREAD, g = i / RP, r = i % RP;
@@ -277,6 +282,14 @@ __global__ void __maxnreg__(168)
               p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = v[0];
           }
         }
+      }
+      if (++slab == p.nslab) {
+        slab = 0;
+        ++band;
+      }
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
       }
     }
   }
