@@ -12,9 +12,9 @@
 namespace spec {
 namespace {
 
-constexpr int kBandRows = 44;         // GEMV band: 11 consumer warps x 4 rows
-constexpr int kMaxBandsPerBlock = 46;  // per-block tile of the GEMV (logits kept in smem)
-constexpr int kGemvThreads = 12 * 32;  // 11 consumer warps + 1 producer
+constexpr int kBandRows = 60;         // GEMV band: 15 consumer warps x 4 rows
+constexpr int kMaxBandsPerBlock = 34;  // per-block tile of the GEMV (logits kept in smem)
+constexpr int kGemvThreads = 16 * 32;  // 15 consumer warps + 1 producer
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -7,12 +7,12 @@
 // W [V, d] bf16 (or fp32) streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming
 // GEMV: the weight bytes bound it, so the design is about keeping HBM busy with few
 // instructions per weight byte:
-//   * one persistent block per SM; the vocabulary is cut into 44-row bands and block c owns a
+//   * one persistent block per SM; the vocabulary is cut into 60-row bands and block c owns a
 //     contiguous run of bands (balanced to one band, no wave tail, the same cut for any number
 //     of rows);
-//   * a producer warp streams each band as k-slabs of [44 rows x 512 bytes] with 2-D TMA
+//   * a producer warp streams each band as k-slabs of [60 rows x 512 bytes] with 2-D TMA
 //     tensor copies into a ring of shared-memory stages completed on mbarriers;
-//   * eleven consumer warps each own 4 rows of the band and compute their full dot products:
+//   * fifteen consumer warps each own 4 rows of the band and compute their full dot products:
 //     lane l takes bytes [16 l, 16 l + 16) of every slab row, and the H rows sit in shared
 //     memory as fp32 pairs laid out so that one conflict-free 128-bit load feeds packed
 //     fp32x2 FMAs for two H rows; one butterfly (xor 16, 8, 4, 2, 1) per band finishes each
@@ -86,14 +86,14 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
   return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
 }
 
-// 11 consumer warps + 1 producer: 12 warps put 3 on each SM sub-partition, whose 16K
-// registers then allow up to 168 per thread (the 8-row variant needs ~150).
-constexpr int kBandWarps = 11;                     // consumer warps per block
+// 15 consumer warps + 1 producer: 16 warps put 4 on each SM sub-partition (more latency
+// hiding), whose 16K registers then allow up to 128 per thread.
+constexpr int kBandWarps = 15;                     // consumer warps per block
 constexpr int kRowsPerWarp = 4;                    // weight rows per consumer warp per band
-constexpr int kBandRows = kBandWarps * kRowsPerWarp;  // 44
+constexpr int kBandRows = kBandWarps * kRowsPerWarp;  // 60
 constexpr int kSlabBytes = 512;                    // bytes of one weight row per k-slab
 
-// Rows [v0, v1) of block `blk`: a contiguous run of 44-row bands.
+// Rows [v0, v1) of block `blk`: a contiguous run of 60-row bands.
 __device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, int64_t V,
                                           int64_t& v0, int64_t& v1) {
   const int64_t b0 = static_cast<int64_t>(blk) * nbands / nblk;
@@ -114,7 +114,7 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 }
 
 template <int RP, bool BF16>
-__global__ void __maxnreg__(168)
+__global__ void __maxnreg__(128)
     gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
   constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
   constexpr int PP = EPC / 2;               // element pairs per chunk
@@ -127,7 +127,7 @@ __global__ void __maxnreg__(168)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages, NW = kBandWarps, PRODUCER = kBandWarps;
-  uint8_t* stage_base = smem;                                     // ring, [S][44 rows][512 B]
+  uint8_t* stage_base = smem;                                     // ring, [S][60 rows][512 B]
   float4* hs = reinterpret_cast<float4*>(smem + p.ring_bytes);   // H pairs
   float* ztile = reinterpret_cast<float*>(smem + p.ring_bytes + p.hs_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(ztile + static_cast<size_t>(RP) * p.tile_cap);
@@ -182,7 +182,7 @@ __global__ void __maxnreg__(168)
   __syncthreads();
 
   if (warp == PRODUCER) {
-    // ---------------- producer: stream k-slabs of 44-row bands into the stage ring ---------
+    // ---------------- producer: stream k-slabs of 60-row bands into the stage ring ---------
     if (lane == 0) {
       int issued = 0;
       const int y0 = static_cast<int>(v0);
@@ -245,22 +245,24 @@ __global__ void __maxnreg__(168)
       const float4* hp = hs + static_cast<size_t>(slab) * PP * RH * 32 + lane;
 #pragma unroll
       for (int q = 0; q < PP; ++q) {
-        unsigned long long h0[RH], h1[RH];  // (h[2rr][k], h[2rr][k+1]), (h[2rr+1][k], ...)
-#pragma unroll
-        for (int rr = 0; rr < RH; ++rr) lds128_b64(hp + (q * RH + rr) * 32, h0[rr], h1[rr]);
+        unsigned long long wp[G];  // element pair q of each row: (w[2q], w[2q+1]) as fp32
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          unsigned long long wp;
           if constexpr (BF16) {
             const uint32_t u = (q == 0) ? w[g].x : (q == 1) ? w[g].y : (q == 2) ? w[g].z : w[g].w;
-            wp = pack2(u << 16, u & 0xffff0000u);
+            wp[g] = pack2(u << 16, u & 0xffff0000u);
           } else {
-            wp = (q == 0) ? pack2(w[g].x, w[g].y) : pack2(w[g].z, w[g].w);
+            wp[g] = (q == 0) ? pack2(w[g].x, w[g].y) : pack2(w[g].z, w[g].w);
           }
+        }
 #pragma unroll
-          for (int rr = 0; rr < RH; ++rr) {
-            ffma2_acc(acc[g][2 * rr], wp, h0[rr]);
-            if (2 * rr + 1 < RP) ffma2_acc(acc[g][2 * rr + 1], wp, h1[rr]);
+        for (int rr = 0; rr < RH; ++rr) {
+          unsigned long long h0, h1;  // (h[2rr][k], h[2rr][k+1]), (h[2rr+1][k], h[2rr+1][k+1])
+          lds128_b64(hp + (q * RH + rr) * 32, h0, h1);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            ffma2_acc(acc[g][2 * rr], wp[g], h0);
+            if (2 * rr + 1 < RP) ffma2_acc(acc[g][2 * rr + 1], wp[g], h1);
           }
         }
       }

@@ -12,9 +12,9 @@ struct GemvParams {
   int d;            // hidden size
   int nslab;        // 512-byte k-slabs per weight row
   int slab_elems;   // elements per slab
-  int64_t nbands;   // 44-row bands over V
+  int64_t nbands;   // 60-row bands over V
   int stages;
-  int stage_bytes;  // one slab of one band: 44 rows x 512 bytes
+  int stage_bytes;  // one slab of one band: 60 rows x 512 bytes
   int ring_bytes;   // >= stages * stage_bytes; the last block reuses it as scratch
   int hs_bytes;     // shared-memory copy of H as fp32 pairs
   int tile_cap;     // max rows per block tile
@@ -38,7 +38,7 @@ struct GemvParams {
 
 struct GemvLaunch {
   int grid, threads, smem;
-  CUtensorMap wmap;  // W as a 2-D tensor [V rows][d], box [44 rows][512 bytes]
+  CUtensorMap wmap;  // W as a 2-D tensor [V rows][d], box [60 rows][512 bytes]
   GemvParams p;
 };
 
