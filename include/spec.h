@@ -256,6 +256,35 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc *st,
 /* 1 if this build has the batched tensor-core path for more than 8 verify rows per call. */
 int32_t spec_batched_supported(void);
 
+/*
+ * spec_lmhead_verify_noalloc -- spec_lmhead_verify for callers that cannot allocate device
+ * memory. (The pages have no counterpart: this is a deployment convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc at all: a plugin handed only pre-allocated tensors by a
+ * host framework that owns the device memory budget and forbids allocations after start-up, or
+ * code that must not risk the implicit device synchronisation an allocation can cause. This
+ * entry point takes the same inputs and outputs as spec_lmhead_verify but no workspace: its
+ * scratch is a fixed device array of spec_noalloc_scratch_bytes() bytes (128 KiB) compiled into
+ * the library, which every GPU that loads the library holds until the process exits. It
+ * allocates nothing and calls no allocating routine.
+ *
+ *   - The first call on a device looks up the array's device address with that device current
+ *     (one cudaGetSymbolAddress per device); make that first call before any stream capture.
+ *   - Every call shares the one array and clears its counters at the start (an asynchronous
+ *     memset on `stream`); calls whose work overlaps on the GPU (different streams, or several
+ *     host threads) race on it and must be serialised by the caller.
+ *   - A vocabulary or batch whose scratch would exceed the array returns SPEC_ERR_UNSUPPORTED
+ *     (at 152 SMs that is beyond roughly 500,000 vocabulary rows); everything else validates
+ *     and fails like spec_lmhead_verify.
+ */
+spec_status spec_lmhead_verify_noalloc(const void *W, spec_dtype wdt, int64_t V, int64_t d,
+                                       const void *H, int32_t B, int32_t R,
+                                       const float *temperature, float *logits,
+                                       spec_rowstats *stats, spec_stream_t stream);
+
+/* Size of the fixed scratch array used by spec_lmhead_verify_noalloc. */
+size_t spec_noalloc_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

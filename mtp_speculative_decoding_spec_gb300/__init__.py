@@ -87,3 +87,15 @@ def spec_commit_rollback(B, st, acc, k, mode, commit_status=None, stream=None):
     import ctypes
     _check("spec_commit_rollback", _abi.lib().spec_commit_rollback(
         B, ctypes.byref(st), _ptr(acc), _ptr(k), mode, _ptr(commit_status), _stream(stream)))
+
+
+def spec_lmhead_verify_noalloc(W, wdt, V, d, H, B, R, temperature, logits, stats, stream=None):
+    """spec_lmhead_verify without a workspace: for callers that cannot allocate device memory
+    (the library's fixed scratch array is used instead; see include/spec.h)."""
+    _check("spec_lmhead_verify_noalloc", _abi.lib().spec_lmhead_verify_noalloc(
+        _ptr(W), wdt, V, d, _ptr(H), B, R, _ptr(temperature), _ptr(logits), _ptr(stats),
+        _stream(stream)))
+
+
+def spec_noalloc_scratch_bytes():
+    return int(_abi.lib().spec_noalloc_scratch_bytes())

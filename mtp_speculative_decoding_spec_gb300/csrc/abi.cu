@@ -337,3 +337,57 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free variant of spec_lmhead_verify. Its scratch (the cross-block ticket, the error
+// word and the per-block partial statistics) lives in a fixed device array that every GPU
+// loading this library holds until the process exits. Host code must not pass the array's
+// name to a kernel: in host code that name is only a stand-in, not a device address. The device
+// address is fetched once per device with cudaGetSymbolAddress, with that device current.
+// ------------------------------------------------------------------------------------------
+namespace spec {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 128 * 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+void* noalloc_scratch() {
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace spec
+
+extern "C" size_t spec_noalloc_scratch_bytes(void) { return spec::kNoAllocScratchBytes; }
+
+extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt, int64_t V,
+                                                  int64_t d, const void* H, int32_t B, int32_t R,
+                                                  const float* temperature, float* logits,
+                                                  spec_rowstats* stats, spec_stream_t stream) {
+  if (!W || !H || !temperature || !stats) return SPEC_ERR_INVALID;
+  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(H)) return SPEC_ERR_INVALID;
+  if (static_cast<int64_t>(B) * R > kMaxRows) return SPEC_ERR_UNSUPPORTED;
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  // the fixed scratch must hold this call's workspace layout
+  if (ws_layout(V, B, a.sms).total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
+  void* scratch = noalloc_scratch();
+  if (!scratch) return SPEC_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the ticket and the error word must start at zero (a previous call may have been cut short)
+  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return SPEC_ERR_CUDA;
+  return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr, nullptr,
+                  0, nullptr, 0, scratch, kNoAllocScratchBytes, B, s);
+}
