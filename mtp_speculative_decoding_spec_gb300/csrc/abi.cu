@@ -72,19 +72,28 @@ int accept_slices(int64_t V) { return static_cast<int>((V + kAcceptSlice - 1) / 
 //   [0, 256)                    header (GEMV ticket, error word)
 //   [256, part_end)             GEMV per-block partials (grid of the vocabulary size)
 //   [part_end, sums_end)        accept per-slice sums (B * slices * 16 bytes)
+//   [sums_end, gemm_end)        batched path: per-(row, 256-row tile) partials (no counters)
 //   [ws_bytes - tickets, end)   accept tickets, one per request
 struct WsLayout {
-  size_t part, sums, tickets_bytes, total;
+  size_t part, sums, gemm, tickets_bytes, total;
 };
+
+int gemm_rows_max(int32_t max_batch) {
+  const int64_t r = 8 * static_cast<int64_t>(max_batch);
+  return r > kMaxRows ? static_cast<int>(r < 256 ? r : 256) : 0;
+}
 
 WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
   WsLayout w;
   w.part = sizeof(WsHeader);
   w.sums = w.part + align_up(sizeof(GemvPartial) * kMaxRows * gemv_grid(V, sms), 256);
+  w.gemm = w.sums + align_up(sizeof(unsigned long long) * 2 * static_cast<size_t>(max_batch) *
+                                 accept_slices(V),
+                             256);
+  const int64_t ntiles = (V + 255) / 256;
   w.tickets_bytes = align_up(sizeof(uint32_t) * static_cast<size_t>(max_batch), 256);
-  w.total = w.sums +
-            align_up(sizeof(unsigned long long) * 2 * static_cast<size_t>(max_batch) *
-                         accept_slices(V),
+  w.total = w.gemm +
+            align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles,
                      256) +
             w.tickets_bytes;
   return w;
@@ -182,6 +191,54 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// The batched tensor-core path (9..256 rows, bf16, d a multiple of 64).
+spec_status run_gemm(const void* W, int64_t V, int64_t d, const void* H, int nrows,
+                     int rows_per_req, const float* temperature, float* logits,
+                     int64_t logits_stride, spec_rowstats* stats, void* workspace,
+                     size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream) {
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  if (d % gemm_tc_kblock() != 0 || nrows > 256) return SPEC_ERR_UNSUPPORTED;
+  const WsLayout wl = ws_layout(V, batch_for_ws, a.sms);
+  if (workspace_bytes < wl.total || gemm_rows_max(batch_for_ws) < nrows) return SPEC_ERR_INVALID;
+  if (gemm_tc_smem_bytes() > a.smem_optin) return SPEC_ERR_UNSUPPORTED;
+  EncodeTiledFn encode = encode_tiled();
+  if (!encode) return SPEC_ERR_CUDA;
+  GemmLaunch L;
+  memset(&L, 0, sizeof(L));
+  const cuuint64_t hdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(nrows)};
+  const cuuint64_t wdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(V)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(d * 2)};
+  const cuuint32_t hbox[2] = {static_cast<cuuint32_t>(gemm_tc_kblock()), 128};
+  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(gemm_tc_kblock()),
+                              static_cast<cuuint32_t>(gemm_tc_tile_rows())};
+  const cuuint32_t estride[2] = {1, 1};
+  if (encode(&L.hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(H), hdim, gstride,
+             hbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPEC_ERR_CUDA;
+  if (encode(&L.wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), wdim, gstride,
+             wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SPEC_ERR_CUDA;
+  GemmParams& p = L.p;
+  p.V = V;
+  p.d = static_cast<int>(d);
+  p.nrows = nrows;
+  p.rows_per_req = rows_per_req;
+  p.ntiles = static_cast<int>((V + gemm_tc_tile_rows() - 1) / gemm_tc_tile_rows());
+  p.temperature = temperature;
+  p.logits = logits;
+  p.logits_stride = logits_stride;
+  p.stats = stats;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.gemm);
+  L.grid = p.ntiles < a.sms ? p.ntiles : a.sms;
+  L.smem = gemm_tc_smem_bytes();
+  const cudaError_t e = gemm_tc_launch(L, stream);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace spec
 
@@ -206,7 +263,7 @@ const char* spec_status_str(spec_status s) {
   return "SPEC_ERR_UNKNOWN";
 }
 
-int32_t spec_batched_supported(void) { return 0; }
+int32_t spec_batched_supported(void) { return 1; }
 
 spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t d,
                                const void* H, int32_t B, int32_t R, const float* temperature,
@@ -217,7 +274,11 @@ spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t
   if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
     return SPEC_ERR_INVALID;
   if (!aligned16(W) || !aligned16(H) || !aligned16(workspace)) return SPEC_ERR_INVALID;
-  if (static_cast<int64_t>(B) * R > kMaxRows) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * R > kMaxRows) {
+    if (wdt != SPEC_BF16 || static_cast<int64_t>(B) * R > 256) return SPEC_ERR_UNSUPPORTED;
+    return run_gemm(W, V, d, H, B * R, R, temperature, logits, V, stats, workspace,
+                    workspace_bytes, B, reinterpret_cast<cudaStream_t>(stream));
+  }
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
                   nullptr, 0, nullptr, 0, workspace, workspace_bytes, B,
                   reinterpret_cast<cudaStream_t>(stream));

@@ -26,6 +26,7 @@ enum : uint32_t {
   ERR_GEMV_WAIT_EMPTY = 1u << 1,
   ERR_GEMV_WAIT_RED = 1u << 2,
   ERR_GEMV_DRAIN = 1u << 3,
+  ERR_TC_WAIT = 1u << 4,
 };
 
 // Per-block, per-row partial statistics of a GEMV tile (32 bytes).

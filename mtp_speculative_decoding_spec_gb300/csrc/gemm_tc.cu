@@ -1,0 +1,391 @@
+// Batched LM-head projection on the tcgen05 tensor cores: z = H W^T for 9..256 verify rows
+// (e.g. 32 requests x 8 rows) with the per-row statistics fused into the epilogue.
+//
+// At 256 rows the LM head is a dense contraction (2 * 256 * 2560 * 151,936 = 199 GFLOP over
+// 778 MB of weights, ~256 flop per weight byte), so it runs on the 5th-generation tensor cores
+// (lucebox-hub PR #15 "MTP speculative decoding", section "What": one batched verify through
+// the shared LM head; here batched over requests as well as rows):
+//   * one persistent CTA per SM walks vocabulary tiles of 256 rows;
+//   * a producer warp loads, per 64-wide k-block, the two 128-row halves of H and the 256-row
+//     weight tile with 2-D TMA (128-byte swizzle) into a 3-stage ring;
+//   * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128 token rows,
+//     N = 256 vocabulary rows, K = 16) into two TMEM accumulators, one per half of H, and
+//     commits each stage back to the producer and each finished tile to the epilogue;
+//   * four epilogue warps read the accumulators with tcgen05.ld: TMEM lane = token row, so each
+//     thread owns one token row and reduces max / argmax / top-2 and the quantised sum of
+//     exp((z - m)/T) over the tile's 256 vocabulary columns in registers, writes the row's
+//     logits when its temperature is > 0, and stores a per-(row, tile) partial;
+//   * a second small kernel combines the partials of each row (one block per row).
+#include <math.h>
+
+#include "params.cuh"
+
+namespace spec {
+
+constexpr int kTcTileN = 256;       // vocabulary rows per tile (MMA N)
+constexpr int kTcHalfM = 128;       // token rows per accumulator (MMA M)
+constexpr int kTcKBlock = 64;       // bf16 elements per k-block (one 128-byte swizzle row)
+constexpr int kTcStages = 3;
+constexpr int kTcABytes = kTcHalfM * kTcKBlock * 2;   // 16 KB per half of H
+constexpr int kTcBBytes = kTcTileN * kTcKBlock * 2;   // 32 KB per weight tile
+constexpr int kTcStageBytes = 2 * kTcABytes + kTcBBytes;
+constexpr int kTcThreads = 6 * 32;  // producer, MMA, 4 epilogue warps
+constexpr uint32_t kTmemCols = 512;
+
+// --------------------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tc_tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the canonical 128-byte-swizzle layout
+// written by TMA (rows of 128 bytes, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);        // start address
+  d |= static_cast<uint64_t>(1u) << 16;                       // leading offset (unused here)
+  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;   // stride offset: 8 rows
+  d |= static_cast<uint64_t>(1u) << 46;                       // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                       // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ unsigned long long tc_weight(float z, float m, float invT) {
+  return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
+}
+
+// --------------------------------------------------------------------------- main kernel
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_rows_tc_kernel(const __grid_constant__ CUtensorMap hmap,
+                        const __grid_constant__ CUtensorMap wmap, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte-swizzle tiles, whatever the base alignment
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* tmem_full = empty + kTcStages;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = p.d / kTcKBlock;
+  const int nhalf = (p.nrows > kTcHalfM) ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);  // one arrive per epilogue warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {  // allocate the accumulators (all 512 columns; one CTA per SM)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t bytes = static_cast<uint32_t>((nhalf == 2 ? 2 : 1) * kTcABytes + kTcBBytes);
+      int s = 0;
+      uint32_t eph = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.ntiles && !*reinterpret_cast<volatile int*>(abort_flag);
+           tile += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          if (it >= kTcStages && !mbar_wait_bounded(&empty[s], eph)) {
+            atomicOr(&p.hdr->error, ERR_TC_WAIT);
+            atomicExch(abort_flag, 1);
+            break;
+          }
+          uint8_t* st = stages + s * kTcStageBytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tc_tma_load_2d(st, &hmap, kb * kTcKBlock, 0, &full[s]);
+          if (nhalf == 2) tc_tma_load_2d(st + kTcABytes, &hmap, kb * kTcKBlock, kTcHalfM, &full[s]);
+          tc_tma_load_2d(st + 2 * kTcABytes, &wmap, kb * kTcKBlock, tile * kTcTileN, &full[s]);
+          if (++s == kTcStages) {
+            s = 0;
+            if (it + 1 > kTcStages) eph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(kTcHalfM, kTcTileN);
+      int s = 0;
+      uint32_t fph = 0;
+      int tcount = 0;
+      for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
+        if (tcount > 0 && !mbar_wait_bounded(tmem_empty, (tcount - 1) & 1)) {
+          atomicOr(&p.hdr->error, ERR_TC_WAIT);
+          atomicExch(abort_flag, 1);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&full[s], fph)) {
+            atomicOr(&p.hdr->error, ERR_TC_WAIT);
+            atomicExch(abort_flag, 1);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stages + s * kTcStageBytes);
+#pragma unroll
+          for (int ks = 0; ks < kTcKBlock / 16; ++ks) {
+            const uint64_t bdesc = smem_desc_sw128(st + 2 * kTcABytes + ks * 32);
+            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+            tc_mma(tmem_base, smem_desc_sw128(st + ks * 32), bdesc, idesc, acc);
+            if (nhalf == 2)
+              tc_mma(tmem_base + kTcTileN, smem_desc_sw128(st + kTcABytes + ks * 32), bdesc, idesc,
+                     acc);
+          }
+          tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
+          if (++s == kTcStages) {
+            s = 0;
+            fph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);  // the tile's accumulators are complete
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int ew = warp & 3;          // TMEM lane quadrant this warp may access
+    const int row_in_half = ew * 32 + lane;
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
+      if (!mbar_wait_bounded(tmem_full, tcount & 1)) {
+        atomicOr(&p.hdr->error, ERR_TC_WAIT);
+        atomicExch(abort_flag, 1);
+        break;
+      }
+      tc_fence_after();
+      const int64_t v0 = static_cast<int64_t>(tile) * kTcTileN;
+      const int nv = static_cast<int>(min(static_cast<int64_t>(kTcTileN), p.V - v0));
+      for (int h = 0; h < nhalf; ++h) {
+        const int q = h * kTcHalfM + row_in_half;  // token row of this thread
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                               static_cast<uint32_t>(h * kTcTileN);
+        const bool live = q < p.nrows;
+        const float T = live ? p.temperature[q / p.rows_per_req] : 0.f;
+        const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+        float* lrow = (live && T > 0.f && p.logits)
+                          ? p.logits + static_cast<size_t>(q) * p.logits_stride + v0
+                          : nullptr;
+        Top2 t = top2_empty();
+        int bad = 0;
+        for (int c = 0; c < kTcTileN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);  // every lane takes part (the load is warp-collective)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c + j;
+            if (col < nv) {
+              const float z = v[j];
+              if (isnan(z) || z == INFINITY)
+                bad = 1;
+              else
+                top2_push(t, z, static_cast<int32_t>(v0 + col));
+              if (lrow) lrow[col] = z;
+            }
+          }
+        }
+        // second pass for the quantised sum; the loads are warp-collective, so every lane
+        // runs them and only the accumulation depends on the lane's own row
+        const bool do_sum = (t.idx != kNoIndex && t.best != -INFINITY);
+        unsigned long long ssum = 0ull;
+        for (int c = 0; c < kTcTileN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float z = v[j];
+            if (do_sum && c + j < nv && !(isnan(z) || z == INFINITY))
+              ssum += tc_weight(z, t.best, invT);
+          }
+        }
+        if (live) {
+          GemvPartial pp;
+          pp.m = t.best;
+          pp.second = t.second;
+          pp.idx = (t.idx == kNoIndex) ? -1 : t.idx;
+          pp.flags = bad;
+          pp.s = ssum;
+          pp.pad = 0ull;
+          p.part[static_cast<size_t>(q) * p.ntiles + tile] = pp;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// --------------------------------------------------------------------------- row combine
+// One block per row: combine the row's per-tile partials in a fixed order (thread-strided,
+// then a fixed tree), exactly like the last block of the GEMV.
+__global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams p) {
+  __shared__ float sm_best[8], sm_second[8];
+  __shared__ int sm_idx[8], sm_bad[8];
+  __shared__ double sm_sum[8];
+  const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const GemvPartial* row = p.part + static_cast<size_t>(q) * p.ntiles;
+  const float T = p.temperature[q / p.rows_per_req];
+  const float Te = T > 0.f ? T : 1.f;
+  Top2 t = top2_empty();
+  int bad = 0;
+  for (int i = tid; i < p.ntiles; i += blockDim.x) {
+    bad |= __ldcg(&row[i].flags);
+    const int32_t idx = __ldcg(&row[i].idx);
+    if (idx >= 0) t = top2_merge(t, Top2{__ldcg(&row[i].m), __ldcg(&row[i].second), idx});
+  }
+  t = warp_top2(t);
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sm_best[warp] = t.best;
+    sm_second[warp] = t.second;
+    sm_idx[warp] = t.idx;
+    sm_bad[warp] = bad;
+  }
+  __syncthreads();
+  Top2 all = top2_empty();
+  int anybad = 0;
+  for (int w = 0; w < 8; ++w) {
+    all = top2_merge(all, Top2{sm_best[w], sm_second[w], sm_idx[w]});
+    anybad |= sm_bad[w];
+  }
+  const bool nonfinite = anybad || all.idx == kNoIndex || all.best == -INFINITY;
+  const float M = all.best;
+  double S = 0.0;
+  if (!nonfinite) {
+    for (int i = tid; i < p.ntiles; i += blockDim.x) {
+      const float mc = __ldcg(&row[i].m);
+      if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY)
+        S += static_cast<double>(__ldcg(&row[i].s)) *
+             exp((static_cast<double>(mc) - static_cast<double>(M)) / static_cast<double>(Te));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  if (lane == 0) sm_sum[warp] = S;
+  __syncthreads();
+  if (tid == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < 8; ++w) tot += sm_sum[w];
+    spec_rowstats st;
+    if (nonfinite) {
+      st.max = __int_as_float(0x7fc00000);
+      st.log_norm = st.max;
+      st.gap = st.max;
+      st.argmax = -1;
+    } else {
+      st.max = M;
+      st.log_norm = static_cast<float>(log(tot) - 27.725887222397812);  // log(S * 2^-40)
+      st.gap = __fsub_rn(M, all.second);
+      st.argmax = all.idx;
+    }
+    p.stats[q] = st;
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream) {
+  static int configured = 0;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_rows_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+    if (e != cudaSuccess) return e;
+    configured = 1;
+  }
+  int fit = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemm_rows_tc_kernel,
+                                                                kTcThreads, L.smem);
+  if (e != cudaSuccess) return e;
+  if (fit < 1) return cudaErrorLaunchOutOfResources;
+  gemm_rows_tc_kernel<<<L.grid, kTcThreads, L.smem, stream>>>(L.hmap, L.wmap, L.p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gemm_rows_combine_kernel<<<L.p.nrows, 256, 0, stream>>>(L.p);
+  return cudaGetLastError();
+}
+
+int gemm_tc_smem_bytes() { return kTcStages * kTcStageBytes + 1024 + 128; }
+int gemm_tc_tile_rows() { return kTcTileN; }
+int gemm_tc_kblock() { return kTcKBlock; }
+
+}  // namespace spec

@@ -71,6 +71,33 @@ struct CommitParams {
   int32_t* commit_status;
 };
 
+// Batched tensor-core path (9..256 rows): see gemm_tc.cu.
+struct GemmParams {
+  int64_t V;
+  int d;
+  int nrows;
+  int rows_per_req;
+  int ntiles;  // 256-row vocabulary tiles
+  const float* temperature;
+  float* logits;  // nullable
+  int64_t logits_stride;
+  spec_rowstats* stats;
+  WsHeader* hdr;
+  GemvPartial* part;  // [nrows][ntiles]
+};
+
+struct GemmLaunch {
+  int grid, smem;
+  CUtensorMap hmap;  // H [nrows][d] bf16, box [128 rows][64], 128-byte swizzle
+  CUtensorMap wmap;  // W [V][d] bf16, box [256 rows][64], 128-byte swizzle
+  GemmParams p;
+};
+
+cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream);
+int gemm_tc_smem_bytes();
+int gemm_tc_tile_rows();
+int gemm_tc_kblock();
+
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
 cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
