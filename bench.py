@@ -276,6 +276,7 @@ def run_ours(args, rank, local_rank, world):
         if not args.no_sweep:
             res["sweep"] = sweep(dev, W, Wd, hbm_peak)
             res["commit"] = commit_bench(dev, hbm_peak)
+            res["batched"] = batched_bench(dev, W, Wd, hbm_peak, tf_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         res["cpu_baseline"] = cpu_baseline(cfg, W, args.cpu_seconds)
     if world > 1:
@@ -289,8 +290,9 @@ def run_ours(args, rank, local_rank, world):
 
 def profile_extras(dev, W, Wd):
     """Launches for ncu captures after the greedy section: 5 sampled k=7 cycles (7 draft
-    steps, an 8-row verify, acceptance with residual/bonus draws), then 3 snapshot commits and
-    3 replay commits of the 64K-context state."""
+    steps, an 8-row verify, acceptance with residual/bonus draws), 3 snapshot commits and 3
+    replay commits of the 64K-context state, then 5 batched 256-row verifies on the tensor
+    cores (each followed by a 32-request acceptance)."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -307,6 +309,7 @@ def profile_extras(dev, W, Wd):
         eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
     torch.cuda.synchronize()
     commit_bench(dev, 6736.5, reps=3, warm=0)
+    batched_bench(dev, W, Wd, 6736.5, 1898.3, reps=2, with_commit=False)
 
 
 def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
@@ -468,6 +471,122 @@ def commit_bench(dev, hbm_peak, reps=20, warm=3):
         out[name] = {"us": round(t * 1e6, 2), "bytes": moved,
                      "gbs": round(moved / t / 1e9, 1), "frac": round(moved / t / 1e9 / hbm_peak, 4)}
     return out
+
+
+def batched_bench(dev, W, Wd, hbm_peak, tf_peak, reps=20, with_commit=True):
+    """32 requests x 8 rows: tensor-core LM head (256 rows), acceptance for 32 requests (half
+    greedy, half T = 1 with one-hot q), and the 32 requests' snapshot commit at 16K context."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    cfg = configs.get(4)
+    B, R = cfg.batch, cfg.rows_per_request
+    rng = np.random.default_rng(4)
+    H, _, targets = gen.planted_rows(cfg, W, B * R, rng)
+    H_d = torch.from_numpy(H.view(np.int16)).to(dev)
+    ws = torch.zeros(spec.spec_workspace_bytes(cfg.V, B), dtype=torch.uint8, device=dev)
+    logits = torch.empty((B * R, cfg.V), dtype=torch.float32, device=dev)
+    stats = torch.zeros(B * R * spec.ROWSTATS_BYTES, dtype=torch.uint8, device=dev)
+    temps = torch.tensor(cfg.temps, dtype=torch.float32, device=dev)
+    ks = rng.integers(1, 8, B).astype(np.int32)
+    drafts = np.zeros((B, 7), dtype=np.int32)
+    for b in range(B):
+        drafts[b, :ks[b]] = targets[b * R:b * R + ks[b]]
+    k_d = torch.from_numpy(ks).to(dev)
+    dr_d = torch.from_numpy(drafts).to(dev)
+    seeds = torch.arange(B, dtype=torch.int64, device=dev)
+    pos = torch.full((B,), cfg.context, dtype=torch.int64, device=dev)
+    out = torch.zeros(B * spec.ACCEPT_OUT_BYTES, dtype=torch.uint8, device=dev)
+    cnt = torch.zeros(B * spec.COUNTERS_BYTES, dtype=torch.uint8, device=dev)
+
+    def verify():
+        spec.spec_lmhead_verify(Wd, spec.SPEC_BF16, cfg.V, cfg.d, H_d, B, R, temps, logits, stats,
+                                ws)
+
+    def accept():
+        spec.spec_accept(B, 7, k_d, dr_d, logits, stats, cfg.V, R, None, None, cfg.Vd, cfg.Vd,
+                         temps, cfg.eos_id, seeds, pos, out, cnt, ws)
+
+    st = None
+    if with_commit:
+        st = BatchedState(cfg, B, dev)
+
+    def commit():
+        st.kv_len.fill_(cfg.context)
+        spec.spec_commit_rollback(B, st.desc, out, k_d, spec.SPEC_COMMIT_SNAPSHOT)
+
+    for _ in range(3):
+        verify()
+        accept()
+        if st:
+            commit()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        verify()
+        ev[i][1].record()
+        accept()
+        ev[i][2].record()
+        if st:
+            commit()
+        ev[i][3].record()
+    torch.cuda.synchronize()
+    tv = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    ta = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    tc = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    o = out.cpu().numpy().view(spec.ACCEPT_OUT_DTYPE)
+    flops = 2.0 * B * R * cfg.d * cfg.V
+    gemm_bytes = cfg.V * cfg.d * 2 + B * R * cfg.d * 2 + (B // 2) * R * cfg.V * 4
+    res = {"workload": "32 requests x 8 rows, d=2560, V=151936 bf16, half T=0 / half T=1, "
+                       "16K context state",
+           "verify_us": round(tv * 1e6, 2), "tflops": round(flops / tv / 1e12, 1),
+           "tensor_frac": round(flops / tv / 1e12 / tf_peak, 4),
+           "hbm_gbs": round(gemm_bytes / tv / 1e9, 1),
+           "hbm_frac": round(gemm_bytes / tv / 1e9 / hbm_peak, 4),
+           "accept_us": round(ta * 1e6, 2),
+           "emitted_tokens_per_cycle": int(o["n_emit"].sum()),
+           "verify_cycles_s": round(1.0 / (tv + ta), 1),
+           "tokens_s_verify_accept": round(float(o["n_emit"].sum()) / (tv + ta), 1),
+           "workspace_error": int(ws[4:8].cpu().numpy().view(np.uint32)[0])}
+    if st:
+        moved = B * (2 * 4 * (st.rec_elems + st.conv_elems))
+        res.update({"commit_us": round(tc * 1e6, 2), "commit_bytes": moved,
+                    "commit_gbs": round(moved / tc / 1e9, 1),
+                    "commit_frac": round(moved / tc / 1e9 / hbm_peak, 4),
+                    "full_cycles_s": round(1.0 / (tv + ta + tc), 1)})
+        del st
+    return res
+
+
+class BatchedState:
+    """Device state of B requests at the batched workload's sizes (KV, recurrent, conv, 9
+    snapshot slots) for the commit timing; contents are random, the commit copies them."""
+
+    def __init__(self, cfg, B, dev):
+        import torch
+
+        import mtp_speculative_decoding_spec_gb300 as spec
+        ns = 9
+        L, H, dk, dv = cfg.rec_layers, cfg.rec_heads, cfg.rec_dk, cfg.rec_dv
+        self.rec_elems = L * H * dk * dv
+        self.conv_elems = L * cfg.conv_rows * cfg.conv_width
+        kvb = cfg.kv_layers * 2 * cfg.kv_capacity * cfg.kv_row_bytes
+        self.kv = torch.zeros(B * kvb, dtype=torch.uint8, device=dev)
+        self.kv_len = torch.full((B,), cfg.context, dtype=torch.int64, device=dev)
+        self.live = torch.zeros(B * self.rec_elems, device=dev)
+        self.slots = torch.randn(B * ns * self.rec_elems, device=dev)
+        self.clive = torch.zeros(B * self.conv_elems, device=dev)
+        self.cslots = torch.randn(B * ns * self.conv_elems, device=dev)
+        d = spec.spec_state_desc()
+        d.kv, d.kv_request_stride, d.kv_layers = self.kv.data_ptr(), kvb, cfg.kv_layers
+        d.kv_capacity, d.kv_row_bytes = cfg.kv_capacity, cfg.kv_row_bytes
+        d.kv_len = self.kv_len.data_ptr()
+        d.rec_layers, d.rec_heads, d.rec_dk, d.rec_dv = L, H, dk, dv
+        d.rec_live, d.rec_slots = self.live.data_ptr(), self.slots.data_ptr()
+        d.conv_rows, d.conv_width = cfg.conv_rows, cfg.conv_width
+        d.conv_live, d.conv_slots, d.n_slots = self.clive.data_ptr(), self.cslots.data_ptr(), ns
+        self.desc = d
 
 
 def cpu_baseline(cfg, W, seconds):
