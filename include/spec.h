@@ -273,9 +273,9 @@ int32_t spec_batched_supported(void);
  *   - Every call shares the one array and clears its counters at the start (an asynchronous
  *     memset on `stream`); calls whose work overlaps on the GPU (different streams, or several
  *     host threads) race on it and must be serialised by the caller.
- *   - A vocabulary or batch whose scratch would exceed the array returns SPEC_ERR_UNSUPPORTED
- *     (at 152 SMs that is beyond roughly 500,000 vocabulary rows); everything else validates
- *     and fails like spec_lmhead_verify.
+ *   - A vocabulary whose scratch would exceed the array returns SPEC_ERR_UNSUPPORTED (at 152
+ *     SMs that is beyond about 900,000 vocabulary rows); everything else validates and fails
+ *     like spec_lmhead_verify (more than 8 rows in total: SPEC_ERR_UNSUPPORTED).
  */
 spec_status spec_lmhead_verify_noalloc(const void *W, spec_dtype wdt, int64_t V, int64_t d,
                                        const void *H, int32_t B, int32_t R,

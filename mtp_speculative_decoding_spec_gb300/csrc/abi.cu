@@ -442,13 +442,14 @@ extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt,
   if (static_cast<int64_t>(B) * R > kMaxRows) return SPEC_ERR_UNSUPPORTED;
   const DevAttr a = dev_attr();
   if (a.sms <= 0) return SPEC_ERR_CUDA;
-  // the fixed scratch must hold this call's workspace layout
-  if (ws_layout(V, B, a.sms).total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
+  // the fixed scratch must hold the GEMV's part of the workspace layout (header and per-block
+  // partials); a batch-1 layout covers it for any B*R <= 8
+  if (ws_layout(V, 1, a.sms).total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
   void* scratch = noalloc_scratch();
   if (!scratch) return SPEC_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the ticket and the error word must start at zero (a previous call may have been cut short)
   if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return SPEC_ERR_CUDA;
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr, nullptr,
-                  0, nullptr, 0, scratch, kNoAllocScratchBytes, B, s);
+                  0, nullptr, 0, scratch, kNoAllocScratchBytes, 1, s);
 }
