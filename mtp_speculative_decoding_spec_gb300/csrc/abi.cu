@@ -93,7 +93,8 @@ WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
   const int64_t ntiles = (V + 255) / 256;
   w.tickets_bytes = align_up(sizeof(uint32_t) * static_cast<size_t>(max_batch), 256);
   w.total = w.gemm +
-            align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles,
+            align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles *
+                         2,
                      256) +
             w.tickets_bytes;
   return w;
@@ -227,6 +228,7 @@ spec_status run_gemm(const void* W, int64_t V, int64_t d, const void* H, int nro
   p.nrows = nrows;
   p.rows_per_req = rows_per_req;
   p.ntiles = static_cast<int>((V + gemm_tc_tile_rows() - 1) / gemm_tc_tile_rows());
+  p.vec_store = (logits_stride % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
   p.temperature = temperature;
   p.logits = logits;
   p.logits_stride = logits_stride;

@@ -29,7 +29,9 @@ constexpr int kTcStages = 3;
 constexpr int kTcABytes = kTcHalfM * kTcKBlock * 2;   // 16 KB per half of H
 constexpr int kTcBBytes = kTcTileN * kTcKBlock * 2;   // 32 KB per weight tile
 constexpr int kTcStageBytes = 2 * kTcABytes + kTcBBytes;
-constexpr int kTcThreads = 6 * 32;  // producer, MMA, 4 epilogue warps
+constexpr int kTcThreads = 10 * 32;  // producer, MMA, 8 epilogue warps
+constexpr int kTcEpiWarps = 8;      // two per TMEM lane quadrant, 128 columns each
+constexpr int kTcSubTiles = 2;      // per-row partials per tile (one per column half)
 constexpr uint32_t kTmemCols = 512;
 
 // --------------------------------------------------------------------------- PTX wrappers
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);  // one arrive per epilogue warp
+    mbar_init(tmem_empty, kTcEpiWarps);  // one arrive per epilogue warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -215,7 +217,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int ew = warp & 3;          // TMEM lane quadrant this warp may access
+    const int ew = warp & 3;                // TMEM lane quadrant this warp may access
+    const int ch = (warp - 2) / 4;          // column half of the tile: [128*ch, 128*ch + 128)
     const int row_in_half = ew * 32 + lane;
     int tcount = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
@@ -225,12 +228,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int64_t v0 = static_cast<int64_t>(tile) * kTcTileN;
-      const int nv = static_cast<int>(min(static_cast<int64_t>(kTcTileN), p.V - v0));
+      const int64_t v0 = static_cast<int64_t>(tile) * kTcTileN + ch * (kTcTileN / 2);
+      const int nv = static_cast<int>(
+          max(static_cast<int64_t>(0), min(static_cast<int64_t>(kTcTileN / 2), p.V - v0)));
       for (int h = 0; h < nhalf; ++h) {
         const int q = h * kTcHalfM + row_in_half;  // token row of this thread
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                               static_cast<uint32_t>(h * kTcTileN);
+                               static_cast<uint32_t>(h * kTcTileN + ch * (kTcTileN / 2));
         const bool live = q < p.nrows;
         const float T = live ? p.temperature[q / p.rows_per_req] : 0.f;
         const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
@@ -239,19 +243,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           : nullptr;
         Top2 t = top2_empty();
         int bad = 0;
-        for (int c = 0; c < kTcTileN; c += 32) {
+        for (int c = 0; c < kTcTileN / 2; c += 32) {
           float v[32];
           tmem_ld32(taddr + c, v);  // every lane takes part (the load is warp-collective)
+          if (lrow) {
+            if (p.vec_store && c + 32 <= nv) {
+              float4* dst = reinterpret_cast<float4*>(lrow + c);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c + j < nv) lrow[c + j] = v[j];
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int col = c + j;
-            if (col < nv) {
+            if (c + j < nv) {
               const float z = v[j];
               if (isnan(z) || z == INFINITY)
                 bad = 1;
               else
-                top2_push(t, z, static_cast<int32_t>(v0 + col));
-              if (lrow) lrow[col] = z;
+                top2_push(t, z, static_cast<int32_t>(v0 + c + j));
             }
           }
         }
@@ -259,7 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // runs them and only the accumulation depends on the lane's own row
         const bool do_sum = (t.idx != kNoIndex && t.best != -INFINITY);
         unsigned long long ssum = 0ull;
-        for (int c = 0; c < kTcTileN; c += 32) {
+        for (int c = 0; c < kTcTileN / 2; c += 32) {
           float v[32];
           tmem_ld32(taddr + c, v);
 #pragma unroll
@@ -277,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pp.flags = bad;
           pp.s = ssum;
           pp.pad = 0ull;
-          p.part[static_cast<size_t>(q) * p.ntiles + tile] = pp;
+          p.part[static_cast<size_t>(q) * p.ntiles * kTcSubTiles + tile * kTcSubTiles + ch] = pp;
         }
       }
       tc_fence_before();
@@ -304,12 +318,13 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   __shared__ int sm_idx[8], sm_bad[8];
   __shared__ double sm_sum[8];
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const GemvPartial* row = p.part + static_cast<size_t>(q) * p.ntiles;
+  const int nparts = p.ntiles * kTcSubTiles;
+  const GemvPartial* row = p.part + static_cast<size_t>(q) * nparts;
   const float T = p.temperature[q / p.rows_per_req];
   const float Te = T > 0.f ? T : 1.f;
   Top2 t = top2_empty();
   int bad = 0;
-  for (int i = tid; i < p.ntiles; i += blockDim.x) {
+  for (int i = tid; i < nparts; i += blockDim.x) {
     bad |= __ldcg(&row[i].flags);
     const int32_t idx = __ldcg(&row[i].idx);
     if (idx >= 0) t = top2_merge(t, Top2{__ldcg(&row[i].m), __ldcg(&row[i].second), idx});
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   const float M = all.best;
   double S = 0.0;
   if (!nonfinite) {
-    for (int i = tid; i < p.ntiles; i += blockDim.x) {
+    for (int i = tid; i < nparts; i += blockDim.x) {
       const float mc = __ldcg(&row[i].m);
       if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY)
         S += static_cast<double>(__ldcg(&row[i].s)) *
@@ -386,6 +401,7 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream) {
 
 int gemm_tc_smem_bytes() { return kTcStages * kTcStageBytes + 1024 + 128; }
 int gemm_tc_tile_rows() { return kTcTileN; }
+int gemm_tc_subtiles() { return kTcSubTiles; }
 int gemm_tc_kblock() { return kTcKBlock; }
 
 }  // namespace spec

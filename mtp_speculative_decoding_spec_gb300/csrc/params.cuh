@@ -77,13 +77,14 @@ struct GemmParams {
   int d;
   int nrows;
   int rows_per_req;
-  int ntiles;  // 256-row vocabulary tiles
+  int ntiles;     // 256-row vocabulary tiles
+  int vec_store;  // logits rows 16-byte aligned (V % 4 == 0)
   const float* temperature;
   float* logits;  // nullable
   int64_t logits_stride;
   spec_rowstats* stats;
   WsHeader* hdr;
-  GemvPartial* part;  // [nrows][ntiles]
+  GemvPartial* part;  // [nrows][ntiles][2]
 };
 
 struct GemmLaunch {
@@ -97,6 +98,7 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream);
 int gemm_tc_smem_bytes();
 int gemm_tc_tile_rows();
 int gemm_tc_kblock();
+int gemm_tc_subtiles();
 
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
