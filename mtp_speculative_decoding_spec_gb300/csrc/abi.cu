@@ -90,7 +90,7 @@ WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
   w.gemm = w.sums + align_up(sizeof(unsigned long long) * 2 * static_cast<size_t>(max_batch) *
                                  accept_slices(V),
                              256);
-  const int64_t ntiles = (V + 255) / 256;
+  const int64_t ntiles = (V + 127) / 128;  // batched path: 128-row vocabulary tiles
   w.tickets_bytes = align_up(sizeof(uint32_t) * static_cast<size_t>(max_batch), 256);
   w.total = w.gemm +
             align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles *

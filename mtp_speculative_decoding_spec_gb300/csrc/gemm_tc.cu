@@ -5,12 +5,14 @@
 // 778 MB of weights, ~256 flop per weight byte), so it runs on the 5th-generation tensor cores
 // (lucebox-hub PR #15 "MTP speculative decoding", section "What": one batched verify through
 // the shared LM head; here batched over requests as well as rows):
-//   * one persistent CTA per SM walks vocabulary tiles of 256 rows;
-//   * a producer warp loads, per 64-wide k-block, the two 128-row halves of H and the 256-row
-//     weight tile with 2-D TMA (128-byte swizzle) into a 3-stage ring;
+//   * one persistent CTA per SM walks vocabulary tiles of 128 rows;
+//   * a producer warp loads, per 64-wide k-block, the two 128-row halves of H and the 128-row
+//     weight tile with 2-D TMA (128-byte swizzle) into a 4-stage ring;
 //   * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128 token rows,
-//     N = 256 vocabulary rows, K = 16) into two TMEM accumulators, one per half of H, and
-//     commits each stage back to the producer and each finished tile to the epilogue;
+//     N = 128 vocabulary rows, K = 16) into two TMEM accumulators, one per half of H, and
+//     commits each stage back to the producer and each finished tile to the epilogue; the
+//     accumulators are double-buffered (2 x 2 x 128 of the 512 TMEM columns), so the epilogue
+//     of one tile overlaps the MMAs of the next;
 //   * four epilogue warps read the accumulators with tcgen05.ld: TMEM lane = token row, so each
 //     thread owns one token row and reduces max / argmax / top-2 and the quantised sum of
 //     exp((z - m)/T) over the tile's 256 vocabulary columns in registers, writes the row's
@@ -22,15 +24,15 @@
 
 namespace spec {
 
-constexpr int kTcTileN = 256;       // vocabulary rows per tile (MMA N)
+constexpr int kTcTileN = 128;       // vocabulary rows per tile (MMA N)
 constexpr int kTcHalfM = 128;       // token rows per accumulator (MMA M)
 constexpr int kTcKBlock = 64;       // bf16 elements per k-block (one 128-byte swizzle row)
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr int kTcABytes = kTcHalfM * kTcKBlock * 2;   // 16 KB per half of H
-constexpr int kTcBBytes = kTcTileN * kTcKBlock * 2;   // 32 KB per weight tile
+constexpr int kTcBBytes = kTcTileN * kTcKBlock * 2;   // 16 KB per weight tile
 constexpr int kTcStageBytes = 2 * kTcABytes + kTcBBytes;
 constexpr int kTcThreads = 10 * 32;  // producer, MMA, 8 epilogue warps
-constexpr int kTcEpiWarps = 8;      // two per TMEM lane quadrant, 128 columns each
+constexpr int kTcEpiWarps = 8;      // two per TMEM lane quadrant, 64 columns each
 constexpr int kTcSubTiles = 2;      // per-row partials per tile (one per column half)
 constexpr uint32_t kTmemCols = 512;
 
@@ -116,9 +118,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
-  uint64_t* tmem_full = empty + kTcStages;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
+  uint64_t* tmem_full = empty + kTcStages;  // [2]: one per accumulator buffer
+  uint64_t* tmem_empty = tmem_full + 2;     // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,8 +132,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kTcEpiWarps);  // one arrive per epilogue warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], kTcEpiWarps);  // one arrive per epilogue warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -180,12 +184,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t fph = 0;
       int tcount = 0;
       for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
-        if (tcount > 0 && !mbar_wait_bounded(tmem_empty, (tcount - 1) & 1)) {
+        // accumulator buffer of this tile: the epilogue of the previous tile drains the other
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !mbar_wait_bounded(&tmem_empty[buf], (use - 1) & 1)) {
           atomicOr(&p.hdr->error, ERR_TC_WAIT);
           atomicExch(abort_flag, 1);
           break;
         }
         tc_fence_after();
+        const uint32_t dacc = tmem_base + static_cast<uint32_t>(buf * 2 * kTcTileN);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(&full[s], fph)) {
@@ -200,10 +207,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int ks = 0; ks < kTcKBlock / 16; ++ks) {
             const uint64_t bdesc = smem_desc_sw128(st + 2 * kTcABytes + ks * 32);
             const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-            tc_mma(tmem_base, smem_desc_sw128(st + ks * 32), bdesc, idesc, acc);
+            tc_mma(dacc, smem_desc_sw128(st + ks * 32), bdesc, idesc, acc);
             if (nhalf == 2)
-              tc_mma(tmem_base + kTcTileN, smem_desc_sw128(st + kTcABytes + ks * 32), bdesc, idesc,
-                     acc);
+              tc_mma(dacc + kTcTileN, smem_desc_sw128(st + kTcABytes + ks * 32), bdesc, idesc, acc);
           }
           tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
           if (++s == kTcStages) {
@@ -212,17 +218,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(tmem_full);  // the tile's accumulators are complete
+        tc_commit(&tmem_full[tcount & 1]);  // the tile's accumulators are complete
       }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
     const int ew = warp & 3;                // TMEM lane quadrant this warp may access
-    const int ch = (warp - 2) / 4;          // column half of the tile: [128*ch, 128*ch + 128)
+    const int ch = (warp - 2) / 4;          // column half of the tile: [64*ch, 64*ch + 64)
     const int row_in_half = ew * 32 + lane;
     int tcount = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
-      if (!mbar_wait_bounded(tmem_full, tcount & 1)) {
+      const int buf = tcount & 1;
+      if (!mbar_wait_bounded(&tmem_full[buf], (tcount >> 1) & 1)) {
         atomicOr(&p.hdr->error, ERR_TC_WAIT);
         atomicExch(abort_flag, 1);
         break;
@@ -234,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int h = 0; h < nhalf; ++h) {
         const int q = h * kTcHalfM + row_in_half;  // token row of this thread
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                               static_cast<uint32_t>(h * kTcTileN + ch * (kTcTileN / 2));
+                               static_cast<uint32_t>((buf * 2 + h) * kTcTileN + ch * (kTcTileN / 2));
         const bool live = q < p.nrows;
         const float T = live ? p.temperature[q / p.rows_per_req] : 0.f;
         const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
+      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
     }
   }
 

@@ -77,7 +77,7 @@ struct GemmParams {
   int d;
   int nrows;
   int rows_per_req;
-  int ntiles;     // 256-row vocabulary tiles
+  int ntiles;     // 128-row vocabulary tiles
   int vec_store;  // logits rows 16-byte aligned (V % 4 == 0)
   const float* temperature;
   float* logits;  // nullable
@@ -90,7 +90,7 @@ struct GemmParams {
 struct GemmLaunch {
   int grid, smem;
   CUtensorMap hmap;  // H [nrows][d] bf16, box [128 rows][64], 128-byte swizzle
-  CUtensorMap wmap;  // W [V][d] bf16, box [256 rows][64], 128-byte swizzle
+  CUtensorMap wmap;  // W [V][d] bf16, box [128 rows][64], 128-byte swizzle
   GemmParams p;
 };
 
