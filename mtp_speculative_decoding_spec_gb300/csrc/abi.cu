@@ -234,8 +234,9 @@ spec_status run_gemm(const void* W, int64_t V, int64_t d, const void* H, int nro
   p.logits_stride = logits_stride;
   p.stats = stats;
   p.hdr = static_cast<WsHeader*>(workspace);
-  p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.gemm);
+  p.part = reinterpret_cast<GemmPartial*>(static_cast<uint8_t*>(workspace) + wl.gemm);
   L.grid = p.ntiles < a.sms ? p.ntiles : a.sms;
+  p.nblocks = L.grid;
   L.smem = gemm_tc_smem_bytes();
   const cudaError_t e = gemm_tc_launch(L, stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

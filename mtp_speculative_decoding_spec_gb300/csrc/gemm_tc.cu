@@ -224,8 +224,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int ew = warp & 3;                // TMEM lane quadrant this warp may access
-    const int ch = (warp - 2) / 4;          // column half of the tile: [64*ch, 64*ch + 64)
+    const int ch = (warp - 2) / 4;          // column half of every tile: [64*ch, 64*ch + 64)
     const int row_in_half = ew * 32 + lane;
+    // running statistics of this thread's rows over the CTA's tiles, in tile order: exact
+    // top-2; the normaliser as S * 2^-40 = sum exp((z - M)/T) relative to the running max M,
+    // rescaled in fp64 when M grows (a fixed order, so the result is deterministic)
+    Top2 run[2] = {top2_empty(), top2_empty()};
+    int run_bad[2] = {0, 0};
+    double run_s[2] = {0.0, 0.0};
+    float run_T[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = h * kTcHalfM + row_in_half;
+      run_T[h] = (q < p.nrows) ? p.temperature[q / p.rows_per_req] : 0.f;
+    }
     int tcount = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
       const int buf = tcount & 1;
@@ -238,13 +250,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t v0 = static_cast<int64_t>(tile) * kTcTileN + ch * (kTcTileN / 2);
       const int nv = static_cast<int>(
           max(static_cast<int64_t>(0), min(static_cast<int64_t>(kTcTileN / 2), p.V - v0)));
-      for (int h = 0; h < nhalf; ++h) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (h >= nhalf) break;
         const int q = h * kTcHalfM + row_in_half;  // token row of this thread
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
                                static_cast<uint32_t>((buf * 2 + h) * kTcTileN + ch * (kTcTileN / 2));
         const bool live = q < p.nrows;
-        const float T = live ? p.temperature[q / p.rows_per_req] : 0.f;
-        const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+        const float T = run_T[h];
+        const float Te = T > 0.f ? T : 1.f;
+        const float invT = __fdiv_rn(1.f, Te);
         float* lrow = (live && T > 0.f && p.logits)
                           ? p.logits + static_cast<size_t>(q) * p.logits_stride + v0
                           : nullptr;
@@ -276,8 +291,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        // second pass for the quantised sum; the loads are warp-collective, so every lane
-        // runs them and only the accumulation depends on the lane's own row
+        // second pass for the tile's quantised sum; the loads are warp-collective, so every
+        // lane runs them and only the accumulation depends on the lane's own row
         const bool do_sum = (t.idx != kNoIndex && t.best != -INFINITY);
         unsigned long long ssum = 0ull;
         for (int c = 0; c < kTcTileN / 2; c += 32) {
@@ -290,20 +305,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               ssum += tc_weight(z, t.best, invT);
           }
         }
-        if (live) {
-          GemvPartial pp;
-          pp.m = t.best;
-          pp.second = t.second;
-          pp.idx = (t.idx == kNoIndex) ? -1 : t.idx;
-          pp.flags = bad;
-          pp.s = ssum;
-          pp.pad = 0ull;
-          p.part[static_cast<size_t>(q) * p.ntiles * kTcSubTiles + tile * kTcSubTiles + ch] = pp;
+        // fold the tile into the running statistics
+        run_bad[h] |= bad;
+        if (do_sum) {
+          const double st = static_cast<double>(ssum);
+          if (run_s[h] == 0.0 && !(run[h].idx != kNoIndex && run[h].best != -INFINITY)) {
+            run_s[h] = st;
+          } else if (t.best > run[h].best) {
+            run_s[h] = run_s[h] * exp((static_cast<double>(run[h].best) - t.best) / Te) + st;
+          } else {
+            run_s[h] += st * exp((static_cast<double>(t.best) - run[h].best) / Te);
+          }
         }
+        if (t.idx != kNoIndex) run[h] = top2_merge(run[h], t);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+    }
+    // one partial per (row, CTA, column half)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = h * kTcHalfM + row_in_half;
+      if (h < nhalf && q < p.nrows) {
+        GemmPartial pp;
+        pp.m = run[h].best;
+        pp.second = run[h].second;
+        pp.idx = (run[h].idx == kNoIndex) ? -1 : run[h].idx;
+        pp.flags = run_bad[h];
+        pp.s = run_s[h];
+        pp.pad = 0.0;
+        p.part[(static_cast<size_t>(q) * gridDim.x + blockIdx.x) * kTcSubTiles + ch] = pp;
+      }
     }
   }
 
@@ -325,8 +358,8 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   __shared__ int sm_idx[8], sm_bad[8];
   __shared__ double sm_sum[8];
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nparts = p.ntiles * kTcSubTiles;
-  const GemvPartial* row = p.part + static_cast<size_t>(q) * nparts;
+  const int nparts = p.nblocks * kTcSubTiles;
+  const GemmPartial* row = p.part + static_cast<size_t>(q) * nparts;
   const float T = p.temperature[q / p.rows_per_req];
   const float Te = T > 0.f ? T : 1.f;
   Top2 t = top2_empty();
@@ -357,9 +390,9 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   if (!nonfinite) {
     for (int i = tid; i < nparts; i += blockDim.x) {
       const float mc = __ldcg(&row[i].m);
-      if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY)
-        S += static_cast<double>(__ldcg(&row[i].s)) *
-             exp((static_cast<double>(mc) - static_cast<double>(M)) / static_cast<double>(Te));
+      const double sc = __ldcg(&row[i].s);
+      if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY && sc > 0.0)
+        S += sc * exp((static_cast<double>(mc) - static_cast<double>(M)) / static_cast<double>(Te));
     }
   }
 #pragma unroll

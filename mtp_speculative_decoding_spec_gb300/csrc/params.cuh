@@ -72,19 +72,30 @@ struct CommitParams {
 };
 
 // Batched tensor-core path (9..256 rows): see gemm_tc.cu.
+struct GemmPartial {  // a row's statistics over one CTA's tiles and one column half (32 bytes)
+  float m;            // largest finite logit (-inf if none)
+  float second;
+  int32_t idx;        // -1 if none
+  int32_t flags;      // bit 0: NaN or +Inf seen
+  double s;           // sum of exp((z - m)/T), in units of 2^-40
+  double pad;
+};
+static_assert(sizeof(GemmPartial) == 32, "partial is 32 bytes");
+
 struct GemmParams {
   int64_t V;
   int d;
   int nrows;
   int rows_per_req;
   int ntiles;     // 128-row vocabulary tiles
+  int nblocks;    // CTAs of the tensor-core kernel (partials per row = 2 * nblocks)
   int vec_store;  // logits rows 16-byte aligned (V % 4 == 0)
   const float* temperature;
   float* logits;  // nullable
   int64_t logits_stride;
   spec_rowstats* stats;
   WsHeader* hdr;
-  GemvPartial* part;  // [nrows][ntiles][2]
+  GemmPartial* part;  // [nrows][nblocks][2]
 };
 
 struct GemmLaunch {
