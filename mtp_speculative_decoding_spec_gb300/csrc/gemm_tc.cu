@@ -13,10 +13,11 @@
 //     commits each stage back to the producer and each finished tile to the epilogue; the
 //     accumulators are double-buffered (2 x 2 x 128 of the 512 TMEM columns), so the epilogue
 //     of one tile overlaps the MMAs of the next;
-//   * four epilogue warps read the accumulators with tcgen05.ld: TMEM lane = token row, so each
-//     thread owns one token row and reduces max / argmax / top-2 and the quantised sum of
-//     exp((z - m)/T) over the tile's 256 vocabulary columns in registers, writes the row's
-//     logits when its temperature is > 0, and stores a per-(row, tile) partial;
+//   * eight epilogue warps (two per TMEM lane quadrant, one per 64-column half of the tile)
+//     read the accumulators with tcgen05.ld: TMEM lane = token row, so each thread owns one
+//     token row; it writes the row's logits when its temperature is > 0 and folds the tile's
+//     max / argmax / runner-up (a register tree) and sum of exp((z - m)/T) into running
+//     statistics over the CTA's tiles, stored once as a per-(row, CTA, column half) partial;
 //   * a second small kernel combines the partials of each row (one block per row).
 #include <math.h>
 
@@ -85,26 +86,52 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread). The wait is in
+// the same asm statement, so no use of the registers can be scheduled before the load completes.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ unsigned long long tc_weight(float z, float m, float invT) {
-  return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
+// Top-2 of two candidates where every index of `a` is below every index of `b`, so ties go to
+// `a` (the lower vocabulary index) without comparing indices.
+__device__ __forceinline__ Top2 top2_merge_lr(const Top2& a, const Top2& b) {
+  const bool bw = b.best > a.best;
+  return Top2{bw ? b.best : a.best, bw ? fmaxf(b.second, a.best) : fmaxf(a.second, b.best),
+              bw ? b.idx : a.idx};
+}
+
+// Top-2 (value, lowest index of the maximum, runner-up value) of 64 register values by a balanced
+// tree: six levels of independent merges instead of a 64-long dependent chain.
+__device__ __forceinline__ Top2 top2_of_64(const float* v) {
+  Top2 t[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = v[2 * i], b = v[2 * i + 1];
+    const bool bw = b > a;
+    t[i] = Top2{bw ? b : a, bw ? a : b, bw ? 2 * i + 1 : 2 * i};
+  }
+#pragma unroll
+  for (int n = 16; n >= 1; n >>= 1) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) t[i] = top2_merge_lr(t[2 * i], t[2 * i + 1]);
+  }
+  return t[0];
 }
 
 // --------------------------------------------------------------------------- main kernel
@@ -227,8 +254,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ch = (warp - 2) / 4;          // column half of every tile: [64*ch, 64*ch + 64)
     const int row_in_half = ew * 32 + lane;
     // running statistics of this thread's rows over the CTA's tiles, in tile order: exact
-    // top-2; the normaliser as S * 2^-40 = sum exp((z - M)/T) relative to the running max M,
-    // rescaled in fp64 when M grows (a fixed order, so the result is deterministic)
+    // top-2; the normaliser S = sum exp((z - M)/T) relative to the running max M, rescaled
+    // when M grows (a fixed order, so the result is deterministic)
     Top2 run[2] = {top2_empty(), top2_empty()};
     int run_bad[2] = {0, 0};
     double run_s[2] = {0.0, 0.0};
@@ -258,66 +285,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                static_cast<uint32_t>((buf * 2 + h) * kTcTileN + ch * (kTcTileN / 2));
         const bool live = q < p.nrows;
         const float T = run_T[h];
-        const float Te = T > 0.f ? T : 1.f;
-        const float invT = __fdiv_rn(1.f, Te);
         float* lrow = (live && T > 0.f && p.logits)
                           ? p.logits + static_cast<size_t>(q) * p.logits_stride + v0
                           : nullptr;
-        Top2 t = top2_empty();
-        int bad = 0;
-        for (int c = 0; c < kTcTileN / 2; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + c, v);  // every lane takes part (the load is warp-collective)
-          if (lrow) {
-            if (p.vec_store && c + 32 <= nv) {
-              float4* dst = reinterpret_cast<float4*>(lrow + c);
+        float v[kTcTileN / 2];
+        tmem_ld64(taddr, v);  // every lane takes part (the load is warp-collective)
+        if (nv <= 0) continue;  // column half past the vocabulary (uniform across the warp)
+        if (lrow) {
+          if (p.vec_store && nv == kTcTileN / 2) {
+            float4* dst = reinterpret_cast<float4*>(lrow);
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            } else {
+            for (int j = 0; j < kTcTileN / 8; ++j)
+              dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c + j < nv) lrow[c + j] = v[j];
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c + j < nv) {
-              const float z = v[j];
-              if (isnan(z) || z == INFINITY)
-                bad = 1;
-              else
-                top2_push(t, z, static_cast<int32_t>(v0 + c + j));
-            }
+            for (int j = 0; j < kTcTileN / 2; ++j)
+              if (j < nv) lrow[j] = v[j];
           }
         }
-        // second pass for the tile's quantised sum; the loads are warp-collective, so every
-        // lane runs them and only the accumulation depends on the lane's own row
-        const bool do_sum = (t.idx != kNoIndex && t.best != -INFINITY);
-        unsigned long long ssum = 0ull;
-        for (int c = 0; c < kTcTileN / 2; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + c, v);
+        if (nv < kTcTileN / 2) {  // ragged last tile: columns past V take no part
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float z = v[j];
-            if (do_sum && c + j < nv && !(isnan(z) || z == INFINITY))
-              ssum += tc_weight(z, t.best, invT);
-          }
+          for (int j = 0; j < kTcTileN / 2; ++j)
+            if (j >= nv) v[j] = -INFINITY;
         }
-        // fold the tile into the running statistics
-        run_bad[h] |= bad;
-        if (do_sum) {
-          const double st = static_cast<double>(ssum);
-          if (run_s[h] == 0.0 && !(run[h].idx != kNoIndex && run[h].best != -INFINITY)) {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < kTcTileN / 2; ++j) bad |= !(v[j] < INFINITY);  // NaN or +inf
+        Top2 t = top2_of_64(v);
+        t.idx += static_cast<int32_t>(v0);
+        run_bad[h] |= bad ? 1 : 0;
+        if (t.best != -INFINITY && !bad) {
+          // the tile's sum of exp((z - m_tile)/T) in fp32 (64 terms in eight chains), folded
+          // into the running fp64 sum with an fp32 rescale factor when the running max moves
+          const float k2 = __fmul_rn(__fdiv_rn(1.f, T > 0.f ? T : 1.f), 1.4426950408889634f);
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < kTcTileN / 2; ++j)
+            acc[j & 7] += exp2f(__fmul_rn(__fsub_rn(v[j], t.best), k2));
+          const double st = static_cast<double>(((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                                                ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+          if (run[h].idx == kNoIndex || run[h].best == -INFINITY) {
             run_s[h] = st;
           } else if (t.best > run[h].best) {
-            run_s[h] = run_s[h] * exp((static_cast<double>(run[h].best) - t.best) / Te) + st;
+            run_s[h] = run_s[h] * static_cast<double>(exp2f(__fmul_rn(__fsub_rn(run[h].best, t.best), k2))) + st;
           } else {
-            run_s[h] += st * exp((static_cast<double>(t.best) - run[h].best) / Te);
+            run_s[h] += st * static_cast<double>(exp2f(__fmul_rn(__fsub_rn(t.best, run[h].best), k2)));
           }
         }
-        if (t.idx != kNoIndex) run[h] = top2_merge(run[h], t);
+        run[h] = top2_merge(run[h], t);
       }
       tc_fence_before();
       __syncwarp();
@@ -361,7 +376,7 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   const int nparts = p.nblocks * kTcSubTiles;
   const GemmPartial* row = p.part + static_cast<size_t>(q) * nparts;
   const float T = p.temperature[q / p.rows_per_req];
-  const float Te = T > 0.f ? T : 1.f;
+  const float k2 = __fmul_rn(__fdiv_rn(1.f, T > 0.f ? T : 1.f), 1.4426950408889634f);
   Top2 t = top2_empty();
   int bad = 0;
   for (int i = tid; i < nparts; i += blockDim.x) {
@@ -392,7 +407,7 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
       const float mc = __ldcg(&row[i].m);
       const double sc = __ldcg(&row[i].s);
       if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY && sc > 0.0)
-        S += sc * exp((static_cast<double>(mc) - static_cast<double>(M)) / static_cast<double>(Te));
+        S += sc * static_cast<double>(exp2f(__fmul_rn(__fsub_rn(mc, M), k2)));
     }
   }
 #pragma unroll
@@ -410,7 +425,7 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
       st.argmax = -1;
     } else {
       st.max = M;
-      st.log_norm = static_cast<float>(log(tot) - 27.725887222397812);  // log(S * 2^-40)
+      st.log_norm = static_cast<float>(log(tot));
       st.gap = __fsub_rn(M, all.second);
       st.argmax = all.idx;
     }

@@ -369,8 +369,8 @@ __global__ void __maxnreg__(128)
       const float mc = __ldcg(&pp->m);
       const unsigned long long sc = __ldcg(&pp->s);
       double f = 0.0;
-      if (!nonfinite && __ldcg(&pp->idx) >= 0 && mc != -INFINITY)
-        f = exp((static_cast<double>(mc) - static_cast<double>(M)) / static_cast<double>(Te));
+      if (!nonfinite && __ldcg(&pp->idx) >= 0 && mc != -INFINITY)  // fp32 factor, fp64 sums
+        f = static_cast<double>(expf(__fmul_rn(__fsub_rn(mc, M), invT)));
       blk_f[cc] = f;
       blk_w[cc] = static_cast<double>(sc) * f;
       S += blk_w[cc];

@@ -77,7 +77,7 @@ struct GemmPartial {  // a row's statistics over one CTA's tiles and one column 
   float second;
   int32_t idx;        // -1 if none
   int32_t flags;      // bit 0: NaN or +Inf seen
-  double s;           // sum of exp((z - m)/T), in units of 2^-40
+  double s;           // sum of exp((z - m)/T)
   double pad;
 };
 static_assert(sizeof(GemmPartial) == 32, "partial is 32 bytes");
