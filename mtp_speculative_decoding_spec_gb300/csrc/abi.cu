@@ -104,6 +104,90 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int next_pow2_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
+// The tensor-core variant (bf16 weights, 16-byte aligned W and H): same parameters, same grid
+// and workspace as the CUDA-core kernel, the vocabulary partitioned in 32-row bands.
+spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int nrows,
+                        int rows_per_req, const float* temperature, float* logits,
+                        int64_t logits_stride, spec_rowstats* stats, int draft,
+                        const uint64_t* seed, const int64_t* pos, int pos_offset,
+                        int32_t* token_out, int token_stride, void* workspace,
+                        const WsLayout& wl, int grid, const DevAttr& a, EncodeTiledFn encode,
+                        cudaStream_t stream) {
+  GemvTcLaunch L;
+  memset(&L, 0, sizeof(L));
+  GemvParams& p = L.p;
+  const int band = gemv_tc_band_rows();
+  const int64_t nbands = (V + band - 1) / band;
+  const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * band);
+  if (tile_cap > gemv_tc_max_block_rows()) return SPEC_ERR_UNSUPPORTED;
+  // after streaming, the ring holds the rows' logit tile and then the epilogue's scratch
+  const size_t after =
+      align_up(static_cast<size_t>(nrows) * tile_cap * 4, 1024) +
+      static_cast<size_t>(gemv_tc_threads() / 32) * 2 * static_cast<size_t>(grid) * sizeof(double);
+  const size_t fixed = 512 + 1024;  // barriers, TMEM slot, flags, temperatures; alignment slack
+  const size_t budget = static_cast<size_t>(a.smem_optin);
+  int stages = 16;
+  size_t ring = 0, smem_total = 0;
+  for (; stages >= 2; --stages) {
+    ring = static_cast<size_t>(stages) * gemv_tc_stage_bytes();
+    if (ring < after) ring = align_up(after, 1024);
+    smem_total = ring + fixed;
+    if (smem_total <= budget) break;
+  }
+  if (stages < 2) return SPEC_ERR_UNSUPPORTED;
+
+  const int64_t row_bytes = d * 2;
+  const cuuint32_t estride[2] = {1, 1};
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(V)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_tc_kblock()),
+                               static_cast<cuuint32_t>(gemv_tc_box_rows())};
+    if (encode(&L.wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride,
+               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_CUDA;
+  }
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(nrows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_tc_kblock()),
+                               static_cast<cuuint32_t>(gemv_tc_h_rows())};
+    if (encode(&L.hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(H), gdim, gstride,
+               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_CUDA;
+  }
+  p.V = V;
+  p.d = static_cast<int>(d);
+  p.nbands = nbands;
+  p.band_rows = band;
+  p.stages = stages;
+  p.stage_bytes = gemv_tc_stage_bytes();
+  p.ring_bytes = static_cast<int>(ring);
+  p.tile_cap = tile_cap;
+  p.H = static_cast<const uint8_t*>(H);
+  p.h_row_bytes = static_cast<int>(row_bytes);
+  p.nrows = nrows;
+  p.rows_per_req = rows_per_req;
+  p.temperature = temperature;
+  p.logits = logits;
+  p.logits_stride = logits_stride;
+  p.stats = stats;
+  p.draft = draft;
+  p.seed = seed;
+  p.pos = pos;
+  p.pos_offset = pos_offset;
+  p.token_out = token_out;
+  p.token_stride = token_stride;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  L.grid = grid;
+  L.smem = static_cast<int>(smem_total);
+  const cudaError_t e = gemv_tc_launch(L, stream);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 // Configure and launch the GEMV for `nrows` rows over the first V rows of W.
 spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const void* H,
                      int nrows, int rows_per_req, const float* temperature, float* logits,
@@ -122,10 +206,15 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   EncodeTiledFn encode = encode_tiled();
   if (!encode) return SPEC_ERR_CUDA;
 
+  const int grid = gemv_grid(V, a.sms);
+  if (wdt == SPEC_BF16 && aligned16(W) && aligned16(H))
+    return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
+                       draft, seed, pos, pos_offset, token_out, token_stride, workspace, wl, grid,
+                       a, encode, stream);
+
   GemvLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
-  const int grid = gemv_grid(V, a.sms);
   const int rp = next_pow2_rows(nrows);
   const int slab_elems = 512 / elt;
   const int nslab = static_cast<int>((d + slab_elems - 1) / slab_elems);
@@ -164,6 +253,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.nslab = nslab;
   p.slab_elems = slab_elems;
   p.nbands = nbands;
+  p.band_rows = kBandRows;
   p.stages = stages;
   p.stage_bytes = stage_bytes;
   p.ring_bytes = static_cast<int>(ring);

@@ -1,0 +1,255 @@
+// LM-head projection of 1..8 rows (verify rows, or one draft row per request) on the tcgen05
+// tensor cores, for bf16 weights, with the same fused row statistics and draft draw as the
+// CUDA-core kernel in gemv.cu.
+//
+// The projection z = H W^T streams W [V, d] once from HBM (lucebox-hub PR #15 "MTP speculative
+// decoding", section "What": the trunk verifies k drafts in one batched forward of k+1 rows
+// through the shared LM head). On the CUDA cores every weight costs one fp32 FMA per row, so at
+// 5..8 rows the FMA pipe, not HBM, sets the pace; here the multiply-adds go to the tensor cores
+// and the kernel is left with streaming alone:
+//   * one persistent CTA per SM owns a contiguous run of 32-row bands of the vocabulary and
+//     walks it in tiles of 128 rows (the last one partial);
+//   * a producer warp loads, per stage, 512 contiguous bytes of each of the tile's weight rows
+//     (four 64-wide k-blocks as 2-D TMA boxes of 32 rows, 128-byte swizzle; only the boxes the
+//     tile needs) and the matching 16-row H blocks (rows past the live ones read as zero) into
+//     a ring of shared-memory stages. Requests of 512 contiguous bytes per row keep HBM far
+//     busier than 128-byte ones;
+//   * one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32, M = 128 weight rows,
+//     N = 16 H rows, K = 16); every tile of the block has its own 16-column TMEM accumulator,
+//     so the shared memory goes to the stages alone (three of 72 KB at any row count);
+//   * four warps (one per TMEM lane quadrant) read each finished accumulator with tcgen05.ld
+//     (lane = vocabulary row, column = H row) and write the logits of rows at T > 0
+//     (coalesced); when streaming is over they copy all accumulators into the block's logit
+//     tile in the now idle stage ring;
+//   * then the same block epilogue as the CUDA-core kernel: per-block top-2 / normaliser
+//     partials, the last block's combine and the draft draw.
+// Batch invariance (section "Exactness": verify stays batch-invariant up to eight rows): every
+// call with bf16 weights runs this kernel whatever the number of rows, H row r always sits in
+// MMA column r, and a column's result depends only on that column's operands.
+#include "gemv_epilogue.cuh"
+#include "tcgen05.cuh"
+
+namespace spec {
+
+constexpr int kSkTileRows = 128;  // weight rows per tile (MMA M)
+constexpr int kSkBoxRows = 32;    // rows per TMA box (and the band of the block partition)
+constexpr int kSkN = 16;          // H rows per MMA (N); rows past the live ones are zero
+constexpr int kSkKBlock = 64;     // bf16 elements per k-block (one 128-byte swizzle row)
+constexpr int kSkKB = 4;          // k-blocks per stage: 512 contiguous bytes of each weight row
+constexpr int kSkBoxBytes = kSkBoxRows * kSkKBlock * 2;  // 4 KB
+constexpr int kSkWBytes = kSkTileRows * kSkKBlock * 2;   // 16 KB per k-block
+constexpr int kSkHBytes = kSkN * kSkKBlock * 2;          // 2 KB per k-block
+constexpr int kSkStageBytes = kSkKB * (kSkWBytes + kSkHBytes);  // 72 KB, a multiple of 1024
+constexpr int kSkThreads = 8 * 32;  // producer, MMA issuer, two idle warps, four drain warps
+constexpr int kSkDrainWarp0 = 4;    // warps 4..7: TMEM lane quadrants 0..3
+constexpr int kSkMaxTiles = 16;     // tiles per block: 16 x 16 = 256 TMEM columns at most
+
+__global__ void __launch_bounds__(kSkThreads, 1)
+    gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                   const __grid_constant__ CUtensorMap hmap, const GemvParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  // the ring of stages; once streaming is over it holds the block's logit tile and then the
+  // epilogue's scratch
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.ring_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* tile_done = empty + S;  // [kSkMaxTiles]: one phase each
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_done + kSkMaxTiles);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last block
+  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] temperature of each row
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int64_t v0, v1;
+  block_rows(blockIdx.x, gridDim.x, p.nbands, kSkBoxRows, p.V, v0, v1);
+  const int nt = static_cast<int>(v1 - v0);
+  const int ntile = (nt + kSkTileRows - 1) / kSkTileRows;
+  const int nkb = (p.d + kSkKBlock - 1) / kSkKBlock;  // k-blocks per row
+  const int nks = (nkb + kSkKB - 1) / kSkKB;           // stages per tile
+  const int nr = min(p.nrows, kMaxRows);
+  // one 16-column accumulator per tile of the block, all resident until the end
+  const int ntile_cap = (p.tile_cap + kSkTileRows - 1) / kSkTileRows;
+  uint32_t tcols = 32;
+  while (tcols < static_cast<uint32_t>(ntile_cap * kSkN)) tcols <<= 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < kSkMaxTiles; ++t) mbar_init(&tile_done[t], 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (tid < kMaxRows)
+    s_temp[tid] = (tid < p.nrows && p.logits) ? p.temperature[tid / p.rows_per_req] : 0.f;
+  if (warp == 1) tmem_alloc(tmem_slot, tcols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0, s = 0;
+      for (int t = 0; t < ntile && !*reinterpret_cast<volatile int*>(&flags[0]); ++t) {
+        const int rows = min(kSkTileRows, nt - t * kSkTileRows);
+        const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
+        const int y = static_cast<int>(v0) + t * kSkTileRows;
+        bool ok = true;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          // stage s is reused every S iterations: wait until the MMAs of its last use are done
+          if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((it / S) & 1) ^ 1))) {
+            atomicOr(&p.hdr->error, ERR_TC_WAIT);
+            atomicExch(&flags[0], 1);
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
+          const int nk = min(kSkKB, nkb - ks * kSkKB);  // k-blocks in this stage
+          mbar_arrive_expect_tx(&full[s],
+                                static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
+          for (int kk = 0; kk < nk; ++kk) {
+            const int x = (ks * kSkKB + kk) * kSkKBlock;
+            for (int b = 0; b < nbox; ++b)
+              tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, y + b * kSkBoxRows,
+                             &full[s]);
+            tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
+          }
+          if (++s == S) s = 0;
+        }
+        if (!ok) break;
+      }
+      // every issued copy must have landed before the ring is reused or the block exits
+      for (int j = max(0, it - S); j < it; ++j) {
+        if (!mbar_wait_bounded(&full[j % S], static_cast<uint32_t>((j / S) & 1))) {
+          atomicOr(&p.hdr->error, ERR_GEMV_DRAIN);
+          break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(kSkTileRows, kSkN);
+      int it = 0, s = 0;
+      for (int t = 0; t < ntile; ++t) {
+        const uint32_t dacc = tmem_base + static_cast<uint32_t>(t * kSkN);
+        bool ok = true;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
+            atomicOr(&p.hdr->error, ERR_TC_WAIT);
+            atomicExch(&flags[0], 1);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(ring + static_cast<size_t>(s) * kSkStageBytes);
+          const int nk = min(kSkKB, nkb - ks * kSkKB);
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint32_t a = st + kk * kSkWBytes, b = st + kSkKB * kSkWBytes + kk * kSkHBytes;
+#pragma unroll
+            for (int k16 = 0; k16 < kSkKBlock / 16; ++k16)
+              tc_mma(dacc, smem_desc_sw128(a + k16 * 32), smem_desc_sw128(b + k16 * 32), idesc,
+                     (ks > 0 || kk > 0 || k16 > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
+          if (++s == S) s = 0;
+        }
+        if (!ok) break;
+        tc_commit(&tile_done[t]);  // the tile's accumulator is complete
+      }
+    }
+  } else if (warp >= kSkDrainWarp0) {
+    // ---------------------------------------- logits of rows at T > 0, tile by tile
+    const int ew = warp & 3;  // TMEM lane quadrant this warp may access
+    bool hot = false;
+    for (int r = 0; r < nr; ++r) hot |= s_temp[r] > 0.f;
+    for (int t = 0; t < ntile; ++t) {
+      if (!mbar_wait_bounded(&tile_done[t], 0u)) {
+        atomicOr(&p.hdr->error, ERR_TC_WAIT);
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      if (hot) {
+        tc_fence_after();
+        float v[8];
+        tmem_ld8(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                     static_cast<uint32_t>(t * kSkN),
+                 v);  // warp-collective: every lane takes part
+        const int local = t * kSkTileRows + ew * 32 + lane;
+        if (local < nt) {
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r)
+            if (r < nr && s_temp[r] > 0.f)
+              p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = v[r];
+        }
+      }
+    }
+  }
+
+  // every tile's MMAs have completed and every copy has landed: the ring is free
+  tc_fence_before();
+  __syncthreads();
+  float* ztile = reinterpret_cast<float*>(ring);  // [nrows][tile_cap]
+  if (warp >= kSkDrainWarp0 && !*reinterpret_cast<volatile int*>(&flags[0])) {
+    tc_fence_after();
+    const int ew = warp & 3;
+    for (int t = 0; t < ntile; ++t) {
+      float v[8];
+      tmem_ld8(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                   static_cast<uint32_t>(t * kSkN),
+               v);
+      const int local = t * kSkTileRows + ew * 32 + lane;
+      if (local < nt) {
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r)
+          if (r < nr) ztile[static_cast<size_t>(r) * p.tile_cap + local] = v[r];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+  uint8_t* scratch = ring + ((static_cast<size_t>(nr) * p.tile_cap * sizeof(float) + 1023) &
+                             ~static_cast<size_t>(1023));
+  gemv_block_epilogue(p, ztile, v0, nt, scratch, flags, kSkThreads / 32);
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------
+
+int gemv_tc_band_rows() { return kSkBoxRows; }
+int gemv_tc_box_rows() { return kSkBoxRows; }
+int gemv_tc_kblock() { return kSkKBlock; }
+int gemv_tc_h_rows() { return kSkN; }
+int gemv_tc_stage_bytes() { return kSkStageBytes; }
+int gemv_tc_threads() { return kSkThreads; }
+int gemv_tc_max_block_rows() { return kSkMaxTiles * kSkTileRows; }
+
+cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream) {
+  static int configured_smem = 0;
+  if (L.smem > configured_smem) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+    if (e != cudaSuccess) return e;
+    configured_smem = L.smem;
+  }
+  int fit = 0;  // shared memory must admit one block per SM
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_tc_kernel, kSkThreads, L.smem);
+  if (e != cudaSuccess) return e;
+  if (fit < 1) return cudaErrorLaunchOutOfResources;
+  gemv_tc_kernel<<<L.grid, kSkThreads, L.smem, stream>>>(L.wmap, L.hmap, L.p);
+  return cudaGetLastError();
+}
+
+}  // namespace spec

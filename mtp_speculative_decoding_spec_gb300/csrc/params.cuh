@@ -12,7 +12,8 @@ struct GemvParams {
   int d;            // hidden size
   int nslab;        // 512-byte k-slabs per weight row
   int slab_elems;   // elements per slab
-  int64_t nbands;   // 60-row bands over V
+  int64_t nbands;   // bands of band_rows rows over V (the unit of the block partition)
+  int band_rows;    // 60 (CUDA-core kernel) or 32 (tensor-core kernel)
   int stages;
   int stage_bytes;  // one slab of one band: 60 rows x 512 bytes
   int ring_bytes;   // >= stages * stage_bytes; the last block reuses it as scratch
@@ -112,6 +113,23 @@ int gemm_tc_kblock();
 int gemm_tc_subtiles();
 
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
+
+// Tensor-core variant of the 1..8-row projection for bf16 weights: see gemv_tc.cu.
+struct GemvTcLaunch {
+  int grid, smem;
+  CUtensorMap wmap;  // W [V][d] bf16, box [32 rows][64], 128-byte swizzle
+  CUtensorMap hmap;  // H [nrows][d] bf16, box [16 rows][64], 128-byte swizzle
+  GemvParams p;
+};
+
+cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream);
+int gemv_tc_band_rows();
+int gemv_tc_box_rows();
+int gemv_tc_kblock();
+int gemv_tc_h_rows();
+int gemv_tc_stage_bytes();
+int gemv_tc_threads();
+int gemv_tc_max_block_rows();
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
 cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
                           cudaStream_t stream);

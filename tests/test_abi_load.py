@@ -119,7 +119,7 @@ def test_no_cpu_fallback_in_product_package():
 
 
 # threads per block of each kernel, as launched by abi.cu / gemv.cu
-_BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemm_rows_tc_kernel": 10 * 32,
+_BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemm_rows_tc_kernel": 10 * 32,
                   "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_kernel": 256}
 
 
