@@ -120,10 +120,9 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   const int64_t nbands = (V + band - 1) / band;
   const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * band);
   if (tile_cap > gemv_tc_max_block_rows()) return SPEC_ERR_UNSUPPORTED;
-  // after streaming, the ring holds the rows' logit tile and then the epilogue's scratch
+  // after streaming, the ring holds the per-block statistics and then the combine's scratch
   const size_t after =
-      align_up(static_cast<size_t>(nrows) * tile_cap * 4, 1024) +
-      static_cast<size_t>(gemv_tc_threads() / 32) * 2 * static_cast<size_t>(grid) * sizeof(double);
+      static_cast<size_t>(gemv_tc_stat_bytes()) + gemv_finish_scratch_bytes(grid);
   const size_t fixed = 512 + 1024;  // barriers, TMEM slot, flags, temperatures; alignment slack
   const size_t budget = static_cast<size_t>(a.smem_optin);
   int stages = 16;
@@ -207,7 +206,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   if (!encode) return SPEC_ERR_CUDA;
 
   const int grid = gemv_grid(V, a.sms);
-  if (wdt == SPEC_BF16 && aligned16(W) && aligned16(H))
+  if (wdt == SPEC_BF16)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, workspace, wl, grid,
                        a, encode, stream);
@@ -224,8 +223,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const int pairs = (elt == 2) ? 4 : 2;
   const int row_pairs = rp >= 2 ? rp / 2 : 1;
   const size_t hs_bytes = static_cast<size_t>(nslab) * pairs * row_pairs * 32 * 16;
-  // the last block reuses the stage ring for two doubles per block per warp
-  const size_t scratch = static_cast<size_t>(kGemvThreads / 32) * 2 * grid * sizeof(double);
+  // the last block reuses the stage ring for the combine's scratch
+  const size_t scratch = gemv_finish_scratch_bytes(grid);
   const size_t fixed = hs_bytes + static_cast<size_t>(rp) * tile_cap * 4 + 128;  // + flags, temps
   const size_t budget = static_cast<size_t>(a.smem_optin);
   int stages = 8;

@@ -187,9 +187,19 @@ __device__ __forceinline__ unsigned long long cdf_target(uint32_t u24, unsigned 
   return (hi << 40) | (lo >> 24);
 }
 
-// Quantise a weight in [0, 1] to integer units of 2^-40 (round to nearest).
+// Quantise a weight in [0, 1] to integer units of 2^-40, rounded to nearest (ties to even),
+// without a 64-bit conversion instruction (those run on the narrow FP64 path): x = w * 2^40 is
+// exact in fp32; below 2^23 adding 2^23 rounds x to an integer held in the low significand
+// bits; from 2^23 up x is already an integer, rebuilt from its significand and exponent. Zero,
+// negative inputs, NaN and x >= 2^41 (none of which the callers produce) give 0.
 __device__ __forceinline__ unsigned long long quantise(float w) {
-  return __float2ull_rn(__fmul_rn(w, kQuantScale));
+  const float x = __fmul_rn(w, kQuantScale);
+  const uint32_t small = __float_as_uint(__fadd_rn(x, 8388608.f)) - 0x4B000000u;
+  const uint32_t b = __float_as_uint(x);
+  const unsigned long long big = static_cast<unsigned long long>((b & 0x7FFFFFu) | 0x800000u)
+                                 << (((b >> 23) - 150u) & 63u);
+  // both forms are computed and one is selected: no divergent branch per element
+  return (x < 8388608.f) ? ((x > 0.f) ? small : 0ull) : ((x < 2199023255552.f) ? big : 0ull);
 }
 
 // ----------------------------------------------------------------------------------------

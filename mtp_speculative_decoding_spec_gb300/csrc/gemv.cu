@@ -1,12 +1,13 @@
-// LM-head projection of 1..8 rows (verify rows, or one draft row per request) with the row
+// LM-head projection of 1..8 rows (verify rows, or one draft row per request) on the CUDA
+// cores, for fp32 weights (bf16 weights run on the tensor cores, gemv_tc.cu), with the row
 // statistics and, for the draft head, the token choice fused in.
 //
 // Shape of the work (lucebox-hub PR #15 "MTP speculative decoding", section "What": the trunk
 // verifies k drafts in one batched forward of k+1 rows through the shared LM head; the draft
 // head covers the first 64,000 vocabulary rows and picks its token on the GPU): z = H W^T with
-// W [V, d] bf16 (or fp32) streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming
-// GEMV: the weight bytes bound it, so the design is about keeping HBM busy with few
-// instructions per weight byte:
+// W [V, d] streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming GEMV: the weight
+// bytes bound it, so the design is about keeping HBM busy with few instructions per weight
+// byte (the kernel is templated on the weight type; only fp32 is instantiated):
 //   * one persistent block per SM; the vocabulary is cut into 60-row bands and block c owns a
 //     contiguous run of bands (balanced to one band, no wave tail, the same cut for any number
 //     of rows);
@@ -23,7 +24,7 @@
 //     sum of exp((z - m)/T) quantised to 2^-40 units in 64-bit integers (exact, so the sum
 //     does not depend on order either), and the last block to finish combines the per-block
 //     partials; for the draft head at T > 0 it also draws the token by inverse CDF and writes
-//     it to device memory.
+//     it to device memory (gemv_epilogue.cuh, shared with the tensor-core kernel).
 #include <math.h>
 
 #include "gemv_epilogue.cuh"
@@ -300,14 +301,7 @@ static cudaError_t launch_variant(const GemvLaunch& L, cudaStream_t stream) {
 }
 
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream) {
-  if (bf16) {
-    switch (rp) {
-      case 1: return launch_variant<1, true>(L, stream);
-      case 2: return launch_variant<2, true>(L, stream);
-      case 4: return launch_variant<4, true>(L, stream);
-      default: return launch_variant<8, true>(L, stream);
-    }
-  }
+  if (bf16) return cudaErrorNotSupported;  // bf16 weights run on the tensor cores (gemv_tc.cu)
   switch (rp) {
     case 1: return launch_variant<1, false>(L, stream);
     case 2: return launch_variant<2, false>(L, stream);

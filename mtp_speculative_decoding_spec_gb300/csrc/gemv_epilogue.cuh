@@ -20,10 +20,10 @@ __device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, in
   if (v1 < v0) v1 = v0;
 }
 
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// uint64 (below 2^53) to fp32 from its two 32-bit halves: 32-bit conversions only.
+__device__ __forceinline__ float u64_to_f32(unsigned long long v) {
+  return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(v >> 32)), 4294967296.f,
+                   __uint2float_rn(static_cast<uint32_t>(v)));
 }
 
 // Weight of one logit in the tile's integer sum: exp((z - m) / T) in [0, 1], in 2^-40 units.
@@ -33,17 +33,13 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
   return quantise(expf(__fmul_rn(__fsub_rn(z, m), invT)));
 }
 
-// Per-block partials, ticket and (last block) the combine and the draft draw. All `nwarps`
-// warps of the block call it after a __syncthreads that publishes ztile; `scratch` needs
-// nwarps * 2 * gridDim.x doubles; flags[1] is a free shared int.
-static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, const float* ztile,
-                                                           int64_t v0, int nt, uint8_t* scratch,
-                                                           int* flags, int nwarps) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int GR = gridDim.x, blk = blockIdx.x;
-  const int NWALL = nwarps;
-  // ---------------- per-block partial statistics of each row ----------------
-  for (int q = warp; q < p.nrows; q += NWALL) {
+// One block's partial statistics of each row from its logit tile in shared memory: top-2 and
+// NaN / +Inf flag, and the exact integer sum of tile_weight(z, m) relative to the block max m.
+// Called by all `nwarps` warps after a __syncthreads that publishes ztile.
+static __device__ __forceinline__ void gemv_block_partials(const GemvParams& p, const float* ztile,
+                                                           int64_t v0, int nt, int nwarps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int q = warp; q < p.nrows; q += nwarps) {
     const float T = p.temperature[q / p.rows_per_req];
     const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
     const float* zr = ztile + static_cast<size_t>(q) * p.tile_cap;
@@ -74,9 +70,19 @@ static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, 
       pp.flags = bad;
       pp.s = ssum;
       pp.pad = 0ull;
-      p.part[static_cast<size_t>(blk) * kMaxRows + q] = pp;
+      p.part[static_cast<size_t>(blockIdx.x) * kMaxRows + q] = pp;
     }
   }
+}
+
+// After every block has written its partials: the ticket, and in the last block the combine
+// of each row's partials into its statistics and, for the draft head, the token. All `nwarps`
+// (>= 8) warps call it; `scratch` (free shared memory, 8-byte aligned) needs
+// gemv_finish_scratch_bytes(gridDim.x) bytes; flags[1] is a free shared int.
+static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t* scratch,
+                                                   int* flags, int nwarps) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int GR = gridDim.x;
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -88,38 +94,61 @@ static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, 
   __threadfence();
 
   // ---------------- last block: combine the partials of every block ----------------
-  // The scratch (free shared memory) holds per-block weights and scale factors.
-  double* blk_w = reinterpret_cast<double*>(scratch) + static_cast<size_t>(warp) * 2 * GR;
-  double* blk_f = blk_w + GR;
-  for (int q = warp; q < p.nrows; q += NWALL) {
+  // All threads first copy the partials of every (block, row) into shared memory in one round
+  // of loads. Row q's region of the scratch holds blk_s (uint64 integer sums), blk_m (block
+  // maxima, later the scale factors f = exp((m_c - M)/T)), blk_w (runners-up, later the block
+  // weights s_c * f) and blk_i (argmax indices). The combine runs in fp32 (a fixed order, so
+  // deterministic; relative error ~1e-6), keeping the 64-bit work on the integer units.
+  const int nr = min(p.nrows, kMaxRows);
+  const size_t rstride = gemv_finish_row_bytes(GR);
+  int* s_rbad = reinterpret_cast<int*>(scratch + kMaxRows * rstride);  // [8]
+  if (tid < kMaxRows) s_rbad[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < GR * nr; i += blockDim.x) {
+    const int cc = i / nr, q = i - cc * nr;
+    const uint4* pp = reinterpret_cast<const uint4*>(p.part + static_cast<size_t>(cc) * kMaxRows + q);
+    const uint4 a = __ldcg(pp), b = __ldcg(pp + 1);
+    uint8_t* base = scratch + q * rstride;
+    const int32_t idx = static_cast<int32_t>(a.z);
+    reinterpret_cast<unsigned long long*>(base)[cc] = (static_cast<unsigned long long>(b.y) << 32) | b.x;
+    reinterpret_cast<float*>(base + 8 * GR)[cc] = (idx >= 0) ? __uint_as_float(a.x) : -INFINITY;
+    reinterpret_cast<float*>(base + 12 * GR)[cc] = __uint_as_float(a.y);
+    reinterpret_cast<int32_t*>(base + 16 * GR)[cc] = idx;
+    if (a.w) atomicOr(&s_rbad[q], 1);
+  }
+  __syncthreads();
+  for (int q = warp; q < nr; q += nwarps) {
+    uint8_t* base = scratch + q * rstride;
+    unsigned long long* blk_s = reinterpret_cast<unsigned long long*>(base);
+    float* blk_m = reinterpret_cast<float*>(base + 8 * GR);
+    float* blk_w = reinterpret_cast<float*>(base + 12 * GR);
+    const int32_t* blk_i = reinterpret_cast<const int32_t*>(base + 16 * GR);
     const float T = p.temperature[q / p.rows_per_req];
     const float Te = T > 0.f ? T : 1.f;
     const float invT = __fdiv_rn(1.f, Te);
+    // the draw's inputs are fetched now so that their latency overlaps the combine
+    const uint64_t seed_q = (p.draft && T > 0.f) ? p.seed[q] : 0ull;
+    const int64_t pos_q = (p.draft && T > 0.f) ? p.pos[q] : 0;
     Top2 t = top2_empty();
-    int bad = 0;
     for (int cc = lane; cc < GR; cc += 32) {
-      const GemvPartial* pp = p.part + static_cast<size_t>(cc) * kMaxRows + q;
-      bad |= __ldcg(&pp->flags);
-      const int32_t idx = __ldcg(&pp->idx);
-      if (idx >= 0) t = top2_merge(t, Top2{__ldcg(&pp->m), __ldcg(&pp->second), idx});
+      const int32_t idx = blk_i[cc];
+      if (idx >= 0) t = top2_merge(t, Top2{blk_m[cc], blk_w[cc], idx});
     }
+    int bad = s_rbad[q];
     t = warp_top2(t);
-    bad = __any_sync(0xffffffffu, bad);
     const bool nonfinite = bad || t.idx == kNoIndex || t.best == -INFINITY;
     const float M = t.best;
-    double S = 0.0;
-    for (int cc = lane; cc < GR; cc += 32) {
-      const GemvPartial* pp = p.part + static_cast<size_t>(cc) * kMaxRows + q;
-      const float mc = __ldcg(&pp->m);
-      const unsigned long long sc = __ldcg(&pp->s);
-      double f = 0.0;
-      if (!nonfinite && __ldcg(&pp->idx) >= 0 && mc != -INFINITY)  // fp32 factor, fp64 sums
-        f = static_cast<double>(expf(__fmul_rn(__fsub_rn(mc, M), invT)));
-      blk_f[cc] = f;
-      blk_w[cc] = static_cast<double>(sc) * f;
-      S += blk_w[cc];
+    float S = 0.f;
+    for (int cc = lane; cc < GR; cc += 32) {  // entries this lane read above
+      const float mc = blk_m[cc];
+      float f = 0.f;
+      if (!nonfinite && mc != -INFINITY) f = expf(__fmul_rn(__fsub_rn(mc, M), invT));
+      blk_m[cc] = f;
+      blk_w[cc] = __fmul_rn(u64_to_f32(blk_s[cc]), f);
+      S = __fadd_rn(S, blk_w[cc]);
     }
-    S = warp_sum_f64(S);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
     spec_rowstats st;
     if (nonfinite) {
       st.max = __int_as_float(0x7fc00000);
@@ -128,7 +157,7 @@ static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, 
       st.argmax = -1;
     } else {
       st.max = M;
-      st.log_norm = static_cast<float>(log(S) - 27.725887222397812);  // log(S * 2^-40)
+      st.log_norm = __fsub_rn(logf(S), 27.725887222397812f);  // log(S * 2^-40)
       st.gap = __fsub_rn(M, t.second);
       st.argmax = t.idx;
     }
@@ -138,66 +167,102 @@ static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, 
       int32_t tok = -1;
       if (!nonfinite && !(T > 0.f)) tok = t.idx;
       if (!nonfinite && T > 0.f && p.logits) {
-        // inverse CDF: first block whose cumulative weight exceeds u*S, then the first token
-        // inside it whose cumulative integer weight exceeds the remainder
+        // inverse CDF: the first block whose cumulative weight exceeds u*S, then the first token
+        // inside it whose cumulative integer weight exceeds the remainder. Each lane walks a
+        // contiguous chunk of blocks from its exclusive prefix; the first lane with a hit wins.
         __syncwarp();
-        const uint32_t u24 = uniform_u24(p.seed[q], p.pos[q] + p.pos_offset, PURPOSE_DRAFT);
-        const double target = static_cast<double>(u24) * 5.9604644775390625e-08 * S;
-        int cstar = -1;
-        unsigned long long tt = 0ull;
-        if (lane == 0) {
-          double cum = 0.0;
-          int last_nz = -1;
-          for (int cc = 0; cc < GR; ++cc) {
-            const double w = blk_w[cc];
-            if (w > 0.0) last_nz = cc;
-            if (w > 0.0 && cum + w > target) {
-              cstar = cc;
-              break;
-            }
-            cum += w;
-          }
-          const GemvPartial* pp;
-          if (cstar >= 0) {
-            pp = p.part + static_cast<size_t>(cstar) * kMaxRows + q;
-            const unsigned long long sc = __ldcg(&pp->s);
-            double rem = (target - cum) / blk_f[cstar];
-            if (!(rem >= 0.0)) rem = 0.0;
-            tt = static_cast<unsigned long long>(rem);
-            if (tt >= sc) tt = sc - 1ull;
-          } else {
-            cstar = last_nz;
-            if (cstar >= 0) {
-              pp = p.part + static_cast<size_t>(cstar) * kMaxRows + q;
-              tt = __ldcg(&pp->s) - 1ull;
-            }
-          }
+        const uint32_t u24 = uniform_u24(seed_q, pos_q + p.pos_offset, PURPOSE_DRAFT);
+        const float target = __fmul_rn(__fmul_rn(static_cast<float>(u24), 5.9604644775390625e-08f), S);
+        const int nb = (GR + 31) / 32;
+        const int b_lo = min(GR, lane * nb), b_hi = min(GR, b_lo + nb);
+        float lsum = 0.f;
+        for (int cc = b_lo; cc < b_hi; ++cc) lsum = __fadd_rn(lsum, blk_w[cc]);
+        float incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float up = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl = __fadd_rn(incl, up);
         }
-        cstar = __shfl_sync(0xffffffffu, cstar, 0);
-        tt = __shfl_sync(0xffffffffu, tt, 0);
+        float cum = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) cum = 0.f;
+        int hit = -1, last_nz = -1;
+        float cum_hit = 0.f;
+        for (int cc = b_lo; cc < b_hi; ++cc) {
+          const float w = blk_w[cc];
+          if (w > 0.f) last_nz = cc;
+          if (hit < 0 && w > 0.f && __fadd_rn(cum, w) > target) {
+            hit = cc;
+            cum_hit = cum;
+          }
+          cum = __fadd_rn(cum, w);
+        }
+        const unsigned hmask = __ballot_sync(0xffffffffu, hit >= 0);
+        int cstar;
+        unsigned long long tt = 0ull;
+        if (hmask) {
+          const int L = __ffs(hmask) - 1;
+          cstar = __shfl_sync(0xffffffffu, hit, L);
+          cum_hit = __shfl_sync(0xffffffffu, cum_hit, L);
+          const unsigned long long sc = blk_s[cstar];
+          float rem = __fdiv_rn(__fsub_rn(target, cum_hit), blk_m[cstar]);  // blk_m holds f now
+          if (!(rem >= 0.f)) rem = 0.f;
+          tt = (rem < 1.8446744e19f) ? __float2ull_rd(rem) : sc;
+          if (tt >= sc) tt = sc - 1ull;
+        } else {  // rounding left u*S past the total: the last block with weight
+          cstar = last_nz;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) cstar = max(cstar, __shfl_xor_sync(0xffffffffu, cstar, o));
+          if (cstar >= 0) tt = blk_s[cstar] - 1ull;
+        }
         if (cstar >= 0) {
+          // the block's logits in per-lane chunks: integer weights, an exclusive scan of the
+          // chunk sums, then the warp walks the one chunk that holds the target
           int64_t c0, c1;
           block_rows(cstar, GR, p.nbands, p.band_rows, p.V, c0, c1);
           const float mc = __ldcg(&(p.part + static_cast<size_t>(cstar) * kMaxRows + q)->m);
           const float* yrow = p.logits + static_cast<size_t>(q) * p.logits_stride;
-          unsigned long long carry = 0ull;
-          for (int64_t base = c0; base < c1 && tok < 0; base += 32) {
-            const int64_t v = base + lane;
-            unsigned long long w = 0ull;
-            if (v < c1) {
-              const float z = __ldcg(yrow + v);
-              if (!(isnan(z) || z == INFINITY)) w = tile_weight(z, mc, invT);
-            }
-            unsigned long long incl = w;
+          const int64_t n2 = (c1 - c0 + 31) / 32;
+          const int64_t lo = min(c1, c0 + lane * n2), hi = min(c1, lo + n2);
+          unsigned long long lw = 0ull;
+          for (int64_t base = lo; base < hi; base += 8) {  // eight loads in flight per lane
+            float z[8];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const unsigned long long up = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += up;
+            for (int u = 0; u < 8; ++u) z[u] = (base + u < hi) ? __ldcg(yrow + base + u) : -INFINITY;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (base + u < hi && !(isnan(z[u]) || z[u] == INFINITY))
+                lw += tile_weight(z[u], mc, invT);
+          }
+          unsigned long long inc = lw;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long up = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += up;
+          }
+          const unsigned lmask = __ballot_sync(0xffffffffu, lw > 0ull && inc > tt);
+          if (lmask) {
+            // the whole warp walks the winning lane's chunk, 32 tokens per round
+            const int L = __ffs(lmask) - 1;
+            unsigned long long carry = __shfl_sync(0xffffffffu, inc - lw, L);  // exact
+            const int64_t clo = __shfl_sync(0xffffffffu, lo, L);
+            const int64_t chi = __shfl_sync(0xffffffffu, hi, L);
+            for (int64_t base = clo; base < chi && tok < 0; base += 32) {
+              const int64_t v = base + lane;
+              unsigned long long w = 0ull;
+              if (v < chi) {
+                const float z = __ldcg(yrow + v);
+                if (!(isnan(z) || z == INFINITY)) w = tile_weight(z, mc, invT);
+              }
+              unsigned long long incl = w;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long up = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += up;
+              }
+              const unsigned mask = __ballot_sync(0xffffffffu, w > 0ull && carry + incl > tt);
+              if (mask) tok = static_cast<int32_t>(base + __ffs(mask) - 1);
+              carry += __shfl_sync(0xffffffffu, incl, 31);
             }
-            const bool hit = (w > 0ull) && (carry + incl > tt);
-            const unsigned mask = __ballot_sync(0xffffffffu, hit);
-            if (mask) tok = static_cast<int32_t>(base + __ffs(mask) - 1);
-            carry += __shfl_sync(0xffffffffu, incl, 31);
           }
         }
       }
@@ -205,6 +270,14 @@ static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, 
     }
   }
   if (tid == 0) p.hdr->gemv_ticket = 0u;
+}
+
+// Partials from the block's logit tile, then gemv_finish.
+static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, const float* ztile,
+                                                           int64_t v0, int nt, uint8_t* scratch,
+                                                           int* flags, int nwarps) {
+  gemv_block_partials(p, ztile, v0, nt, nwarps);
+  gemv_finish(p, scratch, flags, nwarps);
 }
 
 }  // namespace spec

@@ -18,11 +18,13 @@
 //     N = 16 H rows, K = 16); every tile of the block has its own 16-column TMEM accumulator,
 //     so the shared memory goes to the stages alone (three of 72 KB at any row count);
 //   * four warps (one per TMEM lane quadrant) read each finished accumulator with tcgen05.ld
-//     (lane = vocabulary row, column = H row) and write the logits of rows at T > 0
-//     (coalesced); when streaming is over they copy all accumulators into the block's logit
-//     tile in the now idle stage ring;
-//   * then the same block epilogue as the CUDA-core kernel: per-block top-2 / normaliser
-//     partials, the last block's combine and the draft draw.
+//     (lane = vocabulary row, column = H row), write the logits of rows at T > 0 (coalesced)
+//     and keep a running top-2 of each row while the next tiles stream in; when streaming is
+//     over they merge the quadrants into the block max m and sum the integer weights
+//     rint(exp((z - m)/T) 2^40) of the block's logits straight from TMEM, so the block's
+//     partials cost one pass over TMEM and no logit tile in shared memory;
+//   * then the same finish as the CUDA-core kernel: the last block's combine and the draft
+//     draw.
 // Batch invariance (section "Exactness": verify stays batch-invariant up to eight rows): every
 // call with bf16 weights runs this kernel whatever the number of rows, H row r always sits in
 // MMA column r, and a column's result depends only on that column's operands.
@@ -43,6 +45,7 @@ constexpr int kSkStageBytes = kSkKB * (kSkWBytes + kSkHBytes);  // 72 KB, a mult
 constexpr int kSkThreads = 8 * 32;  // producer, MMA issuer, two idle warps, four drain warps
 constexpr int kSkDrainWarp0 = 4;    // warps 4..7: TMEM lane quadrants 0..3
 constexpr int kSkMaxTiles = 16;     // tiles per block: 16 x 16 = 256 TMEM columns at most
+constexpr int kSkStatBytes = 1024;  // start of the idle ring: per-quadrant top-2, row sums
 
 __global__ void __launch_bounds__(kSkThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -51,8 +54,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  // the ring of stages; once streaming is over it holds the block's logit tile and then the
-  // epilogue's scratch
+  // the ring of stages; once streaming is over it holds the block's statistics and then the
+  // combine's scratch
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.ring_bytes);
   uint64_t* empty = full + S;
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_done + kSkMaxTiles);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last block
   float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] temperature of each row
+  float* s_invT = s_temp + kMaxRows;                     // [8] 1 / T (1 at T = 0)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int64_t v0, v1;
@@ -84,13 +88,25 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     flags[1] = 0;
     fence_mbar_init();
   }
-  if (tid < kMaxRows)
-    s_temp[tid] = (tid < p.nrows && p.logits) ? p.temperature[tid / p.rows_per_req] : 0.f;
+  if (tid < kMaxRows) {
+    const float T = (tid < p.nrows) ? p.temperature[tid / p.rows_per_req] : 1.f;
+    s_temp[tid] = (tid < p.nrows && p.logits) ? T : 0.f;
+    s_invT[tid] = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+  }
   if (warp == 1) tmem_alloc(tmem_slot, tcols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // running top-2 and NaN / +Inf flag of each row over this warp's TMEM lane quadrant (drain
+  // warps only)
+  Top2 run[kMaxRows];
+  int rbad[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    run[r] = top2_empty();
+    rbad[r] = 0;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -165,7 +181,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       }
     }
   } else if (warp >= kSkDrainWarp0) {
-    // ---------------------------------------- logits of rows at T > 0, tile by tile
+    // -------------- per finished tile: logits of rows at T > 0, running top-2 of each row
     const int ew = warp & 3;  // TMEM lane quadrant this warp may access
     bool hot = false;
     for (int r = 0; r < nr; ++r) hot |= s_temp[r] > 0.f;
@@ -175,40 +191,94 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         atomicExch(&flags[0], 1);
         break;
       }
-      if (hot) {
-        tc_fence_after();
-        float v[8];
-        tmem_ld8(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                     static_cast<uint32_t>(t * kSkN),
-                 v);  // warp-collective: every lane takes part
-        const int local = t * kSkTileRows + ew * 32 + lane;
-        if (local < nt) {
+      tc_fence_after();
+      float v[8];
+      tmem_ld8(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                   static_cast<uint32_t>(t * kSkN),
+               v);  // warp-collective: every lane takes part
+      const int local = t * kSkTileRows + ew * 32 + lane;
+      const bool valid = local < nt;
+      if (hot && valid) {
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r)
-            if (r < nr && s_temp[r] > 0.f)
-              p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = v[r];
+        for (int r = 0; r < kMaxRows; ++r)
+          if (r < nr && s_temp[r] > 0.f)
+            p.logits[static_cast<size_t>(r) * p.logits_stride + v0 + local] = v[r];
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < nr) {
+          const float z = v[r];
+          const bool nf = isnan(z) || z == INFINITY;
+          Top2 c = (valid && !nf) ? Top2{z, -INFINITY, static_cast<int32_t>(v0 + local)}
+                                  : top2_empty();
+          c = warp_top2(c);
+          rbad[r] |= __any_sync(0xffffffffu, valid && nf) ? 1 : 0;
+          run[r] = top2_merge(run[r], c);
         }
       }
     }
   }
 
-  // every tile's MMAs have completed and every copy has landed: the ring is free
+  // every tile's MMAs have completed (the drain warps waited for each) and every copy has
+  // landed (the producer waited for each): the ring is free for the block's statistics
   tc_fence_before();
   __syncthreads();
-  float* ztile = reinterpret_cast<float*>(ring);  // [nrows][tile_cap]
-  if (warp >= kSkDrainWarp0 && !*reinterpret_cast<volatile int*>(&flags[0])) {
-    tc_fence_after();
-    const int ew = warp & 3;
-    for (int t = 0; t < ntile; ++t) {
-      float v[8];
-      tmem_ld8(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                   static_cast<uint32_t>(t * kSkN),
-               v);
-      const int local = t * kSkTileRows + ew * 32 + lane;
-      if (local < nt) {
+  Top2* s_top = reinterpret_cast<Top2*>(ring);                             // [4 quadrants][8]
+  int* s_bad = reinterpret_cast<int*>(ring + 4 * kMaxRows * sizeof(Top2));  // [4][8]
+  unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(ring + 512);  // [8]
+  if (warp >= kSkDrainWarp0 && lane == 0) {
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r)
-          if (r < nr) ztile[static_cast<size_t>(r) * p.tile_cap + local] = v[r];
+    for (int r = 0; r < kMaxRows; ++r) {
+      s_top[(warp & 3) * kMaxRows + r] = run[r];
+      s_bad[(warp & 3) * kMaxRows + r] = rbad[r];
+    }
+  }
+  if (tid < kMaxRows) s_sum[tid] = 0ull;
+  __syncthreads();
+
+  // block max of each row (the four quadrants merged in a fixed order), then the exact integer
+  // sum of tile_weight(z, m) over the block's logits, read once more from TMEM by all eight
+  // warps: warps w and w + 4 share lane quadrant w & 3 and take alternate pairs of tiles
+  if (!*reinterpret_cast<volatile int*>(&flags[0])) {
+    tc_fence_after();
+    const int ew = warp & 3, half = warp >> 2;
+    float mref[kMaxRows], invT[kMaxRows];
+    bool dosum[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      Top2 m = top2_empty();
+      for (int w = 0; w < 4; ++w) m = top2_merge(m, s_top[w * kMaxRows + r]);
+      mref[r] = m.best;
+      dosum[r] = r < nr && m.idx != kNoIndex && m.best != -INFINITY;
+      invT[r] = s_invT[r];
+    }
+    unsigned long long acc[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0ull;
+    // two tiles per TMEM load: columns [16 t, 16 t + 32) stay inside the allocation because t
+    // is even and the allocation is a power of two of at least 16 columns per tile and 32
+    for (int t = 2 * half; t < ntile; t += 4) {
+      float v[32];
+      tmem_ld32(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                    static_cast<uint32_t>(t * kSkN),
+                v);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int local = (t + h) * kSkTileRows + ew * 32 + lane;
+        const bool ok = t + h < ntile && local < nt;
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          const float z = v[h * kSkN + r];
+          const unsigned long long w = tile_weight(z, mref[r], invT[r]);
+          acc[r] += (ok && dosum[r] && !(isnan(z) || z == INFINITY)) ? w : 0ull;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < nr) {
+        const unsigned long long a = warp_sum_u64(acc[r]);
+        if (lane == 0) atomicAdd(&s_sum[r], a);  // integers: the order does not matter
       }
     }
   }
@@ -218,9 +288,23 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, tcols);
   }
-  uint8_t* scratch = ring + ((static_cast<size_t>(nr) * p.tile_cap * sizeof(float) + 1023) &
-                             ~static_cast<size_t>(1023));
-  gemv_block_epilogue(p, ztile, v0, nt, scratch, flags, kSkThreads / 32);
+  if (tid < nr) {
+    Top2 m = top2_empty();
+    int bad = 0;
+    for (int w = 0; w < 4; ++w) {
+      m = top2_merge(m, s_top[w * kMaxRows + tid]);
+      bad |= s_bad[w * kMaxRows + tid];
+    }
+    GemvPartial pp;
+    pp.m = m.best;
+    pp.second = m.second;
+    pp.idx = (m.idx == kNoIndex) ? -1 : m.idx;
+    pp.flags = bad;
+    pp.s = s_sum[tid];
+    pp.pad = 0ull;
+    p.part[static_cast<size_t>(blockIdx.x) * kMaxRows + tid] = pp;
+  }
+  gemv_finish(p, ring + kSkStatBytes, flags, kSkThreads / 32);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -234,6 +318,7 @@ int gemv_tc_h_rows() { return kSkN; }
 int gemv_tc_stage_bytes() { return kSkStageBytes; }
 int gemv_tc_threads() { return kSkThreads; }
 int gemv_tc_max_block_rows() { return kSkMaxTiles * kSkTileRows; }
+int gemv_tc_stat_bytes() { return kSkStatBytes; }
 
 cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream) {
   static int configured_smem = 0;

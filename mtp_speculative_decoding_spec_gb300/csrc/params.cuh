@@ -37,6 +37,16 @@ struct GemvParams {
   GemvPartial* part;
 };
 
+// Shared memory the last block's combine needs: per row, for each block, its integer sum (8
+// bytes), max / scale factor, runner-up / weight and argmax (4 bytes each), rounded up; then
+// one flag per row.
+__host__ __device__ constexpr size_t gemv_finish_row_bytes(int nblocks) {
+  return 24 * static_cast<size_t>(nblocks);
+}
+__host__ __device__ constexpr size_t gemv_finish_scratch_bytes(int nblocks) {
+  return kMaxRows * gemv_finish_row_bytes(nblocks) + 64;
+}
+
 struct GemvLaunch {
   int grid, threads, smem;
   CUtensorMap wmap;  // W as a 2-D tensor [V rows][d], box [60 rows][512 bytes]
@@ -130,6 +140,7 @@ int gemv_tc_h_rows();
 int gemv_tc_stage_bytes();
 int gemv_tc_threads();
 int gemv_tc_max_block_rows();
+int gemv_tc_stat_bytes();
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
 cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
                           cudaStream_t stream);
