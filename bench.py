@@ -37,9 +37,11 @@ if ROOT not in sys.path:
 from synth import configs, gen  # noqa: E402
 
 METRIC = "verify cycles/s & emitted tok/s at k=1..7; LM-head HBM GB/s vs 8 TB/s"
-# DRAM traffic of one verify GEMV launch on the headline workload, read from the ncu capture
-# summarised in profiles/ (None until a capture of the current kernel exists).
-GEMV_TRAFFIC_BYTES = None
+# DRAM traffic (bytes read + written) of one 2-row verify launch of gemv_tc_kernel on the
+# headline workload, from the ncu capture summarised in
+# profiles/gemv_tc_kernel_verify_V151936_d2560.md (778,020,608 read + 3,883,264 written).
+# Set back to None whenever the kernel changes until it is captured again.
+GEMV_TRAFFIC_BYTES = 781903872
 
 
 def parse():
@@ -54,6 +56,23 @@ def parse():
     ap.add_argument("--profile", action="store_true",
                     help="few launches, no sweep/baseline: for ncu launch lists")
     return ap.parse_args()
+
+
+def rank_reduce(x, op, device):
+    """All-reduce one float over the ranks ("max" or "sum"); the identity on a single rank.
+    The bench's only collective: timing and unit counts, never the data path."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank, elapsed_max_s, world):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank / elapsed_max_s
 
 
 def rank_info():
@@ -170,20 +189,10 @@ def run_ours(args, rank, local_rank, world):
             dist.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_reduce(x, "max", dev)
 
     def sum_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+        return rank_reduce(x, "sum", dev)
 
     cfg = configs.get(1)
     W = gen.lm_weights(cfg)
@@ -243,7 +252,7 @@ def run_ours(args, rank, local_rank, world):
     err = int(eng.ws[4:8].cpu().numpy().view(np.uint32)[0])
     cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
     elapsed_max = max_over_ranks(elapsed)
-    value = world * K / elapsed_max
+    value = whole_job_value(K, elapsed_max, world)
     algo_bytes = cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16
     achieved = algo_bytes / gemv_mean_s / 1e9
 
@@ -254,7 +263,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"parallelism": f"replicas x{world}",
                                         "step": "verify GEMV (2 rows) + acceptance"}),
-        "roofline": {"bound": "hbm", "kernel": "gemv_rows_kernel (verify, 2 rows)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_tc_kernel (verify, 2 rows)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": algo_bytes,
@@ -308,8 +317,9 @@ def profile_extras(dev, W, Wd):
     for c in range(5):
         eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
     torch.cuda.synchronize()
-    commit_bench(dev, 6736.5, reps=3, warm=0)
-    batched_bench(dev, W, Wd, 6736.5, 1898.3, reps=2, with_commit=False)
+    hbm_peak, tf_peak, _ = measured_peaks()
+    commit_bench(dev, hbm_peak, reps=3, warm=0)
+    batched_bench(dev, W, Wd, hbm_peak, tf_peak, reps=2, with_commit=False)
 
 
 def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
@@ -360,7 +370,7 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
     torch.cuda.synchronize()
     s = max_over_ranks(time.perf_counter() - t0)
     h2d = H_host[0].numel() * 2 + D_host[0].numel() * 4
-    return {"value": round(world * K / s, 2), "unit": "verify cycles/s",
+    return {"value": round(whole_job_value(K, s, world), 2), "unit": "verify cycles/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": spec.ACCEPT_OUT_BYTES,
             "steps": K, "api": "SpecVerifyEngine.verify + spec_accept, pinned host buffers"}
 
