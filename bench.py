@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clocks-dir", default=None,
+                    help="directory for the raw nvidia-smi clock samples (default: temp dir)")
     ap.add_argument("--profile", action="store_true",
                     help="few launches, no sweep/baseline: for ncu launch lists")
     return ap.parse_args()
@@ -106,10 +108,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, csv_dir=None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(csv_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -230,7 +233,7 @@ def run_ours(args, rank, local_rank, world):
           for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank, args.clocks_dir)
     barrier()
     torch.cuda.synchronize()
     with clocks:

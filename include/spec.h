@@ -7,11 +7,11 @@
  * rows and fed to the next draft from device memory; the trunk verifies the k drafts in one
  * batched pass of k+1 rows through the shared LM head; the accepted prefix is committed and
  * the rest rolled back bit-exactly (section "Exactness"). DS4Server issue #98 ("Add Qwen3.8
- * Flash Next native MTP speculation", section "Implementation") adds the sampled variant:
- * probability-ratio acceptance u*q(x) <= p(x), residual correction from max(0, p - q), EOS
- * inside a proposal block, verification-row snapshots and rejected-row trimming. llama.cpp PR
- * #28104 (commit "keep speculative checkpoints on device") is why every call here stays on the
- * device: no call reads a result back to the host.
+ * Flash Next native MTP speculation", section "Implementation") adds the sampled variant: a
+ * draft is kept when u*q(x) <= p(x), a rejection is replaced by a draw from max(0, p - q), an
+ * EOS among the drafts ends the block, the state is snapshotted per verify row and rejected
+ * rows are dropped. llama.cpp PR #28104 moved its speculative checkpoints into device memory to
+ * save host copies per token; in the same spirit no call here reads a result back to the host.
  *
  * Conventions for every call
  *   - All array arguments are DEVICE pointers unless stated; the caller owns and allocates
@@ -92,10 +92,11 @@ typedef struct {
   int32_t reserved[2];
 } spec_accept_out;
 
-/* Per-request telemetry accumulated by spec_accept (DS4Server issue #98, "Implementation":
- * report drafted tokens, accepted tokens, verifier passes and acceptance depth). */
+/* Per-request telemetry accumulated by spec_accept (DS4Server issue #98, "Implementation"
+ * asks for counts of drafted and accepted tokens, of verify passes, and for how deep the
+ * acceptance went). */
 typedef struct {
-  uint64_t cycles;   /* verifier passes */
+  uint64_t cycles;   /* verify passes */
   uint64_t drafted;  /* sum of k */
   uint64_t accepted; /* sum of n_accept */
   uint64_t emitted;  /* sum of n_emit */
@@ -153,8 +154,8 @@ const char *spec_status_str(spec_status s);
 
 /*
  * spec_lmhead_verify -- the shared LM head over the verify rows (lucebox-hub PR #15, "What":
- * the trunk verifies the drafts in one batched forward; "Exactness": verify stays
- * batch-invariant up to eight rows).
+ * all drafts are checked by one batched trunk forward; "Exactness": up to eight rows, a row's
+ * verify logits may not depend on how many rows are verified together).
  *
  *   W           [V, d] LM-head weights, row-major (vocabulary-major), bf16 or fp32 (`wdt`).
  *   H           [B*R, d] verify hidden rows, same dtype as W; row b*R + r is request b's row r.
@@ -174,8 +175,8 @@ spec_status spec_lmhead_verify(const void *W, spec_dtype wdt, int64_t V, int64_t
 /*
  * spec_draft_argmax -- draft-head projection over the first V_draft rows of the same LM head
  * with the token choice fused in; the token stays in device memory for the next draft
- * (lucebox-hub PR #15, "What": "the draft head covers 64,000 vocabulary rows ... picks its
- * token on the GPU and feeds the next draft from device memory").
+ * (lucebox-hub PR #15, "What": the draft head spans the first 64,000 vocabulary rows, chooses
+ * its token on the GPU and hands it to the next draft without a trip to the host).
  *
  *   W, wdt, d   as for spec_lmhead_verify; only rows [0, V_draft) are read.
  *   h           [B, d] draft hidden rows (one per request), B <= 8.
@@ -235,9 +236,10 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t *k, const int32_
 
 /*
  * spec_commit_rollback -- keep the accepted prefix, drop the rest, on the device (DS4Server
- * issue #98, "Implementation": trim rejected rows, commit or replay only accepted recurrent
- * rows; llama.cpp PR #28104: full-checkpoint restore and replay without re-verification,
- * checkpoints kept on device).
+ * issue #98, "Implementation": rejected rows are dropped and only the accepted rows of the
+ * recurrent state are committed or replayed; llama.cpp PR #28104: go back to a whole-state
+ * checkpoint and replay the accepted tokens without checking them again, with the checkpoints
+ * in device memory).
  *
  * With m = out[b].n_emit (m = 0 if out[b].status != 0) and P = kv_len[b] read on the device:
  *   KV rows [P+m, P+k[b]+1) are zero-filled (clipped to capacity), kv_len[b] = P + m;

@@ -2,9 +2,10 @@
 //
 // Rules (lucebox-hub PR #15 "MTP speculative decoding", section "Exactness": a greedy draft
 // is accepted only if it equals the trunk's token; DS4Server issue #98 "Add Qwen3.8 Flash Next
-// native MTP speculation", section "Implementation" and closing comment: probability-ratio
-// acceptance u*q <= p, max(0, p - q) residual correction, zero / non-finite probability
-// handling, EOS inside a proposal block) -- see spec_accept in spec.h for the exact statement.
+// native MTP speculation", section "Implementation" and closing comment: a draft is kept when
+// u*q <= p, a rejection is replaced by a draw from max(0, p - q), zero and non-finite
+// probabilities get defined outcomes, an EOS among the drafts ends the block) -- see
+// spec_accept in spec.h for the exact statement.
 //
 // Work layout: grid (slices, B), one block per 1,024-entry slice of the vocabulary of one
 // request. Every block first takes the O(k) decision for its request (identical in every

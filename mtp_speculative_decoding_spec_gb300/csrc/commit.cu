@@ -2,11 +2,12 @@
 // entirely on the device.
 //
 // DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", section
-// "Implementation": capture verification-row recurrent snapshots, trim rejected attention
-// rows, commit only accepted rows, keep an ordinary-forward repair fallback. llama.cpp PR
-// #28104 ("full checkpoints for MTP rollback", the replay-livelock fix, "keep speculative
-// checkpoints on device"): restore the pre-round checkpoint and replay the accepted tokens
-// without verifying them again, with checkpoints that never leave the device.
+// "Implementation": the recurrent state is snapshotted at every verify row, attention rows of
+// rejected tokens are dropped and only the accepted prefix is kept, with re-running the
+// ordinary forward as the fallback. llama.cpp PR #28104 (its commits on whole-state
+// checkpoints, on a replay that looped forever and on device-resident checkpoints): go back to
+// the checkpoint taken before the round and re-apply the accepted tokens without checking them
+// a second time, with checkpoints that never leave the device.
 //
 // m = n_emit of the request (0 when its acceptance failed) is read from device memory, so no
 // host round-trip sits between acceptance and commit. Block 0 of each request trims the KV

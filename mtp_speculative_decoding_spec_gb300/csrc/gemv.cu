@@ -4,7 +4,7 @@
 //
 // Shape of the work (lucebox-hub PR #15 "MTP speculative decoding", section "What": the trunk
 // verifies k drafts in one batched forward of k+1 rows through the shared LM head; the draft
-// head covers the first 64,000 vocabulary rows and picks its token on the GPU): z = H W^T with
+// head spans the first 64,000 vocabulary rows and chooses its token on the GPU): z = H W^T with
 // W [V, d] streamed once from HBM, H [rows <= 8, d] tiny. This is a streaming GEMV: the weight
 // bytes bound it, so the design is about keeping HBM busy with few instructions per weight
 // byte (the kernel is templated on the weight type; only fp32 is instantiated):
@@ -18,8 +18,8 @@
 //     memory as fp32 pairs laid out so that one conflict-free 128-bit load feeds packed
 //     fp32x2 FMAs for two H rows; one butterfly (xor 16, 8, 4, 2, 1) per band finishes each
 //     dot product. Every step of a row's sum is fixed by k alone, so every row's logits are
-//     bitwise batch-invariant (section "Exactness": verify stays batch-invariant up to eight
-//     rows);
+//     bitwise batch-invariant (section "Exactness": up to eight rows, a row's verify logits may
+//     not depend on how many rows are verified together);
 //   * the block keeps its tile of logits in shared memory, reduces max / argmax / top-2 and a
 //     sum of exp((z - m)/T) quantised to 2^-40 units in 64-bit integers (exact, so the sum
 //     does not depend on order either), and the last block to finish combines the per-block

@@ -25,7 +25,8 @@
 //     partials cost one pass over TMEM and no logit tile in shared memory;
 //   * then the same finish as the CUDA-core kernel: the last block's combine and the draft
 //     draw.
-// Batch invariance (section "Exactness": verify stays batch-invariant up to eight rows): every
+// Batch invariance (section "Exactness": up to eight rows, a row's verify logits may not depend
+// on how many rows are verified together): every
 // call with bf16 weights runs this kernel whatever the number of rows, H row r always sits in
 // MMA column r, and a column's result depends only on that column's operands.
 #include "gemv_epilogue.cuh"

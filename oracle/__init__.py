@@ -11,15 +11,17 @@ What it follows (sources are the pages' titles and sections):
 
 * lucebox-hub PR #15 "feat(qwen4exp): MTP speculative decoding", sections *What* and
   *Exactness*: draft head over the first 64,000 vocabulary rows with an on-GPU argmax; one
-  batched verify of k drafts over k+1 rows; greedy acceptance byte-identical to MTP off;
-  bit-exact rollback of KV and recurrent state.
+  batched verify of k drafts over k+1 rows; greedy acceptance that emits exactly what decoding
+  without drafts emits; rollback that leaves KV and recurrent state bit-identical.
 * DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", sections
-  *Implementation* and the closing comment: probability-ratio acceptance ``u*q <= p``,
-  ``max(0, p - q)`` residual correction, zero/non-finite probability handling, EOS inside a
-  proposal block, verification-row snapshots, rejected-row trimming, replay fallback.
-* llama.cpp PR #28104 "qwen4exp : port NextN/MTP speculative decoding to master", commits
-  "full checkpoints for MTP rollback", the replay-livelock fix and "keep speculative
-  checkpoints on device": restore-and-replay without re-verification, state kept on device.
+  *Implementation* and the closing comment: a draft kept when ``u*q <= p``, a rejection
+  replaced by a draw from ``max(0, p - q)``, defined outcomes for zero and non-finite
+  probabilities, an EOS among the drafts ending the block, per-verify-row state snapshots,
+  rejected rows dropped, a replay fallback.
+* llama.cpp PR #28104 "qwen4exp : port NextN/MTP speculative decoding to master", its commits
+  on rollback through whole-state checkpoints, on a replay that looped forever, and on keeping
+  the checkpoints in device memory: restore, then replay the accepted tokens without checking
+  them again, with the state never leaving the device.
 * Philox4x32-10: Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
   SC'11, section 3 (the Philox S-box) and Table 2 (round constants).
 

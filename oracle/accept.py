@@ -2,15 +2,15 @@
 
 Sources (page titles and sections):
 
-* lucebox-hub PR #15 "MTP speculative decoding", *What*: the draft head picks its token by
-  argmax over the first 64,000 vocabulary rows; the trunk verifies k drafts in one pass of
-  k+1 rows. *Exactness*: a greedy draft is accepted only if it equals the trunk's token, so the
-  output is byte-identical to MTP off. *Speed*: 7.74 tokens per cycle at seven drafts implies
+* lucebox-hub PR #15 "MTP speculative decoding", *What*: the draft head chooses its token as
+  the argmax over the first 64,000 vocabulary rows; one trunk pass over k+1 rows checks k
+  drafts. *Exactness*: a greedy draft survives only when it is the trunk's own token, so the
+  emitted bytes are those of decoding without drafts. *Speed*: 7.74 tokens per cycle at seven drafts implies
   k+1 tokens when every draft passes -- the bonus token from the last verify row.
 * DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", *Implementation* and the
-  closing comment: probability-ratio acceptance ``u*q <= p``, residual correction from
-  ``max(0, p - q)``, zero/non-finite probability handling, EOS inside a proposal block without
-  retaining tokens or state beyond EOS.
+  closing comment: a draft is kept when ``u*q <= p``, a rejection is replaced by a draw from
+  ``max(0, p - q)``, zero and non-finite probabilities get defined outcomes, and an EOS among
+  the drafts ends the block with nothing, token or state, kept past it.
 
 The algorithm, per request (row r of the verify logits predicts the token after input r; draft
 d_i is checked against verify row i-1; ``pos_base`` is the absolute position of the first

@@ -1,9 +1,9 @@
 """LM-head logits and per-row statistics (oracle; test infrastructure only).
 
 The verify step projects the k+1 verify rows through the shared LM head in one batched pass
-(lucebox-hub PR #15 "MTP speculative decoding", section *What*: "the trunk verifies them in one
-batched forward"); the draft head is the same projection restricted to the first 64,000
-vocabulary rows (same page, *What*: "the draft head covers 64,000 vocabulary rows"). A logit
+(lucebox-hub PR #15 "MTP speculative decoding", section *What*: all drafts are checked by a
+single batched trunk forward); the draft head is the same projection restricted to the first
+64,000 vocabulary rows (same page and section). A logit
 is a plain dot product, so the oracle is that definition in float64:
 
     z[r, v] = sum_j H[r, j] * W[v, j]

@@ -6,8 +6,9 @@ Sources (page titles and sections):
 * lucebox-hub PR #15 "MTP speculative decoding", *Exactness*: "Rollback restores the
   KV/recurrent state bit-exactly"; every rollback case is cache- and logit-identical.
 * DS4Server issue #98 "Add Qwen3.8 Flash Next native MTP speculation", *Implementation*:
-  capture verification-row recurrent snapshots, trim rejected attention rows, commit only the
-  accepted rows, keep an ordinary-forward repair fallback; EOS retains no state beyond EOS.
+  the recurrent state is snapshotted at every verify row, attention rows of rejected tokens are
+  dropped, only the accepted prefix is kept, and re-running the ordinary forward is the
+  fallback; nothing after an EOS is kept.
   *Completion requirements*: rejected rows leave every cache and recurrent component identical
   to ordinary decoding; capture-commit and fallback repair are both correct.
 * llama.cpp PR #28104 "qwen4exp : port NextN/MTP speculative decoding to master", commits on
@@ -95,7 +96,7 @@ def commit_snapshot(slots_S, slots_conv, m):
 def commit_replay(S0, conv0, a, b, c, x, m):
     """Restore the pre-cycle state and replay rows 0..m-1 with the synthetic step. The replayed
     rows are state updates only: they are never verified again (llama.cpp PR #28104, the
-    replay-livelock fix)."""
+    fix for a replay that looped forever)."""
     S = np.array(S0, dtype=np.float32, copy=True)
     cv = np.array(conv0, dtype=np.float32, copy=True)
     for r in range(m):

@@ -6,7 +6,8 @@ The target these tests hold the oracle to is fixed by the pages, not by the orac
   the emitted tokens are a sample of the trunk's own autoregressive distribution. Checked
   exactly by enumerating every draft and every cell of the 24-bit uniforms at V = 8, and
   statistically by a chi-square test at V = 4096 over 10^6 seeded cycles.
-* lucebox-hub PR #15, *Exactness*: at temperature 0 the output is byte-identical to MTP off
+* lucebox-hub PR #15, *Exactness*: at temperature 0 the output equals, byte for byte, decoding
+  without drafts
   (sequential greedy decoding, written here with numpy's argmax).
 * Special cases of the ratio rule: p == q accepts every draft; a one-hot q on a token the trunk
   gives probability zero is always rejected and the residual is p itself.

@@ -2,7 +2,8 @@
 
 Target fixed by the pages: "Rejected rows leave every cache and recurrent component identical
 to ordinary decoding" and "capture-commit and fallback repair are both correct" (DS4Server
-issue #98, *Completion requirements*); "Rollback restores the KV/recurrent state bit-exactly"
+issue #98, *Completion requirements*); after a rollback the KV and recurrent state equal, bit
+for bit, those of a run that never drafted
 (lucebox-hub PR #15, *Exactness*). The reference run here is ordinary decoding: the m kept
 inputs fed one at a time.
 """
