@@ -470,10 +470,13 @@ def commit_bench(dev, hbm_peak, reps=20, warm=3):
         for _ in range(warm):
             kv_len.fill_(cfg.context)
             spec.spec_commit_rollback(1, d, acc_d, k_d, mode)
+        kv_len.fill_(cfg.context - 4 * reps)  # each commit keeps 4 rows: P stays below capacity
         torch.cuda.synchronize()
         ts = []
+        # a device-side wait lets the host queue every timed launch before the first one runs,
+        # so the events time back-to-back kernels, not the host's call overhead
+        torch.cuda._sleep(2_000_000)
         for _ in range(reps):
-            kv_len.fill_(cfg.context)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             spec.spec_commit_rollback(1, d, acc_d, k_d, mode)

@@ -122,7 +122,9 @@ typedef struct {
  *             step_c [B][n_slots-1][rec_layers][rec_heads][rec_dv]
  *             conv_in[B][n_slots-1][rec_layers][conv_width]         conv input of row r
  * n_slots >= k_max + 2. All float arrays 16-byte aligned; rec_dv, conv_width multiples of 4;
- * kv_row_bytes and kv_request_stride multiples of 16. */
+ * kv_row_bytes and kv_request_stride multiples of 16; one request's recurrent state
+ * (rec_layers*rec_heads*rec_dk*rec_dv) and conv state (rec_layers*conv_rows*conv_width) each
+ * below 2^33 floats (SPEC_ERR_INVALID otherwise). */
 typedef struct {
   void *kv;
   int64_t kv_request_stride;

@@ -325,6 +325,7 @@ spec_status run_gemm(const void* W, int64_t V, int64_t d, const void* H, int nro
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemmPartial*>(static_cast<uint8_t*>(workspace) + wl.gemm);
   L.grid = p.ntiles < a.sms ? p.ntiles : a.sms;
+  if (L.grid > gemm_tc_max_ctas()) L.grid = gemm_tc_max_ctas();  // the combine's partial limit
   p.nblocks = L.grid;
   L.smem = gemm_tc_smem_bytes();
   const cudaError_t e = gemm_tc_launch(L, stream);
@@ -460,6 +461,12 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
   if (st->rec_layers > 0) {
     if (st->rec_heads < 1 || st->rec_dk < 1 || st->rec_dv < 4 || st->rec_dv % 4 != 0)
       return SPEC_ERR_INVALID;
+    // the kernels index one request's state in 16-byte vectors with 32-bit integers
+    const int64_t rec_vec = static_cast<int64_t>(st->rec_layers) * st->rec_heads * st->rec_dk *
+                            st->rec_dv / 4;
+    const int64_t conv_vec =
+        static_cast<int64_t>(st->rec_layers) * st->conv_rows * st->conv_width / 4;
+    if (rec_vec >= (int64_t(1) << 31) || conv_vec >= (int64_t(1) << 31)) return SPEC_ERR_INVALID;
     if (!st->rec_live || !st->rec_slots || !aligned16(st->rec_live) || !aligned16(st->rec_slots))
       return SPEC_ERR_INVALID;
     if (mode == SPEC_COMMIT_REPLAY &&
@@ -482,7 +489,9 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
   p.k = k;
   p.mode = mode;
   p.commit_status = commit_status;
-  int per_req = (4 * a.sms + B - 1) / B;
+  // blocks resident per SM: 4 for the copy, 2 for the replay (their launch bounds)
+  const int per_sm = (mode == SPEC_COMMIT_SNAPSHOT) ? 4 : 2;
+  int per_req = (per_sm * a.sms + B - 1) / B;
   if (st->rec_layers == 0) per_req = 1;
   if (per_req < 1) per_req = 1;
   const cudaError_t e = commit_launch(p, B, per_req, reinterpret_cast<cudaStream_t>(stream));

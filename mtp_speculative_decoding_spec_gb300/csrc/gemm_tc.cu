@@ -36,6 +36,7 @@ constexpr int kTcStageBytes = 2 * kTcABytes + kTcBBytes;
 constexpr int kTcThreads = 10 * 32;  // producer, MMA, 8 epilogue warps
 constexpr int kTcEpiWarps = 8;      // two per TMEM lane quadrant, 64 columns each
 constexpr int kTcSubTiles = 2;      // per-row partials per tile (one per column half)
+constexpr int kTcMaxParts = 1024;   // partials per row the combine kernel holds (<= 512 CTAs)
 constexpr uint32_t kTmemCols = 512;
 
 // Top-2 of two candidates where every index of `a` is below every index of `b`, so ties go to
@@ -295,20 +296,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // One block per row: combine the row's per-tile partials in a fixed order (thread-strided,
 // then a fixed tree), exactly like the last block of the GEMV.
 __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams p) {
-  __shared__ float sm_best[8], sm_second[8];
+  __shared__ float sm_best[8], sm_second[8], sm_sum[8];
   __shared__ int sm_idx[8], sm_bad[8];
-  __shared__ double sm_sum[8];
+  __shared__ float sm_m[kTcMaxParts], sm_s[kTcMaxParts];  // each partial's max and sum, loaded once
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nparts = p.nblocks * kTcSubTiles;
+  const int nparts = p.nblocks * kTcSubTiles;  // <= kTcMaxParts (checked on the host)
   const GemmPartial* row = p.part + static_cast<size_t>(q) * nparts;
   const float T = p.temperature[q / p.rows_per_req];
   const float k2 = __fmul_rn(__fdiv_rn(1.f, T > 0.f ? T : 1.f), 1.4426950408889634f);
   Top2 t = top2_empty();
   int bad = 0;
   for (int i = tid; i < nparts; i += blockDim.x) {
-    bad |= __ldcg(&row[i].flags);
-    const int32_t idx = __ldcg(&row[i].idx);
-    if (idx >= 0) t = top2_merge(t, Top2{__ldcg(&row[i].m), __ldcg(&row[i].second), idx});
+    const uint4* pp = reinterpret_cast<const uint4*>(row + i);
+    const uint4 a = __ldcg(pp), b = __ldcg(pp + 1);  // {m, second, idx, flags}, {s (double), pad}
+    const int32_t idx = static_cast<int32_t>(a.z);
+    bad |= static_cast<int>(a.w);
+    if (idx >= 0) t = top2_merge(t, Top2{__uint_as_float(a.x), __uint_as_float(a.y), idx});
+    sm_m[i] = (idx >= 0) ? __uint_as_float(a.x) : -INFINITY;
+    sm_s[i] = static_cast<float>(__hiloint2double(static_cast<int>(b.y), static_cast<int>(b.x)));
   }
   t = warp_top2(t);
   bad = __any_sync(0xffffffffu, bad);
@@ -327,22 +332,22 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
   }
   const bool nonfinite = anybad || all.idx == kNoIndex || all.best == -INFINITY;
   const float M = all.best;
-  double S = 0.0;
+  // the normaliser in fp32: thread sums in index order, then fixed trees (deterministic)
+  float S = 0.f;
   if (!nonfinite) {
-    for (int i = tid; i < nparts; i += blockDim.x) {
-      const float mc = __ldcg(&row[i].m);
-      const double sc = __ldcg(&row[i].s);
-      if (__ldcg(&row[i].idx) >= 0 && mc != -INFINITY && sc > 0.0)
-        S += sc * static_cast<double>(exp2f(__fmul_rn(__fsub_rn(mc, M), k2)));
+    for (int i = tid; i < nparts; i += blockDim.x) {  // entries this thread wrote above
+      const float mc = sm_m[i], sc = sm_s[i];
+      if (mc != -INFINITY && sc > 0.f)
+        S = __fadd_rn(S, __fmul_rn(sc, exp2f(__fmul_rn(__fsub_rn(mc, M), k2))));
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  for (int o = 16; o > 0; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
   if (lane == 0) sm_sum[warp] = S;
   __syncthreads();
   if (tid == 0) {
-    double tot = 0.0;
-    for (int w = 0; w < 8; ++w) tot += sm_sum[w];
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot = __fadd_rn(tot, sm_sum[w]);
     spec_rowstats st;
     if (nonfinite) {
       st.max = __int_as_float(0x7fc00000);
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
       st.argmax = -1;
     } else {
       st.max = M;
-      st.log_norm = static_cast<float>(log(tot));
+      st.log_norm = logf(tot);
       st.gap = __fsub_rn(M, all.second);
       st.argmax = all.idx;
     }
@@ -382,6 +387,7 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream) {
 
 int gemm_tc_smem_bytes() { return kTcStages * kTcStageBytes + 1024 + 128; }
 int gemm_tc_tile_rows() { return kTcTileN; }
+int gemm_tc_max_ctas() { return kTcMaxParts / kTcSubTiles; }
 int gemm_tc_subtiles() { return kTcSubTiles; }
 int gemm_tc_kblock() { return kTcKBlock; }
 

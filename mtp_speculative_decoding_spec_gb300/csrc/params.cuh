@@ -121,6 +121,7 @@ int gemm_tc_smem_bytes();
 int gemm_tc_tile_rows();
 int gemm_tc_kblock();
 int gemm_tc_subtiles();
+int gemm_tc_max_ctas();
 
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
 
