@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   __shared__ unsigned long long sh[kAcceptThreads / 32];
   __shared__ int s_last, s_slice, s_tok;
   __shared__ unsigned long long s_before;
+  pdl_trigger();
+  pdl_wait();  // everything below reads what the LM-head kernels wrote
 
   const int b = blockIdx.y, sl = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -369,8 +371,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
 
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream) {
   dim3 grid(prm.NS, prm.B);
-  accept_kernel<<<grid, kAcceptThreads, 0, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_pdl(accept_kernel, grid, dim3(kAcceptThreads), 0, stream, prm);
 }
 
 }  // namespace spec

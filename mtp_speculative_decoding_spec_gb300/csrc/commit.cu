@@ -77,6 +77,7 @@ __device__ __forceinline__ int kept_rows(const CommitParams& p, int b, int& kk, 
 // Snapshot mode: live <- slot m, for the recurrent and the conv state. A pure copy: four
 // blocks per SM with eight 16-byte loads in flight per thread (128 KB per SM).
 __global__ void __launch_bounds__(256, 4) commit_snapshot_kernel(const __grid_constant__ CommitParams p) {
+  pdl_wait();
   const int b = blockIdx.y;
   const spec_state_desc& st = p.st;
   const int ns = st.n_slots;
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(256, 4) commit_snapshot_kernel(const __grid_co
 // separately rounded), two state vectors per thread per step for more loads in flight; conv
 // rows <- the last rows of (slot-0 conv rows, conv inputs of rows 0..m-1).
 __global__ void __launch_bounds__(256, 2) commit_replay_kernel(const __grid_constant__ CommitParams p) {
+  pdl_wait();
   const int b = blockIdx.y;
   const spec_state_desc& st = p.st;
   const int ns = st.n_slots;
@@ -185,10 +187,8 @@ cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request
                           cudaStream_t stream) {
   dim3 grid(blocks_per_request, B);
   if (prm.mode == SPEC_COMMIT_SNAPSHOT)
-    commit_snapshot_kernel<<<grid, 256, 0, stream>>>(prm);
-  else
-    commit_replay_kernel<<<grid, 256, 0, stream>>>(prm);
-  return cudaGetLastError();
+    return launch_pdl(commit_snapshot_kernel, grid, dim3(256), 0, stream, prm);
+  return launch_pdl(commit_replay_kernel, grid, dim3(256), 0, stream, prm);
 }
 
 }  // namespace spec

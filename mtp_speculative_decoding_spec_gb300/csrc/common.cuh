@@ -54,6 +54,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch. pdl_trigger lets the next kernel of the stream (launched with
+// programmatic stream serialization) be scheduled before this one ends; pdl_wait blocks until
+// every kernel this one depends on has completed and its writes are visible. A kernel calls
+// pdl_wait before it touches anything an earlier kernel may write, and only reads data no
+// kernel of the path writes (the weights) before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -69,6 +69,7 @@ __device__ __forceinline__ Top2 top2_of_64(const float* v) {
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_rows_tc_kernel(const __grid_constant__ CUtensorMap hmap,
                         const __grid_constant__ CUtensorMap wmap, const GemmParams p) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzle tiles, whatever the base alignment
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();  // the combine may be scheduled now
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -296,6 +298,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // One block per row: combine the row's per-tile partials in a fixed order (thread-strided,
 // then a fixed tree), exactly like the last block of the GEMV.
 __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams p) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sm_best[8], sm_second[8], sm_sum[8];
   __shared__ int sm_idx[8], sm_bad[8];
   __shared__ float sm_m[kTcMaxParts], sm_s[kTcMaxParts];  // each partial's max and sum, loaded once
@@ -378,11 +382,10 @@ cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream) {
                                                                 kTcThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
-  gemm_rows_tc_kernel<<<L.grid, kTcThreads, L.smem, stream>>>(L.hmap, L.wmap, L.p);
-  e = cudaGetLastError();
+  e = launch_pdl(gemm_rows_tc_kernel, dim3(L.grid), dim3(kTcThreads), L.smem, stream, L.hmap, L.wmap,
+                 L.p);
   if (e != cudaSuccess) return e;
-  gemm_rows_combine_kernel<<<L.p.nrows, 256, 0, stream>>>(L.p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_rows_combine_kernel, dim3(L.p.nrows), dim3(256), 0, stream, L.p);
 }
 
 int gemm_tc_smem_bytes() { return kTcStages * kTcStageBytes + 1024 + 128; }

@@ -94,6 +94,7 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 template <int RP, bool BF16>
 __global__ void __maxnreg__(128)
     gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
+  pdl_wait();
   constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
   constexpr int PP = EPC / 2;               // element pairs per chunk
   constexpr int RH = RP >= 2 ? RP / 2 : 1;  // H row pairs held per 128-bit load
@@ -275,6 +276,7 @@ __global__ void __maxnreg__(128)
   }
   __syncthreads();
 
+  pdl_trigger();
   gemv_block_epilogue(p, ztile, v0, nt, stage_base, flags, NW + 1);
 }
 
@@ -296,8 +298,7 @@ static cudaError_t launch_variant(const GemvLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, L.threads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
-  kern<<<L.grid, L.threads, L.smem, stream>>>(L.wmap, L.p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(L.grid), dim3(L.threads), L.smem, stream, L.wmap, L.p);
 }
 
 cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream) {

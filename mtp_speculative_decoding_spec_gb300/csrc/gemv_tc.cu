@@ -89,16 +89,72 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     flags[1] = 0;
     fence_mbar_init();
   }
-  if (tid < kMaxRows) {
-    const float T = (tid < p.nrows) ? p.temperature[tid / p.rows_per_req] : 1.f;
-    s_temp[tid] = (tid < p.nrows && p.logits) ? T : 0.f;
-    s_invT[tid] = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
-  }
   if (warp == 1) tmem_alloc(tmem_slot, tcols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // The stage schedule: iteration it covers tile it / nks, stage ks = it % nks of that tile.
+  const int total_it = ntile * nks;
+  auto issue_w = [&](int it, int s) {  // the weight boxes of iteration it into stage s
+    const int t = it / nks, ks = it - t * nks;
+    const int rows = min(kSkTileRows, nt - t * kSkTileRows);
+    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
+    const int y = static_cast<int>(v0) + t * kSkTileRows;
+    const int nk = min(kSkKB, nkb - ks * kSkKB);  // k-blocks in this stage
+    uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
+    for (int kk = 0; kk < nk; ++kk)
+      for (int b = 0; b < nbox; ++b)
+        tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
+                       (ks * kSkKB + kk) * kSkKBlock, y + b * kSkBoxRows, &full[s]);
+  };
+  auto issue_h = [&](int it, int s) {  // the H blocks of iteration it into stage s
+    const int t = it / nks, ks = it - t * nks;
+    const int nk = min(kSkKB, nkb - ks * kSkKB);
+    uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
+    for (int kk = 0; kk < nk; ++kk)
+      tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, (ks * kSkKB + kk) * kSkKBlock,
+                     0, &full[s]);
+  };
+  // Steady state: per k-block its four weight boxes, then its H block. This order (k-block outer,
+  // 32-row boxes inner, H between k-blocks) streamed measurably faster than issuing all weight
+  // boxes first or walking each row band's 512 bytes first.
+  auto issue_all = [&](int it, int s) {
+    const int t = it / nks, ks = it - t * nks;
+    const int rows = min(kSkTileRows, nt - t * kSkTileRows);
+    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
+    const int y = static_cast<int>(v0) + t * kSkTileRows;
+    const int nk = min(kSkKB, nkb - ks * kSkKB);
+    uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
+    for (int kk = 0; kk < nk; ++kk) {
+      const int x = (ks * kSkKB + kk) * kSkKBlock;
+      for (int b = 0; b < nbox; ++b)
+        tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, y + b * kSkBoxRows,
+                       &full[s]);
+      tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
+    }
+  };
+  // The weights are never written by the path: the first stages stream in before the wait for
+  // the previous kernel, whose tail they overlap. H, the temperatures, the outputs and the
+  // workspace are only touched after it.
+  const int pre = min(S, total_it);
+  if (warp == 0 && lane == 0) {
+    for (int it = 0; it < pre; ++it) issue_w(it, it);
+    pdl_wait();
+    for (int it = 0; it < pre; ++it) issue_h(it, it);  // the first MMAs wait on nothing else
+  } else {
+    pdl_wait();
+  }
+  if (tid >= 32 && tid < 32 + kMaxRows) {  // lanes of the MMA warp, idle until the barrier
+    const int r = tid - 32;
+    const float T = (r < p.nrows) ? p.temperature[r / p.rows_per_req] : 1.f;
+    s_temp[r] = (r < p.nrows && p.logits) ? T : 0.f;
+    s_invT[r] = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+  }
+  __syncthreads();
   // running top-2 and NaN / +Inf flag of each row over this warp's TMEM lane quadrant (drain
   // warps only)
   Top2 run[kMaxRows];
@@ -112,34 +168,16 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      int it = 0, s = 0;
-      for (int t = 0; t < ntile && !*reinterpret_cast<volatile int*>(&flags[0]); ++t) {
-        const int rows = min(kSkTileRows, nt - t * kSkTileRows);
-        const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
-        const int y = static_cast<int>(v0) + t * kSkTileRows;
-        bool ok = true;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          // stage s is reused every S iterations: wait until the MMAs of its last use are done
-          if (it >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((it / S) & 1) ^ 1))) {
-            atomicOr(&p.hdr->error, ERR_TC_WAIT);
-            atomicExch(&flags[0], 1);
-            ok = false;
-            break;
-          }
-          uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
-          const int nk = min(kSkKB, nkb - ks * kSkKB);  // k-blocks in this stage
-          mbar_arrive_expect_tx(&full[s],
-                                static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
-          for (int kk = 0; kk < nk; ++kk) {
-            const int x = (ks * kSkKB + kk) * kSkKBlock;
-            for (int b = 0; b < nbox; ++b)
-              tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, y + b * kSkBoxRows,
-                             &full[s]);
-            tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
-          }
-          if (++s == S) s = 0;
+      int it = pre, s = pre % S;
+      for (; it < total_it && !*reinterpret_cast<volatile int*>(&flags[0]); ++it) {
+        // stage s is reused every S iterations: wait until the MMAs of its last use are done
+        if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((it / S) & 1) ^ 1))) {
+          atomicOr(&p.hdr->error, ERR_TC_WAIT);
+          atomicExch(&flags[0], 1);
+          break;
         }
-        if (!ok) break;
+        issue_all(it, s);
+        if (++s == S) s = 0;
       }
       // every issued copy must have landed before the ring is reused or the block exits
       for (int j = max(0, it - S); j < it; ++j) {
@@ -221,9 +259,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   }
 
   // every tile's MMAs have completed (the drain warps waited for each) and every copy has
-  // landed (the producer waited for each): the ring is free for the block's statistics
+  // landed (the producer waited for each): the ring is free for the block's statistics. The
+  // next kernel may now be scheduled into this kernel's tail (not earlier: blocks parked in
+  // its wait during the stream cost bandwidth).
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();
   Top2* s_top = reinterpret_cast<Top2*>(ring);                             // [4 quadrants][8]
   int* s_bad = reinterpret_cast<int*>(ring + 4 * kMaxRows * sizeof(Top2));  // [4][8]
   unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(ring + 512);  // [8]
@@ -334,8 +375,8 @@ cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream) {
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_tc_kernel, kSkThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
-  gemv_tc_kernel<<<L.grid, kSkThreads, L.smem, stream>>>(L.wmap, L.hmap, L.p);
-  return cudaGetLastError();
+  return launch_pdl(gemv_tc_kernel, dim3(L.grid), dim3(kSkThreads), L.smem, stream, L.wmap, L.hmap,
+                    L.p);
 }
 
 }  // namespace spec

@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace spec {
@@ -115,6 +117,24 @@ struct GemmLaunch {
   CUtensorMap wmap;  // W [V][d] bf16, box [128 rows][64], 128-byte swizzle
   GemmParams p;
 };
+
+// Launch with programmatic stream serialization: the kernel may be scheduled while the previous
+// kernel of the stream is still running; it calls pdl_wait before touching that kernel's data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream);
 int gemm_tc_smem_bytes();
