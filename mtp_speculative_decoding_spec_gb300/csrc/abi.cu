@@ -123,7 +123,8 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   // after streaming, the ring holds the per-block statistics and then the combine's scratch
   const size_t after =
       static_cast<size_t>(gemv_tc_stat_bytes()) + gemv_finish_scratch_bytes(grid);
-  const size_t fixed = 512 + 1024;  // barriers, TMEM slot, flags, temperatures; alignment slack
+  // barriers (2 per stage + 16), TMEM slot, flags, temperatures, per-row inputs; alignment slack
+  const size_t fixed = 1024 + 1024;
   const size_t budget = static_cast<size_t>(a.smem_optin);
   int stages = 16;
   size_t ring = 0, smem_total = 0;
@@ -225,7 +226,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const size_t hs_bytes = static_cast<size_t>(nslab) * pairs * row_pairs * 32 * 16;
   // the last block reuses the stage ring for the combine's scratch
   const size_t scratch = gemv_finish_scratch_bytes(grid);
-  const size_t fixed = hs_bytes + static_cast<size_t>(rp) * tile_cap * 4 + 128;  // + flags, temps
+  // + flags, temperatures, per-row inputs (with alignment)
+  const size_t fixed = hs_bytes + static_cast<size_t>(rp) * tile_cap * 4 + 512;
   const size_t budget = static_cast<size_t>(a.smem_optin);
   int stages = 8;
   size_t ring = 0, smem_total = 0;

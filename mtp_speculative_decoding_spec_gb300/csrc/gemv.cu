@@ -112,7 +112,9 @@ __global__ void __maxnreg__(128)
   uint64_t* full = reinterpret_cast<uint64_t*>(ztile + static_cast<size_t>(RP) * p.tile_cap);
   uint64_t* empty = full + S;
   int* flags = reinterpret_cast<int*>(empty + S);  // [0] abort, [1] last block
-  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] temperature of each row
+  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] T of rows whose logits are written
+  RowInputs* ri = reinterpret_cast<RowInputs*>(
+      (reinterpret_cast<uintptr_t>(s_temp + kMaxRows) + 7) & ~static_cast<uintptr_t>(7));
 
   const int GR = gridDim.x, blk = blockIdx.x;
   int64_t v0, v1;
@@ -132,6 +134,7 @@ __global__ void __maxnreg__(128)
   }
   if (tid < kMaxRows)
     s_temp[tid] = (tid < p.nrows && p.logits) ? p.temperature[tid / p.rows_per_req] : 0.f;
+  if (tid < kMaxRows) load_row_inputs(p, ri, tid);
   // H rows -> shared memory as fp32 pairs: entry ((s*PP + q)*RH + rr)*32 + l holds
   // (h[2rr][k], h[2rr][k+1], h[2rr+1][k], h[2rr+1][k+1]) with k = s*slab_elems + l*EPC + 2q.
   {
@@ -277,7 +280,7 @@ __global__ void __maxnreg__(128)
   __syncthreads();
 
   pdl_trigger();
-  gemv_block_epilogue(p, ztile, v0, nt, stage_base, flags, NW + 1);
+  gemv_block_epilogue(p, ztile, v0, nt, stage_base, flags, NW + 1, ri);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -20,6 +20,26 @@ __device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, in
   if (v1 < v0) v1 = v0;
 }
 
+// Per-row inputs of the statistics and the draw, read once at the start of the kernel (after
+// its dependency wait) so that the last block's finish does not wait on global loads.
+struct RowInputs {
+  float invT[kMaxRows];     // 1 / T (1 at T <= 0)
+  float T[kMaxRows];        // the row's request temperature
+  uint64_t seed[kMaxRows];  // draft head only
+  int64_t pos[kMaxRows];    // draft head only
+};
+static_assert(sizeof(RowInputs) == 192, "row inputs");
+
+// Called by threads r = 0..7 of the block (each fills its row; rows past nrows get T = 1).
+__device__ __forceinline__ void load_row_inputs(const GemvParams& p, RowInputs* ri, int r) {
+  const bool live = r < p.nrows;
+  const float T = live ? p.temperature[r / p.rows_per_req] : 1.f;
+  ri->T[r] = T;
+  ri->invT[r] = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+  ri->seed[r] = (live && p.draft) ? p.seed[r] : 0ull;
+  ri->pos[r] = (live && p.draft) ? p.pos[r] : 0;
+}
+
 // uint64 (below 2^53) to fp32 from its two 32-bit halves: 32-bit conversions only.
 __device__ __forceinline__ float u64_to_f32(unsigned long long v) {
   return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(v >> 32)), 4294967296.f,
@@ -37,11 +57,11 @@ __device__ __forceinline__ unsigned long long tile_weight(float z, float m, floa
 // NaN / +Inf flag, and the exact integer sum of tile_weight(z, m) relative to the block max m.
 // Called by all `nwarps` warps after a __syncthreads that publishes ztile.
 static __device__ __forceinline__ void gemv_block_partials(const GemvParams& p, const float* ztile,
-                                                           int64_t v0, int nt, int nwarps) {
+                                                           int64_t v0, int nt, int nwarps,
+                                                           const RowInputs* ri) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int q = warp; q < p.nrows; q += nwarps) {
-    const float T = p.temperature[q / p.rows_per_req];
-    const float invT = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+    const float invT = ri->invT[q];
     const float* zr = ztile + static_cast<size_t>(q) * p.tile_cap;
     Top2 t = top2_empty();
     int bad = 0;
@@ -80,7 +100,7 @@ static __device__ __forceinline__ void gemv_block_partials(const GemvParams& p, 
 // (>= 8) warps call it; `scratch` (free shared memory, 8-byte aligned) needs
 // gemv_finish_scratch_bytes(gridDim.x) bytes; flags[1] is a free shared int.
 static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t* scratch,
-                                                   int* flags, int nwarps) {
+                                                   int* flags, int nwarps, const RowInputs* ri) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int GR = gridDim.x;
   __threadfence();
@@ -123,12 +143,10 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
     float* blk_m = reinterpret_cast<float*>(base + 8 * GR);
     float* blk_w = reinterpret_cast<float*>(base + 12 * GR);
     const int32_t* blk_i = reinterpret_cast<const int32_t*>(base + 16 * GR);
-    const float T = p.temperature[q / p.rows_per_req];
-    const float Te = T > 0.f ? T : 1.f;
-    const float invT = __fdiv_rn(1.f, Te);
-    // the draw's inputs are fetched now so that their latency overlaps the combine
-    const uint64_t seed_q = (p.draft && T > 0.f) ? p.seed[q] : 0ull;
-    const int64_t pos_q = (p.draft && T > 0.f) ? p.pos[q] : 0;
+    const float T = ri->T[q];
+    const float invT = ri->invT[q];
+    const uint64_t seed_q = ri->seed[q];
+    const int64_t pos_q = ri->pos[q];
     Top2 t = top2_empty();
     for (int cc = lane; cc < GR; cc += 32) {
       const int32_t idx = blk_i[cc];
@@ -275,9 +293,10 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
 // Partials from the block's logit tile, then gemv_finish.
 static __device__ __forceinline__ void gemv_block_epilogue(const GemvParams& p, const float* ztile,
                                                            int64_t v0, int nt, uint8_t* scratch,
-                                                           int* flags, int nwarps) {
-  gemv_block_partials(p, ztile, v0, nt, nwarps);
-  gemv_finish(p, scratch, flags, nwarps);
+                                                           int* flags, int nwarps,
+                                                           const RowInputs* ri) {
+  gemv_block_partials(p, ztile, v0, nt, nwarps, ri);
+  gemv_finish(p, scratch, flags, nwarps, ri);
 }
 
 }  // namespace spec

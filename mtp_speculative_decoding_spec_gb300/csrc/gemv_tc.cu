@@ -63,8 +63,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint64_t* tile_done = empty + S;  // [kSkMaxTiles]: one phase each
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_done + kSkMaxTiles);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last block
-  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] temperature of each row
-  float* s_invT = s_temp + kMaxRows;                     // [8] 1 / T (1 at T = 0)
+  float* s_temp = reinterpret_cast<float*>(flags + 4);  // [8] T of rows whose logits are written
+  RowInputs* ri = reinterpret_cast<RowInputs*>(
+      (reinterpret_cast<uintptr_t>(s_temp + kMaxRows) + 7) & ~static_cast<uintptr_t>(7));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int64_t v0, v1;
@@ -150,9 +151,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   }
   if (tid >= 32 && tid < 32 + kMaxRows) {  // lanes of the MMA warp, idle until the barrier
     const int r = tid - 32;
-    const float T = (r < p.nrows) ? p.temperature[r / p.rows_per_req] : 1.f;
-    s_temp[r] = (r < p.nrows && p.logits) ? T : 0.f;
-    s_invT[r] = __fdiv_rn(1.f, T > 0.f ? T : 1.f);
+    load_row_inputs(p, ri, r);
+    s_temp[r] = (r < p.nrows && p.logits) ? ri->T[r] : 0.f;
   }
   __syncthreads();
   // running top-2 and NaN / +Inf flag of each row over this warp's TMEM lane quadrant (drain
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       for (int w = 0; w < 4; ++w) m = top2_merge(m, s_top[w * kMaxRows + r]);
       mref[r] = m.best;
       dosum[r] = r < nr && m.idx != kNoIndex && m.best != -INFINITY;
-      invT[r] = s_invT[r];
+      invT[r] = ri->invT[r];
     }
     unsigned long long acc[kMaxRows];
 #pragma unroll
@@ -310,9 +310,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const bool ok = t + h < ntile && local < nt;
 #pragma unroll
         for (int r = 0; r < kMaxRows; ++r) {
-          const float z = v[h * kSkN + r];
-          const unsigned long long w = tile_weight(z, mref[r], invT[r]);
-          acc[r] += (ok && dosum[r] && !(isnan(z) || z == INFINITY)) ? w : 0ull;
+          if (r < nr) {  // uniform: only the live rows cost an exp
+            const float z = v[h * kSkN + r];
+            const unsigned long long w = tile_weight(z, mref[r], invT[r]);
+            acc[r] += (ok && dosum[r] && !(isnan(z) || z == INFINITY)) ? w : 0ull;
+          }
         }
       }
     }
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     pp.pad = 0ull;
     p.part[static_cast<size_t>(blockIdx.x) * kMaxRows + tid] = pp;
   }
-  gemv_finish(p, ring + kSkStatBytes, flags, kSkThreads / 32);
+  gemv_finish(p, ring + kSkStatBytes, flags, kSkThreads / 32, ri);
 }
 
 // ------------------------------------------------------------------------------------------
