@@ -27,6 +27,12 @@ T > 0 (ratio rule), p_r = softmax(z[r]/T) over V, q_i = softmax(y[i]/T) over the
               emit the inverse-CDF draw of r with U(pos_base+i-1, RESIDUAL); stop.
     all k accepted: emit the inverse-CDF draw of p_k with U(pos_base+k, BONUS).
 
+Exact-match mode at T > 0 (``accept_request_exact``): the trunk's own token at each position is
+the inverse-CDF draw of p_{i-1} with U(pos_base+i-1, BONUS); a draft is kept iff it equals that
+token, the first mismatch emits the token, and all k kept emit the draw from p_k. The output is
+then token-identical to decoding without drafts under the same seed (pinned against a sequential
+sampler written independently in the tests).
+
 Inverse CDF: the smallest j (ascending token id) with cumsum(w)[j] > u * sum(w); if rounding
 leaves none, the last j with w[j] > 0. Readings where the pages are silent are listed in the
 design notes (draft rows checked against row i-1, lowest-index argmax ties, ``<=`` in the ratio
@@ -194,6 +200,66 @@ def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
             margins.append(("cdf", m))
             res.update(sample_kind=2, sample_row=k)
             emit(j)
+    res["n_emit"] = len(tokens)
+    return res
+
+
+def accept_request_exact(z, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
+    """Exact-match acceptance at temperature for one request and one cycle (lucebox-hub PR #15
+    "MTP speculative decoding", *Exactness* and *Notes*: a draft is kept only if it is the
+    token the trunk itself samples, so the emitted text is the same as decoding without drafts
+    for the same seed).
+
+    The trunk's own token at position pos is the inverse-CDF draw of p = softmax(z/T) with
+    U(pos, BONUS) -- the draw decoding without drafts makes there. For i = 1..k:
+    t_i = that draw from row i-1 at pos_base+i-1; if d_i == t_i, emit it (stop if EOS) and go
+    on; otherwise emit t_i and stop. All k kept: emit the draw from row k at pos_base+k.
+    T == 0: the draws are argmaxes and the result equals ``accept_request``.
+    Same inputs, validation and result dict as ``accept_request`` (no draft logits needed);
+    sample_kind 3 marks these draws, sample_row is the row of the last one.
+    """
+    if not T > 0:
+        return accept_request(z, None, drafts, k, T, eos_id, uniform, pos_base, k_max)
+    res = dict(status=STATUS_OK, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
+               sample_kind=0, sample_row=-1, margins=[])
+    if k < 0 or k > k_max:
+        res["status"] = STATUS_BAD_K
+        return res
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[1]
+    d = [int(x) for x in drafts[:k]]
+    if any(x < 0 or x >= V for x in d):
+        res["status"] = STATUS_BAD_TOKEN
+        return res
+    if any(lmhead.row_stats(z[r], T)["nonfinite"] for r in range(k + 1)):
+        res["status"] = STATUS_NONFINITE
+        return res
+    tokens, margins = res["tokens"], res["margins"]
+
+    def trunk_token(r):
+        j, m = inverse_cdf(lmhead.probs(z[r], T), uniform(pos_base + r, PURPOSE_BONUS))
+        margins.append(("cdf", m))
+        res.update(sample_kind=3, sample_row=r)
+        return j
+
+    def emit(tok):
+        tokens.append(int(tok))
+        if eos_id >= 0 and tok == eos_id:
+            res["eos_hit"] = True
+            return True
+        return False
+
+    for i in range(1, k + 1):
+        t = trunk_token(i - 1)
+        if d[i - 1] == t:
+            res["n_accept"] += 1
+            if emit(t):
+                break
+        else:
+            emit(t)
+            break
+    else:
+        emit(trunk_token(k))
     res["n_emit"] = len(tokens)
     return res
 

@@ -261,6 +261,88 @@ def test_greedy_identical_to_mtp_off():
         assert accepted > 0 and rejected > 0  # both branches exercised
 
 
+def _sequential_sample(model, T, seed, n, eos):
+    """Decoding without drafts, written here from the definition: at absolute position pos the
+    token is the smallest j with cumsum(p)[j] > u * sum(p), p = softmax(trunk(prefix) / T),
+    u = U(seed, pos, BONUS). Independent of the oracle's helpers (own softmax and search)."""
+    seq = [0]
+    while len(seq) < n:
+        z = model.trunk(seq) / T
+        w = np.exp(z - z.max())
+        c = np.cumsum(w)
+        u = philox.uniform(seed, len(seq), philox.PURPOSE_BONUS)
+        j = int(np.searchsorted(c, u * c[-1], side="right"))
+        # distance to the nearest bin edge, relative to the mass: near-ties are reported
+        lo = c[j - 1] if j > 0 else 0.0
+        near = min(abs(c[j] - u * c[-1]), abs(u * c[-1] - lo)) / c[-1] < 1e-12
+        seq.append(j)
+        if near:
+            return seq, True
+        if j == eos:
+            break
+    return seq, False
+
+
+@pytest.mark.parametrize("k,T,seed", [(1, 1.0, 3), (3, 0.7, 4), (7, 1.0, 5), (7, 1.6, 6)])
+def test_exact_match_at_temperature_equals_sampling_without_drafts(k, T, seed):
+    """NEXT item F1 (lucebox-hub PR #15, *Exactness* / *Notes*): with exact-match acceptance the
+    emitted tokens equal, token for token, decoding without drafts under the same seed -- for
+    drafts from a noisy draft head, so both keeps and mismatches occur."""
+    eos = 5
+    model = ToyModel(32, 24, scale=3.0, noise=0.2, seed=10 + k)
+    ref, near = _sequential_sample(model, T, seed, 200, eos)
+    assert not near
+    src = philox.make_uniform_source(seed)
+    seq = [0]
+    kept = mism = 0
+    while len(seq) < len(ref):
+        d = []
+        for i in range(k):  # drafts: the draft head's own samples (DRAFT purpose)
+            u = src(len(seq) + i, philox.PURPOSE_DRAFT)
+            d.append(accept.draft_token(model.draft(seq + d), T, u)[0])
+        z = np.array([model.trunk(seq + d[:r]) for r in range(k + 1)])
+        r = accept.accept_request_exact(z, d, k, T, eos, src, pos_base=len(seq))
+        assert r["status"] == 0 and 1 <= r["n_emit"] <= k + 1 and r["sample_kind"] == 3
+        kept += r["n_accept"]
+        mism += int(r["n_accept"] < k and not r["eos_hit"])
+        seq.extend(r["tokens"])
+        if r["eos_hit"]:
+            break
+    assert seq[: len(ref)] == ref[: len(seq)]
+    assert kept > 0 and mism > 0
+
+
+def test_exact_match_at_zero_temperature_is_greedy_acceptance():
+    rng = np.random.default_rng(8)
+    src = philox.make_uniform_source(1)
+    for trial in range(50):
+        k = int(rng.integers(0, 8))
+        z = rng.standard_normal((k + 1, 64))
+        d = [int(x) for x in rng.integers(0, 64, k)]
+        for i in range(k):  # plant some agreements
+            if rng.random() < 0.6:
+                d[i] = int(np.argmax(z[i]))
+        a = accept.accept_request(z, None, d, k, 0.0, 7, src, 100)
+        b = accept.accept_request_exact(z, d, k, 0.0, 7, src, 100)
+        assert a == b
+
+
+def test_exact_match_validation_and_eos():
+    src = philox.make_uniform_source(2)
+    z = np.zeros((3, 16))
+    assert accept.accept_request_exact(z, [1, 2], 9, 1.0, 0, src, 0)["status"] == 2
+    assert accept.accept_request_exact(z, [1, 99], 2, 1.0, 0, src, 0)["status"] == 5
+    bad = z.copy()
+    bad[1, 3] = np.nan
+    assert accept.accept_request_exact(bad, [1, 2], 2, 1.0, 0, src, 0)["status"] == 1
+    # a row whose whole mass sits on the EOS id: the trunk samples EOS, a matching draft is
+    # kept and ends the block with no bonus
+    z = np.full((3, 16), -50.0)
+    z[0, 4] = 50.0
+    r = accept.accept_request_exact(z, [4, 9], 2, 1.0, 4, src, 0)
+    assert r["tokens"] == [4] and r["eos_hit"] and r["n_accept"] == 1 and r["n_emit"] == 1
+
+
 def test_eos_at_every_draft_position():
     rng = np.random.default_rng(8)
     V, k, eos = 30, 5, 3
