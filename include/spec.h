@@ -80,7 +80,8 @@ typedef struct {
 
 /* Result of one cycle for one request (64 bytes). tokens[0..n_emit) are the emitted tokens
  * t_1..t_m; unused entries are -1. sample_kind: 0 no draw, 1 residual draw, 2 bonus draw;
- * sample_row = the verify row the draw used (-1 if none). */
+ * sample_row = the verify row the draw used (-1 if none); spec_accept_exact reports kind 3
+ * (the trunk's own draws) with the row of the last draw. */
 typedef struct {
   int32_t status;
   int32_t n_accept; /* drafts accepted */
@@ -237,6 +238,26 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t *k, const int32_
                         spec_stream_t stream);
 
 /*
+ * spec_accept_exact -- exact-match acceptance at temperature (lucebox-hub PR #15,
+ * "Exactness" and "Notes": a draft counts only if it is the token the trunk itself samples, so
+ * the emitted text is the same as decoding without drafts for the same seed).
+ *
+ * For request b at T > 0 the trunk's token at position pos_base[b] + r is the inverse-CDF draw
+ * of p_r = softmax(z_r / T) with U(pos_base + r, BONUS) -- the draw decoding without drafts
+ * makes there. For i = 1..k: while d_i equals the trunk's token of row i-1 it is kept (an EOS
+ * ends the block); the first mismatch emits the trunk's token and stops; all k kept emits the
+ * trunk's token of row k. T <= 0 is greedy acceptance, exactly as spec_accept. No draft logits
+ * are read. out[b].sample_kind = 3 for these draws and sample_row = the row of the last one.
+ * Arguments, layouts, workspace, status codes and counters as for spec_accept.
+ */
+spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t *k, const int32_t *drafts,
+                              const float *logits, const spec_rowstats *stats, int64_t V,
+                              int32_t R, const float *temperature, int32_t eos_id,
+                              const uint64_t *seed, const int64_t *pos_base,
+                              spec_accept_out *out, spec_counters *counters, void *workspace,
+                              size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * spec_commit_rollback -- keep the accepted prefix, drop the rest, on the device (DS4Server
  * issue #98, "Implementation": rejected rows are dropped and only the accepted rows of the
  * recurrent state are committed or replayed; llama.cpp PR #28104: go back to a whole-state
@@ -278,7 +299,7 @@ int32_t spec_batched_supported(void);
  *     memset on `stream`); calls whose work overlaps on the GPU (different streams, or several
  *     host threads) race on it and must be serialised by the caller.
  *   - A vocabulary whose scratch would exceed the array returns SPEC_ERR_UNSUPPORTED (at 152
- *     SMs that is beyond about 900,000 vocabulary rows); everything else validates and fails
+ *     SMs that is beyond about 1,040,000 vocabulary rows); everything else validates and fails
  *     like spec_lmhead_verify (more than 8 rows in total: SPEC_ERR_UNSUPPORTED).
  */
 spec_status spec_lmhead_verify_noalloc(const void *W, spec_dtype wdt, int64_t V, int64_t d,

@@ -82,6 +82,14 @@ def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_d
         _ptr(out), _ptr(counters), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
+def spec_accept_exact(B, k_max, k, drafts, logits, stats, V, R, temperature, eos_id, seed,
+                      pos_base, out, counters, workspace, stream=None):
+    _check("spec_accept_exact", _abi.lib().spec_accept_exact(
+        B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(temperature),
+        eos_id, _ptr(seed), _ptr(pos_base), _ptr(out), _ptr(counters), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)))
+
+
 def spec_commit_rollback(B, st, acc, k, mode, commit_status=None, stream=None):
     """``st`` is a ``spec_state_desc`` (host struct of device pointers)."""
     import ctypes

@@ -16,7 +16,7 @@ REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN 
 
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
 EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
-           "spec_accept", "spec_commit_rollback", "spec_batched_supported",
+           "spec_accept", "spec_accept_exact", "spec_commit_rollback", "spec_batched_supported",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes")
 
 # numpy views of the device structs (for reading results copied to the host)
@@ -86,6 +86,9 @@ def lib():
         L.spec_accept.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, i64, i64, vp, i32,
                                   vp, vp, vp, vp, vp, sz, vp]
         L.spec_accept.restype = i32
+        L.spec_accept_exact.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, i32, vp, vp, vp,
+                                        vp, vp, sz, vp]
+        L.spec_accept_exact.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,
                                            vp]
         L.spec_commit_rollback.restype = i32

@@ -71,7 +71,7 @@ int accept_slices(int64_t V) { return static_cast<int>((V + kAcceptSlice - 1) / 
 // they sit at the END of the caller's buffer:
 //   [0, 256)                    header (GEMV ticket, error word)
 //   [256, part_end)             GEMV per-block partials (grid of the vocabulary size)
-//   [part_end, sums_end)        accept per-slice sums (B * slices * 16 bytes)
+//   [part_end, sums_end)        accept per-slice sums (B * slices * 8 * 8 bytes)
 //   [sums_end, gemm_end)        batched path: per-(row, 256-row tile) partials (no counters)
 //   [ws_bytes - tickets, end)   accept tickets, one per request
 struct WsLayout {
@@ -87,7 +87,7 @@ WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
   WsLayout w;
   w.part = sizeof(WsHeader);
   w.sums = w.part + align_up(sizeof(GemvPartial) * kMaxRows * gemv_grid(V, sms), 256);
-  w.gemm = w.sums + align_up(sizeof(unsigned long long) * 2 * static_cast<size_t>(max_batch) *
+  w.gemm = w.sums + align_up(sizeof(unsigned long long) * kMaxRows * static_cast<size_t>(max_batch) *
                                  accept_slices(V),
                              256);
   const int64_t ntiles = (V + 127) / 128;  // batched path: 128-row vocabulary tiles
@@ -201,8 +201,10 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const int64_t row_bytes = d * elt;
   if (row_bytes % 16 != 0) return SPEC_ERR_INVALID;
   if (d > (wdt == SPEC_BF16 ? 3072 : 1536)) return SPEC_ERR_UNSUPPORTED;
-  const WsLayout wl = ws_layout(V, batch_for_ws, a.sms);
-  if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
+  // batch_for_ws = 0: a scratch that holds only what the LM head uses (header and partials,
+  // which come first in every layout); otherwise the caller's full workspace
+  const WsLayout wl = ws_layout(V, batch_for_ws > 0 ? batch_for_ws : 1, a.sms);
+  if (workspace_bytes < (batch_for_ws > 0 ? wl.total : wl.sums)) return SPEC_ERR_INVALID;
   EncodeTiledFn encode = encode_tiled();
   if (!encode) return SPEC_ERR_CUDA;
 
@@ -334,6 +336,56 @@ spec_status run_gemm(const void* W, int64_t V, int64_t d, const void* H, int nro
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// spec_accept and spec_accept_exact: validation, workspace layout, launch.
+spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
+                       const float* logits, const spec_rowstats* stats, int64_t V, int32_t R,
+                       const float* q_logits, const spec_rowstats* q_stats, int64_t V_draft,
+                       int64_t q_stride, const float* temperature, int32_t eos_id,
+                       const uint64_t* seed, const int64_t* pos_base, spec_accept_out* out,
+                       spec_counters* counters, void* workspace, size_t workspace_bytes,
+                       spec_stream_t stream, int exact) {
+  if (B < 1 || k_max < 0 || k_max > kMaxRows - 1 || R < 1 || R > kMaxRows) return SPEC_ERR_INVALID;
+  if (!k || (k_max > 0 && !drafts) || !stats || !temperature || !seed || !pos_base || !out ||
+      !workspace)
+    return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24)) return SPEC_ERR_INVALID;
+  if (q_logits && (!q_stats || V_draft < 1 || V_draft > V || q_stride < V_draft))
+    return SPEC_ERR_INVALID;
+  const DevAttr a = dev_attr();
+  if (a.sms <= 0) return SPEC_ERR_CUDA;
+  const WsLayout wl = ws_layout(V, B, a.sms);
+  if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
+  AcceptParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.k_max = k_max;
+  p.R = R;
+  p.NS = accept_slices(V);
+  p.k = k;
+  p.drafts = drafts;
+  p.logits = logits;
+  p.stats = stats;
+  p.V = V;
+  p.q_logits = q_logits;
+  p.q_stats = q_stats;
+  p.Vd = q_logits ? V_draft : 0;
+  p.q_stride = q_stride;
+  p.temperature = temperature;
+  p.eos = eos_id;
+  p.seed = seed;
+  p.pos_base = pos_base;
+  p.out = out;
+  p.counters = counters;
+  p.exact = exact;
+  // tickets: the last 4*B bytes of the buffer, its end rounded down to 4 bytes (see WsLayout)
+  const size_t end4 = workspace_bytes & ~static_cast<size_t>(3);
+  p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + end4 -
+                                          sizeof(uint32_t) * static_cast<size_t>(B));
+  p.sums = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + wl.sums);
+  const cudaError_t e = accept_launch(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace spec
 
@@ -404,45 +456,20 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_
                         const uint64_t* seed, const int64_t* pos_base, spec_accept_out* out,
                         spec_counters* counters, void* workspace, size_t workspace_bytes,
                         spec_stream_t stream) {
-  if (B < 1 || k_max < 0 || k_max > kMaxRows - 1 || R < 1 || R > kMaxRows) return SPEC_ERR_INVALID;
-  if (!k || (k_max > 0 && !drafts) || !stats || !temperature || !seed || !pos_base || !out ||
-      !workspace)
-    return SPEC_ERR_INVALID;
-  if (V < 1 || V >= (int64_t(1) << 24)) return SPEC_ERR_INVALID;
-  if (q_logits && (!q_stats || V_draft < 1 || V_draft > V || q_stride < V_draft))
-    return SPEC_ERR_INVALID;
-  const DevAttr a = dev_attr();
-  if (a.sms <= 0) return SPEC_ERR_CUDA;
-  const WsLayout wl = ws_layout(V, B, a.sms);
-  if (workspace_bytes < wl.total) return SPEC_ERR_INVALID;
-  AcceptParams p;
-  memset(&p, 0, sizeof(p));
-  p.B = B;
-  p.k_max = k_max;
-  p.R = R;
-  p.NS = accept_slices(V);
-  p.k = k;
-  p.drafts = drafts;
-  p.logits = logits;
-  p.stats = stats;
-  p.V = V;
-  p.q_logits = q_logits;
-  p.q_stats = q_stats;
-  p.Vd = q_logits ? V_draft : 0;
-  p.q_stride = q_stride;
-  p.temperature = temperature;
-  p.eos = eos_id;
-  p.seed = seed;
-  p.pos_base = pos_base;
-  p.out = out;
-  p.counters = counters;
-  // tickets: the last 4*B bytes of the buffer, its end rounded down to 4 bytes (see WsLayout)
-  const size_t end4 = workspace_bytes & ~static_cast<size_t>(3);
-  p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + end4 -
-                                          sizeof(uint32_t) * static_cast<size_t>(B));
-  p.sums = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + wl.sums);
-  const cudaError_t e = accept_launch(p, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_draft,
+                          q_stride, temperature, eos_id, seed, pos_base, out, counters, workspace,
+                          workspace_bytes, stream, 0);
+}
+
+spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
+                              const float* logits, const spec_rowstats* stats, int64_t V,
+                              int32_t R, const float* temperature, int32_t eos_id,
+                              const uint64_t* seed, const int64_t* pos_base,
+                              spec_accept_out* out, spec_counters* counters, void* workspace,
+                              size_t workspace_bytes, spec_stream_t stream) {
+  return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, nullptr, nullptr, 0, 0,
+                          temperature, eos_id, seed, pos_base, out, counters, workspace,
+                          workspace_bytes, stream, 1);
 }
 
 spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
@@ -547,12 +574,12 @@ extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt,
   if (a.sms <= 0) return SPEC_ERR_CUDA;
   // the fixed scratch must hold the GEMV's part of the workspace layout (header and per-block
   // partials); a batch-1 layout covers it for any B*R <= 8
-  if (ws_layout(V, 1, a.sms).total > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
+  if (ws_layout(V, 1, a.sms).sums > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
   void* scratch = noalloc_scratch();
   if (!scratch) return SPEC_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the ticket and the error word must start at zero (a previous call may have been cut short)
   if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return SPEC_ERR_CUDA;
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr, nullptr,
-                  0, nullptr, 0, scratch, kNoAllocScratchBytes, 1, s);
+                  0, nullptr, 0, scratch, kNoAllocScratchBytes, 0, s);
 }

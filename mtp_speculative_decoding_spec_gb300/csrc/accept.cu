@@ -20,11 +20,13 @@
 
 namespace spec {
 
+constexpr int kAcceptSumSlots = kMaxRows;  // per-slice integer sums: one per verify row
+
 
 struct Decision {
   int status, n_accept, ntok, eos_hit;
   int tokens[8];
-  int need;  // 0 none, 1 residual draw, 2 bonus draw
+  int need;  // 0 none, 1 residual draw, 2 bonus draw, 3 exact-match draws (rows 0..srow)
   int srow;  // verify row of the draw
   int xrej;  // the rejected draft (one-hot q)
   int pad;
@@ -100,6 +102,94 @@ __device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long 
   return before + incl;
 }
 
+// The draw context of verify row `row` of request b: p at temperature T, and for a residual
+// the draft distribution (q rows, or one-hot at the rejected draft `xrej`).
+__device__ __forceinline__ DrawCtx draw_ctx(const AcceptParams& p, int b, int row, bool residual,
+                                            int xrej, float T) {
+  DrawCtx c;
+  const size_t prow = static_cast<size_t>(b) * p.R + row;
+  const spec_rowstats ps = p.stats[prow];
+  c.prow = p.logits + prow * p.V;
+  c.pmax = ps.max;
+  c.pinvT = __fdiv_rn(1.f, T);
+  c.pinv_norm = expf(-ps.log_norm);
+  c.residual = residual;
+  c.qrow = nullptr;
+  c.qmax = 0.f;
+  c.qinv_norm = 0.f;
+  c.Vd = p.Vd;
+  c.xrej = -1;
+  if (residual) {
+    if (p.q_logits) {
+      const size_t qr = static_cast<size_t>(row) * p.B + b;
+      const spec_rowstats qs = p.q_stats[qr];
+      c.qrow = p.q_logits + qr * p.q_stride;
+      c.qmax = qs.max;
+      c.qinv_norm = expf(-qs.log_norm);
+    } else {
+      c.xrej = xrej;
+    }
+  }
+  return c;
+}
+
+// Inverse-CDF draw over request b's vocabulary from slot `slot` of its slice sums (the exact
+// integer weights the context defines: p if use_p, else the residual): the slice whose
+// cumulative weight first exceeds u*total by a block-parallel scan, then the token inside it by
+// rescanning the slice. Called by every thread of the block; returns the token (-1 only if the
+// total is zero, which the callers exclude).
+__device__ int draw_token(const AcceptParams& p, int b, const DrawCtx& c, bool use_p, int slot,
+                          uint32_t u24, unsigned long long* sh, int* s_slice,
+                          unsigned long long* s_before, int* s_tok) {
+  const int tid = threadIdx.x;
+  const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
+  unsigned long long tot = 0ull;
+  for (int i = tid; i < p.NS; i += kAcceptThreads) tot += __ldcg(rs + kAcceptSumSlots * i + slot);
+  tot = block_sum_u64(tot, sh);
+  const unsigned long long target = cdf_target(u24, tot);
+  if (tid == 0) {
+    *s_slice = -1;
+    *s_tok = -1;
+  }
+  {
+    unsigned long long carry = 0ull;
+    for (int base = 0; base < p.NS; base += kAcceptThreads) {
+      const int i = base + tid;
+      const unsigned long long w = (i < p.NS) ? __ldcg(rs + kAcceptSumSlots * i + slot) : 0ull;
+      unsigned long long round_total;
+      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
+      if (w > 0ull && cum > target && cum - w <= target) {
+        *s_slice = i;
+        *s_before = cum - w;
+      }
+      carry += round_total;
+      __syncthreads();
+      if (*s_slice >= 0) break;
+    }
+  }
+  if (*s_slice >= 0) {
+    const int64_t base = static_cast<int64_t>(*s_slice) * kAcceptSlice;
+    unsigned long long carry = *s_before;
+    for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
+      const int64_t j = base + e * kAcceptThreads + tid;
+      unsigned long long w = 0ull;
+      if (j < p.V) {
+        unsigned long long wr, wp;
+        entry_weights(c, j, wr, wp);
+        w = use_p ? wp : wr;
+      }
+      unsigned long long round_total;
+      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
+      if (w > 0ull && cum > target && cum - w <= target) *s_tok = static_cast<int>(j);
+      carry += round_total;
+      __syncthreads();
+      if (*s_tok >= 0) break;
+    }
+  }
+  __syncthreads();
+  return *s_tok;
+}
+
 __device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
   spec_accept_out o;
   o.status = D.status;
@@ -167,8 +257,9 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
         nf = nf || isnan(p.q_stats[static_cast<size_t>(lane) * p.B + b].max);
       if (__any_sync(0xffffffffu, nf)) status = SPEC_REQ_NONFINITE;
     }
+    const bool exact = p.exact && T > 0.f;  // exact-match mode: decided by the draws below
     bool acc = false;
-    if (status == SPEC_REQ_OK && lane < k) {
+    if (status == SPEC_REQ_OK && lane < k && !exact) {
       if (!(T > 0.f)) {
         acc = (x == st.argmax);
       } else {
@@ -206,7 +297,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       d.srow = -1;
       d.xrej = -1;
       d.pad = 0;
-      if (status == SPEC_REQ_OK) {
+      if (status == SPEC_REQ_OK && exact) {
+        d.need = 3;
+        d.srow = k;
+      } else if (status == SPEC_REQ_OK) {
         bool stop = false;
         for (int i = 0; i < k && !stop; ++i) {
           if ((accmask >> i) & 1u) {
@@ -248,50 +342,53 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     return;
   }
 
-  // ---------------- slice sums of the draw's integer weights ----------------
-  DrawCtx c;
-  {
-    const size_t prow = static_cast<size_t>(b) * p.R + D.srow;
-    const spec_rowstats ps = p.stats[prow];
-    c.prow = p.logits + prow * p.V;
-    c.pmax = ps.max;
-    c.pinvT = __fdiv_rn(1.f, T);
-    c.pinv_norm = expf(-ps.log_norm);
-    c.residual = (D.need == 1);
-    c.qrow = nullptr;
-    c.qmax = 0.f;
-    c.qinv_norm = 0.f;
-    c.Vd = p.Vd;
-    c.xrej = -1;
-    if (c.residual) {
-      if (p.q_logits) {
-        const size_t qr = static_cast<size_t>(D.srow) * p.B + b;
-        const spec_rowstats qs = p.q_stats[qr];
-        c.qrow = p.q_logits + qr * p.q_stride;
-        c.qmax = qs.max;
-        c.qinv_norm = expf(-qs.log_norm);
-      } else {
-        c.xrej = D.xrej;
+  // ---------------- slice sums of the draws' integer weights ----------------
+  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
+  unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
+  if (D.need == 3) {
+    // exact-match: the p weights of every row 0..k over this slice, slots 0..k
+    unsigned long long sp[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) sp[r] = 0ull;
+    const float invT = __fdiv_rn(1.f, T);
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r <= k) {
+        const size_t prow = static_cast<size_t>(b) * p.R + r;
+        const spec_rowstats ps = p.stats[prow];
+        const float inv_norm = expf(-ps.log_norm);
+        const float* row = p.logits + prow * p.V;
+        for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
+          const int64_t j = j0 + e * kAcceptThreads + tid;
+          if (j < p.V) sp[r] += quantise(prob_of(__ldcg(row + j), ps.max, invT, inv_norm));
+        }
       }
     }
-  }
-  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
-  unsigned long long sr = 0ull, sp = 0ull;
-  for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
-    const int64_t j = j0 + e * kAcceptThreads + tid;
-    if (j < p.V) {
-      unsigned long long wr, wp;
-      entry_weights(c, j, wr, wp);
-      sr += wr;
-      sp += wp;
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r <= k) {
+        const unsigned long long t = block_sum_u64(sp[r], sh);
+        if (tid == 0) mysum[r] = t;
+      }
     }
-  }
-  sr = block_sum_u64(sr, sh);
-  sp = block_sum_u64(sp, sh);
-  unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * 2;
-  if (tid == 0) {
-    mysum[0] = sr;
-    mysum[1] = sp;
+  } else {
+    const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
+    unsigned long long sr = 0ull, sp = 0ull;
+    for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
+      const int64_t j = j0 + e * kAcceptThreads + tid;
+      if (j < p.V) {
+        unsigned long long wr, wp;
+        entry_weights(c, j, wr, wp);
+        sr += wr;
+        sp += wp;
+      }
+    }
+    sr = block_sum_u64(sr, sh);
+    sp = block_sum_u64(sp, sh);
+    if (tid == 0) {
+      mysum[0] = sr;
+      mysum[1] = sp;
+    }
   }
   __threadfence();
   __syncthreads();
@@ -303,62 +400,56 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   if (!s_last) return;
   __threadfence();
 
-  // ---------------- last block of the request: locate and rescan the slice ----------------
-  const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * 2;
-  unsigned long long tr = 0ull, tp = 0ull;
-  for (int i = tid; i < p.NS; i += kAcceptThreads) {
-    tr += __ldcg(rs + 2 * i);
-    tp += __ldcg(rs + 2 * i + 1);
+  // ---------------- last block of the request: the draws ----------------
+  if (D.need == 3) {
+    // exact-match: the trunk's own token row by row (U(pos_base + r, BONUS)); keep drafts while
+    // they equal it, emit it at the first mismatch, or as the bonus after row k
+    __shared__ int s_stop;
+    __shared__ Decision E;
+    if (tid == 0) {
+      E = D;
+      s_stop = 0;
+    }
+    __syncthreads();
+    for (int r = 0; r <= k; ++r) {
+      const DrawCtx c = draw_ctx(p, b, r, false, -1, T);
+      const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_BONUS);
+      const int tok = draw_token(p, b, c, true, r, u24, sh, &s_slice, &s_before, &s_tok);
+      if (tid == 0) {
+        E.srow = r;
+        E.tokens[E.ntok++] = tok;
+        const bool is_eos = (p.eos >= 0 && tok == p.eos);
+        if (r < k && tok == sx[r]) {
+          E.n_accept++;
+          if (is_eos) {
+            E.eos_hit = 1;
+            s_stop = 1;
+          }
+        } else {
+          if (is_eos) E.eos_hit = 1;
+          s_stop = 1;
+        }
+      }
+      __syncthreads();
+      if (s_stop) break;
+    }
+    if (tid == 0) {
+      finalize(p, b, E, k);
+      p.tickets[b] = 0u;
+    }
+    return;
   }
+
+  // ratio rule: one draw, from the residual (p if the residual is empty) or the bonus row
+  const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
+  const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
+  unsigned long long tr = 0ull;
+  for (int i = tid; i < p.NS; i += kAcceptThreads) tr += __ldcg(rs + kAcceptSumSlots * i);
   tr = block_sum_u64(tr, sh);
-  tp = block_sum_u64(tp, sh);
   const bool use_p = (D.need == 2) || (tr == 0ull);
-  const unsigned long long total = use_p ? tp : tr;
   const uint32_t purpose = (D.need == 1) ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
   const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + D.srow, purpose);
-  const unsigned long long target = cdf_target(u24, total);
-  // locate the slice holding the target: block-parallel scan over the slice sums
-  if (tid == 0) {
-    s_slice = -1;
-    s_tok = -1;
-  }
-  {
-    unsigned long long carry = 0ull;
-    for (int base = 0; base < p.NS; base += kAcceptThreads) {
-      const int i = base + tid;
-      const unsigned long long w = (i < p.NS) ? __ldcg(rs + 2 * i + (use_p ? 1 : 0)) : 0ull;
-      unsigned long long round_total;
-      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
-      if (w > 0ull && cum > target && cum - w <= target) {
-        s_slice = i;
-        s_before = cum - w;
-      }
-      carry += round_total;
-      __syncthreads();
-      if (s_slice >= 0) break;
-    }
-  }
-  int tok = -1;
-  if (s_slice >= 0) {
-    const int64_t base = static_cast<int64_t>(s_slice) * kAcceptSlice;
-    unsigned long long carry = s_before;
-    for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
-      const int64_t j = base + e * kAcceptThreads + tid;
-      unsigned long long w = 0ull;
-      if (j < p.V) {
-        unsigned long long wr, wp;
-        entry_weights(c, j, wr, wp);
-        w = use_p ? wp : wr;
-      }
-      unsigned long long round_total;
-      const unsigned long long cum = carry + block_incl_scan_u64(w, sh, &round_total);
-      if (w > 0ull && cum > target && cum - w <= target) s_tok = static_cast<int>(j);
-      carry += round_total;
-      __syncthreads();
-      if (s_tok >= 0) break;
-    }
-    tok = s_tok;
-  }
+  int tok = draw_token(p, b, c, use_p, use_p ? 1 : 0, u24, sh, &s_slice, &s_before, &s_tok);
   if (tid == 0) {
     Decision d = D;
     if (tok < 0) tok = p.stats[static_cast<size_t>(b) * p.R + D.srow].argmax;  // unreachable

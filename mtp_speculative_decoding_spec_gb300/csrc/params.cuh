@@ -73,7 +73,8 @@ struct AcceptParams {
   spec_accept_out* out;
   spec_counters* counters;
   uint32_t* tickets;         // [B]
-  unsigned long long* sums;  // [B][NS][2]: residual weight, p weight
+  unsigned long long* sums;  // [B][NS][8]: ratio rule: residual, p; exact-match: p of rows 0..k
+  int exact;                 // exact-match acceptance at T > 0
 };
 
 struct CommitParams {
