@@ -386,7 +386,8 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
 
 
 def sweep(dev, W, Wd, hbm_peak):
-    """k = 1..7 at temperature 0 (greedy) and 1 (ratio rule with q rows)."""
+    """k = 1..7 at temperature 0 (greedy) and 1 (ratio rule with q rows); exact-match
+    acceptance at temperature 1 for k = 1, 3, 7."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -394,58 +395,62 @@ def sweep(dev, W, Wd, hbm_peak):
     out = {}
     base = configs.get(2)
     n_pool, K = 32, 200
-    for T in (0.0, 1.0):
-        for k in range(1, 8):
-            cfg = configs.Config(**{**base.__dict__, "k": k, "temps": (T,)})
-            Hp, Hdp = build_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
-            Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
-            Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
-            eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
-                                   cfg.eos_id, device=dev, want_q_logits=True)
-            eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k])
-            for c in range(5):
-                eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
-            torch.cuda.synchronize()
-            eng.counters.zero_()
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                   torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-            # pass 1: events around each verify and acceptance (launch durations)
-            for c in range(K):
-                cc = c % n_pool
-                for i in range(1, k + 1):
-                    eng.draft_step(i, Hdp_d[cc, i - 1:i])
-                ev[c][0].record()
-                eng.verify(Hp_d[cc])
-                ev[c][1].record()
-                eng.accept()
-                ev[c][2].record()
-            torch.cuda.synchronize()
-            eng.counters.zero_()
-            # pass 2: the same cycles with no events between kernels (full-cycle rate)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            for c in range(K):
-                cc = c % n_pool
-                for i in range(1, k + 1):
-                    eng.draft_step(i, Hdp_d[cc, i - 1:i])
-                eng.verify(Hp_d[cc])
-                eng.accept()
-            b.record()
-            torch.cuda.synchronize()
-            s = a.elapsed_time(b) / 1e3
-            verify_s = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
-            gemv_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
-            cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
-            gbs = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 +
-                   (k + 1) * cfg.V * 4 * (T > 0)) / gemv_s / 1e9
-            out[f"T{T:g}_k{k}"] = {
-                "verify_cycles_s": round(K / verify_s, 1),
-                "full_cycles_s": round(K / s, 1),
-                "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
-                "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
-                "acceptance": round(float(cnt["accepted"]) / max(1, float(cnt["drafted"])), 3),
-                "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4)}
-            del eng, Hp_d, Hdp_d
+    points = [(T, k, "ratio") for T in (0.0, 1.0) for k in range(1, 8)]
+    points += [(1.0, k, "exact") for k in (1, 3, 7)]
+    for T, k, mode in points:
+        cfg = configs.Config(**{**base.__dict__, "k": k, "temps": (T,)})
+        Hp, Hdp = build_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
+        Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+        Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+        eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
+                               cfg.eos_id, device=dev, want_q_logits=True,
+                               acceptance=mode)
+        eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k])
+        for c in range(5):
+            eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
+        torch.cuda.synchronize()
+        eng.counters.zero_()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        # pass 1: events around each verify and acceptance (launch durations)
+        for c in range(K):
+            cc = c % n_pool
+            for i in range(1, k + 1):
+                eng.draft_step(i, Hdp_d[cc, i - 1:i])
+            ev[c][0].record()
+            eng.verify(Hp_d[cc])
+            ev[c][1].record()
+            eng.accept()
+            ev[c][2].record()
+        torch.cuda.synchronize()
+        eng.counters.zero_()
+        # pass 2: the same cycles with no events between kernels (full-cycle rate)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for c in range(K):
+            cc = c % n_pool
+            for i in range(1, k + 1):
+                eng.draft_step(i, Hdp_d[cc, i - 1:i])
+            eng.verify(Hp_d[cc])
+            eng.accept()
+        b.record()
+        torch.cuda.synchronize()
+        s = a.elapsed_time(b) / 1e3
+        verify_s = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
+        gemv_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+        cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+        gbs = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 +
+               (k + 1) * cfg.V * 4 * (T > 0)) / gemv_s / 1e9
+        accept_us = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
+        out[f"T{T:g}_k{k}" + ("_exact" if mode == "exact" else "")] = {
+            "verify_cycles_s": round(K / verify_s, 1),
+            "full_cycles_s": round(K / s, 1),
+            "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
+            "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
+            "acceptance": round(float(cnt["accepted"]) / max(1, float(cnt["drafted"])), 3),
+            "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4),
+            "accept_us": round(accept_us, 2)}
+        del eng, Hp_d, Hdp_d
     return out
 
 

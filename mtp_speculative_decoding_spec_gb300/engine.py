@@ -10,12 +10,18 @@ results back, all asynchronously on the stream.
 import torch
 
 from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_BF16, spec_accept,
-               spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify, spec_workspace_bytes)
+               spec_accept_exact, spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
+               spec_workspace_bytes)
 
 
 class SpecVerifyEngine:
     def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
-                 want_q_logits=True):
+                 want_q_logits=True, acceptance="ratio"):
+        """acceptance: "ratio" (u*q <= p with residual correction; spec_accept) or "exact"
+        (a draft counts only if it is the trunk's own sample; spec_accept_exact)."""
+        if acceptance not in ("ratio", "exact"):
+            raise ValueError(f"acceptance must be 'ratio' or 'exact', not {acceptance!r}")
+        self.acceptance = acceptance
         self.W, self.wdt, self.V, self.d, self.Vd = W, wdt, V, d, Vd
         self.B, self.R, self.k_max, self.eos_id = B, R, k_max, eos_id
         dev = torch.device(device)
@@ -64,6 +70,11 @@ class SpecVerifyEngine:
                            self.logits, self.stats, self.ws)
 
     def accept(self, use_q=True):
+        if self.acceptance == "exact":
+            spec_accept_exact(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats,
+                              self.V, self.R, self.temps, self.eos_id, self.seeds, self.pos,
+                              self.out, self.counters, self.ws)
+            return
         q = self.q if (use_q and self.q is not None) else None
         spec_accept(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats, self.V,
                     self.R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
