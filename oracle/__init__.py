@@ -22,6 +22,9 @@ What it follows (sources are the pages' titles and sections):
   on rollback through whole-state checkpoints, on a replay that looped forever, and on keeping
   the checkpoints in device memory: restore, then replay the accepted tokens without checking
   them again, with the state never leaving the device.
+* Adaptive verify width (``adapt``; lucebox-hub PR #15, *What* and *Speed*): a per-depth moving
+  average of acceptance and a cycle-cost table choose the next width (the controller is this
+  build's reading; the pages give none).
 * Philox4x32-10: Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
   SC'11, section 3 (the Philox S-box) and Table 2 (round constants).
 
@@ -32,4 +35,4 @@ closed forms, brute force, library routines or published test vectors; the one e
 recorded as "parity unpinned" in its docstring.
 """
 
-from . import philox, lmhead, accept, state  # noqa: F401
+from . import philox, lmhead, accept, state, adapt  # noqa: F401

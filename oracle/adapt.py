@@ -1,0 +1,77 @@
+"""Adaptive verify width, chosen on the device each cycle (oracle; test infrastructure only).
+
+lucebox-hub PR #15 "MTP speculative decoding", *What* and *Speed*: the default verify width is
+adaptive -- it settles at seven drafts on a prompt the draft head predicts well and stays small
+where it does not. The pages do not give the controller; this is the plain reading SURVEY's
+NEXT item states: an exponential moving average of the acceptance rate at each draft depth plus a
+cycle-cost table, choosing the width with the most expected tokens per unit of cost.
+
+State per request (all float64 here): rate[d] for depth d = 1..7 -- the average, over the
+cycles that reached depth d, of "draft d was accepted given drafts 1..d-1 were" -- and the
+number of cycles observed.
+
+Update from one cycle's acceptance result (status, n_accept, eos_hit) at width k:
+    depth d = 1..n_accept: accepted (x = 1);
+    depth d = n_accept + 1 <= k, unless the block ended at an accepted EOS: rejected (x = 0);
+    deeper depths: not observed.
+    An observed depth moves as rate[d] += alpha * (x - rate[d]); a depth observed for the first
+    time starts at x. A request whose status is not OK leaves its state unchanged. Depths never
+    observed hold the prior 0.5.
+
+Choice: expected tokens at width k, with the depths independent at their rates,
+    E(k) = 1 + sum_{j=1..k} prod_{i=1..j} rate[i]
+(each accepted draft is a token, and the cycle always ends with one more: the correction or the
+bonus); the next width is the k in [0, k_max] maximising E(k) / cost[k], the smallest on ties.
+
+Pinned by: E(k) against exhaustive enumeration of the 2^k accept/reject patterns with those
+rates, and against a Monte Carlo of the acceptance chain; the EMA against its closed form; the
+choice at the corner cases (rates 1 -> k_max, rates 0 -> 0, flat cost -> the largest width).
+"""
+
+import numpy as np
+
+PRIOR = 0.5
+STATUS_OK = 0
+
+
+def new_state(k_max=7):
+    return {"rate": [None] * (k_max + 1), "cycles": 0}
+
+
+def observe(state, status, n_accept, eos_hit, k, alpha):
+    """Update the per-depth rates from one cycle's result (see the module doc)."""
+    if status != STATUS_OK:
+        return state
+    rate = state["rate"]
+    for d in range(1, k + 1):
+        if d <= n_accept:
+            x = 1.0
+        elif d == n_accept + 1 and not eos_hit:
+            x = 0.0
+        else:
+            break
+        rate[d] = x if rate[d] is None else rate[d] + alpha * (x - rate[d])
+    state["cycles"] += 1
+    return state
+
+
+def rates(state):
+    return [PRIOR if r is None else float(r) for r in state["rate"]]
+
+
+def expected_tokens(rate, k):
+    """E(k) = 1 + sum_j prod_{i<=j} rate[i] (rate[0] unused)."""
+    total, run = 1.0, 1.0
+    for j in range(1, k + 1):
+        run *= rate[j]
+        total += run
+    return total
+
+
+def choose(state, cost, k_max):
+    """The width in [0, k_max] with the most expected tokens per unit of cost (smallest on
+    ties). Returns (k, values)."""
+    r = rates(state)
+    vals = [expected_tokens(r, k) / cost[k] for k in range(k_max + 1)]
+    best = max(range(k_max + 1), key=lambda k: (vals[k], -k))
+    return best, vals

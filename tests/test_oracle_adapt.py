@@ -1,0 +1,73 @@
+"""Pins of the adaptive-width oracle (oracle/adapt.py) against what does not depend on it:
+exhaustive enumeration and a Monte Carlo of the acceptance chain for E(k), the closed form of
+the moving average, and the corner cases of the choice."""
+
+import itertools
+
+import numpy as np
+import pytest
+
+from oracle import adapt
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_expected_tokens_equals_enumeration(seed):
+    """E(k) against all 2^k accept/reject patterns: the cycle keeps drafts up to the first
+    rejection and always emits one more token."""
+    rng = np.random.default_rng(seed)
+    rate = [0.0] + list(rng.uniform(0, 1, 7))
+    for k in range(0, 8):
+        exp = 0.0
+        for pattern in itertools.product((0, 1), repeat=k):
+            pr = 1.0
+            for d, x in enumerate(pattern, start=1):
+                pr *= rate[d] if x else 1.0 - rate[d]
+            kept = next((i for i, x in enumerate(pattern) if not x), k)
+            exp += pr * (kept + 1)
+        assert adapt.expected_tokens(rate, k) == pytest.approx(exp, rel=1e-12, abs=1e-12)
+
+
+def test_expected_tokens_monte_carlo():
+    rng = np.random.default_rng(7)
+    rate = [0.0, 0.9, 0.8, 0.7, 0.6, 0.5, 0.4, 0.3]
+    n, k = 200_000, 7
+    u = rng.uniform(size=(n, k))
+    ok = u < np.array(rate[1:k + 1])
+    kept = np.where(ok.all(axis=1), k, np.argmin(ok, axis=1))
+    assert adapt.expected_tokens(rate, k) == pytest.approx((kept + 1).mean(), rel=5e-3)
+
+
+def test_moving_average_closed_form():
+    """With depth 1 accepted in every cycle after a first rejection, rate[1] after n cycles is
+    1 - (1 - alpha)^(n - 1) (it starts at the first observation, 0)."""
+    alpha = 0.1
+    st = adapt.new_state()
+    adapt.observe(st, 0, 0, False, 3, alpha)
+    for n in range(2, 30):
+        adapt.observe(st, 0, 3, False, 3, alpha)
+        assert st["rate"][1] == pytest.approx(1 - (1 - alpha) ** (n - 1), rel=1e-12)
+    assert st["cycles"] == 29
+
+
+def test_observation_rules():
+    st = adapt.new_state()
+    adapt.observe(st, 0, 2, False, 5, 0.5)  # depths 1, 2 kept, 3 rejected, 4-5 unseen
+    assert st["rate"][1:6] == [1.0, 1.0, 0.0, None, None]
+    adapt.observe(st, 0, 1, True, 5, 0.5)  # depth 1 kept and it was EOS: nothing else seen
+    assert st["rate"][1:4] == [1.0, 1.0, 0.0]
+    adapt.observe(st, 1, 0, False, 5, 0.5)  # a failed request changes nothing
+    assert st["cycles"] == 2
+    assert adapt.rates(st)[4] == adapt.PRIOR
+
+
+def test_choice_corner_cases():
+    cost = [1.0 + 0.3 * k for k in range(8)]
+    st = adapt.new_state()
+    st["rate"] = [None] + [1.0] * 7
+    assert adapt.choose(st, cost, 7)[0] == 7
+    st["rate"] = [None] + [0.0] * 7
+    assert adapt.choose(st, cost, 7)[0] == 0
+    flat = [1.0] * 8
+    st["rate"] = [None] + [0.2] * 7
+    assert adapt.choose(st, flat, 7)[0] == 7  # more width never loses when it costs nothing
+    assert adapt.choose(st, flat, 3)[0] == 3
