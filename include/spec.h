@@ -192,13 +192,18 @@ spec_status spec_lmhead_verify(const void *W, spec_dtype wdt, int64_t V, int64_t
  *   q_logits    [B, q_stride] float32 (row b at q_logits + b*q_stride, first V_draft used) or
  *               NULL; required when any temperature > 0 (a request with T > 0 and no q_logits
  *               gets token -1). q_stats [B] or NULL.
+ *   k_active    [B] int32 device array or NULL: this call is draft pos_offset + 1 of the cycle,
+ *               and request b needs it only if k_active[b] > pos_offset. When no request needs
+ *               it the launch returns at once and writes nothing, so a host can always enqueue
+ *               k_max draft steps and let widths chosen on the device (spec_adapt_width) decide
+ *               how many do work. Outputs of requests that do not need the step are not used.
  */
 spec_status spec_draft_argmax(const void *W, spec_dtype wdt, int64_t V_draft, int64_t d,
                               const void *h, int32_t B, const float *temperature,
                               const uint64_t *seed, const int64_t *pos, int32_t pos_offset,
                               int32_t *token_out, int32_t token_stride, float *q_logits,
-                              int64_t q_stride, spec_rowstats *q_stats, void *workspace,
-                              size_t workspace_bytes, spec_stream_t stream);
+                              int64_t q_stride, spec_rowstats *q_stats, const int32_t *k_active,
+                              void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
  * spec_accept -- acceptance, residual correction, bonus token and EOS truncation for B
@@ -256,6 +261,35 @@ spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t *k, const 
                               const uint64_t *seed, const int64_t *pos_base,
                               spec_accept_out *out, spec_counters *counters, void *workspace,
                               size_t workspace_bytes, spec_stream_t stream);
+
+/* Adaptive width state of one request (64 bytes, zero-filled before the first cycle). */
+typedef struct {
+  float rate[8];    /* rate[d], d = 1..7: moving average of "draft d accepted, given 1..d-1 were" */
+  uint32_t seen;    /* bit d set once depth d has been observed (until then rate[d] counts 0.5) */
+  uint32_t cycles;  /* cycles observed */
+  int32_t k;        /* the width chosen for the next cycle */
+  int32_t reserved[5];
+} spec_width_state;
+
+/*
+ * spec_adapt_width -- choose each request's next verify width on the device (lucebox-hub PR
+ * #15, "What" and "Speed": the default width is adaptive; the controller below is this
+ * library's, the pages give none).
+ *
+ * From request b's result out[b] of a cycle run at width k_used[b]: depths 1..n_accept were
+ * accepted, depth n_accept + 1 (if <= k_used and the block did not end at an accepted EOS) was
+ * rejected, deeper ones were not observed. Each observed depth moves its rate by
+ * alpha * (x - rate) (x = 1 accepted, 0 rejected; every depth starts at 0.5). A request whose
+ * status is not OK keeps its rates. Then, with E(k) = 1 + sum_{j<=k} prod_{i<=j} rate[i] the
+ * expected tokens of a cycle at width k, the next width is the k in [1, k_max] maximising
+ * E(k) / cost[k] (the smallest on ties; never 0, so depth 1 stays observed and a request whose
+ * drafts start failing can recover), written to k_next[b] and state[b].k.
+ *   cost    [k_max + 1] float device array: the relative time of a cycle at each width.
+ *   alpha   in (0, 1].  k_used and k_next may be the same array.
+ */
+spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out *out,
+                             const int32_t *k_used, const float *cost, float alpha,
+                             spec_width_state *state, int32_t *k_next, spec_stream_t stream);
 
 /*
  * spec_commit_rollback -- keep the accepted prefix, drop the rest, on the device (DS4Server

@@ -11,11 +11,12 @@ from . import _abi
 from ._abi import (ACCEPT_OUT_DTYPE, COUNTERS_DTYPE, REQ_BAD_K, REQ_BAD_TOKEN,  # noqa: F401
                    REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_NONFINITE, REQ_OK, ROWSTATS_DTYPE,
                    SPEC_BF16, SPEC_COMMIT_REPLAY, SPEC_COMMIT_SNAPSHOT, SPEC_F32,
-                   spec_state_desc)
+                   WIDTH_STATE_DTYPE, spec_state_desc)
 
 ROWSTATS_BYTES = ROWSTATS_DTYPE.itemsize
 ACCEPT_OUT_BYTES = ACCEPT_OUT_DTYPE.itemsize
 COUNTERS_BYTES = COUNTERS_DTYPE.itemsize
+WIDTH_STATE_BYTES = WIDTH_STATE_DTYPE.itemsize
 
 
 class SpecError(RuntimeError):
@@ -67,11 +68,12 @@ def spec_lmhead_verify(W, wdt, V, d, H, B, R, temperature, logits, stats, worksp
 
 
 def spec_draft_argmax(W, wdt, V_draft, d, h, B, temperature, seed, pos, pos_offset, token_out,
-                      token_stride, q_logits, q_stride, q_stats, workspace, stream=None):
+                      token_stride, q_logits, q_stride, q_stats, k_active, workspace,
+                      stream=None):
     _check("spec_draft_argmax", _abi.lib().spec_draft_argmax(
         _ptr(W), wdt, V_draft, d, _ptr(h), B, _ptr(temperature), _ptr(seed), _ptr(pos),
         pos_offset, _ptr(token_out), token_stride, _ptr(q_logits), q_stride, _ptr(q_stats),
-        _ptr(workspace), _nbytes(workspace), _stream(stream)))
+        _ptr(k_active), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
 def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_draft, q_stride,
@@ -80,6 +82,12 @@ def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_d
         B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(q_logits),
         _ptr(q_stats), V_draft, q_stride, _ptr(temperature), eos_id, _ptr(seed), _ptr(pos_base),
         _ptr(out), _ptr(counters), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def spec_adapt_width(B, k_max, out, k_used, cost, alpha, state, k_next, stream=None):
+    _check("spec_adapt_width", _abi.lib().spec_adapt_width(
+        B, k_max, _ptr(out), _ptr(k_used), _ptr(cost), float(alpha), _ptr(state), _ptr(k_next),
+        _stream(stream)))
 
 
 def spec_accept_exact(B, k_max, k, drafts, logits, stats, V, R, temperature, eos_id, seed,

@@ -16,7 +16,8 @@ REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN 
 
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
 EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
-           "spec_accept", "spec_accept_exact", "spec_commit_rollback", "spec_batched_supported",
+           "spec_accept", "spec_accept_exact", "spec_adapt_width", "spec_commit_rollback",
+           "spec_batched_supported",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes")
 
 # numpy views of the device structs (for reading results copied to the host)
@@ -26,6 +27,8 @@ ACCEPT_OUT_DTYPE = np.dtype([("status", "<i4"), ("n_accept", "<i4"), ("n_emit", 
                              ("eos_hit", "<i4"), ("tokens", "<i4", (8,)),
                              ("sample_kind", "<i4"), ("sample_row", "<i4"),
                              ("reserved", "<i4", (2,))])
+WIDTH_STATE_DTYPE = np.dtype([("rate", "<f4", (8,)), ("seen", "<u4"), ("cycles", "<u4"),
+                              ("k", "<i4"), ("reserved", "<i4", (5,))])
 COUNTERS_DTYPE = np.dtype([("cycles", "<u8"), ("drafted", "<u8"), ("accepted", "<u8"),
                            ("emitted", "<u8"), ("eos", "<u8"), ("errors", "<u8"),
                            ("depth", "<u8", (8,))])
@@ -81,7 +84,7 @@ def lib():
         L.spec_lmhead_verify.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, vp, sz, vp]
         L.spec_lmhead_verify.restype = i32
         L.spec_draft_argmax.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp, i32, vp, i32, vp,
-                                        i64, vp, vp, sz, vp]
+                                        i64, vp, vp, vp, sz, vp]
         L.spec_draft_argmax.restype = i32
         L.spec_accept.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, i64, i64, vp, i32,
                                   vp, vp, vp, vp, vp, sz, vp]
@@ -89,6 +92,8 @@ def lib():
         L.spec_accept_exact.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, i32, vp, vp, vp,
                                         vp, vp, sz, vp]
         L.spec_accept_exact.restype = i32
+        L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+        L.spec_adapt_width.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,
                                            vp]
         L.spec_commit_rollback.restype = i32

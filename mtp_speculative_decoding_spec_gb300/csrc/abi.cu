@@ -110,9 +110,9 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
                         int rows_per_req, const float* temperature, float* logits,
                         int64_t logits_stride, spec_rowstats* stats, int draft,
                         const uint64_t* seed, const int64_t* pos, int pos_offset,
-                        int32_t* token_out, int token_stride, void* workspace,
-                        const WsLayout& wl, int grid, const DevAttr& a, EncodeTiledFn encode,
-                        cudaStream_t stream) {
+                        int32_t* token_out, int token_stride, const int32_t* kact,
+                        void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
+                        EncodeTiledFn encode, cudaStream_t stream) {
   GemvTcLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
@@ -180,6 +180,7 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   p.pos_offset = pos_offset;
   p.token_out = token_out;
   p.token_stride = token_stride;
+  p.kact = kact;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
@@ -193,7 +194,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
                      int nrows, int rows_per_req, const float* temperature, float* logits,
                      int64_t logits_stride, spec_rowstats* stats, int draft,
                      const uint64_t* seed, const int64_t* pos, int pos_offset,
-                     int32_t* token_out, int token_stride, void* workspace,
+                     int32_t* token_out, int token_stride, const int32_t* kact, void* workspace,
                      size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream) {
   const DevAttr a = dev_attr();
   if (a.sms <= 0) return SPEC_ERR_CUDA;
@@ -211,8 +212,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   const int grid = gemv_grid(V, a.sms);
   if (wdt == SPEC_BF16)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
-                       draft, seed, pos, pos_offset, token_out, token_stride, workspace, wl, grid,
-                       a, encode, stream);
+                       draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
+                       grid, a, encode, stream);
 
   GemvLaunch L;
   memset(&L, 0, sizeof(L));
@@ -276,6 +277,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.pos_offset = pos_offset;
   p.token_out = token_out;
   p.token_stride = token_stride;
+  p.kact = kact;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
@@ -427,7 +429,7 @@ spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t
                     workspace_bytes, B, reinterpret_cast<cudaStream_t>(stream));
   }
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
-                  nullptr, 0, nullptr, 0, workspace, workspace_bytes, B,
+                  nullptr, 0, nullptr, 0, nullptr, workspace, workspace_bytes, B,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -435,8 +437,8 @@ spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, in
                               const void* h, int32_t B, const float* temperature,
                               const uint64_t* seed, const int64_t* pos, int32_t pos_offset,
                               int32_t* token_out, int32_t token_stride, float* q_logits,
-                              int64_t q_stride, spec_rowstats* q_stats, void* workspace,
-                              size_t workspace_bytes, spec_stream_t stream) {
+                              int64_t q_stride, spec_rowstats* q_stats, const int32_t* k_active,
+                              void* workspace, size_t workspace_bytes, spec_stream_t stream) {
   if (!W || !h || !temperature || !seed || !pos || !token_out || !workspace)
     return SPEC_ERR_INVALID;
   if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
@@ -445,8 +447,8 @@ spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, in
   if (token_stride < 1 || (q_logits && q_stride < V_draft)) return SPEC_ERR_INVALID;
   if (!aligned16(W) || !aligned16(h) || !aligned16(workspace)) return SPEC_ERR_INVALID;
   return run_gemv(W, wdt, V_draft, d, h, B, 1, temperature, q_logits, q_stride, q_stats, 1,
-                  seed, pos, pos_offset, token_out, token_stride, workspace, workspace_bytes,
-                  B, reinterpret_cast<cudaStream_t>(stream));
+                  seed, pos, pos_offset, token_out, token_stride, k_active, workspace,
+                  workspace_bytes, B, reinterpret_cast<cudaStream_t>(stream));
 }
 
 spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
@@ -459,6 +461,25 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_
   return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_draft,
                           q_stride, temperature, eos_id, seed, pos_base, out, counters, workspace,
                           workspace_bytes, stream, 0);
+}
+
+spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* out,
+                             const int32_t* k_used, const float* cost, float alpha,
+                             spec_width_state* state, int32_t* k_next, spec_stream_t stream) {
+  if (B < 1 || k_max < 0 || k_max > kMaxRows - 1) return SPEC_ERR_INVALID;
+  if (!out || !k_used || !cost || !state || !k_next) return SPEC_ERR_INVALID;
+  if (!(alpha > 0.f && alpha <= 1.f)) return SPEC_ERR_INVALID;
+  spec::AdaptParams p;
+  p.B = B;
+  p.k_max = k_max;
+  p.out = out;
+  p.k_used = k_used;
+  p.cost = cost;
+  p.alpha = alpha;
+  p.state = state;
+  p.k_next = k_next;
+  const cudaError_t e = spec::adapt_launch(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
@@ -581,5 +602,5 @@ extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt,
   // the ticket and the error word must start at zero (a previous call may have been cut short)
   if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return SPEC_ERR_CUDA;
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr, nullptr,
-                  0, nullptr, 0, scratch, kNoAllocScratchBytes, 0, s);
+                  0, nullptr, 0, nullptr, scratch, kNoAllocScratchBytes, 0, s);
 }

@@ -460,6 +460,58 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Adaptive width: one thread per request updates the per-depth acceptance rates from the cycle's
+// result and picks the next width (see spec_adapt_width in spec.h).
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
+  pdl_trigger();
+  pdl_wait();  // reads the acceptance results of the previous kernel
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  spec_width_state s = p.state[b];
+  const spec_accept_out o = p.out[b];
+  const int k = p.k_used[b];
+  if (o.status == SPEC_REQ_OK && k >= 0 && k <= kMaxRows - 1) {
+    for (int d = 1; d <= k; ++d) {
+      float x;
+      if (d <= o.n_accept)
+        x = 1.f;
+      else if (d == o.n_accept + 1 && !o.eos_hit)
+        x = 0.f;
+      else
+        break;
+      const float r = ((s.seen >> d) & 1u) ? s.rate[d] : 0.5f;  // unobserved: the prior
+      s.rate[d] = __fadd_rn(r, __fmul_rn(p.alpha, __fsub_rn(x, r)));
+      s.seen |= 1u << d;
+    }
+    s.cycles += 1u;
+  }
+  // expected tokens E(k) = 1 + sum_j prod_{i<=j} rate[i]; the best E(k) / cost[k] over
+  // k in [1, k_max] (never 0: the first draft is always tried, so depth 1 stays observed)
+  float e = 1.f, run = 1.f, best = -1.f;
+  const int lo = p.k_max < 1 ? p.k_max : 1;
+  int kb = lo;
+  for (int kk = 0; kk <= p.k_max; ++kk) {
+    if (kk > 0) {
+      run = __fmul_rn(run, ((s.seen >> kk) & 1u) ? s.rate[kk] : 0.5f);
+      e = __fadd_rn(e, run);
+    }
+    const float v = __fdiv_rn(e, p.cost[kk]);
+    if (kk >= lo && v > best) {
+      best = v;
+      kb = kk;
+    }
+  }
+  s.k = kb;
+  p.state[b] = s;
+  p.k_next[b] = kb;
+}
+
+cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream) {
+  return launch_pdl(adapt_width_kernel, dim3((prm.B + 127) / 128), dim3(128), 0, stream, prm);
+}
+
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream) {
   dim3 grid(prm.NS, prm.B);
   return launch_pdl(accept_kernel, grid, dim3(kAcceptThreads), 0, stream, prm);

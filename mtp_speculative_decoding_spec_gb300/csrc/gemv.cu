@@ -95,6 +95,7 @@ template <int RP, bool BF16>
 __global__ void __maxnreg__(128)
     gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
   pdl_wait();
+  if (draft_step_idle(p)) return;
   constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
   constexpr int PP = EPC / 2;               // element pairs per chunk
   constexpr int RH = RP >= 2 ? RP / 2 : 1;  // H row pairs held per 128-bit load

@@ -20,6 +20,17 @@ __device__ __forceinline__ void block_rows(int blk, int nblk, int64_t nbands, in
   if (v1 < v0) v1 = v0;
 }
 
+// Draft head with device-chosen widths: true when no row of this launch needs the step (every
+// k_active[b] <= pos_offset). Waits for the previous kernel first: the widths are written by
+// it. Uniform across the block (every thread reads the same values).
+__device__ __forceinline__ bool draft_step_idle(const GemvParams& p) {
+  if (p.kact == nullptr) return false;
+  pdl_wait();
+  for (int r = 0; r < p.nrows && r < kMaxRows; ++r)
+    if (p.kact[r] > p.pos_offset) return false;
+  return true;
+}
+
 // Per-row inputs of the statistics and the draw, read once at the start of the kernel (after
 // its dependency wait) so that the last block's finish does not wait on global loads.
 struct RowInputs {

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  if (draft_step_idle(p)) return;  // before any setup: nothing allocated, nothing in flight
   const int S = p.stages;
   // the ring of stages; once streaming is over it holds the block's statistics and then the
   // combine's scratch

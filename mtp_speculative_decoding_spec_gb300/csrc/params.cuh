@@ -35,6 +35,7 @@ struct GemvParams {
   int pos_offset;
   int32_t* token_out;
   int token_stride;
+  const int32_t* kact;  // draft head: row b needs this step only if kact[b] > pos_offset (nullable)
   WsHeader* hdr;
   GemvPartial* part;
 };
@@ -166,5 +167,16 @@ int gemv_tc_stat_bytes();
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
 cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
                           cudaStream_t stream);
+
+struct AdaptParams {
+  int B, k_max;
+  const spec_accept_out* out;
+  const int32_t* k_used;
+  const float* cost;
+  float alpha;
+  spec_width_state* state;
+  int32_t* k_next;
+};
+cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream);
 
 }  // namespace spec

@@ -9,16 +9,21 @@ results back, all asynchronously on the stream.
 
 import torch
 
-from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_BF16, spec_accept,
-               spec_accept_exact, spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
+from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_BF16,
+               WIDTH_STATE_BYTES, spec_accept, spec_accept_exact, spec_adapt_width,
+               spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
                spec_workspace_bytes)
 
 
 class SpecVerifyEngine:
     def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
-                 want_q_logits=True, acceptance="ratio"):
+                 want_q_logits=True, acceptance="ratio", adaptive_cost=None, alpha=0.1):
         """acceptance: "ratio" (u*q <= p with residual correction; spec_accept) or "exact"
-        (a draft counts only if it is the trunk's own sample; spec_accept_exact)."""
+        (a draft counts only if it is the trunk's own sample; spec_accept_exact).
+        adaptive_cost: None for fixed widths (set_requests(k=...)), or the relative cost of a
+        cycle at widths 0..k_max: each cycle then ends with spec_adapt_width choosing every
+        request's next width on the device, and ``cycle`` always enqueues k_max draft steps,
+        of which those past every request's width return at once."""
         if acceptance not in ("ratio", "exact"):
             raise ValueError(f"acceptance must be 'ratio' or 'exact', not {acceptance!r}")
         self.acceptance = acceptance
@@ -44,6 +49,13 @@ class SpecVerifyEngine:
         self.commit_status = torch.zeros(B, dtype=torch.int32, device=dev)
         self.state = None
         self.dtype_bytes = 2 if wdt == SPEC_BF16 else 4
+        self.adaptive = adaptive_cost is not None
+        self.alpha = alpha
+        if self.adaptive:
+            if len(adaptive_cost) != k_max + 1:
+                raise ValueError("adaptive_cost needs k_max + 1 entries")
+            self.cost = torch.tensor(adaptive_cost, dtype=torch.float32, device=dev)
+            self.width_state = torch.zeros(B * WIDTH_STATE_BYTES, dtype=torch.uint8, device=dev)
 
     # ---------------------------------------------------------------- configuration
     def set_requests(self, temps=None, seeds=None, pos=None, k=None):
@@ -63,7 +75,8 @@ class SpecVerifyEngine:
         spec_draft_argmax(self.W, self.wdt, self.Vd, self.d, h, B, self.temps, self.seeds,
                           self.pos, i - 1, self.drafts[:, i - 1:], self.drafts.shape[1],
                           None if self.q is None else self.q[(i - 1) * B:], self.Vd,
-                          self.qs[(i - 1) * B * ROWSTATS_BYTES:], self.ws)
+                          self.qs[(i - 1) * B * ROWSTATS_BYTES:],
+                          self.k if self.adaptive else None, self.ws)
 
     def verify(self, H):
         spec_lmhead_verify(self.W, self.wdt, self.V, self.d, H, self.B, self.R, self.temps,
@@ -85,15 +98,23 @@ class SpecVerifyEngine:
             spec_commit_rollback(self.B, self.state, self.out, self.k, self.state_mode,
                                  self.commit_status)
 
+    def adapt(self):
+        if self.adaptive:
+            spec_adapt_width(self.B, self.k_max, self.out, self.k, self.cost, self.alpha,
+                             self.width_state, self.k)
+
     def verify_cycle(self, H):
-        """Verify + accept (+ commit): one verify cycle on device-resident inputs."""
+        """Verify + accept (+ commit, + the next width when adaptive): one verify cycle on
+        device-resident inputs."""
         self.verify(H)
         self.accept()
         self.commit()
+        self.adapt()
 
     def cycle(self, H, Hd, k):
-        """Full cycle: k draft steps (Hd [k, B, d]), verify, accept, commit."""
-        for i in range(1, k + 1):
+        """Full cycle: k draft steps (Hd [k, B, d]; k_max of them when adaptive), verify,
+        accept, commit."""
+        for i in range(1, (self.k_max if self.adaptive else k) + 1):
             self.draft_step(i, Hd[i - 1])
         self.verify_cycle(H)
 

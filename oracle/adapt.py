@@ -14,18 +14,19 @@ Update from one cycle's acceptance result (status, n_accept, eos_hit) at width k
     depth d = 1..n_accept: accepted (x = 1);
     depth d = n_accept + 1 <= k, unless the block ended at an accepted EOS: rejected (x = 0);
     deeper depths: not observed.
-    An observed depth moves as rate[d] += alpha * (x - rate[d]); a depth observed for the first
-    time starts at x. A request whose status is not OK leaves its state unchanged. Depths never
-    observed hold the prior 0.5.
+    Every depth starts at the prior 0.5 and each observation moves it as
+    rate[d] += alpha * (x - rate[d]). A request whose status is not OK leaves its state unchanged.
 
 Choice: expected tokens at width k, with the depths independent at their rates,
     E(k) = 1 + sum_{j=1..k} prod_{i=1..j} rate[i]
 (each accepted draft is a token, and the cycle always ends with one more: the correction or the
-bonus); the next width is the k in [0, k_max] maximising E(k) / cost[k], the smallest on ties.
+bonus); the next width is the k in [1, k_max] maximising E(k) / cost[k], the smallest on ties.
+The width never drops to 0: at least the first draft is always tried, so depth 1 stays observed
+and a request whose drafts start failing can recover (at width 0 nothing would be observed).
 
 Pinned by: E(k) against exhaustive enumeration of the 2^k accept/reject patterns with those
 rates, and against a Monte Carlo of the acceptance chain; the EMA against its closed form; the
-choice at the corner cases (rates 1 -> k_max, rates 0 -> 0, flat cost -> the largest width).
+choice at the corner cases (rates 1 -> k_max, rates 0 -> 1, flat cost -> the largest width).
 """
 
 import numpy as np
@@ -50,7 +51,8 @@ def observe(state, status, n_accept, eos_hit, k, alpha):
             x = 0.0
         else:
             break
-        rate[d] = x if rate[d] is None else rate[d] + alpha * (x - rate[d])
+        r = PRIOR if rate[d] is None else rate[d]
+        rate[d] = r + alpha * (x - r)
     state["cycles"] += 1
     return state
 
@@ -69,9 +71,10 @@ def expected_tokens(rate, k):
 
 
 def choose(state, cost, k_max):
-    """The width in [0, k_max] with the most expected tokens per unit of cost (smallest on
-    ties). Returns (k, values)."""
+    """The width in [min(1, k_max), k_max] with the most expected tokens per unit of cost
+    (smallest on ties). Returns (k, values) with values[k] for every k in [0, k_max]."""
     r = rates(state)
     vals = [expected_tokens(r, k) / cost[k] for k in range(k_max + 1)]
-    best = max(range(k_max + 1), key=lambda k: (vals[k], -k))
+    lo = min(1, k_max)
+    best = max(range(lo, k_max + 1), key=lambda k: (vals[k], -k))
     return best, vals

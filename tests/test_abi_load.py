@@ -84,7 +84,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_lmhead_verify(fake, 0, 1 << 24, 64, fake, 1, 1, fake, null, fake, fake,
                                   1 << 20, null) == 1
     assert lib.spec_draft_argmax(fake, 0, 10, 64, fake, 9, fake, fake, fake, 0, fake, 1, null,
-                                 0, null, fake, 1 << 20, null) == 1
+                                 0, null, null, fake, 1 << 20, null) == 1
     assert lib.spec_accept(0, 3, fake, fake, fake, fake, 10, 4, null, null, 10, 10, fake, 2,
                            fake, fake, fake, null, fake, 1 << 20, null) == 1
     assert lib.spec_accept(1, 8, fake, fake, fake, fake, 10, 4, null, null, 10, 10, fake, 2,
@@ -121,7 +121,7 @@ def test_no_cpu_fallback_in_product_package():
 # threads per block of each kernel, as launched by abi.cu / gemv.cu
 _BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemm_rows_tc_kernel": 10 * 32,
                   "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_snapshot_kernel": 256,
-                  "commit_replay_kernel": 256}
+                  "commit_replay_kernel": 256, "adapt_width_kernel": 128}
 
 
 def test_register_budget_per_sub_partition(lib):

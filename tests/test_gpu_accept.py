@@ -55,7 +55,7 @@ class Cycle:
         B, Vd = self.B, self.cfg.Vd
         spec.spec_draft_argmax(self.Wd, wdt_of(self.cfg), Vd, self.cfg.d, h, B, temps, seeds, pos,
                                i - 1, self.drafts[:, i - 1:], self.k_max, self.q[(i - 1) * B:],
-                               Vd, self.qs[(i - 1) * B * spec.ROWSTATS_BYTES:], self.ws)
+                               Vd, self.qs[(i - 1) * B * spec.ROWSTATS_BYTES:], None, self.ws)
 
     def verify(self, H, temps):
         spec.spec_lmhead_verify(self.Wd, wdt_of(self.cfg), self.cfg.V, self.cfg.d, H, self.B,

@@ -166,7 +166,7 @@ def _draft_case(cfg, W, Wd, Vd, h, temps, seeds, pos, off):
     spec.spec_draft_argmax(Wd, wdt_of(cfg), Vd, cfg.d, to_dev(h), B,
                            torch.tensor(temps, dtype=torch.float32, device=dev()),
                            to_dev(np.array(seeds, dtype=np.uint64)),
-                           to_dev(np.array(pos, dtype=np.int64)), off, tok, 1, q, Vd, qs, ws)
+                           to_dev(np.array(pos, dtype=np.int64)), off, tok, 1, q, Vd, qs, None, ws)
     torch.cuda.synchronize()
     assert ws_error(ws) == 0
     tok, q, qs = to_np(tok), to_np(q), to_np(qs, spec.ROWSTATS_DTYPE)

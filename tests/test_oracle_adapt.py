@@ -38,23 +38,25 @@ def test_expected_tokens_monte_carlo():
 
 
 def test_moving_average_closed_form():
-    """With depth 1 accepted in every cycle after a first rejection, rate[1] after n cycles is
-    1 - (1 - alpha)^(n - 1) (it starts at the first observation, 0)."""
+    """From the prior 0.5, one rejection of depth 1 and then n - 1 acceptances leave
+    rate[1] = 1 - (1 - 0.5 (1 - alpha)) (1 - alpha)^(n - 1)."""
     alpha = 0.1
     st = adapt.new_state()
     adapt.observe(st, 0, 0, False, 3, alpha)
+    assert st["rate"][1] == pytest.approx(0.5 * (1 - alpha), rel=1e-12)
     for n in range(2, 30):
         adapt.observe(st, 0, 3, False, 3, alpha)
-        assert st["rate"][1] == pytest.approx(1 - (1 - alpha) ** (n - 1), rel=1e-12)
+        want = 1 - (1 - 0.5 * (1 - alpha)) * (1 - alpha) ** (n - 1)
+        assert st["rate"][1] == pytest.approx(want, rel=1e-12)
     assert st["cycles"] == 29
 
 
 def test_observation_rules():
     st = adapt.new_state()
     adapt.observe(st, 0, 2, False, 5, 0.5)  # depths 1, 2 kept, 3 rejected, 4-5 unseen
-    assert st["rate"][1:6] == [1.0, 1.0, 0.0, None, None]
+    assert st["rate"][1:6] == [0.75, 0.75, 0.25, None, None]
     adapt.observe(st, 0, 1, True, 5, 0.5)  # depth 1 kept and it was EOS: nothing else seen
-    assert st["rate"][1:4] == [1.0, 1.0, 0.0]
+    assert st["rate"][1:4] == [0.875, 0.75, 0.25]
     adapt.observe(st, 1, 0, False, 5, 0.5)  # a failed request changes nothing
     assert st["cycles"] == 2
     assert adapt.rates(st)[4] == adapt.PRIOR
@@ -66,7 +68,8 @@ def test_choice_corner_cases():
     st["rate"] = [None] + [1.0] * 7
     assert adapt.choose(st, cost, 7)[0] == 7
     st["rate"] = [None] + [0.0] * 7
-    assert adapt.choose(st, cost, 7)[0] == 0
+    assert adapt.choose(st, cost, 7)[0] == 1  # never below one draft: depth 1 stays observed
+    assert adapt.choose(st, cost, 0)[0] == 0
     flat = [1.0] * 8
     st["rate"] = [None] + [0.2] * 7
     assert adapt.choose(st, flat, 7)[0] == 7  # more width never loses when it costs nothing
