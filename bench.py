@@ -39,9 +39,9 @@ from synth import configs, gen  # noqa: E402
 METRIC = "verify cycles/s & emitted tok/s at k=1..7; LM-head HBM GB/s vs 8 TB/s"
 # DRAM traffic (bytes read + written) of one 2-row verify launch of gemv_tc_kernel on the
 # headline workload, from the ncu capture summarised in
-# profiles/gemv_tc_kernel_verify_V151936_d2560.md (778,042,368 read + 3,998,208 written).
+# profiles/gemv_tc_kernel_verify_V151936_d2560.md (778,043,392 read + 3,574,528 written).
 # Set back to None whenever the kernel changes until it is captured again.
-GEMV_TRAFFIC_BYTES = 782040576
+GEMV_TRAFFIC_BYTES = 781617920
 
 
 def parse():
@@ -294,6 +294,9 @@ def run_ours(args, rank, local_rank, world):
                          max_over_ranks)
         if not args.no_sweep:
             res["sweep"] = sweep(dev, W, Wd, hbm_peak)
+            step_us = elapsed_max / K * 1e6
+            draft_us = max(1.0, 1e6 / res["full_cycle"]["cycles_s"] - step_us)
+            res["adaptive"] = adaptive_bench(dev, W, Wd, step_us, draft_us)
             res["commit"] = commit_bench(dev, hbm_peak)
             res["batched"] = batched_bench(dev, W, Wd, hbm_peak, tf_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
@@ -452,6 +455,70 @@ def sweep(dev, W, Wd, hbm_peak):
             "accept_us": round(accept_us, 2)}
         del eng, Hp_d, Hdp_d
     return out
+
+
+def adaptive_bench(dev, W, Wd, step_us, draft_us, K=400):
+    """Adaptive verify width on the k-sweep's greedy workload: the width of every cycle is
+    chosen on the device (spec_adapt_width) from a cost table built from this run's measured
+    verify + acceptance step and draft step; k_max = 7 draft steps are enqueued per cycle and
+    those past the chosen width return at once. Compare with the sweep's fixed-width points."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
+    k_max, n_pool = 7, 32
+    cfg = configs.Config(**{**configs.get(2).__dict__, "k": k_max, "temps": (0.0,)})
+    Hp, Hdp = build_inputs(cfg, W, n_pool, k_max, 0.0, rng_seed=7 * k_max)
+    Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+    Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+    cost = [(step_us + k * draft_us) / step_us for k in range(k_max + 1)]
+    eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
+                           cfg.eos_id, device=dev, adaptive_cost=cost, alpha=0.1)
+    eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])
+    for c in range(20):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
+    torch.cuda.synchronize()
+    eng.counters.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for c in range(K):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
+    b.record()
+    torch.cuda.synchronize()
+    s = a.elapsed_time(b) / 1e3
+    cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+    st = eng.width_state.cpu().numpy().view(spec.WIDTH_STATE_DTYPE)[0]
+    res = {"full_cycles_s": round(K / s, 1),
+           "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
+           "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
+           "mean_width": round(float(cnt["drafted"]) / K, 3),
+           "final_width": int(st["k"]),
+           "rates": [round(float(st["rate"][d]), 3) if (int(st["seen"]) >> d) & 1 else None
+                     for d in range(1, k_max + 1)],
+           "cost": [round(x, 3) for x in cost],
+           "workload": "k = 7 greedy sweep inputs, k_max = 7 draft steps enqueued per cycle"}
+    del eng
+    # every fixed width on the same inputs (the first k + 1 verify rows and k draft rows)
+    fixed = {}
+    for k in range(1, k_max + 1):
+        eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
+                               cfg.eos_id, device=dev)
+        eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[k])
+        for c in range(5):
+            eng.cycle(Hp_d[c, :k + 1], Hdp_d[c, :k, None, :], k)
+        torch.cuda.synchronize()
+        eng.counters.zero_()
+        a.record()
+        for c in range(K):
+            eng.cycle(Hp_d[c % n_pool, :k + 1], Hdp_d[c % n_pool, :k, None, :], k)
+        b.record()
+        torch.cuda.synchronize()
+        s = a.elapsed_time(b) / 1e3
+        cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+        fixed[f"k{k}"] = round(float(cnt["emitted"]) / s, 1)
+        del eng
+    res["fixed_emitted_tok_s"] = fixed
+    return res
 
 
 def commit_bench(dev, hbm_peak, reps=20, warm=3):

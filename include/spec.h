@@ -265,7 +265,8 @@ spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t *k, const 
 /* Adaptive width state of one request (64 bytes, zero-filled before the first cycle). */
 typedef struct {
   float rate[8];    /* rate[d], d = 1..7: moving average of "draft d accepted, given 1..d-1 were" */
-  uint32_t seen;    /* bit d set once depth d has been observed (until then rate[d] counts 0.5) */
+  uint32_t seen;    /* bit d set once depth d has been observed (until then it is believed to
+                       do as well as depth d - 1; depth 1 starts at 0.5) */
   uint32_t cycles;  /* cycles observed */
   int32_t k;        /* the width chosen for the next cycle */
   int32_t reserved[5];
@@ -279,8 +280,10 @@ typedef struct {
  * From request b's result out[b] of a cycle run at width k_used[b]: depths 1..n_accept were
  * accepted, depth n_accept + 1 (if <= k_used and the block did not end at an accepted EOS) was
  * rejected, deeper ones were not observed. Each observed depth moves its rate by
- * alpha * (x - rate) (x = 1 accepted, 0 rejected; every depth starts at 0.5). A request whose
- * status is not OK keeps its rates. Then, with E(k) = 1 + sum_{j<=k} prod_{i<=j} rate[i] the
+ * alpha * (x - rate) (x = 1 accepted, 0 rejected). A depth not yet observed is believed to do
+ * as well as the depth above it (0.5 for depth 1), so widths grow while drafts keep being
+ * accepted. A request whose status is not OK keeps its rates. Then, with
+ * E(k) = 1 + sum_{j<=k} prod_{i<=j} belief[i] the
  * expected tokens of a cycle at width k, the next width is the k in [1, k_max] maximising
  * E(k) / cost[k] (the smallest on ties; never 0, so depth 1 stays observed and a request whose
  * drafts start failing can recover), written to k_next[b] and state[b].k.

@@ -472,6 +472,11 @@ __global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
   spec_width_state s = p.state[b];
   const spec_accept_out o = p.out[b];
   const int k = p.k_used[b];
+  // beliefs: an observed depth's rate, else the belief of the depth above (0.5 for depth 1)
+  float bel[kMaxRows];
+  bel[0] = 0.5f;
+  for (int d = 1; d < kMaxRows; ++d)
+    bel[d] = ((s.seen >> d) & 1u) ? s.rate[d] : (d > 1 ? bel[d - 1] : 0.5f);
   if (o.status == SPEC_REQ_OK && k >= 0 && k <= kMaxRows - 1) {
     for (int d = 1; d <= k; ++d) {
       float x;
@@ -481,20 +486,21 @@ __global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
         x = 0.f;
       else
         break;
-      const float r = ((s.seen >> d) & 1u) ? s.rate[d] : 0.5f;  // unobserved: the prior
-      s.rate[d] = __fadd_rn(r, __fmul_rn(p.alpha, __fsub_rn(x, r)));
+      s.rate[d] = __fadd_rn(bel[d], __fmul_rn(p.alpha, __fsub_rn(x, bel[d])));
       s.seen |= 1u << d;
     }
     s.cycles += 1u;
   }
   // expected tokens E(k) = 1 + sum_j prod_{i<=j} rate[i]; the best E(k) / cost[k] over
   // k in [1, k_max] (never 0: the first draft is always tried, so depth 1 stays observed)
+  for (int d = 1; d < kMaxRows; ++d)  // beliefs after this cycle's update
+    bel[d] = ((s.seen >> d) & 1u) ? s.rate[d] : (d > 1 ? bel[d - 1] : 0.5f);
   float e = 1.f, run = 1.f, best = -1.f;
   const int lo = p.k_max < 1 ? p.k_max : 1;
   int kb = lo;
   for (int kk = 0; kk <= p.k_max; ++kk) {
     if (kk > 0) {
-      run = __fmul_rn(run, ((s.seen >> kk) & 1u) ? s.rate[kk] : 0.5f);
+      run = __fmul_rn(run, bel[kk]);
       e = __fadd_rn(e, run);
     }
     const float v = __fdiv_rn(e, p.cost[kk]);

@@ -14,10 +14,15 @@ Update from one cycle's acceptance result (status, n_accept, eos_hit) at width k
     depth d = 1..n_accept: accepted (x = 1);
     depth d = n_accept + 1 <= k, unless the block ended at an accepted EOS: rejected (x = 0);
     deeper depths: not observed.
-    Every depth starts at the prior 0.5 and each observation moves it as
-    rate[d] += alpha * (x - rate[d]). A request whose status is not OK leaves its state unchanged.
+    Each observation moves the depth's belief b[d] as rate[d] = b[d] + alpha * (x - b[d]), b
+    taken before the cycle's update. The belief of an observed depth is its rate; that of a
+    depth never observed is the belief of the depth above it (0.5 for depth 1): a deeper draft
+    is assumed to do as well as the last one seen until it is tried, so widths grow while drafts
+    keep being accepted (with a fixed 0.5 for unseen depths a width of 1 never looks worth
+    extending and depth 2 is never observed). A request whose status is not OK leaves its
+    state unchanged.
 
-Choice: expected tokens at width k, with the depths independent at their rates,
+Choice: expected tokens at width k, with the depths independent at their beliefs,
     E(k) = 1 + sum_{j=1..k} prod_{i=1..j} rate[i]
 (each accepted draft is a token, and the cycle always ends with one more: the correction or the
 bonus); the next width is the k in [1, k_max] maximising E(k) / cost[k], the smallest on ties.
@@ -44,6 +49,7 @@ def observe(state, status, n_accept, eos_hit, k, alpha):
     if status != STATUS_OK:
         return state
     rate = state["rate"]
+    before = rates(state)
     for d in range(1, k + 1):
         if d <= n_accept:
             x = 1.0
@@ -51,14 +57,19 @@ def observe(state, status, n_accept, eos_hit, k, alpha):
             x = 0.0
         else:
             break
-        r = PRIOR if rate[d] is None else rate[d]
-        rate[d] = r + alpha * (x - r)
+        rate[d] = before[d] + alpha * (x - before[d])
     state["cycles"] += 1
     return state
 
 
 def rates(state):
-    return [PRIOR if r is None else float(r) for r in state["rate"]]
+    """Beliefs b[0..k_max]: the rate of an observed depth, else the belief of the depth above
+    (PRIOR for depth 1); b[0] is unused."""
+    b = [PRIOR] * len(state["rate"])
+    for d in range(1, len(b)):
+        r = state["rate"][d]
+        b[d] = float(r) if r is not None else (b[d - 1] if d > 1 else PRIOR)
+    return b
 
 
 def expected_tokens(rate, k):

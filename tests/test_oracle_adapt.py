@@ -59,7 +59,19 @@ def test_observation_rules():
     assert st["rate"][1:4] == [0.875, 0.75, 0.25]
     adapt.observe(st, 1, 0, False, 5, 0.5)  # a failed request changes nothing
     assert st["cycles"] == 2
-    assert adapt.rates(st)[4] == adapt.PRIOR
+    assert adapt.rates(st)[4] == st["rate"][3]  # unseen depth: the belief of the one above
+
+
+def test_unseen_depths_follow_the_last_seen_one():
+    """Only depth 1 observed (accepted every cycle): every deeper depth is believed as good, so
+    the width grows past 1 where a fixed 0.5 for unseen depths would keep it at 1."""
+    st = adapt.new_state()
+    for _ in range(40):
+        adapt.observe(st, 0, 1, False, 1, 0.1)
+    b = adapt.rates(st)
+    assert b[1] > 0.95 and b[2:] == [b[1]] * 6
+    cost = [1.0 + 0.5 * k for k in range(8)]
+    assert adapt.choose(st, cost, 7)[0] > 1
 
 
 def test_choice_corner_cases():
