@@ -25,14 +25,17 @@ What it follows (sources are the pages' titles and sections):
 * Adaptive verify width (``adapt``; lucebox-hub PR #15, *What* and *Speed*): a per-depth moving
   average of acceptance and a cycle-cost table choose the next width (the controller is this
   build's reading; the pages give none).
+* 4-bit affine LM-head weights (``quant``; DS4Server issue #98, closing comment: 4-bit affine
+  values in groups of 32): the byte layout and the once-rounded bf16 dequantisation are this
+  build's reading.
 * Philox4x32-10: Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
   SC'11, section 3 (the Philox S-box) and Table 2 (round constants).
 
 Modules: ``philox`` (uniforms), ``lmhead`` (logits and row statistics), ``accept`` (drafting,
 acceptance, residual and bonus sampling, EOS), ``state`` (KV trim, snapshot commit, replay on
-the synthetic recurrent step). Every function is pinned by a ``-m "not gpu"`` test against
+the synthetic recurrent step), ``adapt`` (adaptive width), ``quant`` (4-bit weights). Every function is pinned by a ``-m "not gpu"`` test against
 closed forms, brute force, library routines or published test vectors; the one exception is
 recorded as "parity unpinned" in its docstring.
 """
 
-from . import philox, lmhead, accept, state, adapt  # noqa: F401
+from . import philox, lmhead, accept, state, adapt, quant  # noqa: F401

@@ -123,3 +123,58 @@ def state_inputs(cfg, k, seed=0, capacity=None, P=None, n_slots=None):
     for arr in (a, b, c, x):
         arr[k + 1:] = 0
     return dict(kv_pre=kv_pre, kv_rows=kv_rows, P=P, S0=S0, conv0=conv0, a=a, b=b, c=c, x=x)
+
+
+_Q4_CACHE = {}
+
+
+def q4_pack(q, s_bits, b_bits):
+    """4-bit codes q [V, d] (0..15) and bf16 scale / bias bits [V, d/32] -> rows of 5d/8 bytes:
+    d/2 bytes of codes (in each little-endian 32-bit word of 8 consecutive codes e0..e7, e_{2i}
+    in bits 4i..4i+3 and e_{2i+1} in bits 16+4i..16+4i+3), then the (scale, bias) pairs."""
+    q = np.asarray(q, dtype=np.uint32)
+    V, d = q.shape
+    e = q.reshape(V, d // 8, 8)
+    words = np.zeros((V, d // 8), dtype=np.uint32)
+    for i in range(4):
+        words |= e[:, :, 2 * i] << np.uint32(4 * i)
+        words |= e[:, :, 2 * i + 1] << np.uint32(16 + 4 * i)
+    sb = np.stack([np.asarray(s_bits, np.uint16), np.asarray(b_bits, np.uint16)], axis=-1)
+    out = np.empty((V, 5 * d // 8), dtype=np.uint8)
+    out[:, :d // 2] = words.astype("<u4").view(np.uint8).reshape(V, d // 2)
+    out[:, d // 2:] = sb.astype("<u2").view(np.uint8).reshape(V, d // 8)
+    return out
+
+
+def q4_quantise(W):
+    """Min/max affine quantisation of weights [V, d] (bf16 bits or float32) in groups of 32:
+    s = bf16((max - min) / 15), b = bf16(min), q = clip(rint((w - b) / s), 0, 15). Input
+    construction only: the quantised matrix is the workload, however it was made."""
+    w = as_f32(W)
+    V, d = w.shape
+    g = w.reshape(V, d // 32, 32)
+    lo, hi = g.min(axis=-1), g.max(axis=-1)
+    s_bits = f32_to_bf16((hi - lo) / np.float32(15))
+    b_bits = f32_to_bf16(lo)
+    s, b = bf16_to_f32(s_bits)[..., None], bf16_to_f32(b_bits)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s > 0, np.rint((g - b) / np.where(s > 0, s, 1)), 0)
+    q = np.clip(q, 0, 15).astype(np.uint8).reshape(V, d)
+    return q4_pack(q, s_bits, b_bits)
+
+
+def q4_weights(cfg, seed=0, cache=True):
+    """The bf16 LM head of ``cfg`` (lm_weights, same seed) quantised to 4-bit affine codes in
+    groups of 32: [V, 5d/8] uint8. Planted hidden rows keep using the bf16 matrix."""
+    key = (cfg.V, cfg.d, seed)
+    if cache and key in _Q4_CACHE:
+        return _Q4_CACHE[key]
+    from dataclasses import replace
+    W = lm_weights(replace(cfg, wdtype="bf16"), seed=seed, cache=cache)
+    out = np.empty((cfg.V, 5 * cfg.d // 8), dtype=np.uint8)
+    step = 16384
+    for v0 in range(0, cfg.V, step):
+        out[v0:v0 + step] = q4_quantise(W[v0:v0 + step])
+    if cache:
+        _Q4_CACHE[key] = out
+    return out
