@@ -41,7 +41,7 @@ METRIC = "verify cycles/s & emitted tok/s at k=1..7; LM-head HBM GB/s vs 8 TB/s"
 # headline workload, from the ncu capture summarised in
 # profiles/gemv_tc_kernel_verify_V151936_d2560.md (778,043,392 read + 3,574,528 written).
 # Set back to None whenever the kernel changes until it is captured again.
-GEMV_TRAFFIC_BYTES = 781617920
+GEMV_TRAFFIC_BYTES = None
 
 
 def parse():
@@ -298,6 +298,7 @@ def run_ours(args, rank, local_rank, world):
             draft_us = max(1.0, 1e6 / res["full_cycle"]["cycles_s"] - step_us)
             res["adaptive"] = adaptive_bench(dev, W, Wd, step_us, draft_us)
             res["commit"] = commit_bench(dev, hbm_peak)
+            res["q4"] = q4_bench(dev, W, hbm_peak)
             res["batched"] = batched_bench(dev, W, Wd, hbm_peak, tf_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         res["cpu_baseline"] = cpu_baseline(cfg, W, args.cpu_seconds)
@@ -313,8 +314,9 @@ def run_ours(args, rank, local_rank, world):
 def profile_extras(dev, W, Wd):
     """Launches for ncu captures after the greedy section: 5 sampled k=7 cycles (7 draft
     steps, an 8-row verify, acceptance with residual/bonus draws), 3 snapshot commits and 3
-    replay commits of the 64K-context state, then 5 batched 256-row verifies on the tensor
-    cores (each followed by a 32-request acceptance)."""
+    replay commits of the 64K-context state, 5 batched 256-row verifies on the tensor
+    cores (each followed by a 32-request acceptance), then the 4-bit head's section with 20
+    steps (20 warm-up cycles, 20 verify + acceptance steps, 20 cycles)."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -333,6 +335,7 @@ def profile_extras(dev, W, Wd):
     hbm_peak, tf_peak, _ = measured_peaks()
     commit_bench(dev, hbm_peak, reps=3, warm=0)
     batched_bench(dev, W, Wd, hbm_peak, tf_peak, reps=2, with_commit=False)
+    q4_bench(dev, W, hbm_peak, K=20)
 
 
 def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
@@ -519,6 +522,65 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=400):
         del eng
     res["fixed_emitted_tok_s"] = fixed
     return res
+
+
+def q4_bench(dev, W, hbm_peak, K=2000):
+    """The headline step (greedy, k = 1: verify 2 rows + acceptance) over the same LM head
+    quantised to 4-bit affine codes in groups of 32 (SPEC_Q4A32, 1,600 bytes per row): verify
+    launches bracketed by events in one step of ten (their mean is the kernel's duration alone),
+    the steps back to back, and full cycles with the draft head over the same quantised rows."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
+    cfg = configs.get(1)
+    Wq = gen.q4_weights(cfg)
+    Wq_d = torch.from_numpy(Wq).to(dev)
+    n_pool, k = 64, 1
+    Hp, Hdp = build_inputs(cfg, W, n_pool, k, 0.0, rng_seed=300)
+    Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
+    Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
+    eng = SpecVerifyEngine(Wq_d, spec.SPEC_Q4A32, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k, cfg.eos_id,
+                           device=dev, want_q_logits=False)
+    eng.set_requests(temps=[0.0], seeds=[0], pos=[0], k=[k])
+    for c in range(20):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K // 10)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for c in range(K):
+        if c % 10 == 0:
+            ev[c // 10][0].record()
+        eng.verify(Hp_d[c % n_pool])
+        if c % 10 == 0:
+            ev[c // 10][1].record()
+        eng.accept()
+    b.record()
+    torch.cuda.synchronize()
+    step_s = a.elapsed_time(b) / 1e3
+    launch_s = statistics.mean(x.elapsed_time(y) for x, y in ev) / 1e3
+    eng.counters.zero_()
+    a.record()
+    for c in range(K):
+        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k)
+    b.record()
+    torch.cuda.synchronize()
+    cyc_s = a.elapsed_time(b) / 1e3
+    cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+    err = int(eng.ws[4:8].cpu().numpy().view(np.uint32)[0])
+    algo = cfg.V * (5 * cfg.d // 8) + (k + 1) * cfg.d * 2 + (k + 1) * 16
+    gbs = algo / launch_s / 1e9
+    return {"kernel": "gemv_q4_kernel (verify, 2 rows)", "verify_cycles_s": round(K / step_s, 1),
+            "mean_launch_us": round(launch_s * 1e6, 2), "algorithmic_bytes_per_launch": algo,
+            "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4),
+            "full_cycles_s": round(K / cyc_s, 1),
+            "emitted_tok_s": round(float(cnt["emitted"]) / cyc_s, 1),
+            "acceptance": round(float(cnt["accepted"]) / max(1.0, float(cnt["drafted"])), 4),
+            "workspace_error": err,
+            "workload": "greedy k = 1 step over the 4-bit affine head (group 32), "
+                        "inputs larger than L2"}
 
 
 def commit_bench(dev, hbm_peak, reps=20, warm=3):

@@ -31,7 +31,8 @@
  *     bounded wait gives up; 0 means no error.
  *   - Limits: 1..8 verify rows per request (k = 0..7 drafts), at most 8 rows in total per
  *     spec_lmhead_verify / spec_draft_argmax call on the GEMV path; hidden size d with
- *     d * element_size a multiple of 16 bytes and d <= 3072 (bf16) / 1536 (fp32); V < 2^24.
+ *     d * element_size a multiple of 16 bytes and d <= 3072 (bf16) / 1536 (fp32), or d a
+ *     multiple of 128 up to 4096 (SPEC_Q4A32); V < 2^24.
  */
 #ifndef SPEC_H
 #define SPEC_H
@@ -52,7 +53,18 @@ typedef enum {
   SPEC_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
 } spec_status;
 
-typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+/*
+ * LM-head weight formats. SPEC_BF16 and SPEC_F32: [V, d] row-major. SPEC_Q4A32: 4-bit affine
+ * weights in groups of 32 (DS4Server issue #98, closing comment; the byte layout is this
+ * library's): each vocabulary row is 5d/8 bytes, d a multiple of 128 and at most 4096. Bytes
+ * [0, d/2) hold the codes q in 0..15: the codes of elements 8w..8w+7 (e0..e7) form the
+ * little-endian 32-bit word w, e_{2i} in bits 4i..4i+3 and e_{2i+1} in bits 16+4i..16+4i+3.
+ * Bytes [d/2, 5d/8) hold, per group g of elements 32g..32g+31, the bf16 scale s_g then the
+ * bf16 bias b_g. The weight the projection uses is bf16(s_g * q + b_g), rounded once to nearest
+ * even; H rows are bf16. The first V_draft rows of such a matrix are themselves a complete
+ * matrix, so the draft head reads the same buffer. The 9..256-row batched path takes bf16 only.
+ */
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1, SPEC_Q4A32 = 2 } spec_dtype;
 
 /* Per-request status written by spec_accept / spec_commit_rollback. */
 enum {
@@ -160,8 +172,10 @@ const char *spec_status_str(spec_status s);
  * all drafts are checked by one batched trunk forward; "Exactness": up to eight rows, a row's
  * verify logits may not depend on how many rows are verified together).
  *
- *   W           [V, d] LM-head weights, row-major (vocabulary-major), bf16 or fp32 (`wdt`).
- *   H           [B*R, d] verify hidden rows, same dtype as W; row b*R + r is request b's row r.
+ *   W           [V, d] LM-head weights, row-major (vocabulary-major), bf16 or fp32, or V rows
+ *               of 4-bit codes and pairs (`wdt`, see spec_dtype).
+ *   H           [B*R, d] verify hidden rows, same dtype as W (bf16 for SPEC_Q4A32); row
+ *               b*R + r is request b's row r.
  *   temperature [B] float; <= 0 means greedy for that request.
  *   logits      [B*R, V] float32 or NULL. Rows of requests with temperature > 0 receive
  *               z = H W^T; rows of greedy requests are left untouched. NULL = statistics only.

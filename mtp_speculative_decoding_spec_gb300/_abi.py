@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libspec.so")
 
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
-SPEC_BF16, SPEC_F32 = 0, 1
+SPEC_BF16, SPEC_F32, SPEC_Q4A32 = 0, 1, 2
 SPEC_COMMIT_SNAPSHOT, SPEC_COMMIT_REPLAY = 0, 1
 REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN = range(6)
 

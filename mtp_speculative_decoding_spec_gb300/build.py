@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec.so")
-SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "accept.cu", "commit.cu", "abi.cu"]
+SOURCES = ["gemv.cu", "gemv_tc.cu", "gemv_q4.cu", "gemm_tc.cu", "accept.cu", "commit.cu", "abi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]

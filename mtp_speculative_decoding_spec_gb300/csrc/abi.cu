@@ -102,6 +102,8 @@ WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool known_wdt(spec_dtype w) { return w == SPEC_BF16 || w == SPEC_F32 || w == SPEC_Q4A32; }
+
 int next_pow2_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
 // The tensor-core variant (bf16 weights, 16-byte aligned W and H): same parameters, same grid
@@ -189,6 +191,99 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// The 4-bit affine variant: rows of 5d/8 bytes (d/2 of codes, then d/32 bf16 (scale, bias)
+// pairs), the same grid, partials and finish as the bf16 tensor-core kernel.
+spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int nrows,
+                        int rows_per_req, const float* temperature, float* logits,
+                        int64_t logits_stride, spec_rowstats* stats, int draft,
+                        const uint64_t* seed, const int64_t* pos, int pos_offset,
+                        int32_t* token_out, int token_stride, const int32_t* kact,
+                        void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
+                        EncodeTiledFn encode, cudaStream_t stream) {
+  GemvQ4Launch L;
+  memset(&L, 0, sizeof(L));
+  GemvParams& p = L.p;
+  const int band = gemv_q4_band_rows();
+  const int64_t nbands = (V + band - 1) / band;
+  const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * band);
+  if (tile_cap > gemv_q4_max_block_rows()) return SPEC_ERR_UNSUPPORTED;
+  const size_t after =
+      static_cast<size_t>(gemv_q4_stat_bytes()) + gemv_finish_scratch_bytes(grid);
+  const size_t fixed = gemv_q4_fixed_bytes(static_cast<int>(d));
+  const size_t budget = static_cast<size_t>(a.smem_optin);
+  int stages = 8;
+  size_t ring = 0, smem_total = 0;
+  for (; stages >= 2; --stages) {
+    ring = static_cast<size_t>(stages) * gemv_q4_stage_bytes();
+    if (ring < after) ring = align_up(after, 1024);
+    smem_total = ring + fixed;
+    if (smem_total <= budget) break;
+  }
+  if (stages < 2) return SPEC_ERR_UNSUPPORTED;
+
+  const cuuint64_t pitch[1] = {static_cast<cuuint64_t>(5 * d / 8)};
+  const cuuint32_t estride[2] = {1, 1};
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(V)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_code_box_bytes()),
+                               static_cast<cuuint32_t>(gemv_q4_box_rows())};
+    if (encode(&L.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), gdim, pitch, box,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_CUDA;
+  }
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 8), static_cast<cuuint64_t>(V)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_pair_box_bytes()),
+                               static_cast<cuuint32_t>(gemv_q4_box_rows())};
+    void* pairs = static_cast<uint8_t*>(const_cast<void*>(W)) + d / 2;  // 16-byte aligned
+    if (encode(&L.smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pairs, gdim, pitch, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_CUDA;
+  }
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(nrows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(2 * d)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_h_box_elems()),
+                               static_cast<cuuint32_t>(gemv_q4_h_rows())};
+    if (encode(&L.hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(H), gdim, gstride,
+               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_CUDA;
+  }
+  p.V = V;
+  p.d = static_cast<int>(d);
+  p.nbands = nbands;
+  p.band_rows = band;
+  p.stages = stages;
+  p.stage_bytes = gemv_q4_stage_bytes();
+  p.ring_bytes = static_cast<int>(ring);
+  p.hs_bytes = static_cast<int>(gemv_q4_abuf_bytes());
+  p.tile_cap = tile_cap;
+  p.H = static_cast<const uint8_t*>(H);
+  p.h_row_bytes = static_cast<int>(2 * d);
+  p.nrows = nrows;
+  p.rows_per_req = rows_per_req;
+  p.temperature = temperature;
+  p.logits = logits;
+  p.logits_stride = logits_stride;
+  p.stats = stats;
+  p.draft = draft;
+  p.seed = seed;
+  p.pos = pos;
+  p.pos_offset = pos_offset;
+  p.token_out = token_out;
+  p.token_stride = token_stride;
+  p.kact = kact;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  L.grid = grid;
+  L.smem = static_cast<int>(smem_total);
+  const cudaError_t e = gemv_q4_launch(L, stream);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 // Configure and launch the GEMV for `nrows` rows over the first V rows of W.
 spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const void* H,
                      int nrows, int rows_per_req, const float* temperature, float* logits,
@@ -200,8 +295,13 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   if (a.sms <= 0) return SPEC_ERR_CUDA;
   const int elt = (wdt == SPEC_BF16) ? 2 : 4;
   const int64_t row_bytes = d * elt;
-  if (row_bytes % 16 != 0) return SPEC_ERR_INVALID;
-  if (d > (wdt == SPEC_BF16 ? 3072 : 1536)) return SPEC_ERR_UNSUPPORTED;
+  if (wdt == SPEC_Q4A32) {
+    if (d % 128 != 0) return SPEC_ERR_INVALID;  // whole words of codes, 16-byte row pitch
+    if (d > 4096) return SPEC_ERR_UNSUPPORTED;
+  } else {
+    if (row_bytes % 16 != 0) return SPEC_ERR_INVALID;
+    if (d > (wdt == SPEC_BF16 ? 3072 : 1536)) return SPEC_ERR_UNSUPPORTED;
+  }
   // batch_for_ws = 0: a scratch that holds only what the LM head uses (header and partials,
   // which come first in every layout); otherwise the caller's full workspace
   const WsLayout wl = ws_layout(V, batch_for_ws > 0 ? batch_for_ws : 1, a.sms);
@@ -210,6 +310,10 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   if (!encode) return SPEC_ERR_CUDA;
 
   const int grid = gemv_grid(V, a.sms);
+  if (wdt == SPEC_Q4A32)  // every entry point has checked that W and H are 16-byte aligned
+    return run_gemv_q4(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
+                       draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
+                       grid, a, encode, stream);
   if (wdt == SPEC_BF16)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
@@ -419,7 +523,7 @@ spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t
                                float* logits, spec_rowstats* stats, void* workspace,
                                size_t workspace_bytes, spec_stream_t stream) {
   if (!W || !H || !temperature || !stats || !workspace) return SPEC_ERR_INVALID;
-  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
   if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
     return SPEC_ERR_INVALID;
   if (!aligned16(W) || !aligned16(H) || !aligned16(workspace)) return SPEC_ERR_INVALID;
@@ -441,7 +545,7 @@ spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, in
                               void* workspace, size_t workspace_bytes, spec_stream_t stream) {
   if (!W || !h || !temperature || !seed || !pos || !token_out || !workspace)
     return SPEC_ERR_INVALID;
-  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
   if (V_draft < 1 || V_draft >= (int64_t(1) << 24) || d < 1 || B < 1 || B > kMaxRows)
     return SPEC_ERR_INVALID;
   if (token_stride < 1 || (q_logits && q_stride < V_draft)) return SPEC_ERR_INVALID;
@@ -586,7 +690,7 @@ extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt,
                                                   const float* temperature, float* logits,
                                                   spec_rowstats* stats, spec_stream_t stream) {
   if (!W || !H || !temperature || !stats) return SPEC_ERR_INVALID;
-  if (wdt != SPEC_BF16 && wdt != SPEC_F32) return SPEC_ERR_INVALID;
+  if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
   if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
     return SPEC_ERR_INVALID;
   if (!aligned16(W) || !aligned16(H)) return SPEC_ERR_INVALID;

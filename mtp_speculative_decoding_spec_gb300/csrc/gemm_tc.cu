@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0;
       uint32_t fph = 0;
       int tcount = 0;
+      const uint64_t stages_desc = smem_desc_sw128(smem_u32(stages));
       for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tcount) {
         // accumulator buffer of this tile: the epilogue of the previous tile drains the other
         const int buf = tcount & 1, use = tcount >> 1;
@@ -159,14 +160,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(stages + s * kTcStageBytes);
+          const uint64_t st = desc_advance(stages_desc, static_cast<uint32_t>(s * kTcStageBytes));
 #pragma unroll
           for (int ks = 0; ks < kTcKBlock / 16; ++ks) {
-            const uint64_t bdesc = smem_desc_sw128(st + 2 * kTcABytes + ks * 32);
+            const uint64_t bdesc = desc_advance(st, 2 * kTcABytes + ks * 32);
             const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-            tc_mma(dacc, smem_desc_sw128(st + ks * 32), bdesc, idesc, acc);
+            tc_mma(dacc, desc_advance(st, ks * 32), bdesc, idesc, acc);
             if (nhalf == 2)
-              tc_mma(dacc + kTcTileN, smem_desc_sw128(st + kTcABytes + ks * 32), bdesc, idesc, acc);
+              tc_mma(dacc + kTcTileN, desc_advance(st, kTcABytes + ks * 32), bdesc, idesc, acc);
           }
           tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
           if (++s == kTcStages) {

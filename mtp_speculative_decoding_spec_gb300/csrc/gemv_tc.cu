@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc_idesc(kSkTileRows, kSkN);
+      const uint64_t ring_desc = smem_desc_sw128(smem_u32(ring));
       int it = 0, s = 0;
       for (int t = 0; t < ntile; ++t) {
         const uint32_t dacc = tmem_base + static_cast<uint32_t>(t * kSkN);
@@ -204,13 +205,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(ring + static_cast<size_t>(s) * kSkStageBytes);
+          const uint64_t st = desc_advance(ring_desc, static_cast<uint32_t>(s * kSkStageBytes));
           const int nk = min(kSkKB, nkb - ks * kSkKB);
           for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t a = st + kk * kSkWBytes, b = st + kSkKB * kSkWBytes + kk * kSkHBytes;
+            const uint64_t a = desc_advance(st, static_cast<uint32_t>(kk * kSkWBytes));
+            const uint64_t b =
+                desc_advance(st, static_cast<uint32_t>(kSkKB * kSkWBytes + kk * kSkHBytes));
 #pragma unroll
             for (int k16 = 0; k16 < kSkKBlock / 16; ++k16)
-              tc_mma(dacc, smem_desc_sw128(a + k16 * 32), smem_desc_sw128(b + k16 * 32), idesc,
+              tc_mma(dacc, desc_advance(a, k16 * 32), desc_advance(b, k16 * 32), idesc,
                      (ks > 0 || kk > 0 || k16 > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);  // frees the stage once these MMAs have read it

@@ -156,6 +156,27 @@ struct GemvTcLaunch {
 };
 
 cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream);
+
+struct GemvQ4Launch {
+  int grid, smem;
+  CUtensorMap cmap;  // codes: [V rows][d/2 bytes], row pitch 5d/8, box [32 rows][128 B], swizzled
+  CUtensorMap smap;  // (scale, bias) pairs: [V rows][d/8 bytes] from byte d/2, box [32][64 B]
+  CUtensorMap hmap;  // H [nrows][d] bf16, box [16 rows][64], 128-byte swizzle
+  GemvParams p;      // hs_bytes = the shared-memory A buffers
+};
+
+cudaError_t gemv_q4_launch(const GemvQ4Launch& L, cudaStream_t stream);
+int gemv_q4_band_rows();
+int gemv_q4_stage_bytes();
+int gemv_q4_max_block_rows();
+int gemv_q4_stat_bytes();
+int gemv_q4_code_box_bytes();
+int gemv_q4_pair_box_bytes();
+int gemv_q4_box_rows();
+int gemv_q4_h_rows();
+int gemv_q4_h_box_elems();
+size_t gemv_q4_abuf_bytes();
+size_t gemv_q4_fixed_bytes(int d);
 int gemv_tc_band_rows();
 int gemv_tc_box_rows();
 int gemv_tc_kblock();

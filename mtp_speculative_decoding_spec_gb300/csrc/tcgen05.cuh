@@ -27,6 +27,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor of the same operand layout starting `bytes` further on. The start-address
+// field holds the shared-memory address in 16-byte units in the descriptor's low 14 bits, and
+// shared addresses stay below 2^18, so the offset adds without carrying into other fields. The
+// MMA loops build each descriptor once and step it with this one add: rebuilding it from the
+// address before every MMA is a chain of dependent 64-bit operations that, on the single
+// issuing thread, costs more than the MMA itself at N = 16.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t tc_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |

@@ -9,7 +9,7 @@ results back, all asynchronously on the stream.
 
 import torch
 
-from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_BF16,
+from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_F32,
                WIDTH_STATE_BYTES, spec_accept, spec_accept_exact, spec_adapt_width,
                spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
                spec_workspace_bytes)
@@ -48,7 +48,7 @@ class SpecVerifyEngine:
         self.k = torch.full((B,), k_max, dtype=torch.int32, device=dev)
         self.commit_status = torch.zeros(B, dtype=torch.int32, device=dev)
         self.state = None
-        self.dtype_bytes = 2 if wdt == SPEC_BF16 else 4
+        self.dtype_bytes = 4 if wdt == SPEC_F32 else 2  # bytes per hidden-row element
         self.adaptive = adaptive_cost is not None
         self.alpha = alpha
         if self.adaptive:
