@@ -33,6 +33,14 @@ token, the first mismatch emits the token, and all k kept emit the draw from p_k
 then token-identical to decoding without drafts under the same seed (pinned against a sequential
 sampler written independently in the tests).
 
+Filtered sampling (``accept_request_filtered``; llama.cpp PR #28104, *Result*: the trunk samples
+at temperature 1.0 with top-p 0.95 and top-k 20). The target becomes p'_r = the temperature-T
+distribution of row r kept to its top_k tokens (largest logits, ties to the lower id), then to
+the smallest prefix of those in descending probability whose mass over the top-k set reaches
+top_p, renormalised. Drafts are the draft head's argmax picks and q is one-hot at the draft, so
+the ratio rule keeps d_i when u <= p'_{i-1}(d_i), a rejection draws from p'_{i-1} without d_i,
+and the bonus draws from p'_k: the emitted tokens follow the filtered target law exactly.
+
 Inverse CDF: the smallest j (ascending token id) with cumsum(w)[j] > u * sum(w); if rounding
 leaves none, the last j with w[j] > 0. Readings where the pages are silent are listed in the
 design notes (draft rows checked against row i-1, lowest-index argmax ties, ``<=`` in the ratio
@@ -277,3 +285,89 @@ def draft_chain_tokens(y_rows, T, uniform, pos_base):
         toks.append(t)
         margins.append(("gap" if T == 0 else "cdf", m))
     return toks, margins
+
+
+def filtered_probs(z, T, top_k, top_p):
+    """p' for one logits row z (float64 [V]) at temperature T > 0 (see the module docstring).
+
+    Returns (p' float64 [V], kept token ids in descending probability, margins) with margins
+    ('gap', logit gap between the last kept and the first dropped token of the top-k cut;
+    +inf when nothing is dropped) and ('cdf', |mass of the top-p prefix before its last token
+    - top_p|, the distance of the top-p cut from flipping, in probability units).
+    """
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[0]
+    order = np.lexsort((np.arange(V), -z))      # descending logit, ties to the lower id
+    kk = min(int(top_k), V)
+    top = order[:kk]
+    gap = float(z[order[kk - 1]] - z[order[kk]]) if kk < V else float("inf")
+    w = np.exp((z[top] - z[top[0]]) / T)
+    pk = w / w.sum()
+    before = np.concatenate(([0.0], np.cumsum(pk)[:-1]))  # mass ahead of each kept token
+    n = int(np.sum(before < top_p))              # keep while the mass ahead is below top_p
+    kept = top[:n]
+    out = np.zeros(V)
+    out[kept] = w[:n] / w[:n].sum()
+    cut = min(abs(before[n - 1] - top_p), abs(before[n] - top_p) if n < kk else float("inf"))
+    return out, kept, [("gap", gap), ("cdf", float(cut))]
+
+
+def accept_request_filtered(z, drafts, k, T, top_k, top_p, eos_id, uniform, pos_base, k_max=7):
+    """Acceptance against the top-k / top-p filtered target (module docstring) for one request
+    and one cycle, with argmax drafts and q one-hot at each draft. T <= 0 is greedy acceptance
+    (the filters keep the argmax). Same inputs, validation and result dict as
+    ``accept_request``; margins also record each filter's cut."""
+    if not T > 0:
+        return accept_request(z, None, drafts, k, T, eos_id, uniform, pos_base, k_max)
+    res = dict(status=STATUS_OK, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
+               sample_kind=0, sample_row=-1, margins=[])
+    if k < 0 or k > k_max:
+        res["status"] = STATUS_BAD_K
+        return res
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[1]
+    d = [int(x) for x in drafts[:k]]
+    if any(x < 0 or x >= V for x in d):
+        res["status"] = STATUS_BAD_TOKEN
+        return res
+    if any(lmhead.row_stats(z[r], T)["nonfinite"] for r in range(k + 1)):
+        res["status"] = STATUS_NONFINITE
+        return res
+    tokens, margins = res["tokens"], res["margins"]
+
+    def emit(tok):
+        tokens.append(int(tok))
+        if eos_id >= 0 and tok == eos_id:
+            res["eos_hit"] = True
+            return True
+        return False
+
+    for i in range(1, k + 1):
+        x = d[i - 1]
+        p, _, m = filtered_probs(z[i - 1], T, top_k, top_p)
+        margins.extend(m)
+        u = uniform(pos_base + i - 1, PURPOSE_ACCEPT)
+        margins.append(("ratio", abs(u - float(p[x]))))
+        if p[x] > 0.0 and u <= p[x]:
+            res["n_accept"] += 1
+            if emit(x):
+                break
+        else:
+            r = p.copy()
+            r[x] = 0.0
+            if not np.sum(r) > 0.0:
+                r = p
+            j, mc = inverse_cdf(r, uniform(pos_base + i - 1, PURPOSE_RESIDUAL))
+            margins.append(("cdf", mc))
+            res.update(sample_kind=1, sample_row=i - 1)
+            emit(j)
+            break
+    else:
+        p, _, m = filtered_probs(z[k], T, top_k, top_p)
+        margins.extend(m)
+        j, mc = inverse_cdf(p, uniform(pos_base + k, PURPOSE_BONUS))
+        margins.append(("cdf", mc))
+        res.update(sample_kind=2, sample_row=k)
+        emit(j)
+    res["n_emit"] = len(tokens)
+    return res
