@@ -393,7 +393,8 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
 
 def sweep(dev, W, Wd, hbm_peak):
     """k = 1..7 at temperature 0 (greedy) and 1 (ratio rule with q rows); exact-match
-    acceptance at temperature 1 for k = 1, 3, 7."""
+    acceptance, and acceptance against the top-k 20 / top-p 0.95 filtered target (argmax
+    drafts), at temperature 1 for k = 1, 3, 7."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -402,7 +403,7 @@ def sweep(dev, W, Wd, hbm_peak):
     base = configs.get(2)
     n_pool, K = 32, 200
     points = [(T, k, "ratio") for T in (0.0, 1.0) for k in range(1, 8)]
-    points += [(1.0, k, "exact") for k in (1, 3, 7)]
+    points += [(1.0, k, mode) for mode in ("exact", "filtered") for k in (1, 3, 7)]
     for T, k, mode in points:
         cfg = configs.Config(**{**base.__dict__, "k": k, "temps": (T,)})
         Hp, Hdp = build_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
@@ -411,7 +412,7 @@ def sweep(dev, W, Wd, hbm_peak):
         eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
                                cfg.eos_id, device=dev, want_q_logits=True,
                                acceptance=mode)
-        eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k])
+        eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k], top_k=[20], top_p=[0.95])
         for c in range(5):
             eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
         torch.cuda.synchronize()
@@ -448,7 +449,7 @@ def sweep(dev, W, Wd, hbm_peak):
         gbs = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 +
                (k + 1) * cfg.V * 4 * (T > 0)) / gemv_s / 1e9
         accept_us = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
-        out[f"T{T:g}_k{k}" + ("_exact" if mode == "exact" else "")] = {
+        out[f"T{T:g}_k{k}" + ("" if mode == "ratio" else f"_{mode}")] = {
             "verify_cycles_s": round(K / verify_s, 1),
             "full_cycles_s": round(K / s, 1),
             "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),

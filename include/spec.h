@@ -73,7 +73,8 @@ enum {
   SPEC_REQ_BAD_K = 2,       /* k outside [0, k_max] or k + 1 > verify rows */
   SPEC_REQ_KV_OVERFLOW = 3, /* commit: P + k + 1 exceeds the KV capacity (trim clipped) */
   SPEC_REQ_NO_LOGITS = 4,   /* temperature > 0 but the needed logits/q_logits were not given */
-  SPEC_REQ_BAD_TOKEN = 5    /* a draft id outside [0, V) */
+  SPEC_REQ_BAD_TOKEN = 5,   /* a draft id outside [0, V) */
+  SPEC_REQ_BAD_FILTER = 6   /* spec_accept_filtered: top_k outside [1, 32] or top_p outside (0, 1] */
 };
 
 /* Statistics of one logit row z[0..V) at the row's temperature T (T <= 0 means greedy and the
@@ -275,6 +276,35 @@ spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t *k, const 
                               const uint64_t *seed, const int64_t *pos_base,
                               spec_accept_out *out, spec_counters *counters, void *workspace,
                               size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_accept_filtered -- acceptance against a top-k / top-p filtered target (llama.cpp PR
+ * #28104, "Result": the trunk samples at temperature 1.0 with top-p 0.95 and top-k 20).
+ *
+ * For request b at T > 0 the target of verify row r is p'_r: the temperature-T distribution of
+ * the row kept to its top_k[b] tokens (largest logits, ties to the lower id), then to the
+ * smallest prefix of those, in descending probability, whose mass over the top-k set reaches
+ * top_p[b], renormalised. Drafts are taken as the draft head's argmax picks with q one-hot at
+ * each draft (run spec_draft_argmax at temperature 0), so: d_i is kept when
+ * u <= p'_{i-1}(d_i) with u = U(pos_base + i - 1, ACCEPT); the first rejection emits a draw
+ * from p'_{i-1} without d_i (RESIDUAL); all k kept emits a draw from p'_k (BONUS). The emitted
+ * tokens then follow the filtered target exactly. Weights are exp((z - max)/T) quantised to
+ * 2^-40 units; the ratio test compares u * sum(kept) with the draft's weight exactly, the top-p
+ * cut compares the integer mass ahead with top_p times the top-k total, and the draws are
+ * inverse CDFs in ascending token id. T <= 0 is greedy acceptance, exactly as spec_accept.
+ *   top_k [B] int32 in [1, 32]; top_p [B] float in (0, 1]; otherwise the request gets status
+ *   SPEC_REQ_BAD_FILTER. V at most 2^20 (else SPEC_ERR_UNSUPPORTED). No draft logits are read.
+ *   Other arguments, layouts, workspace, status codes and counters as for spec_accept
+ *   (sample_kind 1 residual, 2 bonus).
+ */
+spec_status spec_accept_filtered(int32_t B, int32_t k_max, const int32_t *k,
+                                 const int32_t *drafts, const float *logits,
+                                 const spec_rowstats *stats, int64_t V, int32_t R,
+                                 const float *temperature, const int32_t *top_k,
+                                 const float *top_p, int32_t eos_id, const uint64_t *seed,
+                                 const int64_t *pos_base, spec_accept_out *out,
+                                 spec_counters *counters, void *workspace,
+                                 size_t workspace_bytes, spec_stream_t stream);
 
 /* Adaptive width state of one request (64 bytes, zero-filled before the first cycle). */
 typedef struct {

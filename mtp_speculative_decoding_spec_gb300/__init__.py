@@ -8,7 +8,8 @@ runs in the library's CUDA kernels; nothing here computes, and nothing falls bac
 """
 
 from . import _abi
-from ._abi import (ACCEPT_OUT_DTYPE, COUNTERS_DTYPE, REQ_BAD_K, REQ_BAD_TOKEN,  # noqa: F401
+from ._abi import (ACCEPT_OUT_DTYPE, COUNTERS_DTYPE, REQ_BAD_FILTER, REQ_BAD_K,  # noqa: F401
+                   REQ_BAD_TOKEN,
                    REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_NONFINITE, REQ_OK, ROWSTATS_DTYPE,
                    SPEC_BF16, SPEC_COMMIT_REPLAY, SPEC_COMMIT_SNAPSHOT, SPEC_F32, SPEC_Q4A32,
                    WIDTH_STATE_DTYPE, spec_state_desc)
@@ -96,6 +97,14 @@ def spec_accept_exact(B, k_max, k, drafts, logits, stats, V, R, temperature, eos
         B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(temperature),
         eos_id, _ptr(seed), _ptr(pos_base), _ptr(out), _ptr(counters), _ptr(workspace),
         _nbytes(workspace), _stream(stream)))
+
+
+def spec_accept_filtered(B, k_max, k, drafts, logits, stats, V, R, temperature, top_k, top_p,
+                         eos_id, seed, pos_base, out, counters, workspace, stream=None):
+    _check("spec_accept_filtered", _abi.lib().spec_accept_filtered(
+        B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(temperature),
+        _ptr(top_k), _ptr(top_p), eos_id, _ptr(seed), _ptr(pos_base), _ptr(out), _ptr(counters),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
 def spec_commit_rollback(B, st, acc, k, mode, commit_status=None, stream=None):

@@ -12,11 +12,13 @@ LIB_PATH = os.path.join(HERE, "libspec.so")
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
 SPEC_BF16, SPEC_F32, SPEC_Q4A32 = 0, 1, 2
 SPEC_COMMIT_SNAPSHOT, SPEC_COMMIT_REPLAY = 0, 1
-REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN = range(6)
+REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN, \
+    REQ_BAD_FILTER = range(7)
 
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
 EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
-           "spec_accept", "spec_accept_exact", "spec_adapt_width", "spec_commit_rollback",
+           "spec_accept", "spec_accept_exact", "spec_accept_filtered", "spec_adapt_width",
+           "spec_commit_rollback",
            "spec_batched_supported",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes")
 
@@ -92,6 +94,9 @@ def lib():
         L.spec_accept_exact.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, i32, vp, vp, vp,
                                         vp, vp, sz, vp]
         L.spec_accept_exact.restype = i32
+        L.spec_accept_filtered.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, vp, i32,
+                                           vp, vp, vp, vp, vp, sz, vp]
+        L.spec_accept_filtered.restype = i32
         L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.spec_adapt_width.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,

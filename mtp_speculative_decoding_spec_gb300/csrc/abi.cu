@@ -73,9 +73,10 @@ int accept_slices(int64_t V) { return static_cast<int>((V + kAcceptSlice - 1) / 
 //   [256, part_end)             GEMV per-block partials (grid of the vocabulary size)
 //   [part_end, sums_end)        accept per-slice sums (B * slices * 8 * 8 bytes)
 //   [sums_end, gemm_end)        batched path: per-(row, 256-row tile) partials (no counters)
+//   [gemm_end, cand_end)        filtered accept: per-(request, slice, row) top-k keys
 //   [ws_bytes - tickets, end)   accept tickets, one per request
 struct WsLayout {
-  size_t part, sums, gemm, tickets_bytes, total;
+  size_t part, sums, gemm, cand, tickets_bytes, total;
 };
 
 int gemm_rows_max(int32_t max_batch) {
@@ -92,11 +93,14 @@ WsLayout ws_layout(int64_t V, int32_t max_batch, int sms) {
                              256);
   const int64_t ntiles = (V + 127) / 128;  // batched path: 128-row vocabulary tiles
   w.tickets_bytes = align_up(sizeof(uint32_t) * static_cast<size_t>(max_batch), 256);
-  w.total = w.gemm +
-            align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles *
-                         2,
-                     256) +
-            w.tickets_bytes;
+  w.cand = w.gemm +
+           align_up(sizeof(GemvPartial) * static_cast<size_t>(gemm_rows_max(max_batch)) * ntiles * 2,
+                    256);
+  // the filtered acceptance's candidate keys exist only for vocabularies it accepts
+  const size_t ncand = (V <= kMaxFilteredV) ? static_cast<size_t>(max_batch) * accept_slices(V) *
+                                                  kMaxRows * kMaxTopK
+                                            : 0;
+  w.total = w.cand + align_up(sizeof(unsigned long long) * ncand, 256) + w.tickets_bytes;
   return w;
 }
 
@@ -449,7 +453,8 @@ spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t
                        int64_t q_stride, const float* temperature, int32_t eos_id,
                        const uint64_t* seed, const int64_t* pos_base, spec_accept_out* out,
                        spec_counters* counters, void* workspace, size_t workspace_bytes,
-                       spec_stream_t stream, int exact) {
+                       spec_stream_t stream, int exact, const int32_t* top_k = nullptr,
+                       const float* top_p = nullptr) {
   if (B < 1 || k_max < 0 || k_max > kMaxRows - 1 || R < 1 || R > kMaxRows) return SPEC_ERR_INVALID;
   if (!k || (k_max > 0 && !drafts) || !stats || !temperature || !seed || !pos_base || !out ||
       !workspace)
@@ -483,6 +488,14 @@ spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t
   p.out = out;
   p.counters = counters;
   p.exact = exact;
+  if (top_k) {  // filtered acceptance
+    if (!top_p) return SPEC_ERR_INVALID;
+    if (V > kMaxFilteredV) return SPEC_ERR_UNSUPPORTED;
+    p.filtered = 1;
+    p.top_k = top_k;
+    p.top_p = top_p;
+    p.cand = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + wl.cand);
+  }
   // tickets: the last 4*B bytes of the buffer, its end rounded down to 4 bytes (see WsLayout)
   const size_t end4 = workspace_bytes & ~static_cast<size_t>(3);
   p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + end4 -
@@ -595,6 +608,20 @@ spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t* k, const 
   return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, nullptr, nullptr, 0, 0,
                           temperature, eos_id, seed, pos_base, out, counters, workspace,
                           workspace_bytes, stream, 1);
+}
+
+spec_status spec_accept_filtered(int32_t B, int32_t k_max, const int32_t* k,
+                                 const int32_t* drafts, const float* logits,
+                                 const spec_rowstats* stats, int64_t V, int32_t R,
+                                 const float* temperature, const int32_t* top_k,
+                                 const float* top_p, int32_t eos_id, const uint64_t* seed,
+                                 const int64_t* pos_base, spec_accept_out* out,
+                                 spec_counters* counters, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream) {
+  if (!top_k || !top_p) return SPEC_ERR_INVALID;
+  return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, nullptr, nullptr, 0, 0,
+                          temperature, eos_id, seed, pos_base, out, counters, workspace,
+                          workspace_bytes, stream, 0, top_k, top_p);
 }
 
 spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,

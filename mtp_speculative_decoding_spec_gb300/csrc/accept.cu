@@ -14,6 +14,13 @@
 // to 2^-40 units, in exact 64-bit integers; the last block of the request (a per-request
 // ticket, no inter-block waiting) picks the slice holding the target and rescans it. Integer
 // sums make the drawn token independent of block scheduling and summation order.
+//
+// Filtered mode (spec_accept_filtered: top-k / top-p target, one-hot q): each block reduces
+// every verify row of its slice to the slice's best top_k entries (a 64-bit key orders by
+// logit, then by lower id; warps select from their 128 entries, warp 0 merges the eight
+// lists); the last block merges the slices' sorted lists row by row (a tournament over their
+// heads), cuts at top-p and takes the decisions and draws on the <= 32 survivors in exact
+// integer weights.
 #include <math.h>
 
 #include "params.cuh"
@@ -26,7 +33,8 @@ constexpr int kAcceptSumSlots = kMaxRows;  // per-slice integer sums: one per ve
 struct Decision {
   int status, n_accept, ntok, eos_hit;
   int tokens[8];
-  int need;  // 0 none, 1 residual draw, 2 bonus draw, 3 exact-match draws (rows 0..srow)
+  int need;  // 0 none, 1 residual draw, 2 bonus draw, 3 exact-match draws (rows 0..srow),
+             // 4 filtered decisions (rows 0..srow)
   int srow;  // verify row of the draw
   int xrej;  // the rejected draft (one-hot q)
   int pad;
@@ -190,6 +198,162 @@ __device__ int draw_token(const AcceptParams& p, int b, const DrawCtx& c, bool u
   return *s_tok;
 }
 
+// ---------------------------------------------------------------------- filtered acceptance
+// Order-preserving 64-bit key of (logit, id): larger logit first, then lower id; -0 counts as
+// +0. Real keys are never 0 (that would need a NaN logit), so 0 marks "no entry".
+__device__ __forceinline__ unsigned long long rank_key(float z, int64_t id) {
+  uint32_t u = __float_as_uint(z == 0.f ? 0.f : z);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) |
+         (0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t u = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+__device__ __forceinline__ int key_id(unsigned long long key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v,
+                                                            unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max_u64(v);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0ull;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t = sh[w] > t ? sh[w] : t;
+  return t;
+}
+
+// The best K keys of verify row `row` of request b over slice sl, descending, written to the
+// workspace (0 past the last entry). Called by every thread of the block.
+__device__ void slice_topk(const AcceptParams& p, int b, int sl, int row, int K,
+                           unsigned long long* s_lists /* [8][kMaxTopK] */) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* z = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V;
+  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice + warp * 128;
+  unsigned long long key[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int64_t j = j0 + e * 32 + lane;
+    key[e] = (j < p.V) ? rank_key(__ldcg(z + j), j) : 0ull;
+  }
+  for (int r = 0; r < K; ++r) {  // this warp's 128 entries, best first
+    unsigned long long m = key[0];
+#pragma unroll
+    for (int e = 1; e < 4; ++e) m = key[e] > m ? key[e] : m;
+    const unsigned long long wm = warp_max_u64(m);
+    if (lane == 0) s_lists[warp * kMaxTopK + r] = wm;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (key[e] == wm) key[e] = 0ull;  // keys are unique: only the winner matches
+  }
+  __syncthreads();
+  if (warp == 0) {  // merge the eight lists
+    unsigned long long c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = lane + 32 * i;
+      c[i] = (idx < 8 * K) ? s_lists[(idx / K) * kMaxTopK + idx % K] : 0ull;
+    }
+    unsigned long long* out =
+        p.cand + ((static_cast<size_t>(b) * p.NS + sl) * kMaxRows + row) * kMaxTopK;
+    for (int r = 0; r < K; ++r) {
+      unsigned long long m = c[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) m = c[i] > m ? c[i] : m;
+      const unsigned long long wm = warp_max_u64(m);
+      if (lane == 0) out[r] = wm;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c[i] == wm) c[i] = 0ull;
+    }
+  }
+  __syncthreads();  // the lists are reused by the next row
+}
+
+// The best K keys of row `row` over the whole vocabulary: a tournament over the slices' sorted
+// lists (each thread holds the heads of slices tid + 256 m, m < 4). Called by every thread.
+__device__ void merge_rows_topk(const AcceptParams& p, int b, int row, int K,
+                                unsigned long long* s_top, unsigned long long* sh) {
+  const int tid = threadIdx.x;
+  const unsigned long long* base = p.cand + static_cast<size_t>(b) * p.NS * kMaxRows * kMaxTopK;
+  int ptr[4];
+  unsigned long long head[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int s = tid + kAcceptThreads * m;
+    ptr[m] = 0;
+    head[m] = (s < p.NS) ? __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) * kMaxTopK)
+                         : 0ull;
+  }
+  for (int r = 0; r < K; ++r) {
+    unsigned long long m = head[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i) m = head[i] > m ? head[i] : m;
+    const unsigned long long bm = block_max_u64(m, sh);
+    if (tid == 0) s_top[r] = bm;
+    if (bm != 0ull) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (head[i] == bm) {
+          const int s = tid + kAcceptThreads * i;
+          ++ptr[i];
+          head[i] = (ptr[i] < K) ? __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) *
+                                                     kMaxTopK + ptr[i])
+                                 : 0ull;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// u * W <= w * 2^24 for u = u24 * 2^-24, exactly (128-bit products).
+__device__ __forceinline__ bool u_le_ratio(uint32_t u24, unsigned long long W,
+                                           unsigned long long w) {
+  const unsigned long long lh = __umul64hi(static_cast<unsigned long long>(u24), W);
+  const unsigned long long ll = static_cast<unsigned long long>(u24) * W;
+  const unsigned long long rh = w >> 40, rl = w << 24;
+  return lh < rh || (lh == rh && ll <= rl);
+}
+
+// Inverse-CDF draw over (id, weight) pairs in ascending id: the first entry whose cumulative
+// weight exceeds floor(u * total); -1 if the total is 0.
+__device__ int small_draw(int* id, unsigned long long* w, int n, uint32_t u24) {
+  for (int i = 1; i < n; ++i) {  // insertion sort by id (n <= 32)
+    const int ki = id[i];
+    const unsigned long long kw = w[i];
+    int j = i - 1;
+    while (j >= 0 && id[j] > ki) {
+      id[j + 1] = id[j];
+      w[j + 1] = w[j];
+      --j;
+    }
+    id[j + 1] = ki;
+    w[j + 1] = kw;
+  }
+  unsigned long long tot = 0ull;
+  for (int i = 0; i < n; ++i) tot += w[i];
+  if (tot == 0ull) return -1;
+  const unsigned long long target = cdf_target(u24, tot);
+  unsigned long long cum = 0ull;
+  for (int i = 0; i < n; ++i) {
+    cum += w[i];
+    if (w[i] > 0ull && cum > target) return id[i];
+  }
+  return -1;
+}
+
 __device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
   spec_accept_out o;
   o.status = D.status;
@@ -246,6 +410,12 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     if (status == SPEC_REQ_OK && T > 0.f &&
         (p.logits == nullptr || (p.q_logits != nullptr && p.q_stats == nullptr)))
       status = SPEC_REQ_NO_LOGITS;
+    const bool filt = p.filtered && T > 0.f;  // filtered mode: decided in the last block
+    if (status == SPEC_REQ_OK && filt) {
+      const int tk = p.top_k[b];
+      const float tp = p.top_p[b];
+      if (tk < 1 || tk > kMaxTopK || !(tp > 0.f && tp <= 1.f)) status = SPEC_REQ_BAD_FILTER;
+    }
     spec_rowstats st{0.f, 0.f, 0.f, -1};
     bool nf = false;
     if (status == SPEC_REQ_OK) {
@@ -259,7 +429,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     }
     const bool exact = p.exact && T > 0.f;  // exact-match mode: decided by the draws below
     bool acc = false;
-    if (status == SPEC_REQ_OK && lane < k && !exact) {
+    if (status == SPEC_REQ_OK && lane < k && !exact && !filt) {
       if (!(T > 0.f)) {
         acc = (x == st.argmax);
       } else {
@@ -297,8 +467,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       d.srow = -1;
       d.xrej = -1;
       d.pad = 0;
-      if (status == SPEC_REQ_OK && exact) {
-        d.need = 3;
+      if (status == SPEC_REQ_OK && (exact || filt)) {
+        d.need = exact ? 3 : 4;
         d.srow = k;
       } else if (status == SPEC_REQ_OK) {
         bool stop = false;
@@ -345,7 +515,12 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   // ---------------- slice sums of the draws' integer weights ----------------
   const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
   unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
-  if (D.need == 3) {
+  if (D.need == 4) {
+    // filtered: the slice's best top_k keys of every row 0..k
+    __shared__ unsigned long long s_lists[8 * kMaxTopK];
+    const int K = p.top_k[b];
+    for (int r = 0; r <= k; ++r) slice_topk(p, b, sl, r, K, s_lists);
+  } else if (D.need == 3) {
     // exact-match: the p weights of every row 0..k over this slice, slots 0..k
     unsigned long long sp[kMaxRows];
 #pragma unroll
@@ -435,6 +610,111 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     }
     if (tid == 0) {
       finalize(p, b, E, k);
+      p.tickets[b] = 0u;
+    }
+    return;
+  }
+
+  if (D.need == 4) {
+    // filtered: row by row, the top-k set (tournament over the slices' lists), the top-p cut,
+    // then the ratio test of the draft against p' (q one-hot), a residual draw at the first
+    // rejection, or the bonus draw after row k
+    __shared__ unsigned long long s_top[kMaxTopK];
+    __shared__ int f_stop;
+    __shared__ Decision F;
+    const int K = p.top_k[b];
+    const double tp = static_cast<double>(p.top_p[b]);
+    const float invT = __fdiv_rn(1.f, T);
+    if (tid == 0) {
+      F = D;
+      F.need = 0;
+      F.srow = -1;
+      f_stop = 0;
+    }
+    __syncthreads();
+    for (int r = 0; r <= k; ++r) {
+      merge_rows_topk(p, b, r, K, s_top, sh);
+      if (tid == 0) {
+        int id[kMaxTopK];
+        unsigned long long w[kMaxTopK];
+        int nk = 0;
+        float ztop = 0.f;
+        for (int j = 0; j < K; ++j) {
+          const unsigned long long key = s_top[j];
+          if (key == 0ull) break;
+          const float zj = key_logit(key);
+          if (j == 0) ztop = zj;
+          id[nk] = key_id(key);
+          w[nk] = quantise(expf(__fmul_rn(__fsub_rn(zj, ztop), invT)));
+          ++nk;
+        }
+        unsigned long long W = 0ull;
+        for (int j = 0; j < nk; ++j) W += w[j];
+        // top-p: keep while the mass ahead is below top_p of the top-k mass
+        int n = 0;
+        unsigned long long ahead = 0ull;
+        const double cut = tp * static_cast<double>(W);
+        while (n < nk && static_cast<double>(ahead) < cut) ahead += w[n++];
+        unsigned long long Wk = 0ull;
+        for (int j = 0; j < n; ++j) Wk += w[j];
+        bool emitted_draw = false;
+        int tok = -1;
+        if (r < k) {
+          const int x = sx[r];
+          int jx = -1;
+          for (int j = 0; j < n; ++j)
+            if (id[j] == x) jx = j;
+          const unsigned long long wx = (jx >= 0) ? w[jx] : 0ull;
+          const uint32_t ua = uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_ACCEPT);
+          if (wx > 0ull && u_le_ratio(ua, Wk, wx)) {
+            F.tokens[F.ntok++] = x;
+            F.n_accept++;
+            if (p.eos >= 0 && x == p.eos) {
+              F.eos_hit = 1;
+              f_stop = 1;
+            }
+          } else {  // residual: p' without the draft (p' itself if nothing else is left)
+            int m = 0;
+            for (int j = 0; j < n; ++j) {
+              if (j == jx) continue;
+              id[m] = id[j];
+              w[m] = w[j];
+              ++m;
+            }
+            unsigned long long rest = 0ull;
+            for (int j = 0; j < m; ++j) rest += w[j];
+            if (rest == 0ull) m = 0;
+            if (m == 0) {  // rebuild p' (the cut set) from the keys
+              for (int j = 0; j < n; ++j) {
+                const unsigned long long key = s_top[j];
+                id[j] = key_id(key);
+                w[j] = quantise(expf(__fmul_rn(__fsub_rn(key_logit(key), ztop), invT)));
+              }
+              m = n;
+            }
+            tok = small_draw(id, w, m,
+                             uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_RESIDUAL));
+            F.need = 1;
+            emitted_draw = true;
+          }
+        } else {
+          tok = small_draw(id, w, n, uniform_u24(p.seed[b], p.pos_base[b] + k, PURPOSE_BONUS));
+          F.need = 2;
+          emitted_draw = true;
+        }
+        if (emitted_draw) {
+          if (tok < 0) tok = id[0];  // unreachable: the cut set always has weight
+          F.srow = r;
+          F.tokens[F.ntok++] = tok;
+          if (p.eos >= 0 && tok == p.eos) F.eos_hit = 1;
+          f_stop = 1;
+        }
+      }
+      __syncthreads();
+      if (f_stop) break;
+    }
+    if (tid == 0) {
+      finalize(p, b, F, k);
       p.tickets[b] = 0u;
     }
     return;

@@ -76,7 +76,14 @@ struct AcceptParams {
   uint32_t* tickets;         // [B]
   unsigned long long* sums;  // [B][NS][8]: ratio rule: residual, p; exact-match: p of rows 0..k
   int exact;                 // exact-match acceptance at T > 0
+  int filtered;              // top-k / top-p filtered target at T > 0 (one-hot q)
+  const int32_t* top_k;      // [B] in [1, kMaxTopK]
+  const float* top_p;        // [B] in (0, 1]
+  unsigned long long* cand;  // [B][NS][8 rows][kMaxTopK] each slice's best keys, descending
 };
+
+constexpr int kMaxTopK = 32;               // largest top-k of the filtered acceptance
+constexpr int64_t kMaxFilteredV = 1 << 20;  // its vocabulary limit: at most 4 slices a thread
 
 struct CommitParams {
   spec_state_desc st;

@@ -10,7 +10,8 @@ results back, all asynchronously on the stream.
 import torch
 
 from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_F32,
-               WIDTH_STATE_BYTES, spec_accept, spec_accept_exact, spec_adapt_width,
+               WIDTH_STATE_BYTES, spec_accept, spec_accept_exact, spec_accept_filtered,
+               spec_adapt_width,
                spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
                spec_workspace_bytes)
 
@@ -18,14 +19,17 @@ from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_F32,
 class SpecVerifyEngine:
     def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
                  want_q_logits=True, acceptance="ratio", adaptive_cost=None, alpha=0.1):
-        """acceptance: "ratio" (u*q <= p with residual correction; spec_accept) or "exact"
-        (a draft counts only if it is the trunk's own sample; spec_accept_exact).
+        """acceptance: "ratio" (u*q <= p with residual correction; spec_accept), "exact"
+        (a draft counts only if it is the trunk's own sample; spec_accept_exact) or "filtered"
+        (the top-k / top-p filtered target of set_requests(top_k=..., top_p=...), argmax drafts
+        and one-hot q; spec_accept_filtered; the draft steps then run at temperature 0).
         adaptive_cost: None for fixed widths (set_requests(k=...)), or the relative cost of a
         cycle at widths 0..k_max: each cycle then ends with spec_adapt_width choosing every
         request's next width on the device, and ``cycle`` always enqueues k_max draft steps,
         of which those past every request's width return at once."""
-        if acceptance not in ("ratio", "exact"):
-            raise ValueError(f"acceptance must be 'ratio' or 'exact', not {acceptance!r}")
+        if acceptance not in ("ratio", "exact", "filtered"):
+            raise ValueError(
+                f"acceptance must be 'ratio', 'exact' or 'filtered', not {acceptance!r}")
         self.acceptance = acceptance
         self.W, self.wdt, self.V, self.d, self.Vd = W, wdt, V, d, Vd
         self.B, self.R, self.k_max, self.eos_id = B, R, k_max, eos_id
@@ -43,6 +47,9 @@ class SpecVerifyEngine:
         self.out = torch.zeros(B * ACCEPT_OUT_BYTES, dtype=torch.uint8, device=dev)
         self.counters = torch.zeros(B * COUNTERS_BYTES, dtype=torch.uint8, device=dev)
         self.temps = torch.zeros(B, dtype=torch.float32, device=dev)
+        self.zero_temps = torch.zeros(B, dtype=torch.float32, device=dev)
+        self.top_k = torch.full((B,), 20, dtype=torch.int32, device=dev)
+        self.top_p = torch.full((B,), 0.95, dtype=torch.float32, device=dev)
         self.seeds = torch.zeros(B, dtype=torch.int64, device=dev)
         self.pos = torch.zeros(B, dtype=torch.int64, device=dev)
         self.k = torch.full((B,), k_max, dtype=torch.int32, device=dev)
@@ -58,9 +65,9 @@ class SpecVerifyEngine:
             self.width_state = torch.zeros(B * WIDTH_STATE_BYTES, dtype=torch.uint8, device=dev)
 
     # ---------------------------------------------------------------- configuration
-    def set_requests(self, temps=None, seeds=None, pos=None, k=None):
+    def set_requests(self, temps=None, seeds=None, pos=None, k=None, top_k=None, top_p=None):
         for dst, src in ((self.temps, temps), (self.seeds, seeds), (self.pos, pos),
-                         (self.k, k)):
+                         (self.k, k), (self.top_k, top_k), (self.top_p, top_p)):
             if src is not None:
                 dst.copy_(torch.as_tensor(src, dtype=dst.dtype), non_blocking=True)
 
@@ -72,7 +79,8 @@ class SpecVerifyEngine:
     def draft_step(self, i, h):
         """Draft i (1-based) for every request from draft-head hidden rows h [B, d]."""
         B = self.B
-        spec_draft_argmax(self.W, self.wdt, self.Vd, self.d, h, B, self.temps, self.seeds,
+        temps = self.zero_temps if self.acceptance == "filtered" else self.temps
+        spec_draft_argmax(self.W, self.wdt, self.Vd, self.d, h, B, temps, self.seeds,
                           self.pos, i - 1, self.drafts[:, i - 1:], self.drafts.shape[1],
                           None if self.q is None else self.q[(i - 1) * B:], self.Vd,
                           self.qs[(i - 1) * B * ROWSTATS_BYTES:],
@@ -83,6 +91,11 @@ class SpecVerifyEngine:
                            self.logits, self.stats, self.ws)
 
     def accept(self, use_q=True):
+        if self.acceptance == "filtered":
+            spec_accept_filtered(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats,
+                                 self.V, self.R, self.temps, self.top_k, self.top_p, self.eos_id,
+                                 self.seeds, self.pos, self.out, self.counters, self.ws)
+            return
         if self.acceptance == "exact":
             spec_accept_exact(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats,
                               self.V, self.R, self.temps, self.eos_id, self.seeds, self.pos,
