@@ -28,6 +28,9 @@
 namespace spec {
 
 constexpr int kAcceptSumSlots = kMaxRows;  // per-slice integer sums: one per verify row
+// shared memory for one row's candidate keys in the filtered mode's last block (40 KB: up to
+// 160 slices x 32, or V = 151,936 at any top-k); larger rows are merged from L2
+constexpr int kFilterStageKeys = 5120;
 
 
 struct Decision {
@@ -235,66 +238,60 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
 }
 
 // The best K keys of verify row `row` of request b over slice sl, descending, written to the
-// workspace (0 past the last entry). Called by every thread of the block.
-__device__ void slice_topk(const AcceptParams& p, int b, int sl, int row, int K,
-                           unsigned long long* s_lists /* [8][kMaxTopK] */) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// workspace (0 past the last entry). Called by one warp: lane l holds entries l + 32 i.
+__device__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, int K) {
+  const int lane = threadIdx.x & 31;
   const float* z = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V;
-  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice + warp * 128;
-  unsigned long long key[4];
+  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
+  unsigned long long key[kAcceptSlice / 32];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < kAcceptSlice / 32; ++e) {
     const int64_t j = j0 + e * 32 + lane;
     key[e] = (j < p.V) ? rank_key(__ldcg(z + j), j) : 0ull;
   }
-  for (int r = 0; r < K; ++r) {  // this warp's 128 entries, best first
+  unsigned long long* out =
+      p.cand + ((static_cast<size_t>(b) * p.NS + sl) * kMaxRows + row) * kMaxTopK;
+  for (int r = 0; r < K; ++r) {
     unsigned long long m = key[0];
 #pragma unroll
-    for (int e = 1; e < 4; ++e) m = key[e] > m ? key[e] : m;
+    for (int e = 1; e < kAcceptSlice / 32; ++e) m = key[e] > m ? key[e] : m;
     const unsigned long long wm = warp_max_u64(m);
-    if (lane == 0) s_lists[warp * kMaxTopK + r] = wm;
+    if (lane == 0) out[r] = wm;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < kAcceptSlice / 32; ++e)
       if (key[e] == wm) key[e] = 0ull;  // keys are unique: only the winner matches
   }
-  __syncthreads();
-  if (warp == 0) {  // merge the eight lists
-    unsigned long long c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = lane + 32 * i;
-      c[i] = (idx < 8 * K) ? s_lists[(idx / K) * kMaxTopK + idx % K] : 0ull;
-    }
-    unsigned long long* out =
-        p.cand + ((static_cast<size_t>(b) * p.NS + sl) * kMaxRows + row) * kMaxTopK;
-    for (int r = 0; r < K; ++r) {
-      unsigned long long m = c[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) m = c[i] > m ? c[i] : m;
-      const unsigned long long wm = warp_max_u64(m);
-      if (lane == 0) out[r] = wm;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (c[i] == wm) c[i] = 0ull;
-    }
-  }
-  __syncthreads();  // the lists are reused by the next row
 }
 
 // The best K keys of row `row` over the whole vocabulary: a tournament over the slices' sorted
-// lists (each thread holds the heads of slices tid + 256 m, m < 4). Called by every thread.
+// lists (each thread holds the heads of slices tid + 256 m, m < 4). When the row's NS x K keys
+// fit in `stage` (dynamic shared memory) they are first copied there in one coalesced pass, so
+// that a round's winner reads its next key from shared memory: read from L2 instead, that load
+// sits on the critical path of every round. Called by every thread.
 __device__ void merge_rows_topk(const AcceptParams& p, int b, int row, int K,
-                                unsigned long long* s_top, unsigned long long* sh) {
+                                unsigned long long* s_top, unsigned long long* sh,
+                                unsigned long long* stage, int stage_keys) {
   const int tid = threadIdx.x;
   const unsigned long long* base = p.cand + static_cast<size_t>(b) * p.NS * kMaxRows * kMaxTopK;
+  const bool staged = p.NS * K <= stage_keys;
+  if (staged) {
+    for (int i = tid; i < p.NS * K; i += kAcceptThreads) {
+      const int s = i / K, j = i - s * K;
+      stage[i] = __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) * kMaxTopK + j);
+    }
+    __syncthreads();
+  }
+  auto at = [&](int s, int j) {
+    return staged ? stage[s * K + j]
+                  : __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) * kMaxTopK + j);
+  };
   int ptr[4];
   unsigned long long head[4];
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int s = tid + kAcceptThreads * m;
     ptr[m] = 0;
-    head[m] = (s < p.NS) ? __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) * kMaxTopK)
-                         : 0ull;
+    head[m] = (s < p.NS) ? at(s, 0) : 0ull;
   }
   for (int r = 0; r < K; ++r) {
     unsigned long long m = head[0];
@@ -308,9 +305,7 @@ __device__ void merge_rows_topk(const AcceptParams& p, int b, int row, int K,
         if (head[i] == bm) {
           const int s = tid + kAcceptThreads * i;
           ++ptr[i];
-          head[i] = (ptr[i] < K) ? __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) *
-                                                     kMaxTopK + ptr[i])
-                                 : 0ull;
+          head[i] = (ptr[i] < K) ? at(s, ptr[i]) : 0ull;
         }
       }
     }
@@ -516,10 +511,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
   unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
   if (D.need == 4) {
-    // filtered: the slice's best top_k keys of every row 0..k
-    __shared__ unsigned long long s_lists[8 * kMaxTopK];
-    const int K = p.top_k[b];
-    for (int r = 0; r <= k; ++r) slice_topk(p, b, sl, r, K, s_lists);
+    // filtered: the slice's best top_k keys of every row 0..k, one warp per row
+    if (warp <= k) slice_topk_warp(p, b, sl, warp, p.top_k[b]);
   } else if (D.need == 3) {
     // exact-match: the p weights of every row 0..k over this slice, slots 0..k
     unsigned long long sp[kMaxRows];
@@ -632,8 +625,9 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       f_stop = 0;
     }
     __syncthreads();
+    extern __shared__ unsigned long long f_stage[];  // kFilterStageKeys when launched filtered
     for (int r = 0; r <= k; ++r) {
-      merge_rows_topk(p, b, r, K, s_top, sh);
+      merge_rows_topk(p, b, r, K, s_top, sh, f_stage, p.filtered ? kFilterStageKeys : 0);
       if (tid == 0) {
         int id[kMaxTopK];
         unsigned long long w[kMaxTopK];
@@ -800,7 +794,9 @@ cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream) {
 
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream) {
   dim3 grid(prm.NS, prm.B);
-  return launch_pdl(accept_kernel, grid, dim3(kAcceptThreads), 0, stream, prm);
+  const int smem = prm.filtered ? kFilterStageKeys * static_cast<int>(sizeof(unsigned long long))
+                                : 0;
+  return launch_pdl(accept_kernel, grid, dim3(kAcceptThreads), smem, stream, prm);
 }
 
 }  // namespace spec
