@@ -41,6 +41,13 @@ top_p, renormalised. Drafts are the draft head's argmax picks and q is one-hot a
 the ratio rule keeps d_i when u <= p'_{i-1}(d_i), a rejection draws from p'_{i-1} without d_i,
 and the bonus draws from p'_k: the emitted tokens follow the filtered target law exactly.
 
+Draft set: lucebox-hub PR #15, *What*: the draft head covers 64,000 rows, the control and
+special tokens plus the lowest ids. Read as two ranges, the lowest n_low ids and n_high rows
+from hi_first (where a tokenizer keeps its special tokens): draft row r is vocabulary id r for
+r < n_low, hi_first + r - n_low after. ``rows`` (the vocabulary ids of the draft rows, in
+order) carries that map through ``draft_token``, ``draft_chain_tokens`` and ``accept_request``;
+without it the draft rows are ids 0 .. Vd-1. q is zero at ids outside the set.
+
 Inverse CDF: the smallest j (ascending token id) with cumsum(w)[j] > u * sum(w); if rounding
 leaves none, the last j with w[j] > 0. Readings where the pages are silent are listed in the
 design notes (draft rows checked against row i-1, lowest-index argmax ties, ``<=`` in the ratio
@@ -93,8 +100,14 @@ def inverse_cdf(w, u):
     return j, float(margin)
 
 
-def draft_token(y, T, u=None):
-    """The draft head's token from its logits row ``y`` (float64 [Vd]).
+def draft_rows(n_low, hi_first, n_high):
+    """Vocabulary ids of the draft rows: [0, n_low) then [hi_first, hi_first + n_high)."""
+    return np.concatenate([np.arange(n_low), hi_first + np.arange(n_high)]).astype(np.int64)
+
+
+def draft_token(y, T, u=None, rows=None):
+    """The draft head's token from its logits row ``y`` (float64 [Vd]; row r is vocabulary id
+    rows[r], or r without ``rows``).
 
     T == 0: argmax (lowest index on ties) -- lucebox-hub PR #15, *What*: the draft head "picks
     its token on the GPU". T > 0: inverse-CDF draw of softmax(y/T) with ``u`` =
@@ -105,22 +118,18 @@ def draft_token(y, T, u=None):
     if st["nonfinite"]:
         return -1, 0.0
     if T == 0:
-        return st["argmax"], st["gap"]
-    return inverse_cdf(lmhead.probs(y, T), u)
+        j, m = st["argmax"], st["gap"]
+    else:
+        j, m = inverse_cdf(lmhead.probs(y, T), u)
+    return (int(rows[j]) if rows is not None else j), m
 
 
-def _q_at(y, x, T):
-    """q_i(x) for draft logits row y over the draft rows (0 beyond them)."""
-    if x >= y.shape[0]:
-        return 0.0
-    return float(lmhead.probs(y, T)[x])
-
-
-def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
+def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7, rows=None):
     """Acceptance for one request and one cycle.
 
     z:       float64 [>= k+1, V] verify logits; row r predicts position pos_base + r.
-    y:       float64 [>= k, Vd] draft logits (row i-1 belongs to draft i) or None (one-hot q).
+    y:       float64 [>= k, Vd] draft logits (row i-1 belongs to draft i) or None (one-hot q);
+             column r is vocabulary id rows[r] (r without ``rows``), q is 0 elsewhere.
     drafts:  ints, drafts[i-1] = d_i.
     uniform: callable (pos, purpose) -> u in [0, 1) (the request's seeded Philox stream).
     Returns dict(status, n_accept, tokens, n_emit, eos_hit, sample_kind, sample_row, margins)
@@ -183,7 +192,10 @@ def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
             else:
                 qd = lmhead.probs(y[i - 1], T)
                 q = np.zeros(V)
-                q[: qd.shape[0]] = qd
+                if rows is None:
+                    q[: qd.shape[0]] = qd
+                else:
+                    q[np.asarray(rows)] = qd
             px, qx = float(p[x]), float(q[x])
             u = uniform(pos_base + i - 1, PURPOSE_ACCEPT)
             margins.append(("ratio", abs(u * qx - px)))
@@ -272,7 +284,7 @@ def accept_request_exact(z, drafts, k, T, eos_id, uniform, pos_base, k_max=7):
     return res
 
 
-def draft_chain_tokens(y_rows, T, uniform, pos_base):
+def draft_chain_tokens(y_rows, T, uniform, pos_base, rows=None):
     """Draft tokens for one request from precomputed draft logits rows (row i-1 -> draft i).
 
     Each draft is an independent call of ``draft_token`` with U(pos_base+i-1, DRAFT). Returns
@@ -281,7 +293,7 @@ def draft_chain_tokens(y_rows, T, uniform, pos_base):
     toks, margins = [], []
     for i in range(1, len(y_rows) + 1):
         u = uniform(pos_base + i - 1, PURPOSE_DRAFT) if T > 0 else None
-        t, m = draft_token(y_rows[i - 1], T, u)
+        t, m = draft_token(y_rows[i - 1], T, u, rows)
         toks.append(t)
         margins.append(("gap" if T == 0 else "cdf", m))
     return toks, margins
