@@ -221,6 +221,26 @@ spec_status spec_draft_argmax(const void *W, spec_dtype wdt, int64_t V_draft, in
                               void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * spec_draft_argmax_rows -- spec_draft_argmax over a draft set of two row ranges (lucebox-hub
+ * PR #15, "What": the draft head covers the control and special tokens plus the lowest ids).
+ * Draft row r (r < n_low + n_high) is vocabulary row r for r < n_low and row
+ * hi_first + r - n_low after; the special tokens a tokenizer keeps at the top of the vocabulary
+ * form the second range. q_logits/q_stats are in draft-row order (V_draft = n_low + n_high
+ * columns); token_out and q_stats.argmax are vocabulary ids. n_high = 0 is spec_draft_argmax.
+ * Requires hi_first >= n_low, hi_first + n_high <= the rows of W, and, when n_high > 0, bf16 or
+ * SPEC_Q4A32 weights with n_low a multiple of 32 (whole 32-row boxes); else
+ * SPEC_ERR_INVALID / SPEC_ERR_UNSUPPORTED. Other arguments as for spec_draft_argmax.
+ */
+spec_status spec_draft_argmax_rows(const void *W, spec_dtype wdt, int64_t n_low, int64_t hi_first,
+                                   int64_t n_high, int64_t d, const void *h, int32_t B,
+                                   const float *temperature, const uint64_t *seed,
+                                   const int64_t *pos, int32_t pos_offset, int32_t *token_out,
+                                   int32_t token_stride, float *q_logits, int64_t q_stride,
+                                   spec_rowstats *q_stats, const int32_t *k_active,
+                                   void *workspace, size_t workspace_bytes,
+                                   spec_stream_t stream);
+
+/*
  * spec_accept -- acceptance, residual correction, bonus token and EOS truncation for B
  * requests (greedy rule: lucebox-hub PR #15, "Exactness"; ratio rule, residual, zero and
  * non-finite handling, EOS: DS4Server issue #98, "Implementation" and closing comment).
@@ -256,6 +276,22 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t *k, const int32_
                         const uint64_t *seed, const int64_t *pos_base, spec_accept_out *out,
                         spec_counters *counters, void *workspace, size_t workspace_bytes,
                         spec_stream_t stream);
+
+/*
+ * spec_accept_rows -- spec_accept with q over the two-range draft set of
+ * spec_draft_argmax_rows: q_i(x) is read from draft row x (x < n_low) or n_low + x - hi_first
+ * (hi_first <= x < hi_first + n_high), and is zero at every other id, in the ratio test and in
+ * the residual max(0, p - q). q_logits rows hold n_low + n_high columns in draft-row order.
+ * Requires hi_first >= n_low and hi_first + n_high <= V. n_high = 0 is spec_accept.
+ */
+spec_status spec_accept_rows(int32_t B, int32_t k_max, const int32_t *k, const int32_t *drafts,
+                             const float *logits, const spec_rowstats *stats, int64_t V,
+                             int32_t R, const float *q_logits, const spec_rowstats *q_stats,
+                             int64_t n_low, int64_t hi_first, int64_t n_high, int64_t q_stride,
+                             const float *temperature, int32_t eos_id, const uint64_t *seed,
+                             const int64_t *pos_base, spec_accept_out *out,
+                             spec_counters *counters, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
 
 /*
  * spec_accept_exact -- exact-match acceptance at temperature (lucebox-hub PR #15,

@@ -77,6 +77,25 @@ def spec_draft_argmax(W, wdt, V_draft, d, h, B, temperature, seed, pos, pos_offs
         _ptr(k_active), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
+def spec_draft_argmax_rows(W, wdt, n_low, hi_first, n_high, d, h, B, temperature, seed, pos,
+                           pos_offset, token_out, token_stride, q_logits, q_stride, q_stats,
+                           k_active, workspace, stream=None):
+    _check("spec_draft_argmax_rows", _abi.lib().spec_draft_argmax_rows(
+        _ptr(W), wdt, n_low, hi_first, n_high, d, _ptr(h), B, _ptr(temperature), _ptr(seed),
+        _ptr(pos), pos_offset, _ptr(token_out), token_stride, _ptr(q_logits), q_stride,
+        _ptr(q_stats), _ptr(k_active), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def spec_accept_rows(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, n_low,
+                     hi_first, n_high, q_stride, temperature, eos_id, seed, pos_base, out,
+                     counters, workspace, stream=None):
+    _check("spec_accept_rows", _abi.lib().spec_accept_rows(
+        B, k_max, _ptr(k), _ptr(drafts), _ptr(logits), _ptr(stats), V, R, _ptr(q_logits),
+        _ptr(q_stats), n_low, hi_first, n_high, q_stride, _ptr(temperature), eos_id, _ptr(seed),
+        _ptr(pos_base), _ptr(out), _ptr(counters), _ptr(workspace), _nbytes(workspace),
+        _stream(stream)))
+
+
 def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_draft, q_stride,
                 temperature, eos_id, seed, pos_base, out, counters, workspace, stream=None):
     _check("spec_accept", _abi.lib().spec_accept(

@@ -18,6 +18,7 @@ REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN,
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
 EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
            "spec_accept", "spec_accept_exact", "spec_accept_filtered", "spec_adapt_width",
+           "spec_draft_argmax_rows", "spec_accept_rows",
            "spec_commit_rollback",
            "spec_batched_supported",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes")
@@ -97,6 +98,12 @@ def lib():
         L.spec_accept_filtered.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, vp, i32,
                                            vp, vp, vp, vp, vp, sz, vp]
         L.spec_accept_filtered.restype = i32
+        L.spec_draft_argmax_rows.argtypes = [vp, i32, i64, i64, i64, i64, vp, i32, vp, vp, vp,
+                                             i32, vp, i32, vp, i64, vp, vp, vp, sz, vp]
+        L.spec_draft_argmax_rows.restype = i32
+        L.spec_accept_rows.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, i64, i64,
+                                       i64, i64, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.spec_accept_rows.restype = i32
         L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.spec_adapt_width.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,

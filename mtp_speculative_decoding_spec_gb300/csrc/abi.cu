@@ -118,7 +118,8 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
                         const uint64_t* seed, const int64_t* pos, int pos_offset,
                         int32_t* token_out, int token_stride, const int32_t* kact,
                         void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
-                        EncodeTiledFn encode, cudaStream_t stream) {
+                        EncodeTiledFn encode, cudaStream_t stream, int64_t lo_rows,
+                        int64_t hi_row0, int64_t V_rows) {
   GemvTcLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
@@ -145,7 +146,7 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   const int64_t row_bytes = d * 2;
   const cuuint32_t estride[2] = {1, 1};
   {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(V)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(V_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_tc_kblock()),
                                static_cast<cuuint32_t>(gemv_tc_box_rows())};
@@ -187,6 +188,8 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   p.token_out = token_out;
   p.token_stride = token_stride;
   p.kact = kact;
+  p.lo_rows = lo_rows;
+  p.hi_row0 = hi_row0;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
@@ -203,7 +206,8 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
                         const uint64_t* seed, const int64_t* pos, int pos_offset,
                         int32_t* token_out, int token_stride, const int32_t* kact,
                         void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
-                        EncodeTiledFn encode, cudaStream_t stream) {
+                        EncodeTiledFn encode, cudaStream_t stream, int64_t lo_rows,
+                        int64_t hi_row0, int64_t V_rows) {
   GemvQ4Launch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
@@ -228,7 +232,7 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
   const cuuint64_t pitch[1] = {static_cast<cuuint64_t>(5 * d / 8)};
   const cuuint32_t estride[2] = {1, 1};
   {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(V)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(V_rows)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_code_box_bytes()),
                                static_cast<cuuint32_t>(gemv_q4_box_rows())};
     if (encode(&L.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), gdim, pitch, box,
@@ -237,7 +241,7 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
       return SPEC_ERR_CUDA;
   }
   {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 8), static_cast<cuuint64_t>(V)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 8), static_cast<cuuint64_t>(V_rows)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_pair_box_bytes()),
                                static_cast<cuuint32_t>(gemv_q4_box_rows())};
     void* pairs = static_cast<uint8_t*>(const_cast<void*>(W)) + d / 2;  // 16-byte aligned
@@ -280,6 +284,8 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
   p.token_out = token_out;
   p.token_stride = token_stride;
   p.kact = kact;
+  p.lo_rows = lo_rows;
+  p.hi_row0 = hi_row0;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
@@ -294,7 +300,14 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
                      int64_t logits_stride, spec_rowstats* stats, int draft,
                      const uint64_t* seed, const int64_t* pos, int pos_offset,
                      int32_t* token_out, int token_stride, const int32_t* kact, void* workspace,
-                     size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream) {
+                     size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream,
+                     int64_t lo_rows = -1, int64_t hi_row0 = -1) {
+  // rows [0, V) are weight rows [0, V), or [0, lo_rows) then hi_row0.. (a two-range draft set)
+  if (lo_rows < 0 || lo_rows >= V) {
+    lo_rows = V;
+    hi_row0 = V;
+  }
+  const int64_t V_rows = hi_row0 + (V - lo_rows);  // weight rows the tensor maps span
   const DevAttr a = dev_attr();
   if (a.sms <= 0) return SPEC_ERR_CUDA;
   const int elt = (wdt == SPEC_BF16) ? 2 : 4;
@@ -317,11 +330,12 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   if (wdt == SPEC_Q4A32)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_q4(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
-                       grid, a, encode, stream);
+                       grid, a, encode, stream, lo_rows, hi_row0, V_rows);
   if (wdt == SPEC_BF16)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
-                       grid, a, encode, stream);
+                       grid, a, encode, stream, lo_rows, hi_row0, V_rows);
+  if (lo_rows != V) return SPEC_ERR_UNSUPPORTED;  // the fp32 kernel's 60-row bands: [0, V) only
 
   GemvLaunch L;
   memset(&L, 0, sizeof(L));
@@ -386,6 +400,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.token_out = token_out;
   p.token_stride = token_stride;
   p.kact = kact;
+  p.lo_rows = V;
+  p.hi_row0 = V;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   L.grid = grid;
@@ -454,7 +470,7 @@ spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t
                        const uint64_t* seed, const int64_t* pos_base, spec_accept_out* out,
                        spec_counters* counters, void* workspace, size_t workspace_bytes,
                        spec_stream_t stream, int exact, const int32_t* top_k = nullptr,
-                       const float* top_p = nullptr) {
+                       const float* top_p = nullptr, int64_t q_lo = -1, int64_t q_hi0 = -1) {
   if (B < 1 || k_max < 0 || k_max > kMaxRows - 1 || R < 1 || R > kMaxRows) return SPEC_ERR_INVALID;
   if (!k || (k_max > 0 && !drafts) || !stats || !temperature || !seed || !pos_base || !out ||
       !workspace)
@@ -480,6 +496,14 @@ spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t
   p.q_logits = q_logits;
   p.q_stats = q_stats;
   p.Vd = q_logits ? V_draft : 0;
+  // draft rows [0, Vd) are ids [0, Vd), or [0, q_lo) then q_hi0.. (a two-range draft set)
+  if (q_lo < 0 || q_lo >= p.Vd) {
+    q_lo = p.Vd;
+    q_hi0 = p.Vd;
+  }
+  if (q_hi0 < q_lo || q_hi0 + (p.Vd - q_lo) > V) return SPEC_ERR_INVALID;
+  p.q_lo = q_lo;
+  p.q_hi0 = q_hi0;
   p.q_stride = q_stride;
   p.temperature = temperature;
   p.eos = eos_id;
@@ -566,6 +590,46 @@ spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, in
   return run_gemv(W, wdt, V_draft, d, h, B, 1, temperature, q_logits, q_stride, q_stats, 1,
                   seed, pos, pos_offset, token_out, token_stride, k_active, workspace,
                   workspace_bytes, B, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spec_status spec_draft_argmax_rows(const void* W, spec_dtype wdt, int64_t n_low, int64_t hi_first,
+                                   int64_t n_high, int64_t d, const void* h, int32_t B,
+                                   const float* temperature, const uint64_t* seed,
+                                   const int64_t* pos, int32_t pos_offset, int32_t* token_out,
+                                   int32_t token_stride, float* q_logits, int64_t q_stride,
+                                   spec_rowstats* q_stats, const int32_t* k_active,
+                                   void* workspace, size_t workspace_bytes,
+                                   spec_stream_t stream) {
+  if (!W || !h || !temperature || !seed || !pos || !token_out || !workspace)
+    return SPEC_ERR_INVALID;
+  if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
+  if (n_low < 0 || n_high < 0 || hi_first < n_low || n_low + n_high < 1 ||
+      hi_first + n_high >= (int64_t(1) << 24) || d < 1 || B < 1 || B > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (n_high > 0 && (wdt == SPEC_F32 || n_low % gemv_tc_box_rows() != 0))
+    return SPEC_ERR_UNSUPPORTED;  // whole 32-row TMA boxes on the tensor-core kernels only
+  const int64_t V_draft = n_low + n_high;
+  if (token_stride < 1 || (q_logits && q_stride < V_draft)) return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(h) || !aligned16(workspace)) return SPEC_ERR_INVALID;
+  return run_gemv(W, wdt, V_draft, d, h, B, 1, temperature, q_logits, q_stride, q_stats, 1,
+                  seed, pos, pos_offset, token_out, token_stride, k_active, workspace,
+                  workspace_bytes, B, reinterpret_cast<cudaStream_t>(stream),
+                  n_high > 0 ? n_low : -1, hi_first);
+}
+
+spec_status spec_accept_rows(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,
+                             const float* logits, const spec_rowstats* stats, int64_t V,
+                             int32_t R, const float* q_logits, const spec_rowstats* q_stats,
+                             int64_t n_low, int64_t hi_first, int64_t n_high, int64_t q_stride,
+                             const float* temperature, int32_t eos_id, const uint64_t* seed,
+                             const int64_t* pos_base, spec_accept_out* out,
+                             spec_counters* counters, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream) {
+  if (n_low < 0 || n_high < 0 || hi_first < n_low) return SPEC_ERR_INVALID;
+  return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats,
+                          n_low + n_high, q_stride, temperature, eos_id, seed, pos_base, out,
+                          counters, workspace, workspace_bytes, stream, 0, nullptr, nullptr,
+                          n_high > 0 ? n_low : -1, hi_first);
 }
 
 spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,

@@ -43,6 +43,14 @@ struct Decision {
   int pad;
 };
 
+// Draft row holding vocabulary id x: x below lo, lo + x - hi0 from hi0 while inside the Vd
+// draft rows, -1 for ids the draft set does not cover (q = 0 there).
+__device__ __forceinline__ int64_t draft_row_of(int64_t x, int64_t lo, int64_t hi0, int64_t Vd) {
+  if (x < lo) return x;
+  const int64_t r = lo + (x - hi0);
+  return (x >= hi0 && r < Vd) ? r : -1;
+}
+
 // p(v) = exp((z - max)/T) * exp(-log_norm), every operation rounded on its own.
 __device__ __forceinline__ float prob_of(float z, float mx, float invT, float inv_norm) {
   return __fmul_rn(expf(__fmul_rn(__fsub_rn(z, mx), invT)), inv_norm);
@@ -53,7 +61,7 @@ struct DrawCtx {
   float pmax, pinvT, pinv_norm;
   const float* qrow;  // draft logits row (residual with q_logits), else null
   float qmax, qinv_norm;
-  int64_t Vd;
+  int64_t Vd, qlo, qhi0;  // draft rows and their map (draft_row_of)
   int xrej;        // one-hot q position (residual without q_logits), else -1
   bool residual;
 };
@@ -70,7 +78,8 @@ __device__ __forceinline__ void entry_weights(const DrawCtx& c, int64_t j,
   }
   float qj = 0.f;
   if (c.qrow) {
-    if (j < c.Vd) qj = prob_of(__ldcg(c.qrow + j), c.qmax, c.pinvT, c.qinv_norm);
+    const int64_t jr = draft_row_of(j, c.qlo, c.qhi0, c.Vd);
+    if (jr >= 0) qj = prob_of(__ldcg(c.qrow + jr), c.qmax, c.pinvT, c.qinv_norm);
   } else {
     qj = (j == c.xrej) ? 1.f : 0.f;
   }
@@ -129,6 +138,8 @@ __device__ __forceinline__ DrawCtx draw_ctx(const AcceptParams& p, int b, int ro
   c.qmax = 0.f;
   c.qinv_norm = 0.f;
   c.Vd = p.Vd;
+  c.qlo = p.q_lo;
+  c.qhi0 = p.q_hi0;
   c.xrej = -1;
   if (residual) {
     if (p.q_logits) {
@@ -435,10 +446,11 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
         float qx = 1.f;
         if (p.q_logits) {
           qx = 0.f;
-          if (static_cast<int64_t>(x) < p.Vd) {
+          const int64_t xr = draft_row_of(x, p.q_lo, p.q_hi0, p.Vd);
+          if (xr >= 0) {
             const size_t qr = static_cast<size_t>(lane) * p.B + b;
             const spec_rowstats qs = p.q_stats[qr];
-            qx = prob_of(__ldcg(p.q_logits + qr * p.q_stride + x), qs.max, invT,
+            qx = prob_of(__ldcg(p.q_logits + qr * p.q_stride + xr), qs.max, invT,
                          expf(-qs.log_norm));
           }
         }

@@ -31,6 +31,15 @@ __device__ __forceinline__ bool draft_step_idle(const GemvParams& p) {
   return true;
 }
 
+// Vocabulary id of projected row r (-1 stays -1).
+__device__ __forceinline__ int32_t row_id(const GemvParams& p, int64_t r) {
+  return static_cast<int32_t>(r < p.lo_rows ? r : p.hi_row0 + (r - p.lo_rows));
+}
+// Weight row of the TMA box that starts at projected row y (boxes never straddle lo_rows).
+__device__ __forceinline__ int box_row(const GemvParams& p, int y) {
+  return static_cast<int>(y < p.lo_rows ? y : p.hi_row0 + (y - p.lo_rows));
+}
+
 // Per-row inputs of the statistics and the draw, read once at the start of the kernel (after
 // its dependency wait) so that the last block's finish does not wait on global loads.
 struct RowInputs {
@@ -188,7 +197,7 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
       st.max = M;
       st.log_norm = __fsub_rn(logf(S), 27.725887222397812f);  // log(S * 2^-40)
       st.gap = __fsub_rn(M, t.second);
-      st.argmax = t.idx;
+      st.argmax = t.idx < 0 ? t.idx : row_id(p, t.idx);
     }
     if (lane == 0 && p.stats) p.stats[q] = st;
 
@@ -295,7 +304,8 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
           }
         }
       }
-      if (lane == 0) p.token_out[static_cast<size_t>(q) * p.token_stride] = tok;
+      if (lane == 0)
+        p.token_out[static_cast<size_t>(q) * p.token_stride] = tok < 0 ? tok : row_id(p, tok);
     }
   }
   if (tid == 0) p.hdr->gemv_ticket = 0u;

@@ -162,10 +162,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int c = 0; c < nch; ++c)
       for (int b = 0; b < nbox; ++b)
         tc_tma_load_2d(st + c * kQCodeTile + b * kQCodeBox, &cmap, x0 + c * kQChunkBytes,
-                       y + b * kQBoxRows, &full[s]);
+                       box_row(p, y + b * kQBoxRows), &full[s]);
     for (int b = 0; b < nbox; ++b)
       tc_tma_load_2d(st + kQPairOff + b * kQPairBox, &smap, ks * kQPairRowBytes,
-                     y + b * kQBoxRows, &full[s]);
+                     box_row(p, y + b * kQBoxRows), &full[s]);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it
     const int ks = it % nks;

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     for (int kk = 0; kk < nk; ++kk)
       for (int b = 0; b < nbox; ++b)
         tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
-                       (ks * kSkKB + kk) * kSkKBlock, y + b * kSkBoxRows, &full[s]);
+                       (ks * kSkKB + kk) * kSkKBlock, box_row(p, y + b * kSkBoxRows),
+                       &full[s]);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it into stage s
     const int t = it / nks, ks = it - t * nks;
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     for (int kk = 0; kk < nk; ++kk) {
       const int x = (ks * kSkKB + kk) * kSkKBlock;
       for (int b = 0; b < nbox; ++b)
-        tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, y + b * kSkBoxRows,
-                       &full[s]);
+        tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x,
+                       box_row(p, y + b * kSkBoxRows), &full[s]);
       tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
     }
   };

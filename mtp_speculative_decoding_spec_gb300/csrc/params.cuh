@@ -36,6 +36,9 @@ struct GemvParams {
   int32_t* token_out;
   int token_stride;
   const int32_t* kact;  // draft head: row b needs this step only if kact[b] > pos_offset (nullable)
+  // projected row r (r < V) is weight row r below lo_rows and hi_row0 + r - lo_rows from there
+  // (a draft set of two ranges; lo_rows = V when the rows are simply [0, V))
+  int64_t lo_rows, hi_row0;
   WsHeader* hdr;
   GemvPartial* part;
 };
@@ -80,6 +83,9 @@ struct AcceptParams {
   const int32_t* top_k;      // [B] in [1, kMaxTopK]
   const float* top_p;        // [B] in (0, 1]
   unsigned long long* cand;  // [B][NS][8 rows][kMaxTopK] each slice's best keys, descending
+  // draft row of vocabulary id x: x below q_lo, q_lo + x - q_hi0 in [q_hi0, q_hi0 + Vd - q_lo),
+  // none elsewhere (q_lo = Vd when the draft rows are [0, Vd))
+  int64_t q_lo, q_hi0;
 };
 
 constexpr int kMaxTopK = 32;               // largest top-k of the filtered acceptance
