@@ -362,7 +362,8 @@ typedef struct {
  * rejected, deeper ones were not observed. Each observed depth moves its rate by
  * alpha * (x - rate) (x = 1 accepted, 0 rejected). A depth not yet observed is believed to do
  * as well as the depth above it (0.5 for depth 1), so widths grow while drafts keep being
- * accepted. A request whose status is not OK keeps its rates. Then, with
+ * accepted; a depth observed before but not in this cycle relaxes by the same alpha towards
+ * the belief of the depth above it, so a depth that looked poor is tried again. A request whose status is not OK keeps its rates. Then, with
  * E(k) = 1 + sum_{j<=k} prod_{i<=j} belief[i] the
  * expected tokens of a cycle at width k, the next width is the k in [1, k_max] maximising
  * E(k) / cost[k] (the smallest on ties; never 0, so depth 1 stays observed and a request whose

@@ -764,6 +764,7 @@ __global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
   for (int d = 1; d < kMaxRows; ++d)
     bel[d] = ((s.seen >> d) & 1u) ? s.rate[d] : (d > 1 ? bel[d - 1] : 0.5f);
   if (o.status == SPEC_REQ_OK && k >= 0 && k <= kMaxRows - 1) {
+    uint32_t obs = 0u;  // depths observed in this cycle
     for (int d = 1; d <= k; ++d) {
       float x;
       if (d <= o.n_accept)
@@ -774,6 +775,16 @@ __global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
         break;
       s.rate[d] = __fadd_rn(bel[d], __fmul_rn(p.alpha, __fsub_rn(x, bel[d])));
       s.seen |= 1u << d;
+      obs |= 1u << d;
+    }
+    // a depth seen before but not in this cycle relaxes towards the updated belief of the
+    // depth above, in increasing depth, so that one that looked poor is tried again
+    float above = ((s.seen >> 1) & 1u) ? s.rate[1] : 0.5f;
+    for (int d = 2; d < kMaxRows; ++d) {
+      const bool was_seen = (s.seen >> d) & 1u;
+      if (was_seen && !((obs >> d) & 1u))
+        s.rate[d] = __fadd_rn(s.rate[d], __fmul_rn(p.alpha, __fsub_rn(above, s.rate[d])));
+      above = was_seen ? s.rate[d] : above;
     }
     s.cycles += 1u;
   }

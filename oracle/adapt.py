@@ -19,8 +19,12 @@ Update from one cycle's acceptance result (status, n_accept, eos_hit) at width k
     depth never observed is the belief of the depth above it (0.5 for depth 1): a deeper draft
     is assumed to do as well as the last one seen until it is tried, so widths grow while drafts
     keep being accepted (with a fixed 0.5 for unseen depths a width of 1 never looks worth
-    extending and depth 2 is never observed). A request whose status is not OK leaves its
-    state unchanged.
+    extending and depth 2 is never observed). A depth observed before but not in this cycle
+    relaxes towards the belief of the depth above it, rate[d] += alpha * (b'[d-1] - rate[d]),
+    in increasing d with b' the updated beliefs: a depth that once looked poor is tried again
+    once the relaxation makes it pay, instead of never being observed again (measured: a
+    width stuck at 1 after a few early rejections at depth 2). A request whose status is not OK
+    leaves its state unchanged.
 
 Choice: expected tokens at width k, with the depths independent at their beliefs,
     E(k) = 1 + sum_{j=1..k} prod_{i=1..j} rate[i]
@@ -50,6 +54,7 @@ def observe(state, status, n_accept, eos_hit, k, alpha):
         return state
     rate = state["rate"]
     before = rates(state)
+    seen = set()
     for d in range(1, k + 1):
         if d <= n_accept:
             x = 1.0
@@ -58,6 +63,11 @@ def observe(state, status, n_accept, eos_hit, k, alpha):
         else:
             break
         rate[d] = before[d] + alpha * (x - before[d])
+        seen.add(d)
+    for d in range(2, len(rate)):  # relax the depths this cycle did not observe
+        if d not in seen and rate[d] is not None:
+            above = rates(state)[d - 1]
+            rate[d] = rate[d] + alpha * (above - rate[d])
     state["cycles"] += 1
     return state
 

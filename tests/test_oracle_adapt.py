@@ -56,7 +56,9 @@ def test_observation_rules():
     adapt.observe(st, 0, 2, False, 5, 0.5)  # depths 1, 2 kept, 3 rejected, 4-5 unseen
     assert st["rate"][1:6] == [0.75, 0.75, 0.25, None, None]
     adapt.observe(st, 0, 1, True, 5, 0.5)  # depth 1 kept and it was EOS: nothing else seen
-    assert st["rate"][1:4] == [0.875, 0.75, 0.25]
+    # depth 1: 0.75 -> 0.875; depths 2 and 3 relax halfway to the depth above, in order:
+    # 0.75 + (0.875 - 0.75)/2 = 0.8125, then 0.25 + (0.8125 - 0.25)/2 = 0.53125
+    assert st["rate"][1:6] == [0.875, 0.8125, 0.53125, None, None]
     adapt.observe(st, 1, 0, False, 5, 0.5)  # a failed request changes nothing
     assert st["cycles"] == 2
     assert adapt.rates(st)[4] == st["rate"][3]  # unseen depth: the belief of the one above
@@ -72,6 +74,27 @@ def test_unseen_depths_follow_the_last_seen_one():
     assert b[1] > 0.95 and b[2:] == [b[1]] * 6
     cost = [1.0 + 0.5 * k for k in range(8)]
     assert adapt.choose(st, cost, 7)[0] > 1
+
+
+def test_a_depth_that_looked_poor_is_tried_again():
+    """Depth 2 rejected a few times early, then only width 1 chosen: the relaxation brings
+    depth 2 back towards depth 1 until width 2 pays again (with depth 1 at ~0.87 and a draft
+    costing half a cycle)."""
+    st = adapt.new_state()
+    cost = [1.0 + 0.5 * k for k in range(8)]
+    for _ in range(30):
+        adapt.observe(st, 0, 1, False, 1, 0.1)   # depth 1 accepted at width 1
+    for _ in range(4):
+        adapt.observe(st, 0, 1, False, 2, 0.1)   # depth 2 rejected at width 2
+    k, _ = adapt.choose(st, cost, 7)
+    assert k == 1                                # depth 2 now looks poor
+    widths = []
+    for _ in range(60):
+        k, _ = adapt.choose(st, cost, 7)
+        widths.append(k)
+        adapt.observe(st, 0, min(k, 1), False, k, 0.1) if k == 1 else \
+            adapt.observe(st, 0, k, False, k, 0.1)    # deeper drafts are in fact accepted
+    assert max(widths) > 1 and widths[-1] > 1
 
 
 def test_choice_corner_cases():
