@@ -21,7 +21,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// cuTensorMapEncodeTiled from the driver, fetched through the runtime (no -lcuda).
+// cuTensorMapEncodeTiled from the CUDA driver API, fetched through the runtime (no -lcuda).
 EncodeTiledFn encode_tiled() {
   static EncodeTiledFn fn = nullptr;
   static bool tried = false;

@@ -2,8 +2,8 @@
 
 lucebox-hub PR #15 "MTP speculative decoding", *What* and *Speed*: the default verify width is
 adaptive -- it settles at seven drafts on a prompt the draft head predicts well and stays small
-where it does not. The pages do not give the controller; this is the plain reading SURVEY's
-NEXT item states: an exponential moving average of the acceptance rate at each draft depth plus a
+where it does not. The pages do not give the controller; this is a plain reading of it: an
+exponential moving average of the acceptance rate at each draft depth plus a
 cycle-cost table, choosing the width with the most expected tokens per unit of cost.
 
 State per request (all float64 here): rate[d] for depth d = 1..7 -- the average, over the
