@@ -101,6 +101,41 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_commit_rollback(1, None, fake, fake, 0, null, null) == 1
 
 
+def test_host_validation_of_the_later_entry_points(lib):
+    """The exact, filtered, adaptive-width and two-range calls, and the weight formats, reject
+    bad arguments before any CUDA call."""
+    null, fake = None, 256
+    # weight format codes: 0 bf16, 1 fp32, 2 4-bit; anything else is invalid
+    assert lib.spec_lmhead_verify(fake, 3, 10, 128, fake, 1, 1, fake, null, fake, fake, 1 << 20,
+                                  null) == 1
+    assert lib.spec_accept_exact(0, 3, fake, fake, fake, fake, 10, 4, fake, 2, fake, fake, fake,
+                                 null, fake, 1 << 20, null) == 1
+    # filtered acceptance needs both filter arrays
+    assert lib.spec_accept_filtered(1, 3, fake, fake, fake, fake, 10, 4, fake, null, fake, 2,
+                                    fake, fake, fake, null, fake, 1 << 20, null) == 1
+    assert lib.spec_accept_filtered(1, 3, fake, fake, fake, fake, 10, 4, fake, fake, null, 2,
+                                    fake, fake, fake, null, fake, 1 << 20, null) == 1
+    # adaptive width: sizes, pointers, and alpha in (0, 1]
+    assert lib.spec_adapt_width(0, 7, fake, fake, fake, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 8, fake, fake, fake, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, null, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, fake, 0.0, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, fake, 1.5, fake, fake, null) == 1
+    # two-range draft set: the second range may not start inside the first, the set may not be
+    # empty; a split set needs tensor-core weights and whole 32-row boxes
+    rows = lib.spec_draft_argmax_rows
+    # d, h, B, temperature, seed, pos, pos_offset, token_out, token_stride, q_logits, q_stride,
+    # q_stats, k_active, workspace, workspace_bytes, stream
+    args = (64, fake, 1, fake, fake, fake, 0, fake, 1, null, 0, null, null, fake, 1 << 20, null)
+    assert rows(fake, 0, 3072, 3000, 256, *args) == 1
+    assert rows(fake, 0, 0, 0, 0, *args) == 1
+    assert rows(fake, 1, 3072, 3840, 256, *args) == 2
+    assert rows(fake, 0, 3000, 3840, 256, *args) == 2
+    assert lib.spec_accept_rows(1, 3, fake, fake, fake, fake, 4096, 4, fake, fake, 3072, 3000,
+                                256, 3328, fake, 2, fake, fake, fake, null, fake, 1 << 20,
+                                null) == 1
+
+
 def test_binding_raises_on_error(lib):
     import mtp_speculative_decoding_spec_gb300 as spec
     with pytest.raises(spec.SpecError) as e:
