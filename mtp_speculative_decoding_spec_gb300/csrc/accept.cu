@@ -250,7 +250,7 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
 
 // The best K keys of verify row `row` of request b over slice sl, descending, written to the
 // workspace (0 past the last entry). Called by one warp: lane l holds entries l + 32 i.
-__device__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, int K) {
+__device__ __forceinline__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, int K) {
   const int lane = threadIdx.x & 31;
   const float* z = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V;
   const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
@@ -263,10 +263,16 @@ __device__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, i
   unsigned long long* out =
       p.cand + ((static_cast<size_t>(b) * p.NS + sl) * kMaxRows + row) * kMaxTopK;
   for (int r = 0; r < K; ++r) {
-    unsigned long long m = key[0];
+    // the lane's largest key by a 5-level tree (a linear scan is a 31-deep dependent chain)
+    unsigned long long t[kAcceptSlice / 64];
 #pragma unroll
-    for (int e = 1; e < kAcceptSlice / 32; ++e) m = key[e] > m ? key[e] : m;
-    const unsigned long long wm = warp_max_u64(m);
+    for (int e = 0; e < kAcceptSlice / 64; ++e)
+      t[e] = key[2 * e] > key[2 * e + 1] ? key[2 * e] : key[2 * e + 1];
+#pragma unroll
+    for (int w = kAcceptSlice / 128; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) t[e] = t[e] > t[e + w] ? t[e] : t[e + w];
+    const unsigned long long wm = warp_max_u64(t[0]);
     if (lane == 0) out[r] = wm;
 #pragma unroll
     for (int e = 0; e < kAcceptSlice / 32; ++e)
@@ -279,7 +285,7 @@ __device__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, i
 // fit in `stage` (dynamic shared memory) they are first copied there in one coalesced pass, so
 // that a round's winner reads its next key from shared memory: read from L2 instead, that load
 // sits on the critical path of every round. Called by every thread.
-__device__ void merge_rows_topk(const AcceptParams& p, int b, int row, int K,
+__device__ __forceinline__ void merge_rows_topk(const AcceptParams& p, int b, int row, int K,
                                 unsigned long long* s_top, unsigned long long* sh,
                                 unsigned long long* stage, int stage_keys) {
   const int tid = threadIdx.x;
