@@ -33,9 +33,10 @@ What it follows (sources are the pages' titles and sections):
 
 Modules: ``philox`` (uniforms), ``lmhead`` (logits and row statistics), ``accept`` (drafting,
 acceptance, residual and bonus sampling, EOS), ``state`` (KV trim, snapshot commit, replay on
-the synthetic recurrent step), ``adapt`` (adaptive width), ``quant`` (4-bit weights). Every function is pinned by a ``-m "not gpu"`` test against
-closed forms, brute force, library routines or published test vectors; the one exception is
-recorded as "parity unpinned" in its docstring.
+the synthetic recurrent step), ``adapt`` (adaptive width), ``quant`` (4-bit weights). Every
+function is pinned by a ``-m "not gpu"`` test against closed forms, brute force, library routines
+or published test vectors; each module's docstring lists its pins. A function without one would
+say "parity unpinned" in its docstring; none does.
 """
 
 from . import philox, lmhead, accept, state, adapt, quant  # noqa: F401
