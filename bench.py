@@ -123,8 +123,10 @@ class ClockSampler:
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
-        except (OSError, FileNotFoundError):
+        except OSError:  # no nvidia-smi: the line carries no clock record
             self.proc = None
+            if getattr(self, "f", None) is not None:
+                self.f.close()
         return self
 
     def __exit__(self, *a):
@@ -141,7 +143,9 @@ class ClockSampler:
             return None
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        for line in lines:
             w = [x.strip() for x in line.split(",")]
             if len(w) < 9:
                 continue
