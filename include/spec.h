@@ -181,9 +181,12 @@ const char *spec_status_str(spec_status s);
  *   logits      [B*R, V] float32 or NULL. Rows of requests with temperature > 0 receive
  *               z = H W^T; rows of greedy requests are left untouched. NULL = statistics only.
  *   stats       [B*R] spec_rowstats of each row at its request's temperature.
- * Each row's logits and statistics are bitwise independent of how many rows share the call
- * (batch invariance). B*R <= 8 runs the streaming GEMV. Returns SPEC_ERR_UNSUPPORTED for
- * larger batches until the batched path is present in this build (spec_batched_supported()).
+ * B*R <= 8 runs the streaming GEMV (any wdt): there each row's logits and statistics are
+ * bitwise independent of how many rows share the call (batch invariance). 9..256 rows run the
+ * batched tensor-core GEMM (bf16 weights, d a multiple of 64, spec_batched_supported() == 1,
+ * workspace sized for max_batch >= B); it accumulates in another order and is not bitwise
+ * equal to the GEMV. Other combinations return SPEC_ERR_UNSUPPORTED.
+ *   workspace   spec_workspace_bytes(V, max_batch) bytes (see the conventions above).
  */
 spec_status spec_lmhead_verify(const void *W, spec_dtype wdt, int64_t V, int64_t d,
                                const void *H, int32_t B, int32_t R, const float *temperature,

@@ -66,9 +66,10 @@ int gemv_grid(int64_t V, int sms) {
 
 int accept_slices(int64_t V) { return static_cast<int>((V + kAcceptSlice - 1) / kAcceptSlice); }
 
-// Workspace layout. Offsets that depend on the batch would let calls with different batches
-// overlap one another's zero-initialised counters, so only the accept tickets depend on B and
-// they sit at the END of the caller's buffer:
+// Workspace layout. The zero-initialised counters sit at offsets that no call's batch moves:
+// the GEMV ticket in the header, the accept tickets at the END of the caller's buffer. The
+// regions between them hold only values written before they are read within one call, so their
+// batch-dependent offsets may overlap from one call to the next:
 //   [0, 256)                    header (GEMV ticket, error word)
 //   [256, part_end)             GEMV per-block partials (grid of the vocabulary size)
 //   [part_end, sums_end)        accept per-slice sums (B * slices * 8 * 8 bytes)
