@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include <cuda.h>
 
 #include "params.cuh"
@@ -22,18 +24,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // cuTensorMapEncodeTiled from the CUDA driver API, fetched through the runtime (no -lcuda).
+EncodeTiledFn lookup_encode_tiled() {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  return nullptr;
+}
+
 EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+  static const EncodeTiledFn fn = lookup_encode_tiled();  // looked up once, by the first caller
   return fn;
 }
 
@@ -42,17 +44,29 @@ struct DevAttr {
   int smem_optin = 0;
 };
 
+// Per-device attributes, queried on first use. Calls may come from several host threads: the
+// cache is atomic (sms is published last, so a non-zero sms implies smem_optin is set).
 DevAttr dev_attr() {
-  static DevAttr cache[64];
+  struct Slot {
+    std::atomic<int> sms{0};
+    std::atomic<int> smem_optin{0};
+  };
+  static Slot cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevAttr{};
-  if (cache[dev].sms == 0) {
-    DevAttr a;
-    cudaDeviceGetAttribute(&a.sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&a.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cache[dev] = a;
+  DevAttr a;
+  a.sms = cache[dev].sms.load(std::memory_order_acquire);
+  if (a.sms != 0) {
+    a.smem_optin = cache[dev].smem_optin.load(std::memory_order_relaxed);
+    return a;
   }
-  return cache[dev];
+  if (cudaDeviceGetAttribute(&a.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&a.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+    return DevAttr{};
+  cache[dev].smem_optin.store(a.smem_optin, std::memory_order_relaxed);
+  cache[dev].sms.store(a.sms, std::memory_order_release);
+  return a;
 }
 
 int64_t gemv_bands(int64_t V) { return (V + kBandRows - 1) / kBandRows; }
@@ -761,15 +775,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 // Device address of g_noalloc_scratch on the current device (nullptr on failure).
 void* noalloc_scratch() {
-  static void* addr[64] = {nullptr};
+  static std::atomic<void*> addr[64];  // zero-initialised (static storage)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+    addr[dev].store(p, std::memory_order_release);
   }
-  return addr[dev];
+  return p;
 }
 
 }  // namespace
