@@ -136,6 +136,33 @@ def test_host_validation_of_the_later_entry_points(lib):
                                 null) == 1
 
 
+def test_empty_inputs_are_rejected(lib):
+    """Zero requests, zero rows, an empty vocabulary or hidden size: SPEC_ERR_INVALID from every
+    entry point, before any CUDA call (nothing is enqueued for an empty batch)."""
+    null, fake = None, 256
+    verify = lib.spec_lmhead_verify
+    for V, d, B, R in ((0, 64, 1, 1), (10, 0, 1, 1), (10, 64, 0, 1), (10, 64, 1, 0),
+                       (-5, 64, 1, 1), (10, 64, -1, 1)):
+        assert verify(fake, 0, V, d, fake, B, R, fake, null, fake, fake, 1 << 20, null) == 1
+        assert lib.spec_lmhead_verify_noalloc(fake, 0, V, d, fake, B, R, fake, null, fake,
+                                              null) == 1
+    for V, d, B in ((0, 64, 1), (10, 0, 1), (10, 64, 0)):
+        assert lib.spec_draft_argmax(fake, 0, V, d, fake, B, fake, fake, fake, 0, fake, 1, null,
+                                     0, null, null, fake, 1 << 20, null) == 1
+    for B, V, R in ((0, 10, 4), (1, 0, 4), (1, 10, 0)):
+        assert lib.spec_accept(B, 3, fake, fake, fake, fake, V, R, null, null, 10, 10, fake, 2,
+                               fake, fake, fake, null, fake, 1 << 20, null) == 1
+        assert lib.spec_accept_exact(B, 3, fake, fake, fake, fake, V, R, fake, 2, fake, fake,
+                                     fake, null, fake, 1 << 20, null) == 1
+        assert lib.spec_accept_filtered(B, 3, fake, fake, fake, fake, V, R, fake, fake, fake, 2,
+                                        fake, fake, fake, null, fake, 1 << 20, null) == 1
+    import mtp_speculative_decoding_spec_gb300 as spec
+    d = spec.spec_state_desc()
+    d.n_slots = 9
+    assert lib.spec_commit_rollback(0, ctypes.byref(d), fake, fake, 0, null, null) == 1
+    assert lib.spec_workspace_bytes(0, 1) == 0 and lib.spec_workspace_bytes(10, 0) == 0
+
+
 def test_binding_raises_on_error(lib):
     import mtp_speculative_decoding_spec_gb300 as spec
     with pytest.raises(spec.SpecError) as e:
