@@ -57,23 +57,6 @@ struct ReduceScatter {
   }
 };
 
-template <bool BF16>
-__device__ __forceinline__ void unpack16(const uint4 w, float* f) {
-  if constexpr (BF16) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f[2 * k] = __uint_as_float(u[k] << 16);
-      f[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
-    }
-  } else {
-    f[0] = __uint_as_float(w.x);
-    f[1] = __uint_as_float(w.y);
-    f[2] = __uint_as_float(w.z);
-    f[3] = __uint_as_float(w.w);
-  }
-}
-
 // 15 consumer warps + 1 producer: 16 warps put 4 on each SM sub-partition (more latency
 // hiding), whose 16K registers then allow up to 128 per thread.
 constexpr int kBandWarps = 15;                     // consumer warps per block
