@@ -422,7 +422,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   L.grid = grid;
   L.threads = kGemvThreads;
   L.smem = static_cast<int>(smem_total);
-  const cudaError_t e = gemv_dispatch(L, wdt == SPEC_BF16, rp, stream);
+  const cudaError_t e = gemv_dispatch(L, rp, stream);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

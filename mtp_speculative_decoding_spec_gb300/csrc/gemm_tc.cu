@@ -371,16 +371,12 @@ __global__ void __launch_bounds__(256) gemm_rows_combine_kernel(const GemmParams
 
 // --------------------------------------------------------------------------- host side
 cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream) {
-  static int configured = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_rows_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
-    if (e != cudaSuccess) return e;
-    configured = 1;
-  }
+  static SmemAllowance allowed;
+  cudaError_t e = allow_dynamic_smem(gemm_rows_tc_kernel, L.smem, allowed);
+  if (e != cudaSuccess) return e;
   int fit = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemm_rows_tc_kernel,
-                                                                kTcThreads, L.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemm_rows_tc_kernel, kTcThreads,
+                                                    L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
   e = launch_pdl(gemm_rows_tc_kernel, dim3(L.grid), dim3(kTcThreads), L.smem, stream, L.hmap, L.wmap,

@@ -74,12 +74,12 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-template <int RP, bool BF16>
+template <int RP>
 __global__ void __maxnreg__(128)
     gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
   pdl_wait();
   if (draft_step_idle(p)) return;
-  constexpr int EPC = BF16 ? 8 : 4;         // elements per 16-byte chunk
+  constexpr int EPC = 4;                    // fp32 elements per 16-byte chunk
   constexpr int PP = EPC / 2;               // element pairs per chunk
   constexpr int RH = RP >= 2 ? RP / 2 : 1;  // H row pairs held per 128-bit load
   constexpr int G = kRowsPerWarp;
@@ -132,13 +132,7 @@ __global__ void __maxnreg__(128)
         const int r = 2 * rr + (u >> 1), kk = k + (u & 1);
         float hv = 0.f;
         if (r < p.nrows && kk < p.d) {
-          if constexpr (BF16) {
-            const uint16_t bits =
-                reinterpret_cast<const uint16_t*>(p.H + static_cast<size_t>(r) * p.h_row_bytes)[kk];
-            hv = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-          } else {
-            hv = reinterpret_cast<const float*>(p.H + static_cast<size_t>(r) * p.h_row_bytes)[kk];
-          }
+          hv = reinterpret_cast<const float*>(p.H + static_cast<size_t>(r) * p.h_row_bytes)[kk];
         }
         h4[u] = hv;
       }
@@ -214,12 +208,7 @@ __global__ void __maxnreg__(128)
         unsigned long long wp[G];  // element pair q of each row: (w[2q], w[2q+1]) as fp32
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          if constexpr (BF16) {
-            const uint32_t u = (q == 0) ? w[g].x : (q == 1) ? w[g].y : (q == 2) ? w[g].z : w[g].w;
-            wp[g] = pack2(u << 16, u & 0xffff0000u);
-          } else {
-            wp[g] = (q == 0) ? pack2(w[g].x, w[g].y) : pack2(w[g].z, w[g].w);
-          }
+          wp[g] = (q == 0) ? pack2(w[g].x, w[g].y) : pack2(w[g].z, w[g].w);
         }
 #pragma unroll
         for (int rr = 0; rr < RH; ++rr) {
@@ -271,30 +260,25 @@ __global__ void __maxnreg__(128)
 // Host side
 // ------------------------------------------------------------------------------------------
 
-template <int RP, bool BF16>
+template <int RP>
 static cudaError_t launch_variant(const GemvLaunch& L, cudaStream_t stream) {
-  auto kern = gemv_rows_kernel<RP, BF16>;
-  static int configured_smem = 0;  // largest dynamic smem size set so far for this variant
-  if (L.smem > configured_smem) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
-    if (e != cudaSuccess) return e;
-    configured_smem = L.smem;
-  }
+  auto kern = gemv_rows_kernel<RP>;
+  static SmemAllowance allowed;  // per variant
+  cudaError_t e = allow_dynamic_smem(kern, L.smem, allowed);
+  if (e != cudaSuccess) return e;
   int fit = 0;  // registers and shared memory must admit one block per SM
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, L.threads, L.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kern, L.threads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
   return launch_pdl(kern, dim3(L.grid), dim3(L.threads), L.smem, stream, L.wmap, L.p);
 }
 
-cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream) {
-  if (bf16) return cudaErrorNotSupported;  // bf16 weights run on the tensor cores (gemv_tc.cu)
+cudaError_t gemv_dispatch(const GemvLaunch& L, int rp, cudaStream_t stream) {
   switch (rp) {
-    case 1: return launch_variant<1, false>(L, stream);
-    case 2: return launch_variant<2, false>(L, stream);
-    case 4: return launch_variant<4, false>(L, stream);
-    default: return launch_variant<8, false>(L, stream);
+    case 1: return launch_variant<1>(L, stream);
+    case 2: return launch_variant<2>(L, stream);
+    case 4: return launch_variant<4>(L, stream);
+    default: return launch_variant<8>(L, stream);
   }
 }
 

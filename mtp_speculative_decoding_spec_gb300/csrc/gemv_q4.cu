@@ -512,16 +512,11 @@ size_t gemv_q4_abuf_bytes() { return static_cast<size_t>(kQABufs) * kQABufBytes;
 size_t gemv_q4_fixed_bytes(int) { return gemv_q4_abuf_bytes() + 2048; }
 
 cudaError_t gemv_q4_launch(const GemvQ4Launch& L, cudaStream_t stream) {
-  static int configured_smem = 0;
-  if (L.smem > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_q4_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
-    if (e != cudaSuccess) return e;
-    configured_smem = L.smem;
-  }
+  static SmemAllowance allowed;
+  cudaError_t e = allow_dynamic_smem(gemv_q4_kernel, L.smem, allowed);
+  if (e != cudaSuccess) return e;
   int fit = 0;
-  cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_q4_kernel, kQThreads, L.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_q4_kernel, kQThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
   return launch_pdl(gemv_q4_kernel, dim3(L.grid), dim3(kQThreads), L.smem, stream, L.cmap, L.smap,

@@ -388,16 +388,11 @@ int gemv_tc_max_block_rows() { return kSkMaxTiles * kSkTileRows; }
 int gemv_tc_stat_bytes() { return kSkStatBytes; }
 
 cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream) {
-  static int configured_smem = 0;
-  if (L.smem > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
-    if (e != cudaSuccess) return e;
-    configured_smem = L.smem;
-  }
+  static SmemAllowance allowed;
+  cudaError_t e = allow_dynamic_smem(gemv_tc_kernel, L.smem, allowed);
+  if (e != cudaSuccess) return e;
   int fit = 0;  // shared memory must admit one block per SM
-  cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_tc_kernel, kSkThreads, L.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_tc_kernel, kSkThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
   return launch_pdl(gemv_tc_kernel, dim3(L.grid), dim3(kSkThreads), L.smem, stream, L.wmap, L.hmap,

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 
+#include <mutex>
 #include <utility>
 
 #include "common.cuh"
@@ -151,6 +152,28 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// A kernel's dynamic shared-memory limit, raised per device (the attribute belongs to the
+// device's copy of the kernel) and only when a launch needs more than has been allowed there.
+// The mutex keeps two threads' first launches from lowering each other's setting.
+struct SmemAllowance {
+  static constexpr int kDevices = 64;
+  std::mutex mu;
+  int bytes[kDevices] = {};
+};
+
+template <typename... KArgs>
+inline cudaError_t allow_dynamic_smem(void (*kernel)(KArgs...), int bytes, SmemAllowance& a) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < SmemAllowance::kDevices;
+  std::lock_guard<std::mutex> lock(a.mu);
+  if (tracked && bytes <= a.bytes[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) a.bytes[dev] = bytes;
+  return e;
+}
+
 cudaError_t gemm_tc_launch(const GemmLaunch& L, cudaStream_t stream);
 int gemm_tc_smem_bytes();
 int gemm_tc_tile_rows();
@@ -158,7 +181,7 @@ int gemm_tc_kblock();
 int gemm_tc_subtiles();
 int gemm_tc_max_ctas();
 
-cudaError_t gemv_dispatch(const GemvLaunch& L, bool bf16, int rp, cudaStream_t stream);
+cudaError_t gemv_dispatch(const GemvLaunch& L, int rp, cudaStream_t stream);
 
 // Tensor-core variant of the 1..8-row projection for bf16 weights: see gemv_tc.cu.
 struct GemvTcLaunch {
