@@ -214,3 +214,55 @@ def test_register_budget_per_sub_partition(lib):
                 assert alloc * 32 * per_sp <= 16384, (name, regs, warps)
                 seen += 1
     assert seen >= 10
+
+
+def _header_prototypes():
+    """(name, return type, [parameter types]) of every function include/spec.h declares."""
+    src = open(os.path.join(ROOT, "include", "spec.h")).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    protos = []
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(spec_\w+)\s*\(([^;{]*?)\)\s*;", src):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        if ret.startswith("typedef"):
+            continue
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        types = [re.sub(r"\s*\b\w+$", "", p) if not p.endswith("*") else p for p in plist]
+        protos.append((name, ret, types))
+    return protos
+
+
+def _ctype_of(ctype):
+    """The ctypes argument kind a C parameter type needs: (size in bytes, pointer, float)."""
+    t = " ".join(ctype.replace("*", " * ").split())
+    if "*" in t:
+        return (ctypes.sizeof(ctypes.c_void_p), True, False)
+    base = t.replace("const ", "")
+    sizes = {"int32_t": 4, "int64_t": 8, "size_t": ctypes.sizeof(ctypes.c_size_t), "float": 4,
+             "spec_dtype": 4, "spec_status": 4}
+    if base == "spec_stream_t":
+        return (ctypes.sizeof(ctypes.c_void_p), True, False)
+    return (sizes[base], False, base == "float")
+
+
+def _kind(ct):
+    is_ptr = ct in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(ct, "_type_") and \
+        isinstance(ct._type_, type)
+    return (ctypes.sizeof(ct), bool(is_ptr), ct is ctypes.c_float)
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every declared function's ctypes argtypes and restype agree with include/spec.h in count,
+    size, pointer-ness and floating point, so the binding passes each argument as C expects."""
+    protos = _header_prototypes()
+    names = {n for n, _, _ in protos}
+    import mtp_speculative_decoding_spec_gb300._abi as abi
+    assert names == set(abi.EXPORTS)
+    for name, ret, params in protos:
+        fn = getattr(lib, name)
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), params)
+        for i, (ct, p) in enumerate(zip(fn.argtypes, params)):
+            assert _kind(ct) == _ctype_of(p), (name, i, p, ct)
+        if ret.endswith("*"):
+            assert fn.restype in (ctypes.c_char_p, ctypes.c_void_p), name
+        else:
+            assert ctypes.sizeof(fn.restype) == _ctype_of(ret)[0], (name, ret, fn.restype)
