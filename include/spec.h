@@ -16,7 +16,8 @@
  * Conventions for every call
  *   - All array arguments are DEVICE pointers unless stated; the caller owns and allocates
  *     every buffer (weights, activations, outputs, state, workspace). The library allocates
- *     no memory and keeps no state beyond cached device attributes.
+ *     no memory and keeps no state beyond cached device attributes (and the fixed scratch
+ *     array that spec_lmhead_verify_noalloc uses in place of a workspace).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Nothing synchronises with the host.
  *   - Host-detectable errors (null required pointer, sizes out of range, misalignment) return
@@ -366,8 +367,8 @@ typedef struct {
  * alpha * (x - rate) (x = 1 accepted, 0 rejected). A depth not yet observed is believed to do
  * as well as the depth above it (0.5 for depth 1), so widths grow while drafts keep being
  * accepted; a depth observed before but not in this cycle relaxes by the same alpha towards
- * the belief of the depth above it, so a depth that looked poor is tried again. A request whose status is not OK keeps its rates. Then, with
- * E(k) = 1 + sum_{j<=k} prod_{i<=j} belief[i] the
+ * the belief of the depth above it, so a depth that looked poor is tried again. A request whose
+ * status is not OK keeps its rates. Then, with E(k) = 1 + sum_{j<=k} prod_{i<=j} belief[i] the
  * expected tokens of a cycle at width k, the next width is the k in [1, k_max] maximising
  * E(k) / cost[k] (the smallest on ties; never 0, so depth 1 stays observed and a request whose
  * drafts start failing can recover), written to k_next[b] and state[b].k.

@@ -50,11 +50,18 @@ def test_struct_layouts_match_the_c_compiler(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     fields = [f[0] for f in spec.spec_state_desc._fields_]
+    # numpy views of the result structs: (C struct, dtype) with the same field names
+    views = [("spec_rowstats", spec.ROWSTATS_DTYPE), ("spec_accept_out", spec.ACCEPT_OUT_DTYPE),
+             ("spec_counters", spec.COUNTERS_DTYPE), ("spec_width_state", spec.WIDTH_STATE_DTYPE)]
     prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec.h"', "int main(void){",
             'printf("%zu %zu %zu %zu\\n", sizeof(spec_rowstats), sizeof(spec_accept_out), '
             "sizeof(spec_counters), sizeof(spec_state_desc));"]
     for f in fields:
         prog.append(f'printf("%zu\\n", offsetof(spec_state_desc, {f}));')
+    for cname, dt in views:
+        prog.append(f'printf("%zu\\n", sizeof({cname}));')
+        for f in dt.names:
+            prog.append(f'printf("%zu\\n", offsetof({cname}, {f}));')
     prog.append("return 0;}")
     src = tmp_path / "layout.c"
     src.write_text("\n".join(prog))
@@ -65,8 +72,14 @@ def test_struct_layouts_match_the_c_compiler(tmp_path):
     sizes = [int(x) for x in out[:4]]
     assert sizes == [spec.ROWSTATS_BYTES, spec.ACCEPT_OUT_BYTES, spec.COUNTERS_BYTES,
                      ctypes.sizeof(spec.spec_state_desc)]
-    offs = [int(x) for x in out[4:]]
+    offs = [int(x) for x in out[4:4 + len(fields)]]
     assert offs == [getattr(spec.spec_state_desc, f).offset for f in fields]
+    rest = [int(x) for x in out[4 + len(fields):]]
+    for cname, dt in views:
+        assert rest[0] == dt.itemsize, cname
+        assert rest[1:1 + len(dt.names)] == [dt.fields[f][1] for f in dt.names], cname
+        rest = rest[1 + len(dt.names):]
+    assert rest == []
 
 
 def test_host_validation_without_gpu(lib):
