@@ -1,0 +1,100 @@
+"""Host logic of SpecVerifyEngine on the CPU: which library calls one cycle enqueues, in which
+order and with which arguments, for each acceptance mode and for adaptive widths. The library
+calls are replaced by a recorder (no kernel runs); buffers live on the CPU."""
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import mtp_speculative_decoding_spec_gb300 as spec  # noqa: E402
+from mtp_speculative_decoding_spec_gb300 import engine as eng_mod  # noqa: E402
+
+V, d, Vd, B, R, K_MAX = 4096, 256, 1024, 2, 4, 3
+
+
+@pytest.fixture
+def calls(monkeypatch):
+    log = []
+
+    def rec(name):
+        def f(*args, **kw):
+            log.append((name, args))
+        return f
+
+    for name in ("spec_draft_argmax", "spec_lmhead_verify", "spec_accept", "spec_accept_exact",
+                 "spec_accept_filtered", "spec_commit_rollback", "spec_adapt_width"):
+        monkeypatch.setattr(eng_mod, name, rec(name))
+    monkeypatch.setattr(eng_mod, "spec_workspace_bytes", lambda V_, B_: 4096)
+    return log
+
+
+def _engine(**kw):
+    W = torch.zeros((V, d), dtype=torch.float32)
+    return eng_mod.SpecVerifyEngine(W, spec.SPEC_F32, V, d, Vd, B, R, K_MAX, eos_id=2,
+                                    device="cpu", **kw)
+
+
+def _names(log):
+    return [n for n, _ in log]
+
+
+def test_ratio_cycle_order_and_draft_slots(calls):
+    e = _engine()
+    H = torch.zeros((B * R, d))
+    Hd = torch.zeros((K_MAX, B, d))
+    e.cycle(H, Hd, 2)
+    assert _names(calls) == ["spec_draft_argmax", "spec_draft_argmax", "spec_lmhead_verify",
+                             "spec_accept"]
+    for i, (_, a) in enumerate(calls[:2], start=1):
+        assert a[9] == i - 1                      # pos_offset: draft i predicts pos + i - 1
+        assert a[6] is e.temps                    # drafts sampled at the requests' temperatures
+        assert a[15] is None                      # fixed widths: no k_active gate
+        assert a[10].data_ptr() == e.drafts[:, i - 1:].data_ptr()   # draft column i - 1
+        assert a[12].data_ptr() == e.q[(i - 1) * B:].data_ptr()     # q rows draft-major
+    acc = calls[3][1]
+    assert acc[8] is e.q and acc[9] is e.qs       # the ratio rule reads the draft logits
+
+
+def test_exact_and_filtered_modes(calls):
+    e = _engine(acceptance="exact")
+    e.verify_cycle(torch.zeros((B * R, d)))
+    assert _names(calls) == ["spec_lmhead_verify", "spec_accept_exact"]
+    calls.clear()
+    f = _engine(acceptance="filtered")
+    f.set_requests(top_k=[20, 5], top_p=[0.95, 0.5])
+    f.draft_step(1, torch.zeros((B, d)))
+    f.verify_cycle(torch.zeros((B * R, d)))
+    assert _names(calls) == ["spec_draft_argmax", "spec_lmhead_verify", "spec_accept_filtered"]
+    assert calls[0][1][6] is f.zero_temps         # argmax drafts: the draft head runs at T = 0
+    a = calls[2][1]
+    assert a[9] is f.top_k and a[10] is f.top_p
+    assert f.top_k.tolist() == [20, 5] and abs(f.top_p[1].item() - 0.5) < 1e-7
+    with pytest.raises(ValueError):
+        _engine(acceptance="other")
+
+
+def test_adaptive_enqueues_every_draft_step_and_the_width_update(calls):
+    e = _engine(adaptive_cost=[1.0, 1.5, 2.0, 2.5])
+    e.cycle(torch.zeros((B * R, d)), torch.zeros((K_MAX, B, d)), 1)
+    names = _names(calls)
+    assert names == ["spec_draft_argmax"] * K_MAX + ["spec_lmhead_verify", "spec_accept",
+                                                      "spec_adapt_width"]
+    for _, a in calls[:K_MAX]:
+        assert a[15] is e.k                       # steps past a request's width return at once
+    ad = calls[-1][1]
+    assert ad[3] is e.k and ad[7] is e.k          # widths read and written in place
+    with pytest.raises(ValueError):
+        _engine(adaptive_cost=[1.0, 2.0])         # needs k_max + 1 entries
+
+
+def test_commit_only_with_attached_state(calls):
+    e = _engine()
+    e.verify_cycle(torch.zeros((B * R, d)))
+    assert "spec_commit_rollback" not in _names(calls)
+    calls.clear()
+    desc = spec.spec_state_desc()
+    e.attach_state(desc, spec.SPEC_COMMIT_REPLAY)
+    e.verify_cycle(torch.zeros((B * R, d)))
+    assert _names(calls)[-1] == "spec_commit_rollback"
+    a = calls[-1][1]
+    assert a[1] is desc and a[2] is e.out and a[4] == spec.SPEC_COMMIT_REPLAY
