@@ -33,7 +33,11 @@
  *   - Limits: 1..8 verify rows per request (k = 0..7 drafts), at most 8 rows in total per
  *     spec_lmhead_verify / spec_draft_argmax call on the GEMV path; hidden size d with
  *     d * element_size a multiple of 16 bytes and d <= 3072 (bf16) / 1536 (fp32), or d a
- *     multiple of 128 up to 4096 (SPEC_Q4A32); V < 2^24.
+ *     multiple of 128 up to 4096 (SPEC_Q4A32); V < 2^24. The GEMV path's last block combines
+ *     every block's partials in shared memory, which bounds V at about 2.4 million rows for
+ *     bf16 and fp32 weights; SPEC_Q4A32 keeps at most 1,024 rows per block, so V <= 1,024 x
+ *     the device's SM count (155,648 on a 152-SM GB300). Beyond these the calls return
+ *     SPEC_ERR_UNSUPPORTED.
  */
 #ifndef SPEC_H
 #define SPEC_H
