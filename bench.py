@@ -7,11 +7,16 @@ GEMV over the k+1 rows plus acceptance -- on device-resident inputs (drafts prod
 draft head before the timed region). Printed as one JSON line (rank 0):
 
   value        verify cycles/s over all ranks (replicas: every rank runs the same workload)
-  roofline     the verify GEMV: algorithmic bytes per launch / its mean CUDA-event duration,
-               against the measured HBM copy bandwidth
+  roofline     the verify GEMV alone: algorithmic bytes per launch / its mean CUDA-event
+               duration over 3,000 event-bracketed launches (its own loop after the timed steps,
+               with the SM clock sampled over it), against the measured HBM copy bandwidth;
+               step_frac = the same bytes per timed step / the step time
   full_cycle   k draft-head steps + verify + acceptance: cycles/s and emitted tokens/s
-  sweep        k = 1..7 at temperature 0 and 1 (verify rows k+1)
+  sweep        k = 1..7 at temperature 0, and at temperature 1 on the sampled workload's recipe
+               (Philox seeds 0..99, EOS injected in 5% of cycles), 512 distinct cycles a point
   commit       snapshot commit and replay of the 64K-context state
+  c3_cycle     the adaptive-rollback workload's verify cycle (k ~ U{1..7}: verify k+1 rows,
+               acceptance, commit of the 64K-context state) timed end to end
   e2e          the same verify cycle through SpecVerifyEngine with host buffers (pinned H2D of the
                step's hidden rows and drafts, D2H of the 64-byte result) inside the timed region
   cpu_baseline the float64 oracle on the host cores, on a bounded sample
@@ -37,11 +42,47 @@ if ROOT not in sys.path:
 from synth import configs, gen  # noqa: E402
 
 METRIC = "verify cycles/s & emitted tok/s at k=1..7; LM-head HBM GB/s vs 8 TB/s"
-# DRAM traffic (bytes read + written) of one 2-row verify launch of gemv_tc_kernel on the
-# headline workload, from the ncu capture summarised in
-# profiles/gemv_tc_kernel_verify_V151936_d2560.md (778,027,776 read + 3,983,360 written).
-# Set back to None whenever the kernel changes until it is captured again.
-GEMV_TRAFFIC_BYTES = 782011136
+# sources of the verify kernel: an ncu traffic figure holds only for the source it was taken on
+GEMV_TC_SOURCES = ("gemv_tc.cu", "gemv_epilogue.cuh", "tcgen05.cuh", "common.cuh", "params.cuh")
+
+
+def source_digest(names):
+    """First 16 hex digits of the SHA-256 of the named kernel sources, concatenated."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mtp_speculative_decoding_spec_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary, section, sources):
+    """DRAM bytes (read + written) of one launch from an ncu summary under profiles/: the
+    ``- DRAM read:`` and ``- DRAM write:`` lines (Mbyte) of the first section whose heading
+    contains ``section``, used only when the summary's ``source sha256:`` line names the
+    current kernel sources. Returns (bytes or None, note)."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None, "no ncu summary"
+    text = open(path).read()
+    digest = source_digest(sources)
+    if f"source sha256: {digest}" not in text:
+        return None, "kernel source changed since the ncu capture"
+    part = text.split(section, 1)
+    if len(part) < 2:
+        return None, "section not in the ncu summary"
+    vals = {}
+    for line in part[1].splitlines():
+        for key in ("DRAM read", "DRAM write"):
+            if line.startswith(f"- {key}:") and key not in vals:
+                x, unit = line.split(":", 1)[1].split()[:2]
+                vals[key] = float(x) * {"Mbyte": 1e6, "Kbyte": 1e3, "Gbyte": 1e9,
+                                        "byte": 1.0}[unit]
+        if len(vals) == 2:
+            break
+    if len(vals) < 2:
+        return None, "DRAM lines missing"
+    return int(round(vals["DRAM read"] + vals["DRAM write"])), f"ncu, source {digest}"
 
 
 def parse():
@@ -108,11 +149,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index, csv_dir=None):
+    def __init__(self, gpu_index, csv_dir=None, tag=""):
         import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(csv_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(csv_dir or tempfile.gettempdir(),
+                                 f"clocks{tag}_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -233,12 +275,6 @@ def run_ours(args, rank, local_rank, world):
         step(c % n_pool)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    # Events bracket one verify launch in every EV_EVERY steps: the kernel's launch duration for
-    # the roofline. Events between kernels stop the next kernel from starting early (the
-    # programmatic overlap), so the other steps run without them.
-    EV_EVERY = 10
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range((K + EV_EVERY - 1) // EV_EVERY)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank, args.clocks_dir)
@@ -247,27 +283,20 @@ def run_ours(args, rank, local_rank, world):
     with clocks:
         t_start.record(stream)
         for c in range(K):
-            if c % EV_EVERY == 0:
-                ev[c // EV_EVERY][0].record(stream)
-            eng.verify(Hp_d[c % n_pool])
-            if c % EV_EVERY == 0:
-                ev[c // EV_EVERY][1].record(stream)
-            spec.spec_accept(1, k, eng.k, drafts_pool[c % n_pool], eng.logits, eng.stats, cfg.V,
-                             k + 1, None, None, cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id,
-                             eng.seeds, eng.pos, eng.out, eng.counters, eng.ws)
+            step(c % n_pool)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     elapsed = t_start.elapsed_time(t_end) / 1e3
-    gemv_ms = [a.elapsed_time(b) for a, b in ev]
-    gemv_mean_s = statistics.mean(gemv_ms) / 1e3
     err = int(eng.ws[4:8].cpu().numpy().view(np.uint32)[0])
     cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
     elapsed_max = max_over_ranks(elapsed)
     value = whole_job_value(K, elapsed_max, world)
     algo_bytes = cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16
-    achieved = algo_bytes / gemv_mean_s / 1e9
+    roof = verify_launch_roofline(eng, Hp_d, n_pool, algo_bytes, hbm_peak, peak_src, local_rank,
+                                  args.clocks_dir, 8 if args.profile else 3000)
+    roof["step_frac"] = round(algo_bytes / (elapsed_max / K) / 1e9 / hbm_peak, 4)
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "verify cycles/s",
@@ -276,13 +305,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"parallelism": f"replicas x{world}",
                                         "step": "verify GEMV (2 rows) + acceptance"}),
-        "roofline": {"bound": "hbm", "kernel": "gemv_tc_kernel (verify, 2 rows)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": algo_bytes,
-                     "mean_launch_us": round(gemv_mean_s * 1e6, 2),
-                     "launches_timed": len(ev),
-                     "traffic": GEMV_TRAFFIC_BYTES},
+        "roofline": roof,
         "acceptance": round(float(cnt["accepted"]) / max(1.0, float(cnt["drafted"])), 4),
         "gpu_launches": 2 * K,
         "workspace_error": err,
@@ -302,6 +325,7 @@ def run_ours(args, rank, local_rank, world):
             draft_us = max(1.0, 1e6 / res["full_cycle"]["cycles_s"] - step_us)
             res["adaptive"] = adaptive_bench(dev, W, Wd, step_us, draft_us)
             res["commit"] = commit_bench(dev, hbm_peak)
+            res["c3_cycle"] = c3_cycle(dev, W, Wd, hbm_peak)
             res["q4"] = q4_bench(dev, W, hbm_peak)
             res["batched"] = batched_bench(dev, W, Wd, hbm_peak, tf_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
@@ -313,6 +337,41 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def verify_launch_roofline(eng, Hp_d, n_pool, algo_bytes, hbm_peak, peak_src, gpu, clocks_dir,
+                           n):
+    """The verify kernel alone: n launches, each bracketed by CUDA events on the launch stream
+    (events between kernels stop the programmatic overlap, so each launch runs by itself),
+    after 100 warm-up launches, with the SM clock sampled over the loop. The step loop's own
+    figure (algorithmic bytes per step / time per step) is reported beside it as step_frac."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    with ClockSampler(gpu, clocks_dir, tag="roofline") as ck:
+        for c in range(100):
+            eng.verify(Hp_d[c % n_pool])
+        for c in range(n):
+            ev[c][0].record(stream)
+            eng.verify(Hp_d[c % n_pool])
+            ev[c][1].record(stream)
+        torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    mean_s = statistics.mean(us) / 1e6
+    achieved = algo_bytes / mean_s / 1e9
+    traffic, note = profiled_traffic("gemv_tc_kernel_verify_V151936_d2560.md", "## 2-row verify",
+                                     GEMV_TC_SOURCES)
+    cs = ck.summary()
+    return {"bound": "hbm", "kernel": "gemv_tc_kernel (verify, 2 rows)",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": algo_bytes,
+            "mean_launch_us": round(mean_s * 1e6, 2),
+            "median_launch_us": round(statistics.median(us), 2),
+            "launches_timed": n, "traffic": traffic, "traffic_source": note,
+            "sm_mhz": None if cs is None else cs["sm_mhz"],
+            "clock_samples": None if cs is None else cs["samples"]}
 
 
 def profile_extras(dev, W, Wd):
@@ -395,70 +454,109 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
             "steps": K, "api": "SpecVerifyEngine.verify + spec_accept, pinned host buffers"}
 
 
+def recipe_inputs(cfg, W, n_pool, k, T, rng_seed):
+    """Pool of cycle inputs on the recipe of the workload ``cfg``: verify rows [n, k+1, d] and
+    draft rows [n, k, d] (bf16 bits). At T > 0 the EOS id is injected at a random proposal
+    position in cfg.eos_inject of the cycles (the verify row that checks that proposal, and the
+    draft row derived from it, are planted on EOS). Also returns how many cycles carry EOS."""
+    H = np.empty((n_pool, k + 1, cfg.d), dtype=np.uint16)
+    Hd = np.empty((n_pool, max(k, 1), cfg.d), dtype=np.uint16)
+    n_eos = 0
+    for c in range(n_pool):
+        e = gen.eos_injection(cfg, c, k, seed=rng_seed) if T > 0 else 0
+        n_eos += e > 0
+        inp = gen.cycle_inputs(cfg, W, c, seed=rng_seed, k=k, eos_at=e)
+        H[c] = inp["H"]
+        if k:
+            Hd[c, :k] = inp["Hd"]
+    return H, Hd, n_eos
+
+
+def acceptance_rates(cnt, k):
+    """accepted / drafted, and accepted / ratio tests: every draft tested is accepted or ends
+    the chain, and a chain that did not reach depth k ended at a failed test unless it ended on
+    an accepted EOS (cycles that ended on EOS are counted as having no failed test)."""
+    acc, drafted = float(cnt["accepted"]), float(cnt["drafted"])
+    fails = float(cnt["cycles"]) - float(cnt["depth"][k]) - float(cnt["eos"])
+    return (round(acc / max(1.0, drafted), 4), round(acc / max(1.0, acc + max(0.0, fails)), 4))
+
+
 def sweep(dev, W, Wd, hbm_peak):
-    """k = 1..7 at temperature 0 (greedy) and 1 (ratio rule with q rows); exact-match
-    acceptance, and acceptance against the top-k 20 / top-p 0.95 filtered target (argmax
-    drafts), at temperature 1 for k = 1, 3, 7."""
+    """k = 1..7 at temperature 0 (greedy) and at temperature 1 on the sampled workload's recipe
+    (ratio rule with the draft head's q rows, Philox seeds 0..99 cycling over the cycles, EOS
+    injected in 5% of the cycles); exact-match acceptance, and acceptance against the top-k 20 /
+    top-p 0.95 filtered target (argmax drafts), at temperature 1 for k = 1, 3, 7. Each point
+    runs 512 distinct cycles, twice: once with events around each verify and acceptance (launch
+    durations), once without (the full-cycle rate: k draft steps + verify + acceptance)."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
     from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
     out = {}
     base = configs.get(2)
-    n_pool, K = 32, 200
+    n_pool = K = 512
     points = [(T, k, "ratio") for T in (0.0, 1.0) for k in range(1, 8)]
     points += [(1.0, k, mode) for mode in ("exact", "filtered") for k in (1, 3, 7)]
+    seeds_pool = torch.arange(100, dtype=torch.int64, device=dev)
+    pos_pool = torch.arange(n_pool, dtype=torch.int64, device=dev) * 16
     for T, k, mode in points:
         cfg = configs.Config(**{**base.__dict__, "k": k, "temps": (T,)})
-        Hp, Hdp = build_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
+        Hp, Hdp, n_eos = recipe_inputs(cfg, W, n_pool, k, T, rng_seed=7 * k + int(T))
         Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
         Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
         eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
                                cfg.eos_id, device=dev, want_q_logits=True,
                                acceptance=mode)
-        eng.set_requests(temps=[T], seeds=[k], pos=[0], k=[k], top_k=[20], top_p=[0.95])
+        eng.set_requests(temps=[T], seeds=[0], pos=[0], k=[k], top_k=[20], top_p=[0.95])
+
+        def cycle(c, events=None):
+            cc = c % n_pool
+            eng.seeds = seeds_pool[c % 100:c % 100 + 1]  # this cycle's Philox seed and position
+            eng.pos = pos_pool[cc:cc + 1]
+            for i in range(1, k + 1):
+                eng.draft_step(i, Hdp_d[cc, i - 1:i])
+            if events:
+                events[0].record()
+            eng.verify(Hp_d[cc])
+            if events:
+                events[1].record()
+            eng.accept()
+            if events:
+                events[2].record()
+
         for c in range(5):
-            eng.cycle(Hp_d[c], Hdp_d[c, :, None, :], k)
+            cycle(c)
         torch.cuda.synchronize()
         eng.counters.zero_()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        # pass 1: events around each verify and acceptance (launch durations)
-        for c in range(K):
-            cc = c % n_pool
-            for i in range(1, k + 1):
-                eng.draft_step(i, Hdp_d[cc, i - 1:i])
-            ev[c][0].record()
-            eng.verify(Hp_d[cc])
-            ev[c][1].record()
-            eng.accept()
-            ev[c][2].record()
+        for c in range(K):  # pass 1: launch durations
+            cycle(c, ev[c])
         torch.cuda.synchronize()
         eng.counters.zero_()
-        # pass 2: the same cycles with no events between kernels (full-cycle rate)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for c in range(K):
-            cc = c % n_pool
-            for i in range(1, k + 1):
-                eng.draft_step(i, Hdp_d[cc, i - 1:i])
-            eng.verify(Hp_d[cc])
-            eng.accept()
+        for c in range(K):  # pass 2: the full-cycle rate
+            cycle(c)
         b.record()
         torch.cuda.synchronize()
         s = a.elapsed_time(b) / 1e3
         verify_s = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
         gemv_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
         cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
-        gbs = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 +
-               (k + 1) * cfg.V * 4 * (T > 0)) / gemv_s / 1e9
+        va_bytes = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16 +
+                    (k + 1) * cfg.V * 4 * (T > 0))
+        gbs = va_bytes / gemv_s / 1e9
         accept_us = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
+        per_drafted, per_test = acceptance_rates(cnt, k)
         out[f"T{T:g}_k{k}" + ("" if mode == "ratio" else f"_{mode}")] = {
             "verify_cycles_s": round(K / verify_s, 1),
+            "verify_accept_frac": round(va_bytes / (verify_s / K) / 1e9 / hbm_peak, 4),
             "full_cycles_s": round(K / s, 1),
             "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
             "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
-            "acceptance": round(float(cnt["accepted"]) / max(1, float(cnt["drafted"])), 3),
+            "acceptance": per_drafted, "acceptance_per_test": per_test,
+            "eos_cycles": int(n_eos), "cycles": K,
             "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4),
             "accept_us": round(accept_us, 2)}
         del eng, Hp_d, Hdp_d
@@ -526,6 +624,97 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=400):
         fixed[f"k{k}"] = round(float(cnt["emitted"]) / s, 1)
         del eng
     res["fixed_emitted_tok_s"] = fixed
+    return res
+
+
+def c3_cycle(dev, W, Wd, hbm_peak, K=400):
+    """The adaptive-rollback workload's verify cycle, timed end to end: per cycle k ~ U{1..7}
+    (the workload's own draws), the verify LM head over its k+1 rows, greedy acceptance and the
+    snapshot commit of the 64K-context state (one full-attention KV layer of 4 x 256 bf16 at
+    65,536 positions, 36 recurrent layers of [16,128,128] fp32 and [3,8192] conv rows) driven
+    on the device by the acceptance. Drafts come from the draft head before the timed region
+    (a second timing adds the k draft steps: the full cycle). P starts at 63,488 and grows by
+    the kept rows."""
+    import torch
+
+    import mtp_speculative_decoding_spec_gb300 as spec
+    cfg = configs.get(3)
+    n_pool, ns = 256, 9
+    L, Hh, dk, dv = cfg.rec_layers, cfg.rec_heads, cfg.rec_dk, cfg.rec_dv
+    ks, Hs, Hds = [], [], []
+    for c in range(n_pool):
+        inp = gen.cycle_inputs(cfg, W, c, seed=33)
+        ks.append(inp["k"])
+        H = np.zeros((8, cfg.d), dtype=np.uint16)
+        H[:inp["k"] + 1] = inp["H"]
+        Hd = np.zeros((7, cfg.d), dtype=np.uint16)
+        Hd[:inp["k"]] = inp["Hd"]
+        Hs.append(H)
+        Hds.append(Hd)
+    Hp_d = torch.from_numpy(np.stack(Hs).view(np.int16)).to(dev)
+    Hdp_d = torch.from_numpy(np.stack(Hds).view(np.int16)).to(dev)
+    k_pool = torch.tensor(ks, dtype=torch.int32, device=dev)
+    st = BatchedState(cfg, 1, dev)
+    ws = torch.zeros(spec.spec_workspace_bytes(cfg.V, 1), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(8 * spec.ROWSTATS_BYTES, dtype=torch.uint8, device=dev)
+    qs = torch.zeros(7 * spec.ROWSTATS_BYTES, dtype=torch.uint8, device=dev)
+    temps = torch.zeros(1, dtype=torch.float32, device=dev)
+    seeds = torch.zeros(1, dtype=torch.int64, device=dev)
+    pos = torch.zeros(1, dtype=torch.int64, device=dev)
+    drafts_pool = torch.zeros((n_pool, 7), dtype=torch.int32, device=dev)
+    out = torch.zeros(spec.ACCEPT_OUT_BYTES, dtype=torch.uint8, device=dev)
+    cnt = torch.zeros(spec.COUNTERS_BYTES, dtype=torch.uint8, device=dev)
+
+    def drafts_of(c):
+        for i in range(1, ks[c] + 1):
+            spec.spec_draft_argmax(Wd, spec.SPEC_BF16, cfg.Vd, cfg.d, Hdp_d[c, i - 1:i], 1, temps,
+                                   seeds, pos, i - 1, drafts_pool[c, i - 1:], 7, None, cfg.Vd,
+                                   qs[(i - 1) * spec.ROWSTATS_BYTES:], None, ws)
+
+    def verify_cycle(c):
+        k = ks[c]
+        spec.spec_lmhead_verify(Wd, spec.SPEC_BF16, cfg.V, cfg.d, Hp_d[c], 1, k + 1, temps, None,
+                                stats, ws)
+        spec.spec_accept(1, 7, k_pool[c:c + 1], drafts_pool[c:c + 1], None, stats, cfg.V, k + 1,
+                         None, None, cfg.Vd, cfg.Vd, temps, cfg.eos_id, seeds, pos, out, cnt, ws)
+        spec.spec_commit_rollback(1, st.desc, out, k_pool[c:c + 1], spec.SPEC_COMMIT_SNAPSHOT)
+
+    for c in range(n_pool):
+        drafts_of(c)
+    res = {}
+    for name, with_drafts in (("verify_cycle", False), ("full_cycle", True)):
+        st.kv_len.fill_(cfg.context)
+        for c in range(5):
+            verify_cycle(c)
+        st.kv_len.fill_(cfg.context)
+        cnt.zero_()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for c in range(K):
+            if with_drafts:
+                drafts_of(c % n_pool)
+            verify_cycle(c % n_pool)
+        b.record()
+        torch.cuda.synchronize()
+        s_ = a.elapsed_time(b) / 1e3
+        cn = cnt.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+        rows = sum(ks[c % n_pool] + 1 for c in range(K))
+        emitted = float(cn["emitted"])
+        commit_bytes = 2 * 4 * (st.rec_elems + st.conv_elems)
+        zero_fill = (rows - emitted) * 2 * cfg.kv_layers * cfg.kv_row_bytes
+        cyc_bytes = (K * (cfg.V * cfg.d * 2 + commit_bytes) + rows * (cfg.d * 2 + 16) +
+                     zero_fill) / K
+        res[name] = {"cycles_s": round(K / s_, 1), "emitted_tok_s": round(emitted / s_, 1),
+                     "tokens_per_cycle": round(emitted / K, 3), "mean_k": round(rows / K - 1, 3)}
+        if not with_drafts:
+            res[name].update({"algorithmic_bytes_per_cycle": int(cyc_bytes),
+                              "hbm_gbs": round(cyc_bytes * K / s_ / 1e9, 1),
+                              "hbm_frac": round(cyc_bytes * K / s_ / 1e9 / hbm_peak, 4)})
+    res["final_len"] = int(st.kv_len.cpu()[0])
+    res["workload"] = ("k ~ U{1..7}, verify k+1 rows + greedy acceptance + snapshot commit of the "
+                       "64K-context state, P from 63,488")
+    del st
     return res
 
 

@@ -436,6 +436,33 @@ spec_status spec_lmhead_verify_noalloc(const void *W, spec_dtype wdt, int64_t V,
 /* Size of the fixed scratch array used by spec_lmhead_verify_noalloc. */
 size_t spec_noalloc_scratch_bytes(void);
 
+/*
+ * spec_noalloc_error_word -- the error word of spec_lmhead_verify_noalloc's fixed scratch
+ * array: the bits its kernels set if an internal bounded wait gave up (0 = no error; the same
+ * bits as byte offset 4 of a caller's workspace). Enqueues on `stream` a 4-byte copy of the word
+ * into *error_out, which may be device or host memory (pinned host memory keeps the copy
+ * asynchronous). Each spec_lmhead_verify_noalloc call clears the word when it starts, so read
+ * it after the call and before the next one on the same device; a call whose word is non-zero
+ * returned SPEC_OK but its statistics and logits are not to be used. Allocates nothing.
+ */
+spec_status spec_noalloc_error_word(uint32_t *error_out, spec_stream_t stream);
+
+/*
+ * spec_test_verify_stalled -- failure-detection test of the bounded waits (no counterpart on
+ * the pages; not part of the method). Runs the fp32 verify LM head (the CUDA-core kernel, which
+ * holds no tensor memory) with its producer warp issuing no copy at all, so every consumer's
+ * wait for the first stage runs out after wait_limit_us microseconds (1..1,000,000). Each block
+ * then sets bit 0 of the workspace error word, skips the rest of its stream and finishes;
+ * nothing is in flight when the kernel exits, the workspace counters are back at zero and the
+ * statistics written are meaningless. Arguments as spec_lmhead_verify with wdt = SPEC_F32 and
+ * at most 8 rows in total; the call itself returns SPEC_OK.
+ */
+spec_status spec_test_verify_stalled(const void *W, int64_t V, int64_t d, const void *H,
+                                     int32_t B, int32_t R, const float *temperature,
+                                     float *logits, spec_rowstats *stats, uint32_t wait_limit_us,
+                                     void *workspace, size_t workspace_bytes,
+                                     spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

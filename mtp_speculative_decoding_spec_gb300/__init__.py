@@ -143,3 +143,19 @@ def spec_lmhead_verify_noalloc(W, wdt, V, d, H, B, R, temperature, logits, stats
 
 def spec_noalloc_scratch_bytes():
     return int(_abi.lib().spec_noalloc_scratch_bytes())
+
+
+def spec_noalloc_error_word(error_out, stream=None):
+    """Enqueue a copy of spec_lmhead_verify_noalloc's error word into ``error_out`` (a 4-byte
+    device or pinned host tensor)."""
+    _check("spec_noalloc_error_word", _abi.lib().spec_noalloc_error_word(
+        _ptr(error_out), _stream(stream)))
+
+
+def spec_test_verify_stalled(W, V, d, H, B, R, temperature, logits, stats, wait_limit_us,
+                             workspace, stream=None):
+    """Failure-detection test of the bounded waits: the fp32 verify with a producer that
+    issues nothing (see include/spec.h)."""
+    _check("spec_test_verify_stalled", _abi.lib().spec_test_verify_stalled(
+        _ptr(W), V, d, _ptr(H), B, R, _ptr(temperature), _ptr(logits), _ptr(stats),
+        int(wait_limit_us), _ptr(workspace), _nbytes(workspace), _stream(stream)))

@@ -21,7 +21,8 @@ EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spe
            "spec_draft_argmax_rows", "spec_accept_rows",
            "spec_commit_rollback",
            "spec_batched_supported",
-           "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes")
+           "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes",
+           "spec_noalloc_error_word", "spec_test_verify_stalled")
 
 # numpy views of the device structs (for reading results copied to the host)
 ROWSTATS_DTYPE = np.dtype([("max", "<f4"), ("log_norm", "<f4"), ("gap", "<f4"),
@@ -113,5 +114,10 @@ def lib():
         L.spec_lmhead_verify_noalloc.restype = i32
         L.spec_noalloc_scratch_bytes.argtypes = []
         L.spec_noalloc_scratch_bytes.restype = sz
+        L.spec_noalloc_error_word.argtypes = [vp, vp]
+        L.spec_noalloc_error_word.restype = i32
+        L.spec_test_verify_stalled.argtypes = [vp, i64, i64, vp, i32, i32, vp, vp, vp,
+                                               ctypes.c_uint32, vp, sz, vp]
+        L.spec_test_verify_stalled.restype = i32
         _lib = L
     return _lib

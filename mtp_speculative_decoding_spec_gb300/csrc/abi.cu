@@ -316,7 +316,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
                      const uint64_t* seed, const int64_t* pos, int pos_offset,
                      int32_t* token_out, int token_stride, const int32_t* kact, void* workspace,
                      size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream,
-                     int64_t lo_rows = -1, int64_t hi_row0 = -1) {
+                     int64_t lo_rows = -1, int64_t hi_row0 = -1, uint64_t ring_wait_ns = 0,
+                     int stall = 0) {
   // rows [0, V) are weight rows [0, V), or [0, lo_rows) then hi_row0.. (a two-range draft set)
   if (lo_rows < 0 || lo_rows >= V) {
     lo_rows = V;
@@ -419,6 +420,8 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.hi_row0 = V;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  p.ring_wait_ns = ring_wait_ns;
+  p.stall = stall;
   L.grid = grid;
   L.threads = kGemvThreads;
   L.smem = static_cast<int>(smem_total);
@@ -703,6 +706,23 @@ spec_status spec_accept_filtered(int32_t B, int32_t k_max, const int32_t* k,
                           workspace_bytes, stream, 0, top_k, top_p);
 }
 
+spec_status spec_test_verify_stalled(const void* W, int64_t V, int64_t d, const void* H,
+                                     int32_t B, int32_t R, const float* temperature,
+                                     float* logits, spec_rowstats* stats, uint32_t wait_limit_us,
+                                     void* workspace, size_t workspace_bytes,
+                                     spec_stream_t stream) {
+  if (!W || !H || !temperature || !stats || !workspace) return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows ||
+      static_cast<int64_t>(B) * R > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (wait_limit_us < 1 || wait_limit_us > 1000000) return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(H) || !aligned16(workspace)) return SPEC_ERR_INVALID;
+  return run_gemv(W, SPEC_F32, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
+                  nullptr, 0, nullptr, 0, nullptr, workspace, workspace_bytes, B,
+                  reinterpret_cast<cudaStream_t>(stream), -1, -1,
+                  static_cast<uint64_t>(wait_limit_us) * 1000ull, 1);
+}
+
 spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
                                  const spec_accept_out* acc, const int32_t* k, int32_t mode,
                                  int32_t* commit_status, spec_stream_t stream) {
@@ -790,6 +810,17 @@ void* noalloc_scratch() {
 }  // namespace spec
 
 extern "C" size_t spec_noalloc_scratch_bytes(void) { return spec::kNoAllocScratchBytes; }
+
+extern "C" spec_status spec_noalloc_error_word(uint32_t* error_out, spec_stream_t stream) {
+  if (!error_out) return SPEC_ERR_INVALID;
+  void* scratch = spec::noalloc_scratch();
+  if (!scratch) return SPEC_ERR_CUDA;
+  // the error word sits at byte offset 4 of the scratch, as in a caller's workspace
+  const cudaError_t e = cudaMemcpyAsync(error_out, static_cast<uint8_t*>(scratch) + 4,
+                                        sizeof(uint32_t), cudaMemcpyDefault,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 extern "C" spec_status spec_lmhead_verify_noalloc(const void* W, spec_dtype wdt, int64_t V,
                                                   int64_t d, const void* H, int32_t B, int32_t R,

@@ -148,7 +148,7 @@ __global__ void __maxnreg__(128)
       const int y0 = static_cast<int>(v0);
       int s = 0, band = 0, slab = 0;
       uint32_t eph = 0;  // parity of the empty-barrier phase to wait for (second lap onwards)
-      for (int it = 0; it < niter; ++it) {
+      for (int it = 0; it < (p.stall ? 0 : niter); ++it) {
         if (it >= S && !mbar_wait_bounded(&empty[s], eph)) {
           atomicOr(&p.hdr->error, ERR_GEMV_WAIT_EMPTY);
           atomicExch(&flags[0], 1);
@@ -180,6 +180,7 @@ __global__ void __maxnreg__(128)
     const int wrow = warp * G;  // first row of this warp within a band
     // acc[g][r]: packed (even-element, odd-element) partial sums of row g against H row r
     unsigned long long acc[G][RP];
+    const uint64_t ring_wait = p.ring_wait_ns ? p.ring_wait_ns : 2000000000ull;
     int s = 0, band = 0, slab = 0;
     uint32_t ph = 0;
     for (int it = 0; it < niter; ++it) {
@@ -189,7 +190,7 @@ __global__ void __maxnreg__(128)
 #pragma unroll
           for (int r = 0; r < RP; ++r) acc[g][r] = 0ull;
       }
-      if (!mbar_wait_bounded(&full[s], ph)) {
+      if (!mbar_wait_bounded(&full[s], ph, ring_wait)) {
         atomicOr(&p.hdr->error, ERR_GEMV_WAIT_FULL);
         atomicExch(&flags[0], 1);
         break;

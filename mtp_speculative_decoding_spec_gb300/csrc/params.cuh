@@ -42,6 +42,10 @@ struct GemvParams {
   int64_t lo_rows, hi_row0;
   WsHeader* hdr;
   GemvPartial* part;
+  // failure-detection test of the bounded waits (CUDA-core kernel only): when stall is set the
+  // producer issues no copy, and the consumers' waits for a stage give up after ring_wait_ns
+  uint64_t ring_wait_ns;  // 0: the default limit
+  int stall;
 };
 
 // Shared memory the last block's combine needs: per row, for each block, its integer sum (8

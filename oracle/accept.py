@@ -132,11 +132,12 @@ def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7, rows=
              column r is vocabulary id rows[r] (r without ``rows``), q is 0 elsewhere.
     drafts:  ints, drafts[i-1] = d_i.
     uniform: callable (pos, purpose) -> u in [0, 1) (the request's seeded Philox stream).
-    Returns dict(status, n_accept, tokens, n_emit, eos_hit, sample_kind, sample_row, margins)
-    with sample_kind 0 none, 1 residual, 2 bonus draw.
+    Returns dict(status, n_accept, tokens, n_emit, eos_hit, sample_kind, sample_row, margins,
+    ratio_terms) with sample_kind 0 none, 1 residual, 2 bonus draw; ratio_terms lists, per
+    ratio test in order, the two sides (u * q(d_i), p(d_i)) that were compared.
     """
     res = dict(status=STATUS_OK, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
-               sample_kind=0, sample_row=-1, margins=[])
+               sample_kind=0, sample_row=-1, margins=[], ratio_terms=[])
 
     def fail(code):
         res.update(status=code, n_accept=0, tokens=[], n_emit=0, eos_hit=False,
@@ -199,6 +200,7 @@ def accept_request(z, y, drafts, k, T, eos_id, uniform, pos_base, k_max=7, rows=
             px, qx = float(p[x]), float(q[x])
             u = uniform(pos_base + i - 1, PURPOSE_ACCEPT)
             margins.append(("ratio", abs(u * qx - px)))
+            res["ratio_terms"].append((u * qx, px))
             if px > 0.0 and u * qx <= px:
                 res["n_accept"] += 1
                 if emit(x):

@@ -53,10 +53,11 @@ def lm_weights(cfg, seed=0, cache=True):
     return W
 
 
-def planted_rows(cfg, W, n, rng):
+def planted_rows(cfg, W, n, rng, force=None):
     """n trunk hidden rows: g ~ N(0, I), plus s * W[t]/|W[t]| for a planted target t when
-    ``cfg.plant_scale`` > 0 (t from the draft rows with probability pi_draft). Returns
-    (rows encoded like W, float32 copy, targets or -1)."""
+    ``cfg.plant_scale`` > 0 (t from the draft rows with probability pi_draft). ``force`` maps
+    row -> token to plant instead of the drawn one (the draws are made all the same, so the
+    other rows do not change). Returns (rows encoded like W, float32 copy, targets or -1)."""
     g = rng.standard_normal((n, cfg.d), dtype=np.float32)
     targets = np.full(n, -1, dtype=np.int64)
     if cfg.plant_scale > 0:
@@ -64,6 +65,8 @@ def planted_rows(cfg, W, n, rng):
         t_draft = rng.integers(0, cfg.Vd, n)
         t_rest = rng.integers(cfg.Vd, cfg.V, n)
         targets = np.where(in_draft, t_draft, t_rest)
+        for r, tok in (force or {}).items():
+            targets[r] = tok
         Wt = as_f32(W[targets])
         norms = np.linalg.norm(Wt.astype(np.float64), axis=1).astype(np.float32)
         g = g + np.float32(cfg.plant_scale) * Wt / norms[:, None]
@@ -77,15 +80,19 @@ def noisy_rows(rows32, sigma, wdtype, rng):
     return encode(rows32 + noise, wdtype)
 
 
-def cycle_inputs(cfg, W, cycle, seed=0, k=None):
+def cycle_inputs(cfg, W, cycle, seed=0, k=None, eos_at=0):
     """Inputs of one verify cycle for one request.
 
     Returns dict(H [k+1, d] verify rows, Hd [k, d] draft-head rows, k, targets). Draft i uses
-    verify row i-1 plus noise (draft i predicts the position verify row i-1 predicts)."""
+    verify row i-1 plus noise (draft i predicts the position verify row i-1 predicts).
+    eos_at = j > 0 injects the EOS id at proposal position j: verify row j-1 (and so the draft
+    row derived from it) is planted on ``cfg.eos_id``; callers that need the proposal itself to
+    be EOS also force draft j (``eos_injection`` says which cycles and where)."""
     rng = np.random.default_rng([seed, cycle, 0xC1C1E])
     if k is None:
         k = cfg.k if cfg.k_mode == "fixed" else int(rng.integers(1, cfg.k + 1))
-    H, H32, targets = planted_rows(cfg, W, k + 1, rng)
+    force = {eos_at - 1: cfg.eos_id} if 0 < eos_at <= k else None
+    H, H32, targets = planted_rows(cfg, W, k + 1, rng, force=force)
     Hd = noisy_rows(H32[:k], cfg.draft_noise, cfg.wdtype, rng) if k > 0 else H[:0]
     return dict(H=H, Hd=Hd, k=k, targets=targets)
 
@@ -123,6 +130,33 @@ def state_inputs(cfg, k, seed=0, capacity=None, P=None, n_slots=None):
     for arr in (a, b, c, x):
         arr[k + 1:] = 0
     return dict(kv_pre=kv_pre, kv_rows=kv_rows, P=P, S0=S0, conv0=conv0, a=a, b=b, c=c, x=x)
+
+
+def step_inputs(cfg, cycle, k, seed=0, n_slots=9):
+    """Per-cycle inputs of a chained run of cycles (state evolving from one cycle to the next):
+    what each of the cycle's verify rows writes into the KV cache and feeds the recurrent step.
+    Returns dict kv_rows (uint8 [R, layers, 2, row_bytes]), a [R,L,H], b [R,L,H,dk],
+    c [R,L,H,dv], x [R,L,W] with R = n_slots - 1 rows, zero past the k+1 rows of the cycle
+    (same distributions as ``state_inputs``)."""
+    rng = np.random.default_rng([seed, cycle, 0x5E9])
+    L, nh, dk, dv = cfg.rec_layers, cfg.rec_heads, cfg.rec_dk, cfg.rec_dv
+    R = n_slots - 1
+    kv_rows = rng.integers(0, 256, (R, cfg.kv_layers, 2, cfg.kv_row_bytes), dtype=np.uint8)
+    a = rng.uniform(0.9, 1.0, (R, L, nh)).astype(np.float32)
+    b = rng.standard_normal((R, L, nh, dk), dtype=np.float32) * np.float32(0.1)
+    c = rng.standard_normal((R, L, nh, dv), dtype=np.float32) * np.float32(0.1)
+    x = rng.standard_normal((R, L, cfg.conv_width), dtype=np.float32)
+    for arr in (kv_rows, a, b, c, x):
+        arr[k + 1:] = 0
+    return dict(kv_rows=kv_rows, a=a, b=b, c=c, x=x)
+
+
+def tagged(base, tag):
+    """A float32 array with the bits of ``base`` XOR (tag + 1) * 16 in every word: a cheap way to
+    give many state snapshots contents that differ from each other in every element (tag <
+    2^18 keeps the change inside the significand, so finite inputs stay finite)."""
+    bits = np.ascontiguousarray(base, dtype=np.float32).view(np.uint32)
+    return (bits ^ np.uint32((int(tag) + 1) << 4)).view(np.float32)
 
 
 _Q4_CACHE = {}

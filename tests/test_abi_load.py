@@ -147,6 +147,14 @@ def test_host_validation_of_the_later_entry_points(lib):
     assert lib.spec_accept_rows(1, 3, fake, fake, fake, fake, 4096, 4, fake, fake, 3072, 3000,
                                 256, 3328, fake, 2, fake, fake, fake, null, fake, 1 << 20,
                                 null) == 1
+    # the allocation-free entry point's error-word copy needs a destination
+    assert lib.spec_noalloc_error_word(null, null) == 1
+    # the stalled-producer test call: a wait limit in [1 us, 1 s], at most 8 rows in total
+    st = lib.spec_test_verify_stalled
+    assert st(fake, 4096, 256, fake, 1, 4, fake, null, fake, 0, fake, 1 << 20, null) == 1
+    assert st(fake, 4096, 256, fake, 1, 4, fake, null, fake, 1000001, fake, 1 << 20, null) == 1
+    assert st(fake, 4096, 256, fake, 3, 4, fake, null, fake, 1000, fake, 1 << 20, null) == 1
+    assert st(fake, 4096, 256, fake, 1, 4, fake, null, null, 1000, fake, 1 << 20, null) == 1
 
 
 def test_empty_inputs_are_rejected(lib):
@@ -250,8 +258,8 @@ def _ctype_of(ctype):
     if "*" in t:
         return (ctypes.sizeof(ctypes.c_void_p), True, False)
     base = t.replace("const ", "")
-    sizes = {"int32_t": 4, "int64_t": 8, "size_t": ctypes.sizeof(ctypes.c_size_t), "float": 4,
-             "spec_dtype": 4, "spec_status": 4}
+    sizes = {"int32_t": 4, "uint32_t": 4, "int64_t": 8, "size_t": ctypes.sizeof(ctypes.c_size_t),
+             "float": 4, "spec_dtype": 4, "spec_status": 4}
     if base == "spec_stream_t":
         return (ctypes.sizeof(ctypes.c_void_p), True, False)
     return (sizes[base], False, base == "float")

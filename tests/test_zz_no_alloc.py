@@ -4,10 +4,11 @@ or code that must not risk an allocation's implicit synchronisation). It takes n
 uses a fixed scratch array inside the library instead.
 
 Checked through the C ABI against spec_lmhead_verify (which uses a caller-allocated workspace)
-on the same inputs, within the tolerances the other parity tests use, on two calls in a row (the
-second call reuses the scratch the first one left behind). The file is named to be collected
-last, and each test builds all of its own buffers, so it passes alone in a fresh process and
-after the other tests.
+on the same inputs for the fp32, bf16 and 4-bit heads: the statistics and logits must be
+bitwise equal, since the same kernel runs behind both, and the error word read back through
+spec_noalloc_error_word must be zero, on two calls in a row (the second call reuses the scratch
+the first one left behind). The file is named to be collected last, and each test builds all
+of its own buffers, so it passes alone in a fresh process and after the other tests.
 """
 
 import numpy as np
@@ -18,56 +19,60 @@ from synth import configs, gen
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_util import close, dev, ensure_built, to_dev, to_np, wdt_of, workspace, ws_error, \
+from gpu_util import dev, ensure_built, to_dev, to_np, wdt_of, workspace, ws_error, \
     zeros_bytes  # noqa: E402
 import mtp_speculative_decoding_spec_gb300 as spec  # noqa: E402
 
 
-def _both(cfg, Wd, H, B, R, temps):
+def _noalloc_error():
+    """The allocation-free entry point's error word, read through the C ABI."""
+    err = torch.full((1,), -1, dtype=torch.int32, device=dev())
+    spec.spec_noalloc_error_word(err)
+    torch.cuda.synchronize()
+    return int(to_np(err).view(np.uint32)[0])
+
+
+def _both(cfg, Wd, wdt, H, B, R, temps):
     """Run the allocating and the allocation-free entry points on the same inputs."""
     t = torch.tensor(temps, dtype=torch.float32, device=dev())
     Hd = to_dev(H)
     ref_l = torch.full((B * R, cfg.V), float("nan"), device=dev())
     ref_s = zeros_bytes(B * R * spec.ROWSTATS_BYTES)
     ws = workspace(cfg.V, B)
-    spec.spec_lmhead_verify(Wd, wdt_of(cfg), cfg.V, cfg.d, Hd, B, R, t, ref_l, ref_s, ws)
+    spec.spec_lmhead_verify(Wd, wdt, cfg.V, cfg.d, Hd, B, R, t, ref_l, ref_s, ws)
     na_l = torch.full((B * R, cfg.V), float("nan"), device=dev())
     na_s = zeros_bytes(B * R * spec.ROWSTATS_BYTES)
-    spec.spec_lmhead_verify_noalloc(Wd, wdt_of(cfg), cfg.V, cfg.d, Hd, B, R, t, na_l, na_s)
+    spec.spec_lmhead_verify_noalloc(Wd, wdt, cfg.V, cfg.d, Hd, B, R, t, na_l, na_s)
     torch.cuda.synchronize()
     assert ws_error(ws) == 0
-    return (to_np(ref_l), to_np(ref_s, spec.ROWSTATS_DTYPE), to_np(na_l),
-            to_np(na_s, spec.ROWSTATS_DTYPE))
+    assert _noalloc_error() == 0
+    return to_np(ref_l), to_np(ref_s), to_np(na_l), to_np(na_s)
 
 
-def _check(ref_l, ref_s, na_l, na_s, temps, R):
-    for q in range(ref_s.shape[0]):
-        if temps[q // R] > 0:
-            ok, _ = close(na_l[q], ref_l[q])
-            assert ok.all(), q
-        else:
-            assert np.isnan(na_l[q]).all()  # greedy rows stay untouched, as in the original
-        assert na_s[q]["argmax"] == ref_s[q]["argmax"]
-        for f in ("max", "log_norm", "gap"):
-            a, b = float(na_s[q][f]), float(ref_s[q][f])
-            assert (np.isinf(a) and np.isinf(b)) or abs(a - b) <= 2e-2 * abs(b) + 1e-6, (q, f)
-
-
-@pytest.mark.parametrize("cfg_index", [0, 1])
-def test_noalloc_matches_workspace_entry_point_two_calls(cfg_index):
+@pytest.mark.parametrize("case", ["fp32", "bf16", "4-bit"])
+def test_noalloc_matches_workspace_entry_point_two_calls(case):
+    """The same kernel runs behind both entry points, so their outputs are bitwise equal; the
+    second call reuses the scratch the first one left behind."""
     ensure_built()
-    cfg = configs.get(cfg_index)
+    cfg = configs.get(0 if case == "fp32" else 1)
     W = gen.lm_weights(cfg)
-    Wd = to_dev(W)
+    if case == "4-bit":
+        Wd, wdt = to_dev(gen.q4_weights(cfg)), spec.SPEC_Q4A32
+    else:
+        Wd, wdt = to_dev(W), wdt_of(cfg)
     assert spec.spec_noalloc_scratch_bytes() == 128 * 1024
-    rng = np.random.default_rng(77 + cfg_index)
+    rng = np.random.default_rng(77 + len(case))
     for call, (B, R, temps) in enumerate([(1, 8, [1.0]), (2, 3, [0.0, 0.7])]):
         if cfg.plant_scale > 0:
             H, _, _ = gen.planted_rows(cfg, W, B * R, rng)
         else:
             H = gen.encode(rng.standard_normal((B * R, cfg.d), dtype=np.float32), cfg.wdtype)
-        ref_l, ref_s, na_l, na_s = _both(cfg, Wd, H, B, R, temps)
-        _check(ref_l, ref_s, na_l, na_s, temps, R)
+        ref_l, ref_s, na_l, na_s = _both(cfg, Wd, wdt, H, B, R, temps)
+        assert na_s.tobytes() == ref_s.tobytes(), (case, call)
+        # NaN-filled rows of greedy requests stay untouched by both: compare the bit patterns
+        assert na_l.view(np.uint32).tobytes() == ref_l.view(np.uint32).tobytes(), (case, call)
+        if B == 2:  # request 0 is greedy (rows untouched), request 1 at T = 0.7 (written)
+            assert np.isnan(na_l[:R]).all() and np.isfinite(na_l[R:]).all()
 
 
 def test_noalloc_rejects_vocabularies_beyond_its_scratch():
