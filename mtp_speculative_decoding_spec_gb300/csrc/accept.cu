@@ -66,11 +66,12 @@ struct DrawCtx {
   bool residual;
 };
 
-// The two integer weights of vocabulary entry j: residual max(0, p - q) and p itself.
+// The two integer weights of vocabulary entry j: residual max(0, p - q) and p itself. The
+// logit and draft rows are read-only in this kernel, so they are read through L1.
 __device__ __forceinline__ void entry_weights(const DrawCtx& c, int64_t j,
                                               unsigned long long& wr,
                                               unsigned long long& wp) {
-  const float pj = prob_of(__ldcg(c.prow + j), c.pmax, c.pinvT, c.pinv_norm);
+  const float pj = prob_of(__ldg(c.prow + j), c.pmax, c.pinvT, c.pinv_norm);
   wp = quantise(pj);
   if (!c.residual) {
     wr = wp;
@@ -79,11 +80,71 @@ __device__ __forceinline__ void entry_weights(const DrawCtx& c, int64_t j,
   float qj = 0.f;
   if (c.qrow) {
     const int64_t jr = draft_row_of(j, c.qlo, c.qhi0, c.Vd);
-    if (jr >= 0) qj = prob_of(__ldcg(c.qrow + jr), c.qmax, c.pinvT, c.qinv_norm);
+    if (jr >= 0) qj = prob_of(__ldg(c.qrow + jr), c.qmax, c.pinvT, c.qinv_norm);
   } else {
     qj = (j == c.xrej) ? 1.f : 0.f;
   }
   wr = quantise(fmaxf(0.f, __fsub_rn(pj, qj)));
+}
+
+// Weights of the four contiguous entries jb..jb+3 (zero past V): p's if use_p, else the
+// residual's. The loads of all four entries are issued before any is used.
+__device__ __forceinline__ unsigned long long entry_weights4(const DrawCtx& c, int64_t jb,
+                                                             int64_t V, bool use_p,
+                                                             unsigned long long* w) {
+  float z[4], y[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    z[e] = (jb + e < V) ? __ldg(c.prow + jb + e) : -INFINITY;
+    y[e] = -INFINITY;
+    if (c.residual && c.qrow && jb + e < V) {
+      const int64_t jr = draft_row_of(jb + e, c.qlo, c.qhi0, c.Vd);
+      if (jr >= 0) y[e] = __ldg(c.qrow + jr);
+    }
+  }
+  unsigned long long t = 0ull;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int64_t j = jb + e;
+    unsigned long long we = 0ull;
+    if (j < V) {
+      const float pj = prob_of(z[e], c.pmax, c.pinvT, c.pinv_norm);
+      if (use_p || !c.residual) {
+        we = quantise(pj);
+      } else {
+        float qj = 0.f;
+        if (c.qrow)
+          qj = (y[e] == -INFINITY) ? 0.f : prob_of(y[e], c.qmax, c.pinvT, c.qinv_norm);
+        else
+          qj = (j == c.xrej) ? 1.f : 0.f;
+        we = quantise(fmaxf(0.f, __fsub_rn(pj, qj)));
+      }
+    }
+    w[e] = we;
+    t += we;
+  }
+  return t;
+}
+
+// Block sums of two values at once (one pair of barriers); sh holds 2 per warp.
+__device__ __forceinline__ void block_sum2_u64(unsigned long long& a, unsigned long long& b,
+                                               unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum_u64(a);
+  b = warp_sum_u64(b);
+  __syncthreads();
+  if (lane == 0) {
+    sh[2 * warp] = a;
+    sh[2 * warp + 1] = b;
+  }
+  __syncthreads();
+  unsigned long long ta = 0ull, tb = 0ull;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    ta += sh[2 * w];
+    tb += sh[2 * w + 1];
+  }
+  a = ta;
+  b = tb;
 }
 
 __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
@@ -207,6 +268,41 @@ __device__ int draw_token(const AcceptParams& p, int b, const DrawCtx& c, bool u
       __syncthreads();
       if (*s_tok >= 0) break;
     }
+  }
+  __syncthreads();
+  return *s_tok;
+}
+
+// Inverse-CDF draw for a vocabulary of at most kAcceptThreads slices, thread i holding slice
+// i's integer weight w_i (0 from NS on): one block scan finds the slice whose cumulative weight
+// first exceeds floor(u * total), one pass over its 1,024 entries (four contiguous entries a
+// thread, all loads in flight together) and a second scan find the token. Two scans and one
+// round of loads, against a round per 256 entries in draw_token. Called by every thread;
+// returns the token (-1 when the total is zero).
+__device__ int draw_in_slices(const AcceptParams& p, const DrawCtx& c, bool use_p,
+                              unsigned long long w_i, uint32_t u24, unsigned long long* sh,
+                              int* s_slice, unsigned long long* s_before, int* s_tok) {
+  const int tid = threadIdx.x;
+  unsigned long long tot;
+  const unsigned long long incl = block_incl_scan_u64(w_i, sh, &tot);
+  if (tot == 0ull) return -1;  // uniform: every thread holds the same total
+  const unsigned long long target = cdf_target(u24, tot);
+  if (tid == 0) *s_tok = -1;
+  if (w_i > 0ull && incl > target && incl - w_i <= target) {  // exactly one thread
+    *s_slice = tid;
+    *s_before = incl - w_i;
+  }
+  __syncthreads();
+  const int64_t jb = static_cast<int64_t>(*s_slice) * kAcceptSlice + 4 * tid;
+  const unsigned long long before = *s_before;
+  unsigned long long w[4];
+  const unsigned long long ts = entry_weights4(c, jb, p.V, use_p, w);
+  unsigned long long tt;
+  unsigned long long cum = before + block_incl_scan_u64(ts, sh, &tt) - ts;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (w[e] > 0ull && cum <= target && cum + w[e] > target) *s_tok = static_cast<int>(jb + e);
+    cum += w[e];
   }
   __syncthreads();
   return *s_tok;
@@ -402,6 +498,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   __shared__ Decision D;
   __shared__ int sx[8], sam[8];
   __shared__ unsigned long long sh[kAcceptThreads / 32];
+  __shared__ unsigned long long s2[2 * (kAcceptThreads / 32)];
   __shared__ int s_last, s_slice, s_tok;
   __shared__ unsigned long long s_before;
   pdl_trigger();
@@ -409,6 +506,26 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
 
   const int b = blockIdx.y, sl = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
+  if (!kFiltered && warp > 0 && gridDim.y <= 4 && p.logits) {
+    // While warp 0 takes the decision, the other warps pull this slice of every verify row
+    // (and of every draft row) into L1: the draw needs one of them, known only after the
+    // decision. With few requests this costs little L2 bandwidth and takes a round trip off
+    // the slice pass.
+    const int nq = (p.q_logits && p.q_lo == p.Vd) ? min(p.k_max, p.R) : 0;
+    const int lines = (p.R + nq) * (kAcceptSlice / 32);
+    for (int i = tid - 32; i < lines; i += kAcceptThreads - 32) {
+      const int row = i / (kAcceptSlice / 32);
+      const int64_t j = j0 + 32 * (i % (kAcceptSlice / 32));
+      const float* a = nullptr;
+      if (row < p.R) {
+        if (j < p.V) a = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V + j;
+      } else if (j < p.Vd) {
+        a = p.q_logits + (static_cast<size_t>(row - p.R) * p.B + b) * p.q_stride + j;
+      }
+      if (a) asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+  }
   const int k = p.k[b];
   const float T = p.temperature[b];
 
@@ -531,7 +648,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   }
 
   // ---------------- slice sums of the draws' integer weights ----------------
-  const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
   unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
   if (kFiltered && D.need == 4) {
     // filtered: the slice's best top_k keys of every row 0..k, one warp per row
@@ -541,18 +657,11 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     unsigned long long sp[kMaxRows];
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) sp[r] = 0ull;
-    const float invT = __fdiv_rn(1.f, T);
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       if (r <= k) {
-        const size_t prow = static_cast<size_t>(b) * p.R + r;
-        const spec_rowstats ps = p.stats[prow];
-        const float inv_norm = expf(-ps.log_norm);
-        const float* row = p.logits + prow * p.V;
-        for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
-          const int64_t j = j0 + e * kAcceptThreads + tid;
-          if (j < p.V) sp[r] += quantise(prob_of(__ldcg(row + j), ps.max, invT, inv_norm));
-        }
+        unsigned long long w[4];
+        sp[r] = entry_weights4(draw_ctx(p, b, r, false, -1, T), j0 + 4 * tid, p.V, true, w);
       }
     }
 #pragma unroll
@@ -564,18 +673,11 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     }
   } else {
     const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
-    unsigned long long sr = 0ull, sp = 0ull;
-    for (int e = 0; e < kAcceptSlice / kAcceptThreads; ++e) {
-      const int64_t j = j0 + e * kAcceptThreads + tid;
-      if (j < p.V) {
-        unsigned long long wr, wp;
-        entry_weights(c, j, wr, wp);
-        sr += wr;
-        sp += wp;
-      }
-    }
-    sr = block_sum_u64(sr, sh);
-    sp = block_sum_u64(sp, sh);
+    unsigned long long w[4];
+    unsigned long long sr = entry_weights4(c, j0 + 4 * tid, p.V, false, w);
+    unsigned long long sp = sr;
+    if (c.residual) sp = entry_weights4(c, j0 + 4 * tid, p.V, true, w);  // loads hit L1
+    block_sum2_u64(sr, sp, s2);
     if (tid == 0) {
       mysum[0] = sr;
       mysum[1] = sp;
@@ -601,11 +703,16 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       E = D;
       s_stop = 0;
     }
+    const bool fast = p.NS <= kAcceptThreads;
+    const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
     __syncthreads();
     for (int r = 0; r <= k; ++r) {
       const DrawCtx c = draw_ctx(p, b, r, false, -1, T);
       const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_BONUS);
-      const int tok = draw_token(p, b, c, true, r, u24, sh, &s_slice, &s_before, &s_tok);
+      const unsigned long long wr =
+          (fast && tid < p.NS) ? __ldcg(rs + kAcceptSumSlots * tid + r) : 0ull;
+      const int tok = fast ? draw_in_slices(p, c, true, wr, u24, sh, &s_slice, &s_before, &s_tok)
+                           : draw_token(p, b, c, true, r, u24, sh, &s_slice, &s_before, &s_tok);
       if (tid == 0) {
         E.srow = r;
         E.tokens[E.ntok++] = tok;
@@ -740,13 +847,24 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   // ratio rule: one draw, from the residual (p if the residual is empty) or the bonus row
   const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
   const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
-  unsigned long long tr = 0ull;
-  for (int i = tid; i < p.NS; i += kAcceptThreads) tr += __ldcg(rs + kAcceptSumSlots * i);
-  tr = block_sum_u64(tr, sh);
-  const bool use_p = (D.need == 2) || (tr == 0ull);
   const uint32_t purpose = (D.need == 1) ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
   const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + D.srow, purpose);
-  int tok = draw_token(p, b, c, use_p, use_p ? 1 : 0, u24, sh, &s_slice, &s_before, &s_tok);
+  int tok;
+  if (p.NS <= kAcceptThreads) {
+    // slot 0 holds the residual's slice sums, slot 1 p's: both in one round of loads
+    const unsigned long long w_r = (tid < p.NS) ? __ldcg(rs + kAcceptSumSlots * tid) : 0ull;
+    const unsigned long long w_p = (tid < p.NS) ? __ldcg(rs + kAcceptSumSlots * tid + 1) : 0ull;
+    tok = draw_in_slices(p, c, D.need == 2, D.need == 2 ? w_p : w_r, u24, sh, &s_slice,
+                         &s_before, &s_tok);
+    if (tok < 0 && D.need == 1)  // the residual sums to zero: draw from p
+      tok = draw_in_slices(p, c, true, w_p, u24, sh, &s_slice, &s_before, &s_tok);
+  } else {
+    unsigned long long tr = 0ull;
+    for (int i = tid; i < p.NS; i += kAcceptThreads) tr += __ldcg(rs + kAcceptSumSlots * i);
+    tr = block_sum_u64(tr, sh);
+    const bool use_p = (D.need == 2) || (tr == 0ull);
+    tok = draw_token(p, b, c, use_p, use_p ? 1 : 0, u24, sh, &s_slice, &s_before, &s_tok);
+  }
   if (tid == 0) {
     Decision d = D;
     if (tok < 0) tok = p.stats[static_cast<size_t>(b) * p.R + D.srow].argmax;  // unreachable
