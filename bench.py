@@ -486,8 +486,10 @@ def sweep(dev, W, Wd, hbm_peak):
     (ratio rule with the draft head's q rows, Philox seeds 0..99 cycling over the cycles, EOS
     injected in 5% of the cycles); exact-match acceptance, and acceptance against the top-k 20 /
     top-p 0.95 filtered target (argmax drafts), at temperature 1 for k = 1, 3, 7. Each point
-    runs 512 distinct cycles, twice: once with events around each verify and acceptance (launch
-    durations), once without (the full-cycle rate: k draft steps + verify + acceptance)."""
+    runs 512 distinct cycles three times: with events around each verify and acceptance launch
+    (their durations: lmhead_frac, accept_us), verify + acceptance back to back on the cycles'
+    drafts (verify_cycles_s, verify_accept_frac) and whole cycles with their k draft steps
+    (full_cycles_s, emitted_tok_s)."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -508,50 +510,77 @@ def sweep(dev, W, Wd, hbm_peak):
                                cfg.eos_id, device=dev, want_q_logits=True,
                                acceptance=mode)
         eng.set_requests(temps=[T], seeds=[0], pos=[0], k=[k], top_k=[20], top_p=[0.95])
+        # each cycle's drafts and draft rows (q), kept so that verify + acceptance can also be
+        # timed on their own
+        q_pool = torch.empty((n_pool, k, cfg.Vd), dtype=torch.float32, device=dev)
+        qs_pool = torch.zeros((n_pool, k * spec.ROWSTATS_BYTES), dtype=torch.uint8, device=dev)
+        d_pool = torch.zeros((n_pool, 1, k), dtype=torch.int32, device=dev)
 
-        def cycle(c, events=None):
+        def use(c):
             cc = c % n_pool
             eng.seeds = seeds_pool[c % 100:c % 100 + 1]  # this cycle's Philox seed and position
             eng.pos = pos_pool[cc:cc + 1]
+            eng.q, eng.qs, eng.drafts = q_pool[cc], qs_pool[cc], d_pool[cc]
+            return cc
+
+        def drafts(c):
+            cc = use(c)
             for i in range(1, k + 1):
                 eng.draft_step(i, Hdp_d[cc, i - 1:i])
-            if events:
-                events[0].record()
-            eng.verify(Hp_d[cc])
-            if events:
-                events[1].record()
-            eng.accept()
-            if events:
-                events[2].record()
+            return cc
 
+        for c in range(n_pool):
+            drafts(c)
         for c in range(5):
-            cycle(c)
+            eng.verify(Hp_d[use(c)])
+            eng.accept()
         torch.cuda.synchronize()
-        eng.counters.zero_()
+        # pass 1: verify and acceptance launches bracketed by events; each chunk of cycles is
+        # queued behind a short device-side wait so that the host's call overhead is not timed
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for c in range(K):  # pass 1: launch durations
-            cycle(c, ev[c])
+        for c0 in range(0, K, 32):
+            torch.cuda._sleep(20_000_000)
+            for c in range(c0, min(K, c0 + 32)):
+                cc = use(c)
+                ev[c][0].record()
+                eng.verify(Hp_d[cc])
+                ev[c][1].record()
+                eng.accept()
+                ev[c][2].record()
         torch.cuda.synchronize()
-        eng.counters.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # pass 2: verify + acceptance back to back (the verify cycle, overlapped as in use)
         a.record()
-        for c in range(K):  # pass 2: the full-cycle rate
-            cycle(c)
+        for c in range(K):
+            eng.verify(Hp_d[use(c)])
+            eng.accept()
+        b.record()
+        torch.cuda.synchronize()
+        va_s = a.elapsed_time(b) / 1e3
+        eng.counters.zero_()
+        # pass 3: full cycles (k draft steps + verify + acceptance)
+        a.record()
+        for c in range(K):
+            cc = drafts(c)
+            eng.verify(Hp_d[cc])
+            eng.accept()
         b.record()
         torch.cuda.synchronize()
         s = a.elapsed_time(b) / 1e3
-        verify_s = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
         gemv_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
         cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
-        va_bytes = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16 +
+        lm_bytes = (cfg.V * cfg.d * 2 + (k + 1) * cfg.d * 2 + (k + 1) * 16 +
                     (k + 1) * cfg.V * 4 * (T > 0))
-        gbs = va_bytes / gemv_s / 1e9
+        # verify + acceptance: the LM head's bytes plus, at T > 0, one logit row and one draft
+        # row read by the acceptance's draw
+        va_bytes = lm_bytes + (cfg.V + cfg.Vd) * 4 * (T > 0)
+        gbs = lm_bytes / gemv_s / 1e9
         accept_us = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3
         per_drafted, per_test = acceptance_rates(cnt, k)
         out[f"T{T:g}_k{k}" + ("" if mode == "ratio" else f"_{mode}")] = {
-            "verify_cycles_s": round(K / verify_s, 1),
-            "verify_accept_frac": round(va_bytes / (verify_s / K) / 1e9 / hbm_peak, 4),
+            "verify_cycles_s": round(K / va_s, 1),
+            "verify_accept_frac": round(va_bytes / (va_s / K) / 1e9 / hbm_peak, 4),
             "full_cycles_s": round(K / s, 1),
             "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
             "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
@@ -559,7 +588,7 @@ def sweep(dev, W, Wd, hbm_peak):
             "eos_cycles": int(n_eos), "cycles": K,
             "lmhead_gbs": round(gbs, 1), "lmhead_frac": round(gbs / hbm_peak, 4),
             "accept_us": round(accept_us, 2)}
-        del eng, Hp_d, Hdp_d
+        del eng, Hp_d, Hdp_d, q_pool, qs_pool, d_pool
     return out
 
 

@@ -184,16 +184,17 @@ __device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long 
 }
 
 // The draw context of verify row `row` of request b: p at temperature T, and for a residual
-// the draft distribution (q rows, or one-hot at the rejected draft `xrej`).
+// the draft distribution (q rows, or one-hot at the rejected draft `xrej`). pst / qst: the
+// request's verify-row and draft-row statistics, copied to shared memory by the decision.
 __device__ __forceinline__ DrawCtx draw_ctx(const AcceptParams& p, int b, int row, bool residual,
-                                            int xrej, float T) {
+                                            int xrej, float T, const spec_rowstats* pst,
+                                            const spec_rowstats* qst) {
   DrawCtx c;
   const size_t prow = static_cast<size_t>(b) * p.R + row;
-  const spec_rowstats ps = p.stats[prow];
   c.prow = p.logits + prow * p.V;
-  c.pmax = ps.max;
+  c.pmax = pst[row].max;
   c.pinvT = __fdiv_rn(1.f, T);
-  c.pinv_norm = expf(-ps.log_norm);
+  c.pinv_norm = expf(-pst[row].log_norm);
   c.residual = residual;
   c.qrow = nullptr;
   c.qmax = 0.f;
@@ -205,10 +206,9 @@ __device__ __forceinline__ DrawCtx draw_ctx(const AcceptParams& p, int b, int ro
   if (residual) {
     if (p.q_logits) {
       const size_t qr = static_cast<size_t>(row) * p.B + b;
-      const spec_rowstats qs = p.q_stats[qr];
       c.qrow = p.q_logits + qr * p.q_stride;
-      c.qmax = qs.max;
-      c.qinv_norm = expf(-qs.log_norm);
+      c.qmax = qst[row].max;
+      c.qinv_norm = expf(-qst[row].log_norm);
     } else {
       c.xrej = xrej;
     }
@@ -462,7 +462,25 @@ __device__ int small_draw(int* id, unsigned long long* w, int n, uint32_t u24) {
   return -1;
 }
 
-__device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
+// The counters of one cycle; eos_too = false leaves the EOS count to the caller (the ratio
+// rule counts everything else as soon as its decision is known, before the draw).
+__device__ void count_cycle(const AcceptParams& p, int b, const Decision& D, int k, int ntok,
+                            bool eos_too) {
+  if (!p.counters) return;
+  spec_counters* c = p.counters + b;
+  c->cycles += 1ull;
+  if (D.status == SPEC_REQ_OK) {
+    c->drafted += static_cast<unsigned long long>(k);
+    c->accepted += static_cast<unsigned long long>(D.n_accept);
+    c->emitted += static_cast<unsigned long long>(ntok);
+    if (eos_too) c->eos += static_cast<unsigned long long>(D.eos_hit);
+    c->depth[D.n_accept & 7] += 1ull;
+  } else {
+    c->errors += 1ull;
+  }
+}
+
+__device__ void write_result(const AcceptParams& p, int b, const Decision& D) {
   spec_accept_out o;
   o.status = D.status;
   o.n_accept = D.n_accept;
@@ -474,19 +492,11 @@ __device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k)
   o.reserved[0] = 0;
   o.reserved[1] = 0;
   p.out[b] = o;
-  if (p.counters) {
-    spec_counters* c = p.counters + b;
-    c->cycles += 1ull;
-    if (D.status == SPEC_REQ_OK) {
-      c->drafted += static_cast<unsigned long long>(k);
-      c->accepted += static_cast<unsigned long long>(D.n_accept);
-      c->emitted += static_cast<unsigned long long>(D.ntok);
-      c->eos += static_cast<unsigned long long>(D.eos_hit);
-      c->depth[D.n_accept & 7] += 1ull;
-    } else {
-      c->errors += 1ull;
-    }
-  }
+}
+
+__device__ void finalize(const AcceptParams& p, int b, const Decision& D, int k) {
+  write_result(p, b, D);
+  count_cycle(p, b, D, k, D.ntok, true);
 }
 
 // kFiltered: the instantiation for spec_accept_filtered. The ratio-rule and exact-match modes
@@ -497,6 +507,7 @@ template <bool kFiltered>
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptParams p) {
   __shared__ Decision D;
   __shared__ int sx[8], sam[8];
+  __shared__ spec_rowstats s_pst[kMaxRows], s_qst[kMaxRows];
   __shared__ unsigned long long sh[kAcceptThreads / 32];
   __shared__ unsigned long long s2[2 * (kAcceptThreads / 32)];
   __shared__ int s_last, s_slice, s_tok;
@@ -534,10 +545,20 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     int status = SPEC_REQ_OK;
     const bool kbad = (k < 0 || k > p.k_max || k + 1 > p.R);
     if (kbad) status = SPEC_REQ_BAD_K;
+    // this lane's draft, verify-row and draft-row statistics, loaded together whatever k is
+    // (the indices stay inside the arrays' k_max and R rows): one round of loads
+    const int x_any = (lane < p.k_max) ? p.drafts[static_cast<size_t>(b) * p.k_max + lane] : -1;
+    spec_rowstats st_any{0.f, 0.f, 0.f, -1}, qs_any{0.f, 0.f, 0.f, -1};
+    if (lane < p.R) st_any = p.stats[static_cast<size_t>(b) * p.R + lane];
+    if (p.q_logits && lane < p.k_max) qs_any = p.q_stats[static_cast<size_t>(lane) * p.B + b];
+    if (lane < kMaxRows) {
+      s_pst[lane] = st_any;
+      s_qst[lane] = qs_any;
+    }
     int x = -1;
     bool xbad = false;
     if (!kbad && lane < k) {
-      x = p.drafts[static_cast<size_t>(b) * p.k_max + lane];
+      x = x_any;
       xbad = (x < 0 || static_cast<int64_t>(x) >= p.V);
     }
     if (status == SPEC_REQ_OK && __any_sync(0xffffffffu, xbad)) status = SPEC_REQ_BAD_TOKEN;
@@ -554,11 +575,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     bool nf = false;
     if (status == SPEC_REQ_OK) {
       if (lane <= k) {
-        st = p.stats[static_cast<size_t>(b) * p.R + lane];
+        st = st_any;
         nf = isnan(st.max);
       }
-      if (T > 0.f && p.q_logits && lane < k)
-        nf = nf || isnan(p.q_stats[static_cast<size_t>(lane) * p.B + b].max);
+      if (T > 0.f && p.q_logits && lane < k) nf = nf || isnan(qs_any.max);
       if (__any_sync(0xffffffffu, nf)) status = SPEC_REQ_NONFINITE;
     }
     const bool exact = p.exact && T > 0.f;  // exact-match mode: decided by the draws below
@@ -577,9 +597,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
           const int64_t xr = draft_row_of(x, p.q_lo, p.q_hi0, p.Vd);
           if (xr >= 0) {
             const size_t qr = static_cast<size_t>(lane) * p.B + b;
-            const spec_rowstats qs = p.q_stats[qr];
-            qx = prob_of(__ldcg(p.q_logits + qr * p.q_stride + xr), qs.max, invT,
-                         expf(-qs.log_norm));
+            qx = prob_of(__ldcg(p.q_logits + qr * p.q_stride + xr), qs_any.max, invT,
+                         expf(-qs_any.log_norm));
           }
         }
         const float u = u24_to_float(uniform_u24(p.seed[b], p.pos_base[b] + lane, PURPOSE_ACCEPT));
@@ -646,6 +665,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     if (sl == 0 && tid == 0) finalize(p, b, D, k);
     return;
   }
+  // the ratio rule's counters are known now except whether the drawn token is EOS
+  if ((D.need == 1 || D.need == 2) && sl == 0 && tid == 0) count_cycle(p, b, D, k, D.ntok + 1, false);
 
   // ---------------- slice sums of the draws' integer weights ----------------
   unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
@@ -661,7 +682,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     for (int r = 0; r < kMaxRows; ++r) {
       if (r <= k) {
         unsigned long long w[4];
-        sp[r] = entry_weights4(draw_ctx(p, b, r, false, -1, T), j0 + 4 * tid, p.V, true, w);
+        sp[r] = entry_weights4(draw_ctx(p, b, r, false, -1, T, s_pst, s_qst), j0 + 4 * tid, p.V, true, w);
       }
     }
 #pragma unroll
@@ -672,7 +693,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       }
     }
   } else {
-    const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
+    const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T, s_pst, s_qst);
     unsigned long long w[4];
     unsigned long long sr = entry_weights4(c, j0 + 4 * tid, p.V, false, w);
     unsigned long long sp = sr;
@@ -707,7 +728,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
     __syncthreads();
     for (int r = 0; r <= k; ++r) {
-      const DrawCtx c = draw_ctx(p, b, r, false, -1, T);
+      const DrawCtx c = draw_ctx(p, b, r, false, -1, T, s_pst, s_qst);
       const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_BONUS);
       const unsigned long long wr =
           (fast && tid < p.NS) ? __ldcg(rs + kAcceptSumSlots * tid + r) : 0ull;
@@ -845,7 +866,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   }
 
   // ratio rule: one draw, from the residual (p if the residual is empty) or the bonus row
-  const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T);
+  const DrawCtx c = draw_ctx(p, b, D.srow, D.need == 1, D.xrej, T, s_pst, s_qst);
   const unsigned long long* rs = p.sums + static_cast<size_t>(b) * p.NS * kAcceptSumSlots;
   const uint32_t purpose = (D.need == 1) ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
   const uint32_t u24 = uniform_u24(p.seed[b], p.pos_base[b] + D.srow, purpose);
@@ -867,10 +888,11 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   }
   if (tid == 0) {
     Decision d = D;
-    if (tok < 0) tok = p.stats[static_cast<size_t>(b) * p.R + D.srow].argmax;  // unreachable
+    if (tok < 0) tok = s_pst[D.srow].argmax;  // unreachable
     d.tokens[d.ntok++] = tok;
     if (p.eos >= 0 && tok == p.eos) d.eos_hit = 1;
-    finalize(p, b, d, k);
+    write_result(p, b, d);
+    if (p.counters && d.eos_hit) p.counters[b].eos += 1ull;
     p.tickets[b] = 0u;
   }
 }

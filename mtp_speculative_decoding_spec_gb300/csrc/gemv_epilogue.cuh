@@ -236,25 +236,22 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
         }
         const unsigned hmask = __ballot_sync(0xffffffffu, hit >= 0);
         int cstar;
-        unsigned long long tt = 0ull;
+        float frac = 1.f;  // the target's position inside the chosen block, as a fraction of it
         if (hmask) {
           const int L = __ffs(hmask) - 1;
           cstar = __shfl_sync(0xffffffffu, hit, L);
           cum_hit = __shfl_sync(0xffffffffu, cum_hit, L);
-          const unsigned long long sc = blk_s[cstar];
-          float rem = __fdiv_rn(__fsub_rn(target, cum_hit), blk_m[cstar]);  // blk_m holds f now
-          if (!(rem >= 0.f)) rem = 0.f;
-          tt = (rem < 1.8446744e19f) ? __float2ull_rd(rem) : sc;
-          if (tt >= sc) tt = sc - 1ull;
+          frac = __fdiv_rn(__fsub_rn(target, cum_hit), blk_w[cstar]);
+          if (!(frac >= 0.f)) frac = 0.f;
         } else {  // rounding left u*S past the total: the last block with weight
           cstar = last_nz;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) cstar = max(cstar, __shfl_xor_sync(0xffffffffu, cstar, o));
-          if (cstar >= 0) tt = blk_s[cstar] - 1ull;
         }
         if (cstar >= 0) {
-          // the block's logits in per-lane chunks: integer weights, an exclusive scan of the
-          // chunk sums, then the warp walks the one chunk that holds the target
+          // the block's logits in per-lane chunks: exact integer weights against the block max,
+          // an inclusive scan of the chunk sums (its last entry is the block's integer total I),
+          // the target tt = floor(frac * I), then the warp walks the one chunk that holds it
           int64_t c0, c1;
           block_rows(cstar, GR, p.nbands, p.band_rows, p.V, c0, c1);
           const float mc = __ldcg(&(p.part + static_cast<size_t>(cstar) * kMaxRows + q)->m);
@@ -276,6 +273,12 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
           for (int o = 1; o < 32; o <<= 1) {
             const unsigned long long up = __shfl_up_sync(0xffffffffu, inc, o);
             if (lane >= o) inc += up;
+          }
+          const unsigned long long I = __shfl_sync(0xffffffffu, inc, 31);
+          unsigned long long tt = I - 1ull;  // I >= 2^40: the block max itself weighs 2^40
+          if (frac < 1.f) {
+            const unsigned long long t2 = __float2ull_rd(__fmul_rn(frac, u64_to_f32(I)));
+            tt = t2 < tt ? t2 : tt;
           }
           const unsigned lmask = __ballot_sync(0xffffffffu, lw > 0ull && inc > tt);
           if (lmask) {

@@ -19,10 +19,12 @@
 //     so the shared memory goes to the stages alone (three of 72 KB at any row count);
 //   * four warps (one per TMEM lane quadrant) read each finished accumulator with tcgen05.ld
 //     (lane = vocabulary row, column = H row), write the logits of rows at T > 0 (coalesced)
-//     and keep a running top-2 of each row while the next tiles stream in; when streaming is
-//     over they merge the quadrants into the block max m and sum the integer weights
-//     rint(exp((z - m)/T) 2^40) of the block's logits straight from TMEM, so the block's
-//     partials cost one pass over TMEM and no logit tile in shared memory;
+//     and fold the tile into each row's running statistics while the next tiles stream in: the
+//     top-2, and the sum of exp((z - m)/T) kept as (M, S) -- the exact integer sum of
+//     rint(exp((z - m_q)/T) 2^40) over the tile's 32 rows of the warp, against their own max
+//     m_q, scaled onto the running max M in fp32 (a fixed order of separately rounded
+//     operations). A tile takes ~14 us to stream and its statistics well under one, so when
+//     streaming is over only the four quadrants remain to be merged;
 //   * then the same finish as the CUDA-core kernel: the last block's combine and the draft
 //     draw.
 // Batch invariance (section "Exactness": up to eight rows, a row's verify logits may not depend
@@ -80,22 +82,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int ntile_cap = (p.tile_cap + kSkTileRows - 1) / kSkTileRows;
   uint32_t tcols = 32;
   while (tcols < static_cast<uint32_t>(ntile_cap * kSkN)) tcols <<= 1;
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int t = 0; t < kSkMaxTiles; ++t) mbar_init(&tile_done[t], 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, tcols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
 
   // The stage schedule: iteration it covers tile it / nks, stage ks = it % nks of that tile.
   const int total_it = ntile * nks;
@@ -159,16 +145,28 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
   };
   // The weights are never written by the path: the first stages stream in before the wait for
-  // the previous kernel, whose tail they overlap. H, the temperatures, the outputs and the
-  // workspace are only touched after it.
+  // the previous kernel, whose tail they overlap, and before the tensor memory is allocated.
+  // H, the temperatures, the outputs and the workspace are only touched after the wait.
   const int pre = min(S, total_it);
-  if (warp == 0 && lane == 0) {
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < kSkMaxTiles; ++t) mbar_init(&tile_done[t], 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();  // the barriers' initialisation before the copies that complete on them
     for (int it = 0; it < pre; ++it) issue_w(it, it);
-    pdl_wait();
-    for (int it = 0; it < pre; ++it) issue_h(it, it);  // the first MMAs wait on nothing else
-  } else {
-    pdl_wait();
   }
+  if (warp == 1) tmem_alloc(tmem_slot, tcols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  if (tid == 0)
+    for (int it = 0; it < pre; ++it) issue_h(it, it);  // the first MMAs wait on nothing else
   if (tid >= 32 && tid < 32 + kMaxRows) {  // lanes of the MMA warp, idle until the barrier
     const int r = tid - 32;
     load_row_inputs(p, ri, r);
@@ -179,10 +177,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   // warps only)
   Top2 run[kMaxRows];
   int rbad[kMaxRows];
+  float rM[kMaxRows], rS[kMaxRows];  // running max and exp-sum (2^-40 units) against it
 #pragma unroll
   for (int r = 0; r < kMaxRows; ++r) {
     run[r] = top2_empty();
     rbad[r] = 0;
+    rM[r] = -INFINITY;
+    rS[r] = 0.f;
   }
 
   if (warp == 0) {
@@ -276,98 +277,70 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           c = warp_top2(c);
           rbad[r] |= __any_sync(0xffffffffu, valid && nf) ? 1 : 0;
           run[r] = top2_merge(run[r], c);
+          const float mq = c.best;  // warp-uniform: the max of this warp's rows of the tile
+          if (mq != -INFINITY) {
+            const float invT = ri->invT[r];
+            const unsigned long long w = (valid && !nf) ? tile_weight(z, mq, invT) : 0ull;
+            const float sq = u64_to_f32(warp_sum_u64(w));
+            if (mq > rM[r]) {
+              rS[r] = __fadd_rn(__fmul_rn(rS[r], expf(__fmul_rn(__fsub_rn(rM[r], mq), invT))), sq);
+              rM[r] = mq;
+            } else {
+              rS[r] = __fadd_rn(rS[r], __fmul_rn(sq, expf(__fmul_rn(__fsub_rn(mq, rM[r]), invT))));
+            }
+          }
         }
       }
     }
   }
 
   // every tile's MMAs have completed (the drain warps waited for each) and every copy has
-  // landed (the producer waited for each): the ring is free for the block's statistics. The
-  // next kernel may now be scheduled into this kernel's tail (not earlier: blocks parked in
-  // its wait during the stream cost bandwidth).
+  // landed (the producer waited for each): the ring is free for the block's statistics and the
+  // accumulators are no longer needed. The next kernel may now be scheduled into this kernel's
+  // tail (not earlier: blocks parked in its wait during the stream cost bandwidth).
   tc_fence_before();
   __syncthreads();
   pdl_trigger();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
   Top2* s_top = reinterpret_cast<Top2*>(ring);                             // [4 quadrants][8]
   int* s_bad = reinterpret_cast<int*>(ring + 4 * kMaxRows * sizeof(Top2));  // [4][8]
-  unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(ring + 512);  // [8]
+  float2* s_ms = reinterpret_cast<float2*>(ring + 512);                     // [4][8] (M, S)
   if (warp >= kSkDrainWarp0 && lane == 0) {
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       s_top[(warp & 3) * kMaxRows + r] = run[r];
       s_bad[(warp & 3) * kMaxRows + r] = rbad[r];
+      s_ms[(warp & 3) * kMaxRows + r] = make_float2(rM[r], rS[r]);
     }
   }
-  if (tid < kMaxRows) s_sum[tid] = 0ull;
   __syncthreads();
-
-  // block max of each row (the four quadrants merged in a fixed order), then the exact integer
-  // sum of tile_weight(z, m) over the block's logits, read once more from TMEM by all eight
-  // warps: warps w and w + 4 share lane quadrant w & 3 and take alternate pairs of tiles
-  if (!*reinterpret_cast<volatile int*>(&flags[0])) {
-    tc_fence_after();
-    const int ew = warp & 3, half = warp >> 2;
-    float mref[kMaxRows], invT[kMaxRows];
-    bool dosum[kMaxRows];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      Top2 m = top2_empty();
-      for (int w = 0; w < 4; ++w) m = top2_merge(m, s_top[w * kMaxRows + r]);
-      mref[r] = m.best;
-      dosum[r] = r < nr && m.idx != kNoIndex && m.best != -INFINITY;
-      invT[r] = ri->invT[r];
-    }
-    unsigned long long acc[kMaxRows];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0ull;
-    // two tiles per TMEM load: columns [16 t, 16 t + 32) stay inside the allocation because t
-    // is even and the allocation is a power of two of at least 16 columns per tile and 32
-    for (int t = 2 * half; t < ntile; t += 4) {
-      float v[32];
-      tmem_ld32(tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                    static_cast<uint32_t>(t * kSkN),
-                v);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int local = (t + h) * kSkTileRows + ew * 32 + lane;
-        const bool ok = t + h < ntile && local < nt;
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-          if (r < nr) {  // uniform: only the live rows cost an exp
-            const float z = v[h * kSkN + r];
-            const unsigned long long w = tile_weight(z, mref[r], invT[r]);
-            acc[r] += (ok && dosum[r] && !(isnan(z) || z == INFINITY)) ? w : 0ull;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      if (r < nr) {
-        const unsigned long long a = warp_sum_u64(acc[r]);
-        if (lane == 0) atomicAdd(&s_sum[r], a);  // integers: the order does not matter
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, tcols);
-  }
   if (tid < nr) {
+    // the quadrants merged in a fixed order: top-2, NaN / +Inf flag, and the exp-sum against
+    // the block max M (the integer weights' scale, 2^-40 units)
     Top2 m = top2_empty();
     int bad = 0;
     for (int w = 0; w < 4; ++w) {
       m = top2_merge(m, s_top[w * kMaxRows + tid]);
       bad |= s_bad[w * kMaxRows + tid];
     }
+    const float invT = ri->invT[tid];
+    float S = 0.f;
+    if (!*reinterpret_cast<volatile int*>(&flags[0]) && m.best != -INFINITY) {
+      for (int w = 0; w < 4; ++w) {
+        const float2 q = s_ms[w * kMaxRows + tid];
+        if (q.x != -INFINITY)
+          S = __fadd_rn(S, __fmul_rn(q.y, expf(__fmul_rn(__fsub_rn(q.x, m.best), invT))));
+      }
+    }
     GemvPartial pp;
     pp.m = m.best;
     pp.second = m.second;
     pp.idx = (m.idx == kNoIndex) ? -1 : m.idx;
     pp.flags = bad;
-    pp.s = s_sum[tid];
+    pp.s = __float2ull_rn(S);
     pp.pad = 0ull;
     p.part[static_cast<size_t>(blockIdx.x) * kMaxRows + tid] = pp;
   }
