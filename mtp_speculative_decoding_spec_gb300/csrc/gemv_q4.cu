@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int total_it = ntile * nks;
+  const uint64_t wpol = l2_policy_evict_first();  // codes and pairs: read once, not kept in L2
   auto stage_tasks = [&](int ks) { return ks == nks - 1 ? last_tasks : kQTasksPerStage; };
   auto issue_w = [&](int it, int s) {  // codes, pairs (and the byte count of H) of iteration it
     const int t = it / nks, ks = it - t * nks;
@@ -161,11 +162,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                                           stage_tasks(ks) * 2 * kQHBlock));
     for (int c = 0; c < nch; ++c)
       for (int b = 0; b < nbox; ++b)
-        tc_tma_load_2d(st + c * kQCodeTile + b * kQCodeBox, &cmap, x0 + c * kQChunkBytes,
-                       box_row(p, y + b * kQBoxRows), &full[s]);
+        tc_tma_load_2d_hint(st + c * kQCodeTile + b * kQCodeBox, &cmap, x0 + c * kQChunkBytes,
+                            box_row(p, y + b * kQBoxRows), &full[s], wpol);
     for (int b = 0; b < nbox; ++b)
-      tc_tma_load_2d(st + kQPairOff + b * kQPairBox, &smap, ks * kQPairRowBytes,
-                     box_row(p, y + b * kQBoxRows), &full[s]);
+      tc_tma_load_2d_hint(st + kQPairOff + b * kQPairBox, &smap, ks * kQPairRowBytes,
+                          box_row(p, y + b * kQBoxRows), &full[s], wpol);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it
     const int ks = it % nks;

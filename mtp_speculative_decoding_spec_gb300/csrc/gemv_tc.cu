@@ -13,7 +13,9 @@
 //     (four 64-wide k-blocks as 2-D TMA boxes of 32 rows, 128-byte swizzle; only the boxes the
 //     tile needs) and the matching 16-row H blocks (rows past the live ones read as zero) into
 //     a ring of shared-memory stages. Requests of 512 contiguous bytes per row keep HBM far
-//     busier than 128-byte ones;
+//     busier than 128-byte ones. The weight lines carry an evict-first L2 policy: the matrix
+//     is far larger than L2 and read once, and without the hint it pushes the logits written
+//     during the stream out to HBM just before the acceptance reads them back;
 //   * one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32, M = 128 weight rows,
 //     N = 16 H rows, K = 16); every tile of the block has its own 16-column TMEM accumulator,
 //     so the shared memory goes to the stages alone (three of 72 KB at any row count);
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   // measured ~5% slower
   const int lo_rows = static_cast<int>(p.lo_rows);
   const int hi_shift = static_cast<int>(p.hi_row0 - p.lo_rows);
+  const uint64_t wpol = l2_policy_evict_first();  // the weights: read once, never kept in L2
   auto box_rows = [&](int y, int* yb) {
 #pragma unroll
     for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b) {
@@ -111,8 +114,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 #pragma unroll
       for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
         if (b < nbox)
-          tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
-                         (ks * kSkKB + kk) * kSkKBlock, yb[b], &full[s]);
+          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
+                              (ks * kSkKB + kk) * kSkKBlock, yb[b], &full[s], wpol);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it into stage s
     const int t = it / nks, ks = it - t * nks;
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 #pragma unroll
       for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
         if (b < nbox)
-          tc_tma_load_2d(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, yb[b], &full[s]);
+          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, yb[b], &full[s],
+                              wpol);
       tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
     }
   };

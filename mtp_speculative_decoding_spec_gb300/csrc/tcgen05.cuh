@@ -15,6 +15,27 @@ __device__ __forceinline__ void tc_tma_load_2d(void* smem_dst, const CUtensorMap
       : "memory");
 }
 
+// An L2 policy that makes lines the first to go when L2 needs room: for operands that are read
+// once per launch and never again from L2 (an LM head of ~0.8 GB streams through a 129 MB L2
+// every launch), so that they do not push out what the next kernels read back (the logits, draft
+// rows, statistics and partials a verify or draft step leaves for the acceptance and the draw).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tc_tma_load_2d with an L2 cache policy for the copied lines.
+__device__ __forceinline__ void tc_tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, int x,
+                                                    int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand in the canonical 128-byte-swizzle layout
 // written by TMA (rows of 128 bytes, 8-row groups 1024 bytes apart).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
