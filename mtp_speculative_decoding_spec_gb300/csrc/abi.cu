@@ -138,9 +138,7 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   GemvTcLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
-  // 16-row bands (the block runs end on a half box); 32-row bands for a two-range draft set,
-  // whose boxes may not straddle the ranges
-  const int band = (lo_rows == V) ? gemv_tc_band_rows() : gemv_tc_box_rows();
+  const int band = gemv_tc_band_rows();
   const int64_t nbands = (V + band - 1) / band;
   const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * band);
   if (tile_cap > gemv_tc_max_block_rows()) return SPEC_ERR_UNSUPPORTED;
@@ -169,12 +167,6 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
                                static_cast<cuuint32_t>(gemv_tc_box_rows())};
     if (encode(&L.wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride,
                box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SPEC_ERR_CUDA;
-    const cuuint32_t box16[2] = {static_cast<cuuint32_t>(gemv_tc_kblock()),
-                                 static_cast<cuuint32_t>(gemv_tc_box_rows() / 2)};
-    if (encode(&L.wmap16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride,
-               box16, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SPEC_ERR_CUDA;
   }

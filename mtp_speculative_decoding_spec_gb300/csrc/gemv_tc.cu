@@ -7,11 +7,8 @@
 // through the shared LM head). On the CUDA cores every weight costs one fp32 FMA per row, so at
 // 5..8 rows the FMA pipe, not HBM, sets the pace; here the multiply-adds go to the tensor cores
 // and the kernel is left with streaming alone:
-//   * one persistent CTA per SM owns a contiguous run of 16-row bands of the vocabulary (32-row
-//     bands for a draft set of two ranges, so that no box straddles them) and walks it in
-//     tiles of 128 rows (the last one partial). A 16-row band keeps the blocks within 16 rows
-//     of each other: with 32-row bands the 64,000-row draft head left some blocks 6% more
-//     rows than others, and the slowest block sets the kernel's end;
+//   * one persistent CTA per SM owns a contiguous run of 32-row bands of the vocabulary and
+//     walks it in tiles of 128 rows (the last one partial);
 //   * a producer warp loads, per stage, 512 contiguous bytes of each of the tile's weight rows
 //     (four 64-wide k-blocks as 2-D TMA boxes of 32 rows, 128-byte swizzle; only the boxes the
 //     tile needs) and the matching 16-row H blocks (rows past the live ones read as zero) into
@@ -42,8 +39,7 @@
 namespace spec {
 
 constexpr int kSkTileRows = 128;  // weight rows per tile (MMA M)
-constexpr int kSkBoxRows = 32;    // rows per TMA box
-constexpr int kSkHalfRows = 16;   // rows of the half box that ends a run of 16-row bands
+constexpr int kSkBoxRows = 32;    // rows per TMA box (and the band of the block partition)
 constexpr int kSkN = 16;          // H rows per MMA (N); rows past the live ones are zero
 constexpr int kSkKBlock = 64;     // bf16 elements per k-block (one 128-byte swizzle row)
 constexpr int kSkKB = 4;          // k-blocks per stage: 512 contiguous bytes of each weight row
@@ -58,7 +54,6 @@ constexpr int kSkStatBytes = 1024;  // start of the idle ring: per-quadrant top-
 
 __global__ void __launch_bounds__(kSkThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                   const __grid_constant__ CUtensorMap wmap16,
                    const __grid_constant__ CUtensorMap hmap, const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -79,7 +74,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int64_t v0, v1;
-  block_rows(blockIdx.x, gridDim.x, p.nbands, p.band_rows, p.V, v0, v1);
+  block_rows(blockIdx.x, gridDim.x, p.nbands, kSkBoxRows, p.V, v0, v1);
   const int nt = static_cast<int>(v1 - v0);
   const int ntile = (nt + kSkTileRows - 1) / kSkTileRows;
   const int nkb = (p.d + kSkKBlock - 1) / kSkKBlock;  // k-blocks per row
@@ -105,41 +100,22 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       yb[b] = r < lo_rows ? r : r + hi_shift;
     }
   };
-  // A tile's boxes: its rows in 32-row boxes, except that rows ending 16 past a 32-row boundary
-  // end with one 16-row box (runs of 16-row bands balance the blocks to within 16 rows; the
-  // last block's rows end at V and a box reaching past V reads zeros there).
-  auto tile_boxes = [&](int rows, int& n32, bool& half) {
-    n32 = rows / kSkBoxRows;
-    const int rem = rows - n32 * kSkBoxRows;
-    half = rem > 0 && rem <= kSkHalfRows;
-    if (rem > kSkHalfRows) ++n32;
-  };
   auto issue_w = [&](int it, int s) {  // the weight boxes of iteration it into stage s
     const int t = it / nks, ks = it - t * nks;
     const int rows = min(kSkTileRows, nt - t * kSkTileRows);
-    int n32;
-    bool half;
-    tile_boxes(rows, n32, half);
+    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
     const int y = static_cast<int>(v0) + t * kSkTileRows;
     const int nk = min(kSkKB, nkb - ks * kSkKB);  // k-blocks in this stage
     uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
     int yb[kSkTileRows / kSkBoxRows];
     box_rows(y, yb);
-    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(
-                                        nk * (n32 * kSkBoxBytes + (half ? kSkBoxBytes / 2 : 0) +
-                                              kSkHBytes)));
-    for (int kk = 0; kk < nk; ++kk) {
-      const int x = (ks * kSkKB + kk) * kSkKBlock;
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
+    for (int kk = 0; kk < nk; ++kk)
 #pragma unroll
-      for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b) {
-        if (b < n32)
-          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, yb[b], &full[s],
-                              wpol);
-        else if (b == n32 && half)
-          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap16, x, yb[b], &full[s],
-                              wpol);
-      }
-    }
+      for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
+        if (b < nbox)
+          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
+                              (ks * kSkKB + kk) * kSkKBlock, yb[b], &full[s], wpol);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it into stage s
     const int t = it / nks, ks = it - t * nks;
@@ -155,28 +131,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   auto issue_all = [&](int it, int s) {
     const int t = it / nks, ks = it - t * nks;
     const int rows = min(kSkTileRows, nt - t * kSkTileRows);
-    int n32;
-    bool half;
-    tile_boxes(rows, n32, half);
+    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
     const int y = static_cast<int>(v0) + t * kSkTileRows;
     const int nk = min(kSkKB, nkb - ks * kSkKB);
     uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
     int yb[kSkTileRows / kSkBoxRows];
     box_rows(y, yb);
-    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(
-                                        nk * (n32 * kSkBoxBytes + (half ? kSkBoxBytes / 2 : 0) +
-                                              kSkHBytes)));
+    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
     for (int kk = 0; kk < nk; ++kk) {
       const int x = (ks * kSkKB + kk) * kSkKBlock;
 #pragma unroll
-      for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b) {
-        if (b < n32)
+      for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
+        if (b < nbox)
           tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, yb[b], &full[s],
                               wpol);
-        else if (b == n32 && half)
-          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap16, x, yb[b], &full[s],
-                              wpol);
-      }
       tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
     }
   };
@@ -387,7 +355,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 // Host side
 // ------------------------------------------------------------------------------------------
 
-int gemv_tc_band_rows() { return kSkHalfRows; }
+int gemv_tc_band_rows() { return kSkBoxRows; }
 int gemv_tc_box_rows() { return kSkBoxRows; }
 int gemv_tc_kblock() { return kSkKBlock; }
 int gemv_tc_h_rows() { return kSkN; }
@@ -404,8 +372,8 @@ cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, gemv_tc_kernel, kSkThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (fit < 1) return cudaErrorLaunchOutOfResources;
-  return launch_pdl(gemv_tc_kernel, dim3(L.grid), dim3(kSkThreads), L.smem, stream, L.wmap,
-                    L.wmap16, L.hmap, L.p);
+  return launch_pdl(gemv_tc_kernel, dim3(L.grid), dim3(kSkThreads), L.smem, stream, L.wmap, L.hmap,
+                    L.p);
 }
 
 }  // namespace spec

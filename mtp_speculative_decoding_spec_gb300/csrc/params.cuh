@@ -190,9 +190,8 @@ cudaError_t gemv_dispatch(const GemvLaunch& L, int rp, cudaStream_t stream);
 // Tensor-core variant of the 1..8-row projection for bf16 weights: see gemv_tc.cu.
 struct GemvTcLaunch {
   int grid, smem;
-  CUtensorMap wmap;    // W [V][d] bf16, box [32 rows][64], 128-byte swizzle
-  CUtensorMap wmap16;  // the same W, box [16 rows][64]: the half box ending a run
-  CUtensorMap hmap;    // H [nrows][d] bf16, box [16 rows][64], 128-byte swizzle
+  CUtensorMap wmap;  // W [V][d] bf16, box [32 rows][64], 128-byte swizzle
+  CUtensorMap hmap;  // H [nrows][d] bf16, box [16 rows][64], 128-byte swizzle
   GemvParams p;
 };
 
