@@ -769,8 +769,11 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
   p.k = k;
   p.mode = mode;
   p.commit_status = commit_status;
-  // blocks resident per SM: 4 for the copy, 2 for the replay (their launch bounds)
-  const int per_sm = (mode == SPEC_COMMIT_SNAPSHOT) ? 4 : 2;
+  // the replay stages a head's step inputs in at most 48 KB of shared memory
+  if (mode == SPEC_COMMIT_REPLAY && st->rec_layers > 0 && commit_replay_rows(*st) < 1)
+    return SPEC_ERR_UNSUPPORTED;
+  // blocks resident per SM: 4 for the copy, 3 for the replay (their launch bounds)
+  const int per_sm = (mode == SPEC_COMMIT_SNAPSHOT) ? 4 : 3;
   int per_req = (per_sm * a.sms + B - 1) / B;
   if (st->rec_layers == 0) per_req = 1;
   if (per_req < 1) per_req = 1;

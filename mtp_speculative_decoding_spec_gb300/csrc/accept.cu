@@ -518,25 +518,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   const int b = blockIdx.y, sl = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
-  if (!kFiltered && warp > 0 && gridDim.y <= 4 && p.logits) {
-    // While warp 0 takes the decision, the other warps pull this slice of every verify row
-    // (and of every draft row) into L1: the draw needs one of them, known only after the
-    // decision. With few requests this costs little L2 bandwidth and takes a round trip off
-    // the slice pass.
-    const int nq = (p.q_logits && p.q_lo == p.Vd) ? min(p.k_max, p.R) : 0;
-    const int lines = (p.R + nq) * (kAcceptSlice / 32);
-    for (int i = tid - 32; i < lines; i += kAcceptThreads - 32) {
-      const int row = i / (kAcceptSlice / 32);
-      const int64_t j = j0 + 32 * (i % (kAcceptSlice / 32));
-      const float* a = nullptr;
-      if (row < p.R) {
-        if (j < p.V) a = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V + j;
-      } else if (j < p.Vd) {
-        a = p.q_logits + (static_cast<size_t>(row - p.R) * p.B + b) * p.q_stride + j;
-      }
-      if (a) asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
-    }
-  }
   const int k = p.k[b];
   const float T = p.temperature[b];
 

@@ -228,6 +228,7 @@ int gemv_tc_stat_bytes();
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream);
 cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request,
                           cudaStream_t stream);
+int commit_replay_rows(const spec_state_desc& st);
 
 struct AdaptParams {
   int B, k_max;

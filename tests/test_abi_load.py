@@ -204,7 +204,7 @@ def test_no_cpu_fallback_in_product_package():
 # threads per block of each kernel, as launched by abi.cu / gemv.cu
 _BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemv_q4_kernel": 16 * 32, "gemm_rows_tc_kernel": 10 * 32,
                   "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_snapshot_kernel": 256,
-                  "commit_replay_kernel": 256, "adapt_width_kernel": 128}
+                  "commit_replay_kernel": 128, "adapt_width_kernel": 128}
 
 
 def test_register_budget_per_sub_partition(lib):
