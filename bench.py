@@ -271,9 +271,6 @@ def run_ours(args, rank, local_rank, world):
                          eng.out, eng.counters, eng.ws)
 
     K, Wm = args.steps, args.warmup
-    for c in range(Wm):
-        step(c % n_pool)
-    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -281,6 +278,12 @@ def run_ours(args, rank, local_rank, world):
     barrier()
     torch.cuda.synchronize()
     with clocks:
+        # the warm-up steps run after the clock sampler has started (it idles the GPU for a
+        # moment), right before the timed ones
+        for c in range(Wm):
+            step(c % n_pool)
+        torch.cuda.synchronize()
+        barrier()
         t_start.record(stream)
         for c in range(K):
             step(c % n_pool)
@@ -592,16 +595,19 @@ def sweep(dev, W, Wd, hbm_peak):
     return out
 
 
-def adaptive_bench(dev, W, Wd, step_us, draft_us, K=400):
+def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     """Adaptive verify width on the k-sweep's greedy workload: the width of every cycle is
-    chosen on the device (spec_adapt_width) from a cost table built from this run's measured
-    verify + acceptance step and draft step; k_max = 7 draft steps are enqueued per cycle and
-    those past the chosen width return at once. Compare with the sweep's fixed-width points."""
+    chosen on the device (spec_adapt_width) from the per-depth acceptance and the request's
+    cycle-cost fit (cycles timed on the device; a prior table from this run's measured verify
+    step and draft step until the fit is usable). One request: each cycle is a launch of the
+    width graph, whose select kernel picks the body of the chosen width (that many draft steps,
+    a verify of width + 1 rows, acceptance, next width); the cycle's inputs are copied into the
+    graph's input buffers first. Compared with every fixed width on the same inputs."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
     from mtp_speculative_decoding_spec_gb300.engine import SpecVerifyEngine
-    k_max, n_pool = 7, 32
+    k_max, n_pool = 7, 256
     cfg = configs.Config(**{**configs.get(2).__dict__, "k": k_max, "temps": (0.0,)})
     Hp, Hdp = build_inputs(cfg, W, n_pool, k_max, 0.0, rng_seed=7 * k_max)
     Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
@@ -630,8 +636,12 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=400):
            "final_width": int(st["k"]),
            "rates": [round(float(st["rate"][d]), 3) if (int(st["seen"]) >> d) & 1 else None
                      for d in range(1, k_max + 1)],
-           "cost": [round(x, 3) for x in cost],
-           "workload": "k = 7 greedy sweep inputs, k_max = 7 draft steps enqueued per cycle"}
+           "prior_cost": [round(x, 3) for x in cost],
+           "fitted_cost_ratio": round(float(st["rate"][0]), 4),
+           "fit_usable": bool(float(st["rate"][0]) > 0),
+           "mode": "width graph" if eng.width_graph else "k_max gated draft steps",
+           "workload": "k = 7 greedy sweep inputs (256 distinct cycles), k_max = 7"}
+    eng.close()
     del eng
     # every fixed width on the same inputs (the first k + 1 verify rows and k draft rows)
     fixed = {}

@@ -352,18 +352,22 @@ spec_status spec_accept_filtered(int32_t B, int32_t k_max, const int32_t *k,
 
 /* Adaptive width state of one request (64 bytes, zero-filled before the first cycle). */
 typedef struct {
-  float rate[8];    /* rate[d], d = 1..7: moving average of "draft d accepted, given 1..d-1 were" */
+  float rate[8];    /* rate[d], d = 1..7: moving average of "draft d accepted, given 1..d-1 were";
+                       rate[0]: the last usable fitted cost ratio b / a (0 = none yet) */
   uint32_t seen;    /* bit d set once depth d has been observed (until then it is believed to
-                       do as well as depth d - 1; depth 1 starts at 0.5) */
+                       do as well as depth d - 1; depth 1 starts at 0.5); bit 0 once the cost fit
+                       holds an observation */
   uint32_t cycles;  /* cycles observed */
   int32_t k;        /* the width chosen for the next cycle */
-  int32_t reserved[5];
+  uint32_t t_last;  /* %globaltimer / 1024 (ns) at the previous call that timed the cycle itself;
+                       0 = none */
+  float fit[4];     /* moving averages of k, k^2, cost and k * cost over the observed cycles */
 } spec_width_state;
 
 /*
  * spec_adapt_width -- choose each request's next verify width on the device (lucebox-hub PR
- * #15, "What" and "Speed": the default width is adaptive; the controller below is this
- * library's, the pages give none).
+ * #15, "What" and "Speed": the default width is adaptive, from per-depth acceptance and a
+ * per-request cycle-cost fit; the controller's form is this library's, the pages give none).
  *
  * From request b's result out[b] of a cycle run at width k_used[b]: depths 1..n_accept were
  * accepted, depth n_accept + 1 (if <= k_used and the block did not end at an accepted EOS) was
@@ -371,17 +375,50 @@ typedef struct {
  * alpha * (x - rate) (x = 1 accepted, 0 rejected). A depth not yet observed is believed to do
  * as well as the depth above it (0.5 for depth 1), so widths grow while drafts keep being
  * accepted; a depth observed before but not in this cycle relaxes by the same alpha towards
- * the belief of the depth above it, so a depth that looked poor is tried again. A request whose
- * status is not OK keeps its rates. Then, with E(k) = 1 + sum_{j<=k} prod_{i<=j} belief[i] the
- * expected tokens of a cycle at width k, the next width is the k in [1, k_max] maximising
- * E(k) / cost[k] (the smallest on ties; never 0, so depth 1 stays observed and a request whose
+ * the belief of the depth above it, so a depth that looked poor is tried again.
+ * The cycle's cost c (cycle_cost[b], or, when cycle_cost is NULL, the %globaltimer time since
+ * this request's previous call, in units of 1,024 ns) joins the request's cost fit c ~ a + b*k:
+ * the moving averages (rate alpha; the first observation sets them) of k, k^2, c and k*c give
+ * var = E[k^2] - E[k]^2, b = (E[kc] - E[k]E[c]) / var, a = E[c] - b E[k]. The fit is usable
+ * when var >= 1/4 and a, b > 0, and its ratio b / a is then kept in rate[0]; a cost above four
+ * times the usable fit's a + b*k is not folded in, nor a cost <= 0. A request whose status is
+ * not OK keeps its state (t_last still moves). Then, with E(k) = 1 + sum_{j<=k} prod_{i<=j}
+ * belief[i] the expected tokens of a cycle at width k and cost(k) = 1 + rate[0] * k once a
+ * ratio is kept (the caller's cost[k] before), the next width is the k in [1, k_max] maximising
+ * E(k) / cost(k) (the smallest on ties; never 0, so depth 1 stays observed and a request whose
  * drafts start failing can recover), written to k_next[b] and state[b].k.
- *   cost    [k_max + 1] float device array: the relative time of a cycle at each width.
- *   alpha   in (0, 1].  k_used and k_next may be the same array.
+ *   cost       [k_max + 1] float device array: the prior relative cost of a cycle at each width.
+ *   cycle_cost [B] float device array or NULL (measure on the device, see above).
+ *   alpha      in (0, 1].  k_used and k_next may be the same array.
  */
 spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out *out,
-                             const int32_t *k_used, const float *cost, float alpha,
-                             spec_width_state *state, int32_t *k_next, spec_stream_t stream);
+                             const int32_t *k_used, const float *cost, const float *cycle_cost,
+                             float alpha, spec_width_state *state, int32_t *k_next,
+                             spec_stream_t stream);
+
+/*
+ * Adaptive-width cycles as one CUDA graph (no counterpart on the pages: it lets the width
+ * chosen on the device decide how much work a cycle enqueues, with no host round trip and no
+ * idle draft steps).
+ *
+ * spec_width_graph_create builds a graph of two nodes: a select kernel that reads k_next[0..B)
+ * (B <= 128; the widths spec_adapt_width writes) when the graph runs and sets a switch to
+ * w = max_b k_next[b] clamped to [0, n_bodies - 1], then a CUDA switch node that runs body w.
+ * *graph receives the cudaGraph_t; bodies[0..n_bodies) the (empty) body graphs, each to be
+ * filled by capturing this library's calls on a stream between spec_graph_capture_begin and
+ * spec_graph_capture_end (a body for width w typically holds w draft steps, a verify of w + 1
+ * rows, the acceptance, the commit and spec_adapt_width). Then spec_graph_instantiate, and
+ * spec_graph_launch once per cycle; spec_graph_destroy releases both. The graph records the
+ * device pointers of every captured call: the buffers must stay in place while it is used.
+ * Errors: SPEC_ERR_INVALID for bad arguments, SPEC_ERR_CUDA if a CUDA graph call fails.
+ */
+spec_status spec_width_graph_create(int32_t n_bodies, const int32_t *k_next, int32_t B,
+                                    void **graph, void **bodies);
+spec_status spec_graph_capture_begin(void *body, spec_stream_t stream);
+spec_status spec_graph_capture_end(spec_stream_t stream);
+spec_status spec_graph_instantiate(void *graph, void **exec);
+spec_status spec_graph_launch(void *exec, spec_stream_t stream);
+spec_status spec_graph_destroy(void *graph, void *exec);
 
 /*
  * spec_commit_rollback -- keep the accepted prefix, drop the rest, on the device (DS4Server

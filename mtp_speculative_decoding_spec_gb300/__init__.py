@@ -104,10 +104,45 @@ def spec_accept(B, k_max, k, drafts, logits, stats, V, R, q_logits, q_stats, V_d
         _ptr(out), _ptr(counters), _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
-def spec_adapt_width(B, k_max, out, k_used, cost, alpha, state, k_next, stream=None):
+def spec_adapt_width(B, k_max, out, k_used, cost, cycle_cost, alpha, state, k_next,
+                     stream=None):
     _check("spec_adapt_width", _abi.lib().spec_adapt_width(
-        B, k_max, _ptr(out), _ptr(k_used), _ptr(cost), float(alpha), _ptr(state), _ptr(k_next),
-        _stream(stream)))
+        B, k_max, _ptr(out), _ptr(k_used), _ptr(cost), _ptr(cycle_cost), float(alpha),
+        _ptr(state), _ptr(k_next), _stream(stream)))
+
+
+def spec_width_graph_create(n_bodies, k_next, B):
+    """Returns (graph, [body graphs]) as integers (see include/spec.h)."""
+    import ctypes
+    g = ctypes.c_void_p()
+    bodies = (ctypes.c_void_p * n_bodies)()
+    _check("spec_width_graph_create", _abi.lib().spec_width_graph_create(
+        n_bodies, _ptr(k_next), B, ctypes.byref(g), bodies))
+    return g.value, [bodies[i] for i in range(n_bodies)]
+
+
+def spec_graph_capture_begin(body, stream):
+    _check("spec_graph_capture_begin", _abi.lib().spec_graph_capture_begin(body,
+                                                                           _stream(stream)))
+
+
+def spec_graph_capture_end(stream):
+    _check("spec_graph_capture_end", _abi.lib().spec_graph_capture_end(_stream(stream)))
+
+
+def spec_graph_instantiate(graph):
+    import ctypes
+    e = ctypes.c_void_p()
+    _check("spec_graph_instantiate", _abi.lib().spec_graph_instantiate(graph, ctypes.byref(e)))
+    return e.value
+
+
+def spec_graph_launch(exec_, stream=None):
+    _check("spec_graph_launch", _abi.lib().spec_graph_launch(exec_, _stream(stream)))
+
+
+def spec_graph_destroy(graph, exec_):
+    _check("spec_graph_destroy", _abi.lib().spec_graph_destroy(graph, exec_))
 
 
 def spec_accept_exact(B, k_max, k, drafts, logits, stats, V, R, temperature, eos_id, seed,

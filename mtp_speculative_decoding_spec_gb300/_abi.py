@@ -22,7 +22,9 @@ EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spe
            "spec_commit_rollback",
            "spec_batched_supported",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes",
-           "spec_noalloc_error_word", "spec_test_verify_stalled")
+           "spec_noalloc_error_word", "spec_test_verify_stalled",
+           "spec_width_graph_create", "spec_graph_capture_begin", "spec_graph_capture_end",
+           "spec_graph_instantiate", "spec_graph_launch", "spec_graph_destroy")
 
 # numpy views of the device structs (for reading results copied to the host)
 ROWSTATS_DTYPE = np.dtype([("max", "<f4"), ("log_norm", "<f4"), ("gap", "<f4"),
@@ -32,7 +34,7 @@ ACCEPT_OUT_DTYPE = np.dtype([("status", "<i4"), ("n_accept", "<i4"), ("n_emit", 
                              ("sample_kind", "<i4"), ("sample_row", "<i4"),
                              ("reserved", "<i4", (2,))])
 WIDTH_STATE_DTYPE = np.dtype([("rate", "<f4", (8,)), ("seen", "<u4"), ("cycles", "<u4"),
-                              ("k", "<i4"), ("reserved", "<i4", (5,))])
+                              ("k", "<i4"), ("t_last", "<u4"), ("fit", "<f4", (4,))])
 COUNTERS_DTYPE = np.dtype([("cycles", "<u8"), ("drafted", "<u8"), ("accepted", "<u8"),
                            ("emitted", "<u8"), ("eos", "<u8"), ("errors", "<u8"),
                            ("depth", "<u8", (8,))])
@@ -105,7 +107,7 @@ def lib():
         L.spec_accept_rows.argtypes = [i32, i32, vp, vp, vp, vp, i64, i32, vp, vp, i64, i64,
                                        i64, i64, vp, i32, vp, vp, vp, vp, vp, sz, vp]
         L.spec_accept_rows.restype = i32
-        L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+        L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.spec_adapt_width.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,
                                            vp]
@@ -119,5 +121,18 @@ def lib():
         L.spec_test_verify_stalled.argtypes = [vp, i64, i64, vp, i32, i32, vp, vp, vp,
                                                ctypes.c_uint32, vp, sz, vp]
         L.spec_test_verify_stalled.restype = i32
+        pvp = ctypes.POINTER(ctypes.c_void_p)
+        L.spec_width_graph_create.argtypes = [i32, vp, i32, pvp, pvp]
+        L.spec_width_graph_create.restype = i32
+        L.spec_graph_capture_begin.argtypes = [vp, vp]
+        L.spec_graph_capture_begin.restype = i32
+        L.spec_graph_capture_end.argtypes = [vp]
+        L.spec_graph_capture_end.restype = i32
+        L.spec_graph_instantiate.argtypes = [vp, pvp]
+        L.spec_graph_instantiate.restype = i32
+        L.spec_graph_launch.argtypes = [vp, vp]
+        L.spec_graph_launch.restype = i32
+        L.spec_graph_destroy.argtypes = [vp, vp]
+        L.spec_graph_destroy.restype = i32
         _lib = L
     return _lib

@@ -663,8 +663,9 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_
 }
 
 spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* out,
-                             const int32_t* k_used, const float* cost, float alpha,
-                             spec_width_state* state, int32_t* k_next, spec_stream_t stream) {
+                             const int32_t* k_used, const float* cost, const float* cycle_cost,
+                             float alpha, spec_width_state* state, int32_t* k_next,
+                             spec_stream_t stream) {
   if (B < 1 || k_max < 0 || k_max > kMaxRows - 1) return SPEC_ERR_INVALID;
   if (!out || !k_used || !cost || !state || !k_next) return SPEC_ERR_INVALID;
   if (!(alpha > 0.f && alpha <= 1.f)) return SPEC_ERR_INVALID;
@@ -674,6 +675,7 @@ spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* ou
   p.out = out;
   p.k_used = k_used;
   p.cost = cost;
+  p.cycle_cost = cycle_cost;
   p.alpha = alpha;
   p.state = state;
   p.k_next = k_next;
@@ -704,6 +706,92 @@ spec_status spec_accept_filtered(int32_t B, int32_t k_max, const int32_t* k,
   return spec::run_accept(B, k_max, k, drafts, logits, stats, V, R, nullptr, nullptr, 0, 0,
                           temperature, eos_id, seed, pos_base, out, counters, workspace,
                           workspace_bytes, stream, 0, top_k, top_p);
+}
+
+spec_status spec_width_graph_create(int32_t n_bodies, const int32_t* k_next, int32_t B,
+                                    void** graph, void** bodies) {
+  if (n_bodies < 1 || n_bodies > 64 || !k_next || B < 1 || B > 128 || !graph || !bodies)
+    return SPEC_ERR_INVALID;
+  cudaGraph_t g = nullptr;
+  if (cudaGraphCreate(&g, 0) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaGraphConditionalHandle h;
+  if (cudaGraphConditionalHandleCreate(&h, g, 0, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return SPEC_ERR_CUDA;
+  }
+  // node 1: the select kernel (sets the switch from the widths when the graph runs)
+  const int32_t* kn = k_next;
+  int nb = n_bodies, bb = B;
+  void* args[] = {&h, &kn, &bb, &nb};
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.func = const_cast<void*>(width_select_function());
+  kp.gridDim = dim3(1);
+  kp.blockDim = dim3(32);
+  kp.kernelParams = args;
+  cudaGraphNode_t sel;
+  if (cudaGraphAddKernelNode(&sel, g, nullptr, 0, &kp) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return SPEC_ERR_CUDA;
+  }
+  // node 2: the switch over the bodies
+  // (the struct's union has no default constructor: zeroed storage instead)
+  alignas(cudaGraphNodeParams) unsigned char cp_storage[sizeof(cudaGraphNodeParams)];
+  memset(cp_storage, 0, sizeof(cp_storage));
+  cudaGraphNodeParams& cp = *reinterpret_cast<cudaGraphNodeParams*>(cp_storage);
+  cp.type = cudaGraphNodeTypeConditional;
+  cp.conditional.handle = h;
+  cp.conditional.type = cudaGraphCondTypeSwitch;
+  cp.conditional.size = static_cast<unsigned>(n_bodies);
+  cudaGraphNode_t sw;
+  if (cudaGraphAddNode(&sw, g, &sel, nullptr, 1, &cp) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return SPEC_ERR_CUDA;
+  }
+  for (int i = 0; i < n_bodies; ++i) bodies[i] = cp.conditional.phGraph_out[i];
+  *graph = g;
+  return SPEC_OK;
+}
+
+spec_status spec_graph_capture_begin(void* body, spec_stream_t stream) {
+  if (!body || !stream) return SPEC_ERR_INVALID;  // the legacy stream cannot be captured
+  return cudaStreamBeginCaptureToGraph(reinterpret_cast<cudaStream_t>(stream),
+                                       static_cast<cudaGraph_t>(body), nullptr, nullptr, 0,
+                                       cudaStreamCaptureModeRelaxed) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+spec_status spec_graph_capture_end(spec_stream_t stream) {
+  if (!stream) return SPEC_ERR_INVALID;
+  cudaGraph_t g = nullptr;
+  return cudaStreamEndCapture(reinterpret_cast<cudaStream_t>(stream), &g) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+spec_status spec_graph_instantiate(void* graph, void** exec) {
+  if (!graph || !exec) return SPEC_ERR_INVALID;
+  cudaGraphExec_t e = nullptr;
+  if (cudaGraphInstantiate(&e, static_cast<cudaGraph_t>(graph), 0) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  *exec = e;
+  return SPEC_OK;
+}
+
+spec_status spec_graph_launch(void* exec, spec_stream_t stream) {
+  if (!exec) return SPEC_ERR_INVALID;
+  return cudaGraphLaunch(static_cast<cudaGraphExec_t>(exec),
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+spec_status spec_graph_destroy(void* graph, void* exec) {
+  bool ok = true;
+  if (exec) ok = cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(exec)) == cudaSuccess && ok;
+  if (graph) ok = cudaGraphDestroy(static_cast<cudaGraph_t>(graph)) == cudaSuccess && ok;
+  return ok ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status spec_test_verify_stalled(const void* W, int64_t V, int64_t d, const void* H,

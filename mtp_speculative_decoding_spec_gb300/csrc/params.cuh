@@ -235,10 +235,12 @@ struct AdaptParams {
   const spec_accept_out* out;
   const int32_t* k_used;
   const float* cost;
+  const float* cycle_cost;  // [B] or null: timed on the device
   float alpha;
   spec_width_state* state;
   int32_t* k_next;
 };
 cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream);
+const void* width_select_function();  // the select kernel of a width graph (see abi.cu)
 
 }  // namespace spec

@@ -5,6 +5,11 @@ PyTorch provides device memory and the stream; every step runs in libspec.so's k
 here reads a result back to the host except ``cycle_from_host``, which is the end-to-end path:
 it copies one cycle's inputs from pinned host memory, runs the cycle and copies the 64-byte
 results back, all asynchronously on the stream.
+
+In adaptive mode with one request the cycle is a CUDA graph (spec_width_graph_create): a
+select kernel reads the width the device chose and a switch runs the body captured for that
+width -- its draft steps, a verify of width + 1 rows, acceptance, commit and the next width --
+so the host never learns the width and no idle draft step is enqueued.
 """
 
 import torch
@@ -12,21 +17,28 @@ import torch
 from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_F32,
                WIDTH_STATE_BYTES, spec_accept, spec_accept_exact, spec_accept_filtered,
                spec_adapt_width,
-               spec_commit_rollback, spec_draft_argmax, spec_lmhead_verify,
+               spec_commit_rollback, spec_draft_argmax, spec_graph_capture_begin,
+               spec_graph_capture_end, spec_graph_destroy, spec_graph_instantiate,
+               spec_graph_launch, spec_lmhead_verify, spec_width_graph_create,
                spec_workspace_bytes)
 
 
 class SpecVerifyEngine:
     def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
-                 want_q_logits=True, acceptance="ratio", adaptive_cost=None, alpha=0.1):
+                 want_q_logits=True, acceptance="ratio", adaptive_cost=None, alpha=0.1,
+                 cycle_cost=None, width_graph=None):
         """acceptance: "ratio" (u*q <= p with residual correction; spec_accept), "exact"
         (a draft counts only if it is the trunk's own sample; spec_accept_exact) or "filtered"
         (the top-k / top-p filtered target of set_requests(top_k=..., top_p=...), argmax drafts
         and one-hot q; spec_accept_filtered; the draft steps then run at temperature 0).
-        adaptive_cost: None for fixed widths (set_requests(k=...)), or the relative cost of a
-        cycle at widths 0..k_max: each cycle then ends with spec_adapt_width choosing every
-        request's next width on the device, and ``cycle`` always enqueues k_max draft steps,
-        of which those past every request's width return at once."""
+        adaptive_cost: None for fixed widths (set_requests(k=...)), or the prior relative cost
+        of a cycle at widths 0..k_max: each cycle then ends with spec_adapt_width choosing every
+        request's next width on the device.
+        cycle_cost: in adaptive mode, a device tensor [B] of each cycle's measured cost for the
+        cost fit (the caller keeps it current), or None to time the cycles on the device.
+        width_graph: run adaptive cycles as a width graph (default: when B == 1); otherwise
+        ``cycle`` enqueues k_max draft steps, of which those past every request's width return
+        at once, and a verify of R rows."""
         if acceptance not in ("ratio", "exact", "filtered"):
             raise ValueError(
                 f"acceptance must be 'ratio', 'exact' or 'filtered', not {acceptance!r}")
@@ -63,6 +75,16 @@ class SpecVerifyEngine:
                 raise ValueError("adaptive_cost needs k_max + 1 entries")
             self.cost = torch.tensor(adaptive_cost, dtype=torch.float32, device=dev)
             self.width_state = torch.zeros(B * WIDTH_STATE_BYTES, dtype=torch.uint8, device=dev)
+        self.cycle_cost = cycle_cost
+        self.width_graph = self.adaptive and (B == 1 if width_graph is None else width_graph)
+        if self.width_graph and B != 1:
+            raise ValueError("width graphs run one request (the verify rows of a width are "
+                             "contiguous only for one)")
+        self.graph = self.graph_exec = None
+        if self.width_graph:
+            et = torch.float32 if wdt == SPEC_F32 else torch.int16
+            self.H_in = torch.zeros((k_max + 1, d), dtype=et, device=dev)
+            self.Hd_in = torch.zeros((max(k_max, 1), 1, d), dtype=et, device=dev)
 
     # ---------------------------------------------------------------- configuration
     def set_requests(self, temps=None, seeds=None, pos=None, k=None, top_k=None, top_p=None):
@@ -76,7 +98,7 @@ class SpecVerifyEngine:
         self.state, self.state_mode = desc, mode
 
     # ---------------------------------------------------------------- the cycle
-    def draft_step(self, i, h):
+    def draft_step(self, i, h, gate=True):
         """Draft i (1-based) for every request from draft-head hidden rows h [B, d]."""
         B = self.B
         temps = self.zero_temps if self.acceptance == "filtered" else self.temps
@@ -84,26 +106,27 @@ class SpecVerifyEngine:
                           self.pos, i - 1, self.drafts[:, i - 1:], self.drafts.shape[1],
                           None if self.q is None else self.q[(i - 1) * B:], self.Vd,
                           self.qs[(i - 1) * B * ROWSTATS_BYTES:],
-                          self.k if self.adaptive else None, self.ws)
+                          self.k if (self.adaptive and gate) else None, self.ws)
 
-    def verify(self, H):
-        spec_lmhead_verify(self.W, self.wdt, self.V, self.d, H, self.B, self.R, self.temps,
+    def verify(self, H, R=None):
+        spec_lmhead_verify(self.W, self.wdt, self.V, self.d, H, self.B, R or self.R, self.temps,
                            self.logits, self.stats, self.ws)
 
-    def accept(self, use_q=True):
+    def accept(self, use_q=True, R=None):
+        R = R or self.R
         if self.acceptance == "filtered":
             spec_accept_filtered(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats,
-                                 self.V, self.R, self.temps, self.top_k, self.top_p, self.eos_id,
+                                 self.V, R, self.temps, self.top_k, self.top_p, self.eos_id,
                                  self.seeds, self.pos, self.out, self.counters, self.ws)
             return
         if self.acceptance == "exact":
             spec_accept_exact(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats,
-                              self.V, self.R, self.temps, self.eos_id, self.seeds, self.pos,
+                              self.V, R, self.temps, self.eos_id, self.seeds, self.pos,
                               self.out, self.counters, self.ws)
             return
         q = self.q if (use_q and self.q is not None) else None
         spec_accept(self.B, self.k_max, self.k, self.drafts, self.logits, self.stats, self.V,
-                    self.R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
+                    R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
                     self.eos_id, self.seeds, self.pos, self.out, self.counters, self.ws)
 
     def commit(self):
@@ -113,8 +136,8 @@ class SpecVerifyEngine:
 
     def adapt(self):
         if self.adaptive:
-            spec_adapt_width(self.B, self.k_max, self.out, self.k, self.cost, self.alpha,
-                             self.width_state, self.k)
+            spec_adapt_width(self.B, self.k_max, self.out, self.k, self.cost, self.cycle_cost,
+                             self.alpha, self.width_state, self.k)
 
     def verify_cycle(self, H):
         """Verify + accept (+ commit, + the next width when adaptive): one verify cycle on
@@ -124,9 +147,61 @@ class SpecVerifyEngine:
         self.commit()
         self.adapt()
 
+    def _width_body(self, w):
+        """The cycle at width w (w >= 1), on the current stream: what a width graph's body w
+        holds (body 0, never chosen, runs width 1)."""
+        w = max(w, 1)
+        for i in range(1, w + 1):
+            self.draft_step(i, self.Hd_in[i - 1], gate=False)
+        self.verify(self.H_in[:w + 1], R=w + 1)
+        self.accept(R=w + 1)
+        self.commit()
+        self.adapt()
+
+    def _build_width_graph(self):
+        n = self.k_max + 1
+        if self.device.type == "cuda":  # capture on a stream of its own
+            torch.cuda.synchronize(self.device)
+            stream = torch.cuda.Stream(self.device)
+            stream.wait_stream(torch.cuda.current_stream(self.device))
+            ctx = torch.cuda.stream(stream)
+        else:  # the host-logic tests, whose library calls are recorded rather than run
+            import contextlib
+            stream, ctx = None, contextlib.nullcontext()
+        self.graph, bodies = spec_width_graph_create(n, self.k, self.B)
+        with ctx:
+            for w in range(n):
+                spec_graph_capture_begin(bodies[w], stream)
+                try:
+                    self._width_body(w)
+                finally:
+                    spec_graph_capture_end(stream)
+        self.graph_exec = spec_graph_instantiate(self.graph)
+
+    def close(self):
+        """Release the width graph, if any (the engine's tensors are freed by PyTorch)."""
+        if self.graph is not None:
+            spec_graph_destroy(self.graph, self.graph_exec)
+            self.graph = self.graph_exec = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may be gone already
+            pass
+
     def cycle(self, H, Hd, k):
-        """Full cycle: k draft steps (Hd [k, B, d]; k_max of them when adaptive), verify,
-        accept, commit."""
+        """Full cycle: k draft steps (Hd [k, B, d]), verify, accept, commit. Adaptive: the
+        width chosen on the device; H holds k_max + 1 rows and Hd k_max rows, of which the
+        width's first ones are used (a width graph), or k_max draft steps are enqueued, those
+        past every request's width returning at once."""
+        if self.width_graph:
+            if self.graph_exec is None:
+                self._build_width_graph()
+            self.H_in[:H.shape[0]].copy_(H.reshape(H.shape[0], -1))
+            self.Hd_in[:Hd.shape[0]].copy_(Hd.reshape(Hd.shape[0], 1, -1))
+            spec_graph_launch(self.graph_exec)
+            return
         for i in range(1, (self.k_max if self.adaptive else k) + 1):
             self.draft_step(i, Hd[i - 1])
         self.verify_cycle(H)

@@ -33,9 +33,24 @@ bonus); the next width is the k in [1, k_max] maximising E(k) / cost[k], the sma
 The width never drops to 0: at least the first draft is always tried, so depth 1 stays observed
 and a request whose drafts start failing can recover (at width 0 nothing would be observed).
 
+Per-request cycle-cost fit (same page, *What*: the width comes "from per-depth acceptance and
+a per-request cycle-cost fit"; the fit's form is this build's reading). A cycle at width k costs
+about a + b*k: a for the verify and acceptance, b for each draft step. Each observed cycle (its
+width k and its measured cost c > 0, status OK) moves the moving averages of k, k^2, c and k*c
+by alpha (the first observation sets them), which is exponentially weighted least squares:
+    var = E[k^2] - E[k]^2,  b = (E[k c] - E[k] E[c]) / var,  a = E[c] - b E[k].
+The fit is used when the widths have varied enough to separate the two terms (var >= 1/4) and
+a, b > 0; its ratio b / a is then kept, so that once the width settles (var decays) the last
+fitted shape still applies. Without a usable fit, and before any, the caller's cost table is
+the prior. A measured cost above four times the fitted one (a host pause between cycles) is
+not folded in.
+
 Pinned by: E(k) against exhaustive enumeration of the 2^k accept/reject patterns with those
 rates, and against a Monte Carlo of the acceptance chain; the EMA against its closed form; the
-choice at the corner cases (rates 1 -> k_max, rates 0 -> 1, flat cost -> the largest width).
+choice at the corner cases (rates 1 -> k_max, rates 0 -> 1, flat cost -> the largest width);
+the fit against exact linear costs (a and b recovered), against numpy's weighted least squares
+with the same exponential weights, and its fallbacks (one width only -> the prior; a settled
+width -> the kept ratio).
 """
 
 import numpy as np
@@ -44,8 +59,54 @@ PRIOR = 0.5
 STATUS_OK = 0
 
 
+VAR_MIN = 0.25    # widths must have varied at least this much (variance of k) for a fit
+OUTLIER = 4.0     # a cost above OUTLIER times the fitted one is not folded in
+
+
 def new_state(k_max=7):
-    return {"rate": [None] * (k_max + 1), "cycles": 0}
+    return {"rate": [None] * (k_max + 1), "cycles": 0, "fit": None, "ratio": 0.0}
+
+
+def fit_model(state):
+    """(a, b) of the current fit, or None when it is not usable (see the module doc)."""
+    fit = state["fit"]
+    if fit is None:
+        return None
+    mk, mkk, mc, mkc = fit
+    var = mkk - mk * mk
+    if not var >= VAR_MIN:
+        return None
+    b = (mkc - mk * mc) / var
+    a = mc - b * mk
+    if not (a > 0 and b > 0):
+        return None
+    return a, b
+
+
+def observe_cost(state, status, k, cost, alpha):
+    """Fold one cycle's measured cost at width k into the fit (status OK and cost > 0)."""
+    if status != STATUS_OK or not cost > 0:
+        return state
+    x = [float(k), float(k * k), float(cost), float(k * cost)]
+    if state["fit"] is None:
+        state["fit"] = x
+    else:
+        model = fit_model(state)
+        if model is not None and cost > OUTLIER * (model[0] + model[1] * k):
+            return state
+        state["fit"] = [m + alpha * (xi - m) for m, xi in zip(state["fit"], x)]
+    model = fit_model(state)
+    if model is not None:
+        state["ratio"] = model[1] / model[0]
+    return state
+
+
+def costs(state, prior, k_max):
+    """The cost of a cycle at each width 0..k_max: 1 + ratio * k from the fit (its last usable
+    shape), else the caller's prior table."""
+    if state["ratio"] > 0:
+        return [1.0 + state["ratio"] * k for k in range(k_max + 1)]
+    return [float(c) for c in prior[:k_max + 1]]
 
 
 def observe(state, status, n_accept, eos_hit, k, alpha):
@@ -93,8 +154,10 @@ def expected_tokens(rate, k):
 
 def choose(state, cost, k_max):
     """The width in [min(1, k_max), k_max] with the most expected tokens per unit of cost
-    (smallest on ties). Returns (k, values) with values[k] for every k in [0, k_max]."""
+    (smallest on ties), the cost being the fitted one when the state holds a usable fit and
+    the table ``cost`` otherwise. Returns (k, values) with values[k] for every k in [0, k_max]."""
     r = rates(state)
+    cost = costs(state, cost, k_max) if "ratio" in state else cost
     vals = [expected_tokens(r, k) / cost[k] for k in range(k_max + 1)]
     lo = min(1, k_max)
     best = max(range(lo, k_max + 1), key=lambda k: (vals[k], -k))

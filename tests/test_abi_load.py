@@ -129,11 +129,21 @@ def test_host_validation_of_the_later_entry_points(lib):
     assert lib.spec_accept_filtered(1, 3, fake, fake, fake, fake, 10, 4, fake, fake, null, 2,
                                     fake, fake, fake, null, fake, 1 << 20, null) == 1
     # adaptive width: sizes, pointers, and alpha in (0, 1]
-    assert lib.spec_adapt_width(0, 7, fake, fake, fake, 0.1, fake, fake, null) == 1
-    assert lib.spec_adapt_width(1, 8, fake, fake, fake, 0.1, fake, fake, null) == 1
-    assert lib.spec_adapt_width(1, 7, fake, fake, null, 0.1, fake, fake, null) == 1
-    assert lib.spec_adapt_width(1, 7, fake, fake, fake, 0.0, fake, fake, null) == 1
-    assert lib.spec_adapt_width(1, 7, fake, fake, fake, 1.5, fake, fake, null) == 1
+    assert lib.spec_adapt_width(0, 7, fake, fake, fake, null, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 8, fake, fake, fake, null, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, null, null, 0.1, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, fake, null, 0.0, fake, fake, null) == 1
+    assert lib.spec_adapt_width(1, 7, fake, fake, fake, fake, 1.5, fake, fake, null) == 1
+    # width graphs: 1..64 bodies, 1..128 requests, the widths and both outputs required
+    import ctypes
+    g, bodies = ctypes.c_void_p(), (ctypes.c_void_p * 8)()
+    assert lib.spec_width_graph_create(0, fake, 1, ctypes.byref(g), bodies) == 1
+    assert lib.spec_width_graph_create(8, fake, 129, ctypes.byref(g), bodies) == 1
+    assert lib.spec_width_graph_create(8, null, 1, ctypes.byref(g), bodies) == 1
+    assert lib.spec_graph_capture_begin(null, fake) == 1
+    assert lib.spec_graph_capture_begin(fake, null) == 1  # the legacy stream cannot capture
+    assert lib.spec_graph_instantiate(null, ctypes.byref(g)) == 1
+    assert lib.spec_graph_launch(null, null) == 1
     # two-range draft set: the second range may not start inside the first, the set may not be
     # empty; a split set needs tensor-core weights and whole 32-row boxes
     rows = lib.spec_draft_argmax_rows
@@ -204,7 +214,8 @@ def test_no_cpu_fallback_in_product_package():
 # threads per block of each kernel, as launched by abi.cu / gemv.cu
 _BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemv_q4_kernel": 16 * 32, "gemm_rows_tc_kernel": 10 * 32,
                   "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_snapshot_kernel": 256,
-                  "commit_replay_kernel": 128, "adapt_width_kernel": 128}
+                  "commit_replay_kernel": 128, "adapt_width_kernel": 128,
+                  "width_select_kernel": 32}
 
 
 def test_register_budget_per_sub_partition(lib):

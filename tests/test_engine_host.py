@@ -22,15 +22,28 @@ def calls(monkeypatch):
         return f
 
     for name in ("spec_draft_argmax", "spec_lmhead_verify", "spec_accept", "spec_accept_exact",
-                 "spec_accept_filtered", "spec_commit_rollback", "spec_adapt_width"):
+                 "spec_accept_filtered", "spec_commit_rollback", "spec_adapt_width",
+                 "spec_graph_capture_begin", "spec_graph_capture_end", "spec_graph_launch",
+                 "spec_graph_destroy"):
         monkeypatch.setattr(eng_mod, name, rec(name))
+
+    def create(n, k_next, B_):
+        log.append(("spec_width_graph_create", (n, k_next, B_)))
+        return 1000, [2000 + i for i in range(n)]
+
+    def instantiate(g):
+        log.append(("spec_graph_instantiate", (g,)))
+        return 3000
+
+    monkeypatch.setattr(eng_mod, "spec_width_graph_create", create)
+    monkeypatch.setattr(eng_mod, "spec_graph_instantiate", instantiate)
     monkeypatch.setattr(eng_mod, "spec_workspace_bytes", lambda V_, B_: 4096)
     return log
 
 
-def _engine(**kw):
+def _engine(b=B, **kw):
     W = torch.zeros((V, d), dtype=torch.float32)
-    return eng_mod.SpecVerifyEngine(W, spec.SPEC_F32, V, d, Vd, B, R, K_MAX, eos_id=2,
+    return eng_mod.SpecVerifyEngine(W, spec.SPEC_F32, V, d, Vd, b, R, K_MAX, eos_id=2,
                                     device="cpu", **kw)
 
 
@@ -82,9 +95,45 @@ def test_adaptive_enqueues_every_draft_step_and_the_width_update(calls):
     for _, a in calls[:K_MAX]:
         assert a[15] is e.k                       # steps past a request's width return at once
     ad = calls[-1][1]
-    assert ad[3] is e.k and ad[7] is e.k          # widths read and written in place
+    assert ad[3] is e.k and ad[8] is e.k          # widths read and written in place
+    assert ad[4] is e.cost and ad[5] is None      # the prior table; cycles timed on the device
     with pytest.raises(ValueError):
         _engine(adaptive_cost=[1.0, 2.0])         # needs k_max + 1 entries
+    with pytest.raises(ValueError):
+        _engine(adaptive_cost=[1.0, 1.5, 2.0, 2.5], width_graph=True)  # one request only
+
+
+def test_adaptive_single_request_runs_a_width_graph(calls):
+    """One request: the first cycle captures one body per width -- w draft steps (no gate), a
+    verify and an acceptance of w + 1 rows, the width update -- and every cycle launches the
+    graph; no call is enqueued outside it."""
+    e = _engine(b=1, adaptive_cost=[1.0, 1.5, 2.0, 2.5])
+    H, Hd = torch.ones((K_MAX + 1, d)), torch.ones((K_MAX, 1, d))
+    e.cycle(H, Hd, K_MAX)
+    names = _names(calls)
+    assert names[0] == "spec_width_graph_create" and calls[0][1][0] == K_MAX + 1
+    assert calls[0][1][1] is e.k                  # the select kernel reads the chosen widths
+    assert names[-2:] == ["spec_graph_instantiate", "spec_graph_launch"]
+    bodies = names[1:-2]
+    i = 0
+    for w in range(K_MAX + 1):
+        ww = max(w, 1)
+        assert bodies[i] == "spec_graph_capture_begin" and calls[1 + i][1][0] == 2000 + w
+        body = bodies[i + 1:i + 1 + ww + 4]
+        assert body == ["spec_draft_argmax"] * ww + ["spec_lmhead_verify", "spec_accept",
+                                                    "spec_adapt_width",
+                                                    "spec_graph_capture_end"]
+        for j in range(ww):
+            assert calls[2 + i + j][1][15] is None  # the body is the width: no gate
+        assert calls[2 + i + ww][1][6] == ww + 1    # verify of w + 1 rows
+        assert calls[2 + i + ww + 1][1][7] == ww + 1
+        i += ww + 5
+    assert torch.equal(e.H_in, H) and torch.equal(e.Hd_in, Hd)
+    calls.clear()
+    e.cycle(H, Hd, K_MAX)
+    assert _names(calls) == ["spec_graph_launch"]
+    e.close()
+    assert _names(calls)[-1] == "spec_graph_destroy"
 
 
 def test_commit_only_with_attached_state(calls):

@@ -6,8 +6,11 @@ spec_draft_argmax, through the C ABI) against the oracle's ``adapt`` module.
   and the same next width except where two widths' values are within 1e-5 (counted).
 * The gate: a draft step no request needs writes nothing; one that some need gives those
   requests the tokens an ungated call gives.
-* The engine in adaptive mode at C0: the widths it chooses over 40 cycles equal an oracle
-  replay of the acceptance results it produced.
+* The cost fit: the kernel's moving averages and fitted ratio against the oracle's, with
+  explicit per-request cycle costs (noise, missing costs, host pauses).
+* The engine in adaptive mode at C0, as a width graph and as gated draft steps: identical
+  results cycle for cycle, and widths equal to an oracle replay of those results; with no
+  cost given, the graph's cycles are timed on the device.
 """
 
 import numpy as np
@@ -30,6 +33,9 @@ def _near_tie(vals, k):
 
 
 def test_width_kernel_against_oracle():
+    """Rates, cost fit and next width over 60 cycles of synthetic results and measured costs
+    (each request its own a + b*k with noise, some failed cycles, some without a cost, one host
+    pause per request) against the float64 oracle."""
     ensure_built()
     rng = np.random.default_rng(5)
     B, k_max, alpha = 16, 7, 0.15
@@ -38,10 +44,13 @@ def test_width_kernel_against_oracle():
     state = zeros_bytes(B * spec.WIDTH_STATE_BYTES)
     ref = [o_adapt.new_state(k_max) for _ in range(B)]
     k_next = torch.zeros(B, dtype=torch.int32, device=dev())
-    near = 0
+    ca = rng.uniform(80, 160, B)
+    cb = rng.uniform(20, 80, B)
+    near = fitted = 0
     for c in range(60):
         k_used = rng.integers(0, k_max + 1, B).astype(np.int32)
         out = np.zeros(B, dtype=spec.ACCEPT_OUT_DTYPE)
+        cyc = np.zeros(B, dtype=np.float32)
         for b in range(B):
             k = int(k_used[b])
             out[b]["status"] = 0 if rng.random() < 0.9 else 1
@@ -49,8 +58,13 @@ def test_width_kernel_against_oracle():
             out[b]["n_accept"] = n_acc
             out[b]["eos_hit"] = int(n_acc > 0 and rng.random() < 0.1)
             out[b]["n_emit"] = n_acc + (0 if out[b]["eos_hit"] else 1)
+            cyc[b] = ca[b] + cb[b] * k + rng.normal(0, 3.0)
+            if rng.random() < 0.05:
+                cyc[b] = 0.0  # no measurement
+            if c == 40 + b % 10:
+                cyc[b] *= 10.0  # a host pause between two cycles
         spec.spec_adapt_width(B, k_max, to_dev(out.view(np.uint8)), to_dev(k_used), cost_d,
-                              alpha, state, k_next)
+                              to_dev(cyc), alpha, state, k_next)
         torch.cuda.synchronize()
         st = to_np(state, spec.WIDTH_STATE_DTYPE)
         kn = to_np(k_next)
@@ -58,6 +72,7 @@ def test_width_kernel_against_oracle():
             o = out[b]
             o_adapt.observe(ref[b], int(o["status"]), int(o["n_accept"]), bool(o["eos_hit"]),
                             int(k_used[b]), alpha)
+            o_adapt.observe_cost(ref[b], int(o["status"]), int(k_used[b]), float(cyc[b]), alpha)
             kb, vals = o_adapt.choose(ref[b], cost.astype(np.float64), k_max)
             for d in range(1, k_max + 1):
                 seen = bool((int(st[b]["seen"]) >> d) & 1)
@@ -65,11 +80,19 @@ def test_width_kernel_against_oracle():
                 if seen:
                     assert abs(float(st[b]["rate"][d]) - ref[b]["rate"][d]) < 1e-5, (c, b, d)
             assert int(st[b]["cycles"]) == ref[b]["cycles"]
+            assert bool(int(st[b]["seen"]) & 1) == (ref[b]["fit"] is not None), (c, b)
+            if ref[b]["fit"] is not None:
+                assert np.allclose(st[b]["fit"], ref[b]["fit"], rtol=1e-4), (c, b)
+            assert (float(st[b]["rate"][0]) > 0) == (ref[b]["ratio"] > 0), (c, b)
+            if ref[b]["ratio"] > 0:
+                fitted += 1
+                assert abs(float(st[b]["rate"][0]) - ref[b]["ratio"]) <= 1e-3 * ref[b]["ratio"]
             if _near_tie(vals, kb):
                 near += 1
                 continue
             assert int(kn[b]) == kb == int(st[b]["k"]), (c, b)
     assert near < 60 * B // 10
+    assert fitted > 40 * B  # the fit is in use for most of the run
 
 
 @pytest.fixture(scope="module")
@@ -110,27 +133,64 @@ def test_draft_width_gate(c0):
     assert int(to_np(got)[0]) == int(to_np(ref)[0]) >= 0
 
 
+def _adaptive_engine(cfg, Wd, cost, alpha, graph, cycle_cost):
+    eng = SpecVerifyEngine(Wd, wdt_of(cfg), cfg.V, cfg.d, cfg.Vd, 1, cfg.k + 1, cfg.k,
+                           cfg.eos_id, device=dev(), adaptive_cost=cost, alpha=alpha,
+                           cycle_cost=cycle_cost, width_graph=graph)
+    eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[cfg.k])
+    return eng
+
+
 def test_engine_adaptive_widths_replay(c0):
+    """The engine's adaptive cycles, as a width graph (the device-chosen width's body: its draft
+    steps, a verify of width + 1 rows, acceptance, next width) and as k_max gated draft steps
+    with a verify of k_max + 1 rows: the same results cycle for cycle, and widths equal to an
+    oracle replay of those results (no measured costs: the prior cost table decides)."""
     cfg, W, Wd = c0
-    k_max, B, alpha = cfg.k, 1, 0.2
+    k_max, alpha = cfg.k, 0.2
     cost = [1.0 + 0.25 * k for k in range(k_max + 1)]
-    eng = SpecVerifyEngine(Wd, wdt_of(cfg), cfg.V, cfg.d, cfg.Vd, B, k_max + 1, k_max,
-                           cfg.eos_id, device=dev(), adaptive_cost=cost, alpha=alpha)
-    eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[k_max])
+    zero = torch.zeros(1, dtype=torch.float32, device=dev())
+    engs = {"graph": _adaptive_engine(cfg, Wd, cost, alpha, True, zero),
+            "gated": _adaptive_engine(cfg, Wd, cost, alpha, False, zero)}
     ref = o_adapt.new_state(k_max)
     widths = []
     for c in range(40):
         inp = gen.cycle_inputs(cfg, W, c, seed=21, k=k_max)
-        k_used = int(to_np(eng.k)[0])
-        eng.cycle(to_dev(inp["H"]), to_dev(inp["Hd"])[:, None, :], k_max)
-        torch.cuda.synchronize()
-        o = to_np(eng.out, spec.ACCEPT_OUT_DTYPE)[0]
-        assert o["status"] == 0 and o["n_accept"] <= k_used
-        o_adapt.observe(ref, 0, int(o["n_accept"]), bool(o["eos_hit"]), k_used, alpha)
+        res = {}
+        for name, eng in engs.items():
+            k_used = int(to_np(eng.k)[0])
+            eng.cycle(to_dev(inp["H"]), to_dev(inp["Hd"])[:, None, :], k_max)
+            torch.cuda.synchronize()
+            res[name] = (k_used, to_np(eng.out, spec.ACCEPT_OUT_DTYPE)[0].copy(),
+                         int(to_np(eng.k)[0]))
+        (kg, og, ng), (kt, ot, nt) = res["graph"], res["gated"]
+        assert kg == kt and ng == nt and og.tobytes() == ot.tobytes(), c
+        assert og["status"] == 0 and og["n_accept"] <= kg
+        o_adapt.observe(ref, 0, int(og["n_accept"]), bool(og["eos_hit"]), kg, alpha)
         kb, vals = o_adapt.choose(ref, [float(x) for x in cost], k_max)
-        k_new = int(to_np(eng.k)[0])
         if not _near_tie(vals, kb):
-            assert k_new == kb, c
-        widths.append(k_new)
+            assert ng == kb, c
+        widths.append(ng)
+    cg = to_np(engs["graph"].counters, spec.COUNTERS_DTYPE)[0]
+    ct = to_np(engs["gated"].counters, spec.COUNTERS_DTYPE)[0]
+    assert cg.tobytes() == ct.tobytes()
     print(f"\nC0 adaptive widths: {widths}")
-    assert len(set(widths)) >= 1
+    for eng in engs.values():
+        eng.close()
+
+
+def test_engine_width_graph_times_its_cycles(c0):
+    """With no cost given, the width kernel times the cycles on the device: after cycles at
+    several widths the request's fit holds finite moving averages and the last timestamp."""
+    cfg, W, Wd = c0
+    eng = _adaptive_engine(cfg, Wd, [1.0 + 0.25 * k for k in range(cfg.k + 1)], 0.3, True,
+                           None)
+    for c in range(30):
+        inp = gen.cycle_inputs(cfg, W, c, seed=22, k=cfg.k)
+        eng.cycle(to_dev(inp["H"]), to_dev(inp["Hd"])[:, None, :], cfg.k)
+    torch.cuda.synchronize()
+    st = to_np(eng.width_state, spec.WIDTH_STATE_DTYPE)[0]
+    assert int(st["seen"]) & 1 and int(st["t_last"]) != 0
+    assert np.isfinite(st["fit"]).all() and st["fit"][2] > 0  # mean cycle cost > 0
+    assert np.isfinite(st["rate"]).all()
+    eng.close()

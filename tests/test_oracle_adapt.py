@@ -109,3 +109,86 @@ def test_choice_corner_cases():
     st["rate"] = [None] + [0.2] * 7
     assert adapt.choose(st, flat, 7)[0] == 7  # more width never loses when it costs nothing
     assert adapt.choose(st, flat, 3)[0] == 3
+
+
+# ---------------------------------------------------------------- the per-request cost fit
+
+def _feed(st, ks, cs, alpha):
+    for k, c in zip(ks, cs):
+        adapt.observe_cost(st, 0, k, c, alpha)
+
+
+def test_cost_fit_recovers_exact_linear_costs():
+    """Costs exactly a + b*k at varying widths: the moving-average regression returns a and b
+    whatever the weights (the covariance is b times the variance for any weighting)."""
+    st = adapt.new_state()
+    ks = [1, 5, 2, 7, 3, 6, 4] * 6
+    _feed(st, ks, [113.0 + 61.5 * k for k in ks], 0.1)
+    a, b = adapt.fit_model(st)
+    assert a == pytest.approx(113.0, rel=1e-9) and b == pytest.approx(61.5, rel=1e-9)
+    assert st["ratio"] == pytest.approx(61.5 / 113.0, rel=1e-9)
+    assert adapt.costs(st, [9.0] * 8, 7)[3] == pytest.approx(1 + 3 * 61.5 / 113.0, rel=1e-9)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_cost_fit_equals_weighted_least_squares(seed):
+    """The moving averages are least squares with weights (1 - alpha)^(n-1) on the first
+    observation and alpha (1 - alpha)^(n-1-i) on observation i: numpy's weighted polyfit with
+    those weights gives the same line."""
+    rng = np.random.default_rng(seed)
+    alpha, n = 0.1, 60
+    ks = rng.integers(1, 8, n)
+    cs = 120.0 + 60.0 * ks + rng.normal(0, 8.0, n)
+    st = adapt.new_state()
+    _feed(st, ks, cs, alpha)
+    w = np.array([(1 - alpha) ** (n - 1)] + [alpha * (1 - alpha) ** (n - 1 - i)
+                                             for i in range(1, n)])
+    b, a = np.polyfit(ks.astype(float), cs, 1, w=np.sqrt(w))
+    fa, fb = adapt.fit_model(st)
+    assert fa == pytest.approx(a, rel=1e-9) and fb == pytest.approx(b, rel=1e-9)
+
+
+def test_cost_fit_fallbacks():
+    prior = [1.0 + 0.5 * k for k in range(8)]
+    st = adapt.new_state()
+    _feed(st, [3] * 20, [300.0] * 20, 0.1)  # one width only: nothing to separate a from b
+    assert adapt.fit_model(st) is None and adapt.costs(st, prior, 7) == prior
+    adapt.observe_cost(st, 1, 5, 500.0, 0.1)  # a failed cycle is not folded in
+    adapt.observe_cost(st, 0, 5, 0.0, 0.1)    # nor a cycle without a measured cost
+    assert st["fit"] == [3.0, 9.0, 300.0, 900.0]
+    st = adapt.new_state()
+    _feed(st, [1, 7] * 10, [100.0 + 50.0 * k for k in [1, 7] * 10], 0.2)
+    assert adapt.fit_model(st) is not None
+    kept = st["ratio"]
+    assert kept == pytest.approx(0.5, rel=1e-9)
+    _feed(st, [4] * 60, [300.0] * 60, 0.2)  # the width settles: the variance decays
+    assert adapt.fit_model(st) is None
+    assert adapt.costs(st, prior, 7)[2] == pytest.approx(1 + 2 * kept, rel=1e-9)
+
+
+def test_cost_fit_skips_outliers():
+    st = adapt.new_state()
+    ks = [1, 7, 3, 5] * 5
+    _feed(st, ks, [100.0 + 50.0 * k for k in ks], 0.2)
+    before = list(st["fit"])
+    adapt.observe_cost(st, 0, 3, 4.5 * (100.0 + 150.0), 0.2)  # a host pause between cycles
+    assert st["fit"] == before
+    adapt.observe_cost(st, 0, 3, 3.5 * (100.0 + 150.0), 0.2)  # slow, but within the bound
+    assert st["fit"] != before
+
+
+def test_choice_follows_the_fitted_cost():
+    """With every depth accepted at 0.9, a prior that makes draft steps cheap picks the widest
+    width; a fit saying a draft step costs as much as the rest of the cycle picks fewer."""
+    st = adapt.new_state()
+    for _ in range(80):
+        adapt.observe(st, 0, 7, False, 7, 0.1)
+    st["rate"] = [None] + [0.9] * 7
+    cheap = [1.0 + 0.01 * k for k in range(8)]
+    assert adapt.choose(st, cheap, 7)[0] == 7
+    ks = [1, 7, 2, 6] * 10
+    _feed(st, ks, [100.0 + 100.0 * k for k in ks], 0.1)
+    k, vals = adapt.choose(st, cheap, 7)
+    e = [adapt.expected_tokens([0.0] + [0.9] * 7, kk) / (1 + kk) for kk in range(8)]
+    assert k == max(range(1, 8), key=lambda kk: (e[kk], -kk))
+    assert k < 7
