@@ -366,8 +366,9 @@ typedef struct {
 
 /*
  * spec_adapt_width -- choose each request's next verify width on the device (lucebox-hub PR
- * #15, "What" and "Speed": the default width is adaptive, from per-depth acceptance and a
- * per-request cycle-cost fit; the controller's form is this library's, the pages give none).
+ * #15, "What" and "Speed": the default width adapts, following the acceptance seen at each
+ * draft depth and a fit of the request's cycle cost; the controller's form is this library's,
+ * the pages give none).
  *
  * From request b's result out[b] of a cycle run at width k_used[b]: depths 1..n_accept were
  * accepted, depth n_accept + 1 (if <= k_used and the block did not end at an accepted EOS) was

@@ -33,8 +33,9 @@ bonus); the next width is the k in [1, k_max] maximising E(k) / cost[k], the sma
 The width never drops to 0: at least the first draft is always tried, so depth 1 stays observed
 and a request whose drafts start failing can recover (at width 0 nothing would be observed).
 
-Per-request cycle-cost fit (same page, *What*: the width comes "from per-depth acceptance and
-a per-request cycle-cost fit"; the fit's form is this build's reading). A cycle at width k costs
+Per-request cycle-cost fit (same page, *What*: besides the acceptance seen at each draft depth,
+the width follows a fit of what a cycle costs for that request; the fit's form is this build's
+reading). A cycle at width k costs
 about a + b*k: a for the verify and acceptance, b for each draft step. Each observed cycle (its
 width k and its measured cost c > 0, status OK) moves the moving averages of k, k^2, c and k*c
 by alpha (the first observation sets them), which is exponentially weighted least squares:
