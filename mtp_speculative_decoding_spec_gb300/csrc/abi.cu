@@ -230,11 +230,12 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
   const int64_t nbands = (V + band - 1) / band;
   const int tile_cap = static_cast<int>(((nbands + grid - 1) / grid) * band);
   if (tile_cap > gemv_q4_max_block_rows()) return SPEC_ERR_UNSUPPORTED;
+  const size_t h_bytes = align_up(gemv_q4_h_bytes(static_cast<int>(d)), 1024);
   const size_t after =
       static_cast<size_t>(gemv_q4_stat_bytes()) + gemv_finish_scratch_bytes(grid);
-  const size_t fixed = gemv_q4_fixed_bytes(static_cast<int>(d));
+  const size_t fixed = h_bytes + gemv_q4_fixed_bytes();
   const size_t budget = static_cast<size_t>(a.smem_optin);
-  int stages = 8;
+  int stages = 6;
   size_t ring = 0, smem_total = 0;
   for (; stages >= 2; --stages) {
     ring = static_cast<size_t>(stages) * gemv_q4_stage_bytes();
@@ -250,8 +251,10 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(V_rows)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_code_box_bytes()),
                                static_cast<cuuint32_t>(gemv_q4_box_rows())};
+    const CUtensorMapSwizzle sw = gemv_q4_code_box_bytes() == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                                  : CU_TENSOR_MAP_SWIZZLE_64B;
     if (encode(&L.cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), gdim, pitch, box,
-               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SPEC_ERR_CUDA;
   }
@@ -265,16 +268,6 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SPEC_ERR_CUDA;
   }
-  {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(nrows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(2 * d)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(gemv_q4_h_box_elems()),
-                               static_cast<cuuint32_t>(gemv_q4_h_rows())};
-    if (encode(&L.hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(H), gdim, gstride,
-               box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SPEC_ERR_CUDA;
-  }
   p.V = V;
   p.d = static_cast<int>(d);
   p.nbands = nbands;
@@ -282,7 +275,7 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
   p.stages = stages;
   p.stage_bytes = gemv_q4_stage_bytes();
   p.ring_bytes = static_cast<int>(ring);
-  p.hs_bytes = static_cast<int>(gemv_q4_abuf_bytes());
+  p.hs_bytes = static_cast<int>(h_bytes);
   p.tile_cap = tile_cap;
   p.H = static_cast<const uint8_t*>(H);
   p.h_row_bytes = static_cast<int>(2 * d);

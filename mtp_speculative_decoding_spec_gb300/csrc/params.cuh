@@ -199,10 +199,9 @@ cudaError_t gemv_tc_launch(const GemvTcLaunch& L, cudaStream_t stream);
 
 struct GemvQ4Launch {
   int grid, smem;
-  CUtensorMap cmap;  // codes: [V rows][d/2 bytes], row pitch 5d/8, box [32 rows][128 B], swizzled
-  CUtensorMap smap;  // (scale, bias) pairs: [V rows][d/8 bytes] from byte d/2, box [32][64 B]
-  CUtensorMap hmap;  // H [nrows][d] bf16, box [16 rows][64], 128-byte swizzle
-  GemvParams p;      // hs_bytes = the shared-memory A buffers
+  CUtensorMap cmap;  // codes: [V rows][d/2 bytes], row pitch 5d/8, box [32 rows][64 B], swizzled
+  CUtensorMap smap;  // (scale, bias) pairs: [V rows][d/8 bytes] from byte d/2, box [32][16 B]
+  GemvParams p;      // hs_bytes = the shared-memory copy of H
 };
 
 cudaError_t gemv_q4_launch(const GemvQ4Launch& L, cudaStream_t stream);
@@ -213,10 +212,8 @@ int gemv_q4_stat_bytes();
 int gemv_q4_code_box_bytes();
 int gemv_q4_pair_box_bytes();
 int gemv_q4_box_rows();
-int gemv_q4_h_rows();
-int gemv_q4_h_box_elems();
-size_t gemv_q4_abuf_bytes();
-size_t gemv_q4_fixed_bytes(int d);
+size_t gemv_q4_h_bytes(int d);
+size_t gemv_q4_fixed_bytes();
 int gemv_tc_band_rows();
 int gemv_tc_box_rows();
 int gemv_tc_kblock();
