@@ -17,10 +17,10 @@
 //
 // Filtered mode (spec_accept_filtered: top-k / top-p target, one-hot q): each block reduces
 // every verify row of its slice to the slice's best top_k entries (a 64-bit key orders by
-// logit, then by lower id; warps select from their 128 entries, warp 0 merges the eight
-// lists); the last block merges the slices' sorted lists row by row (a tournament over their
-// heads), cuts at top-p and takes the decisions and draws on the <= 32 survivors in exact
-// integer weights.
+// logit, then by lower id; one warp per row: a threshold cut and a bitonic sort of the keys
+// above it); the last block merges the slices' sorted lists, one warp per row (a tournament
+// over their heads), then row by row cuts at top-p and takes the decisions and draws on the
+// <= 32 survivors in exact integer weights.
 #include <math.h>
 
 #include "params.cuh"
@@ -344,9 +344,46 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
   return t;
 }
 
+// One compare-exchange step of a descending bitonic sort over a warp's elements i = lane + 32 h
+// (block size kb, stride j < 32): the lower index of a pair keeps the larger key in a
+// descending block ((i & kb) == 0), the smaller in an ascending one.
+__device__ __forceinline__ unsigned long long bitonic_step(unsigned long long v, int i, int kb,
+                                                           int j) {
+  const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+  const bool desc = (i & kb) == 0, lower = (i & j) == 0;
+  const unsigned long long hi = v > o ? v : o, lo = v > o ? o : v;
+  return (desc == lower) ? hi : lo;
+}
+
+// The K (<= 32) largest of 64 keys, two per lane (positions lane and lane + 32), sorted
+// descending into positions 0..K-1: a bitonic sort over the warp.
+__device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned long long& b) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int kb = 2; kb <= 64; kb <<= 1) {
+#pragma unroll
+    for (int j = kb >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // the pair (lane, lane + 32) sits in one lane
+        const bool desc = (lane & kb) == 0;
+        const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+        a = desc ? hi : lo;
+        b = desc ? lo : hi;
+      } else {
+        a = bitonic_step(a, lane, kb, j);
+        b = bitonic_step(b, lane + 32, kb, j);
+      }
+    }
+  }
+}
+
 // The best K keys of verify row `row` of request b over slice sl, descending, written to the
 // workspace (0 past the last entry). Called by one warp: lane l holds entries l + 32 i.
-__device__ __forceinline__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, int K) {
+// A threshold cut first: the K-th largest of the 32 lane maxima bounds the slice's K-th key
+// from below (those K maxima are keys), so only keys at or above it can be in the top K;
+// when at most 64 are, they are gathered in `buf` (64 keys of shared memory for this warp) and
+// sorted. Otherwise (keys concentrated in a few lanes) K rounds of a warp maximum select them.
+__device__ __forceinline__ void slice_topk_warp(const AcceptParams& p, int b, int sl, int row, int K,
+                                                unsigned long long* buf) {
   const int lane = threadIdx.x & 31;
   const float* z = p.logits + (static_cast<size_t>(b) * p.R + row) * p.V;
   const int64_t j0 = static_cast<int64_t>(sl) * kAcceptSlice;
@@ -358,6 +395,45 @@ __device__ __forceinline__ void slice_topk_warp(const AcceptParams& p, int b, in
   }
   unsigned long long* out =
       p.cand + ((static_cast<size_t>(b) * p.NS + sl) * kMaxRows + row) * kMaxTopK;
+  {
+    unsigned long long t[kAcceptSlice / 64];  // the lane's maximum by a 5-level tree
+#pragma unroll
+    for (int e = 0; e < kAcceptSlice / 64; ++e)
+      t[e] = key[2 * e] > key[2 * e + 1] ? key[2 * e] : key[2 * e + 1];
+#pragma unroll
+    for (int w = kAcceptSlice / 128; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) t[e] = t[e] > t[e + w] ? t[e] : t[e + w];
+    unsigned long long mx = t[0];  // sort the 32 lane maxima descending: position K-1 = L
+#pragma unroll
+    for (int kb = 2; kb <= 32; kb <<= 1)
+#pragma unroll
+      for (int j = kb >> 1; j > 0; j >>= 1) mx = bitonic_step(mx, lane, kb, j);
+    const unsigned long long L = __shfl_sync(0xffffffffu, mx, K - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kAcceptSlice / 32; ++e) cnt += (key[e] != 0ull && key[e] >= L) ? 1 : 0;
+    int incl = cnt;  // inclusive prefix of the counts over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    const int n = __shfl_sync(0xffffffffu, incl, 31);
+    if (L != 0ull && n <= 64) {
+      int at = incl - cnt;
+#pragma unroll
+      for (int e = 0; e < kAcceptSlice / 32; ++e)
+        if (key[e] != 0ull && key[e] >= L) buf[at++] = key[e];
+      __syncwarp();
+      unsigned long long a = lane < n ? buf[lane] : 0ull;
+      unsigned long long c = lane + 32 < n ? buf[lane + 32] : 0ull;
+      __syncwarp();  // buf is free again for the warp's next row
+      warp_sort64_desc(a, c);
+      if (lane < K) out[lane] = a;  // K <= 32: positions 0..K-1 are all in a
+      return;
+    }
+  }
   for (int r = 0; r < K; ++r) {
     // the lane's largest key by a 5-level tree (a linear scan is a 31-deep dependent chain)
     unsigned long long t[kAcceptSlice / 64];
@@ -424,6 +500,48 @@ __device__ __forceinline__ void merge_rows_topk(const AcceptParams& p, int b, in
     }
   }
   __syncthreads();
+}
+
+// The same top-K of row `row` by one warp, for at most 32 * kWarpMergeLists slices: lane l
+// holds the head and the next key of slices l + 32 i in registers; a round is the lane maxima's
+// warp maximum, and the winning lane moves its slice to the prefetched next key and loads the
+// one after (needed no earlier than that slice's next win). Keys are unique, so the result is
+// the block tournament's. With one warp per row all rows merge at once (the block tournament
+// ran the rows one after another, two block barriers a round).
+constexpr int kWarpMergeLists = 8;
+__device__ __forceinline__ void merge_row_topk_warp(const AcceptParams& p, int b, int row, int K,
+                                                    unsigned long long* out) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long* base = p.cand + static_cast<size_t>(b) * p.NS * kMaxRows * kMaxTopK;
+  auto at = [&](int s, int j) {
+    return __ldcg(base + (static_cast<size_t>(s) * kMaxRows + row) * kMaxTopK + j);
+  };
+  unsigned long long head[kWarpMergeLists], next[kWarpMergeLists];
+  int ptr[kWarpMergeLists];
+#pragma unroll
+  for (int i = 0; i < kWarpMergeLists; ++i) {
+    const int s = lane + 32 * i;
+    ptr[i] = 0;
+    head[i] = (s < p.NS) ? at(s, 0) : 0ull;
+    next[i] = (s < p.NS && K > 1) ? at(s, 1) : 0ull;
+  }
+  for (int r = 0; r < K; ++r) {
+    unsigned long long m = head[0];
+#pragma unroll
+    for (int i = 1; i < kWarpMergeLists; ++i) m = head[i] > m ? head[i] : m;
+    const unsigned long long wm = warp_max_u64(m);
+    if (lane == 0) out[r] = wm;
+    if (wm == 0ull) continue;  // every list is exhausted: the rest of out is 0 too
+#pragma unroll
+    for (int i = 0; i < kWarpMergeLists; ++i) {
+      if (head[i] == wm) {
+        const int s = lane + 32 * i;
+        ++ptr[i];
+        head[i] = next[i];
+        next[i] = (ptr[i] + 1 < K) ? at(s, ptr[i] + 1) : 0ull;
+      }
+    }
+  }
 }
 
 // u * W <= w * 2^24 for u = u24 * 2^-24, exactly (128-bit products).
@@ -653,7 +771,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
   unsigned long long* mysum = p.sums + (static_cast<size_t>(b) * p.NS + sl) * kAcceptSumSlots;
   if (kFiltered && D.need == 4) {
     // filtered: the slice's best top_k keys of every row 0..k, one warp per row
-    if (warp <= k) slice_topk_warp(p, b, sl, warp, p.top_k[b]);
+    __shared__ unsigned long long s_cut[kMaxRows][64];  // each row warp's threshold cut
+    if (warp <= k) slice_topk_warp(p, b, sl, warp, p.top_k[b], s_cut[warp]);
   } else if (D.need == 3) {
     // exact-match: the p weights of every row 0..k over this slice, slots 0..k
     unsigned long long sp[kMaxRows];
@@ -744,7 +863,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     // filtered: row by row, the top-k set (tournament over the slices' lists), the top-p cut,
     // then the ratio test of the draft against p' (q one-hot), a residual draw at the first
     // rejection, or the bonus draw after row k
-    __shared__ unsigned long long s_top[kMaxTopK];
+    __shared__ unsigned long long s_topr[kMaxRows][kMaxTopK];  // each row's top-k, descending
     __shared__ int f_stop;
     __shared__ Decision F;
     const int K = p.top_k[b];
@@ -756,10 +875,19 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       F.srow = -1;
       f_stop = 0;
     }
+    // every row's top-k set first: one warp per row, all rows at once (up to 256 slices);
+    // the block tournament row by row above that
+    if (p.NS <= 32 * kWarpMergeLists) {
+      if (warp <= k) merge_row_topk_warp(p, b, warp, K, s_topr[warp]);
+    } else {
+      extern __shared__ unsigned long long f_stage[];  // kFilterStageKeys when launched filtered
+      for (int r = 0; r <= k; ++r) {
+        merge_rows_topk(p, b, r, K, s_topr[r], sh, f_stage, p.filtered ? kFilterStageKeys : 0);
+      }
+    }
     __syncthreads();
-    extern __shared__ unsigned long long f_stage[];  // kFilterStageKeys when launched filtered
     for (int r = 0; r <= k; ++r) {
-      merge_rows_topk(p, b, r, K, s_top, sh, f_stage, p.filtered ? kFilterStageKeys : 0);
+      const unsigned long long* s_top = s_topr[r];
       if (tid == 0) {
         int id[kMaxTopK];
         unsigned long long w[kMaxTopK];

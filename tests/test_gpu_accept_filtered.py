@@ -226,3 +226,56 @@ def test_full_size_filtered_k7(c1):
         kept += r["n_accept"]
         mism += int(r["n_accept"] < k)
     assert compared >= 6 and kept > 0 and mism > 0
+
+
+@pytest.mark.parametrize("top_k,lanes", [(20, (5, 9)), (5, (5,)), (32, (3,))])
+def test_slice_topk_with_concentrated_keys(top_k, lanes):
+    """Logits whose largest entries in every 1,024-entry slice sit at ids = l (mod 32) for the
+    planted l: the slice selection's threshold cut then keeps more than 64 keys (two lanes at
+    top-k 20; top-k 32) and falls back to rounds of a warp maximum, or few (one lane at top-k
+    5). Decisions against the oracle on the same fp32 logits (statistics zero: at T > 0 the
+    filtered mode reads them only for the NaN check)."""
+    ensure_built()
+    B, k, V = 2, 3, 4096
+    R = k + 1
+    rng = np.random.default_rng([61, top_k])
+    z = (rng.standard_normal((B * R, V)) * 0.5).astype(np.float32)
+    for s in range(V // 1024):
+        for li, l in enumerate(lanes):
+            for i in range(32):
+                z[:, s * 1024 + 32 * i + l] = np.float32(3.0 + 0.05 * i + 0.3 * li + 0.001 * s)
+    z += (np.arange(B * R, dtype=np.float32)[:, None] * np.float32(0.01))
+    T = 1.0
+    drafts = np.zeros((B, k), dtype=np.int32)
+    for b in range(B):
+        for i in range(k):
+            row = z[b * R + i]
+            drafts[b, i] = int(np.argmax(row)) if (b + i) % 2 == 0 else int(rng.integers(0, V))
+    ws = workspace(V, B)
+    stats = zeros_bytes(B * R * spec.ROWSTATS_BYTES)
+    out = zeros_bytes(B * spec.ACCEPT_OUT_BYTES)
+    seeds = np.arange(B, dtype=np.uint64) + 71
+    pos = np.arange(B, dtype=np.int64) * 10 + 5
+    top_p = 0.95
+    tp32 = float(np.float32(top_p))
+    temps = torch.full((B,), T, dtype=torch.float32, device=dev())
+    compared = 0
+    for rep in range(8):
+        p_rep = pos + 1000 * rep
+        spec.spec_accept_filtered(B, k, to_dev(np.full(B, k, dtype=np.int32)), to_dev(drafts),
+                                  to_dev(z), stats, V, R, temps,
+                                  to_dev(np.full(B, top_k, dtype=np.int32)),
+                                  to_dev(np.full(B, top_p, dtype=np.float32)), -1,
+                                  to_dev(seeds), to_dev(p_rep), out, None, ws)
+        torch.cuda.synchronize()
+        o = to_np(out, spec.ACCEPT_OUT_DTYPE)
+        for b in range(B):
+            r = o_accept.accept_request_filtered(z[b * R:(b + 1) * R].astype(np.float64),
+                                                 list(drafts[b]), k, T, top_k, tp32, -1,
+                                                 o_ph.make_uniform_source(int(seeds[b])),
+                                                 int(p_rep[b]))
+            if _near(r["margins"]):
+                continue
+            _compare(o[b], r, f"top-k {top_k} lanes {lanes} rep {rep} request {b}")
+            compared += 1
+    assert compared >= 12
