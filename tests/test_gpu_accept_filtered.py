@@ -279,3 +279,50 @@ def test_slice_topk_with_concentrated_keys(top_k, lanes):
             _compare(o[b], r, f"top-k {top_k} lanes {lanes} rep {rep} request {b}")
             compared += 1
     assert compared >= 12
+
+
+@pytest.mark.parametrize("top_k", [16, 20])
+def test_large_vocabulary_block_merge(top_k):
+    """V = 300,000 (293 slices): past the one-warp-per-row merge (up to 256 slices) the last
+    block merges a row's slice lists with the whole block, from shared memory when slices x
+    top-k fits in 5,120 keys (top-k 16) and from L2 otherwise (top-k 20). Random fp32 logits,
+    drafts partly the rows' argmax; against the oracle."""
+    ensure_built()
+    B, k, V = 2, 3, 300_000
+    R = k + 1
+    rng = np.random.default_rng([62, top_k])
+    z = (rng.standard_normal((B * R, V)) * 2.0).astype(np.float32)
+    T = 1.0
+    drafts = np.zeros((B, k), dtype=np.int32)
+    for b in range(B):
+        for i in range(k):
+            drafts[b, i] = (int(np.argmax(z[b * R + i])) if (b + i) % 2 == 0
+                            else int(rng.integers(0, V)))
+    ws = workspace(V, B)
+    stats = zeros_bytes(B * R * spec.ROWSTATS_BYTES)
+    out = zeros_bytes(B * spec.ACCEPT_OUT_BYTES)
+    seeds = np.arange(B, dtype=np.uint64) + 91
+    top_p = 0.95
+    tp32 = float(np.float32(top_p))
+    temps = torch.full((B,), T, dtype=torch.float32, device=dev())
+    zd = to_dev(z)
+    compared = 0
+    for rep in range(6):
+        pos = np.arange(B, dtype=np.int64) * 10 + 1000 * rep + 3
+        spec.spec_accept_filtered(B, k, to_dev(np.full(B, k, dtype=np.int32)), to_dev(drafts),
+                                  zd, stats, V, R, temps,
+                                  to_dev(np.full(B, top_k, dtype=np.int32)),
+                                  to_dev(np.full(B, top_p, dtype=np.float32)), -1,
+                                  to_dev(seeds), to_dev(pos), out, None, ws)
+        torch.cuda.synchronize()
+        o = to_np(out, spec.ACCEPT_OUT_DTYPE)
+        for b in range(B):
+            r = o_accept.accept_request_filtered(z[b * R:(b + 1) * R].astype(np.float64),
+                                                 list(drafts[b]), k, T, top_k, tp32, -1,
+                                                 o_ph.make_uniform_source(int(seeds[b])),
+                                                 int(pos[b]))
+            if _near(r["margins"]):
+                continue
+            _compare(o[b], r, f"V={V} top-k {top_k} rep {rep} request {b}")
+            compared += 1
+    assert compared >= 9
