@@ -99,6 +99,22 @@ def test_verify_c0_ragged_vocab_and_odd_shapes():
         _verify_case(cfg, W, to_dev(W), H, 1, 3, [1.0], f"V={V} d={d}")
 
 
+def test_verify_large_vocabulary_sixteen_tiles_per_block():
+    """V = 300,000 at 152 SMs gives each block up to 62 bands of 32 rows, about 16 tiles of 128
+    rows (the bf16 kernel's limit before its grid grows): logits and statistics against the
+    oracle at T = 1 and T = 0."""
+    ensure_built()
+    V, d = 300_000, 1024
+    cfg = configs.Config(name="wide", d=d, V=V, Vd=V, wdtype="bf16", k=3, k_mode="fixed",
+                         batch=2, rows_per_request=3, temps=(1.0,), cycles=1, seeds=(0,),
+                         plant_scale=0.0, pi_draft=0.0, draft_noise=0.5)
+    W = gen.lm_weights(cfg, seed=300, cache=False)
+    rng = np.random.default_rng(300)
+    H = gen.encode(rng.standard_normal((6, d), dtype=np.float32), "bf16")
+    near = _verify_case(cfg, W, to_dev(W), H, 2, 3, [1.0, 0.0], f"V={V} d={d}")
+    assert near <= 1
+
+
 def test_verify_nonfinite_rows_flagged(c0):
     cfg, W, Wd = c0
     H = np.zeros((2, cfg.d), dtype=np.float32)
