@@ -99,17 +99,17 @@ def test_verify_c0_ragged_vocab_and_odd_shapes():
         _verify_case(cfg, W, to_dev(W), H, 1, 3, [1.0], f"V={V} d={d}")
 
 
-def test_verify_large_vocabulary_sixteen_tiles_per_block():
+@pytest.mark.parametrize("V,d", [(300_000, 1024), (400_000, 512)])
+def test_verify_large_vocabulary_sixteen_tiles_per_block(V, d):
     """V = 300,000 at 152 SMs gives each block up to 62 bands of 32 rows, about 16 tiles of 128
-    rows (the bf16 kernel's limit before its grid grows): logits and statistics against the
-    oracle at T = 1 and T = 0."""
+    rows (the bf16 kernel's limit before its grid grows); V = 400,000 grows the grid past one
+    block per SM. Logits and statistics against the oracle at T = 1 and T = 0."""
     ensure_built()
-    V, d = 300_000, 1024
     cfg = configs.Config(name="wide", d=d, V=V, Vd=V, wdtype="bf16", k=3, k_mode="fixed",
                          batch=2, rows_per_request=3, temps=(1.0,), cycles=1, seeds=(0,),
                          plant_scale=0.0, pi_draft=0.0, draft_noise=0.5)
-    W = gen.lm_weights(cfg, seed=300, cache=False)
-    rng = np.random.default_rng(300)
+    W = gen.lm_weights(cfg, seed=V // 1000, cache=False)
+    rng = np.random.default_rng(V // 1000)
     H = gen.encode(rng.standard_normal((6, d), dtype=np.float32), "bf16")
     near = _verify_case(cfg, W, to_dev(W), H, 2, 3, [1.0, 0.0], f"V={V} d={d}")
     assert near <= 1
