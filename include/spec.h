@@ -446,6 +446,31 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc *st,
 int32_t spec_batched_supported(void);
 
 /*
+ * Host transfers inside the chain of kernels (no counterpart on the pages: a deployment
+ * convenience). A cudaMemcpyAsync between two of this library's kernels ends their programmatic
+ * overlap (the second kernel no longer starts in the first one's tail); these two calls move a
+ * cycle's inputs and results without one, through pinned host memory that is mapped into the
+ * device's address space (cudaHostAlloc / cudaMallocHost memory on a 64-bit system).
+ *
+ * spec_host_alias -- *dev_ptr = the device address of pinned, mapped host memory host_ptr.
+ *   A result pointer of this library's calls (for example spec_accept's `out`) may be such an
+ *   alias: the kernel then writes the result straight into host memory, readable after the
+ *   stream is synchronised. SPEC_ERR_INVALID if host_ptr is not such memory (pageable memory,
+ *   device memory, or NULL). Enqueues nothing.
+ *
+ * spec_copy_from_host -- copy `bytes` (a multiple of 16, src and dst 16-byte aligned) from
+ *   pinned, mapped host memory `src_host` to device memory `dst`, by a kernel on `stream`
+ *   launched as a programmatic dependent like the library's other kernels: it reads the host
+ *   bytes at once and writes `dst` only after the stream's previous kernel has finished, so a
+ *   buffer that kernel reads may be refilled. The host must not change src_host until the
+ *   copy has run. SPEC_ERR_INVALID for misalignment, a size that is not a multiple of 16, or a
+ *   source that is not pinned mapped host memory; bytes = 0 enqueues nothing.
+ */
+spec_status spec_host_alias(const void *host_ptr, void **dev_ptr);
+spec_status spec_copy_from_host(void *dst, const void *src_host, size_t bytes,
+                                spec_stream_t stream);
+
+/*
  * spec_lmhead_verify_noalloc -- spec_lmhead_verify for callers that cannot allocate device
  * memory. (The pages have no counterpart: this is a deployment convenience of this library.)
  *

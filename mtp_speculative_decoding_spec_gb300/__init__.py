@@ -61,6 +61,19 @@ def spec_batched_supported():
     return bool(_abi.lib().spec_batched_supported())
 
 
+def spec_host_alias(host):
+    """Device address (int) of pinned, mapped host memory (a pinned tensor or an address)."""
+    import ctypes
+    out = ctypes.c_void_p()
+    _check("spec_host_alias", _abi.lib().spec_host_alias(_ptr(host), ctypes.byref(out)))
+    return int(out.value)
+
+
+def spec_copy_from_host(dst, src_host, nbytes, stream=None):
+    _check("spec_copy_from_host", _abi.lib().spec_copy_from_host(
+        _ptr(dst), _ptr(src_host), int(nbytes), _stream(stream)))
+
+
 def spec_lmhead_verify(W, wdt, V, d, H, B, R, temperature, logits, stats, workspace,
                        stream=None):
     _check("spec_lmhead_verify", _abi.lib().spec_lmhead_verify(

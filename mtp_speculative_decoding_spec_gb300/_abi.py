@@ -20,7 +20,7 @@ EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spe
            "spec_accept", "spec_accept_exact", "spec_accept_filtered", "spec_adapt_width",
            "spec_draft_argmax_rows", "spec_accept_rows",
            "spec_commit_rollback",
-           "spec_batched_supported",
+           "spec_batched_supported", "spec_host_alias", "spec_copy_from_host",
            "spec_lmhead_verify_noalloc", "spec_noalloc_scratch_bytes",
            "spec_noalloc_error_word", "spec_test_verify_stalled",
            "spec_width_graph_create", "spec_graph_capture_begin", "spec_graph_capture_end",
@@ -87,6 +87,10 @@ def lib():
         L.spec_status_str.restype = ctypes.c_char_p
         L.spec_batched_supported.argtypes = []
         L.spec_batched_supported.restype = i32
+        L.spec_host_alias.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
+        L.spec_host_alias.restype = i32
+        L.spec_copy_from_host.argtypes = [vp, vp, sz, vp]
+        L.spec_copy_from_host.restype = i32
         L.spec_lmhead_verify.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, vp, sz, vp]
         L.spec_lmhead_verify.restype = i32
         L.spec_draft_argmax.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp, i32, vp, i32, vp,

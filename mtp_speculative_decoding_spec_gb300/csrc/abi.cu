@@ -545,6 +545,42 @@ spec_status run_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_t
 
 using namespace spec;
 
+namespace spec {
+
+// Copy of n 16-byte vectors from mapped host memory to device memory: each thread reads its
+// vectors (at most four) at once, then waits for the stream's previous kernel before writing.
+__global__ void __launch_bounds__(256) copy_from_host_kernel(uint4* __restrict__ dst,
+                                                             const uint4* __restrict__ src,
+                                                             int64_t n) {
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (i0 + u * step < n) v[u] = src[i0 + u * step];
+  pdl_wait();
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (i0 + u * step < n) dst[i0 + u * step] = v[u];
+}
+
+// Device-accessible address of p, or nullptr: device or managed memory as it is, pinned host
+// memory through its device alias.
+void* device_accessible(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error this lookup may leave
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+    return const_cast<void*>(p);
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
+}  // namespace spec
+
 extern "C" {
 
 size_t spec_workspace_bytes(int64_t V, int32_t max_batch) {
@@ -565,6 +601,37 @@ const char* spec_status_str(spec_status s) {
 }
 
 int32_t spec_batched_supported(void) { return 1; }
+
+spec_status spec_host_alias(const void* host_ptr, void** dev_ptr) {
+  if (!host_ptr || !dev_ptr) return SPEC_ERR_INVALID;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_INVALID;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return SPEC_ERR_INVALID;
+  *dev_ptr = at.devicePointer;
+  return SPEC_OK;
+}
+
+spec_status spec_copy_from_host(void* dst, const void* src_host, size_t bytes,
+                                spec_stream_t stream) {
+  if (bytes == 0) return SPEC_OK;
+  if (!dst || !src_host || bytes % 16 != 0 || reinterpret_cast<uintptr_t>(dst) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(src_host) % 16 != 0)
+    return SPEC_ERR_INVALID;
+  void* src = nullptr;
+  if (spec_host_alias(src_host, &src) != SPEC_OK) return SPEC_ERR_INVALID;
+  void* d = spec::device_accessible(dst);
+  if (!d) return SPEC_ERR_INVALID;
+  const int64_t n = static_cast<int64_t>(bytes / 16);
+  const int64_t grid = (n + 4 * 256 - 1) / (4 * 256);
+  if (grid > 65535) return SPEC_ERR_UNSUPPORTED;  // 64 MiB per call
+  const cudaError_t e = spec::launch_pdl(spec::copy_from_host_kernel, dim3(static_cast<unsigned>(grid)),
+                                         dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                                         static_cast<uint4*>(d), static_cast<const uint4*>(src), n);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t d,
                                const void* H, int32_t B, int32_t R, const float* temperature,

@@ -215,7 +215,7 @@ def test_no_cpu_fallback_in_product_package():
 _BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemv_q4_kernel": 16 * 32, "gemm_rows_tc_kernel": 10 * 32,
                   "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_snapshot_kernel": 256,
                   "commit_replay_kernel": 128, "adapt_width_kernel": 128,
-                  "width_select_kernel": 32}
+                  "width_select_kernel": 32, "copy_from_host_kernel": 256}
 
 
 def test_register_budget_per_sub_partition(lib):
