@@ -36,9 +36,15 @@
 //     L2 prefetch of later stages, 84 us. At ~2 stages in flight a warp waits ~1 us a stage for
 //     its next slot: the loads take ~4 us, which is the bytes in flight over the ~4.6 TB/s this
 //     access pattern (128 + 32 bytes of every 1,600-byte row per stage) gets from HBM.
-//   * H (the block's up to 8 rows, rows past nrows zero) is copied once to shared memory in the
-//     order of the MMA's B fragments: one 16-byte load gives a thread its four bf16 pairs of a
-//     32-element group;
+//   * the k order inside each 32-element group is permuted, the same way in A and B (the same
+//     products are summed; only the order of the MMA's fp32 additions changes, and it is the
+//     same for every row and every row count): thread c of a quad takes the four pairs of code
+//     word c (elements 8c .. 8c + 7), so one 32-bit shared load gives a thread a row's word and
+//     the four pairs come out of it by constant shifts;
+//   * H (the block's up to 8 rows, rows past nrows zero) is copied once to shared memory as
+//     [d/32 groups][8 rows][32 bf16] (natural order inside a group): under that permutation one
+//     16-byte load gives thread (g, c) its B registers for a group, elements 8c .. 8c + 7 of H
+//     row g;
 //   * after the stream a thread holds, per pass, the logits of 4 vocabulary rows for 2 H rows
 //     (in registers); the logits of rows at T > 0 are stored, and the row statistics and the
 //     shared finish run as in the bf16 kernels.
@@ -90,6 +96,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ uint32_t smem_addr(const void* a) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(a));
 }
+__device__ __forceinline__ uint32_t lds4(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ uint4 lds16(uint32_t a) {
   uint4 v;
   asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -98,14 +109,23 @@ __device__ __forceinline__ uint4 lds16(uint32_t a) {
   return v;
 }
 
-// One A-fragment register: the pair of elements (2c, 2c+1) of the 8-element code word w,
-// dequantised: the bf16 pair (128 + e, 128 + e') (the code lands in the low mantissa bits of
-// 128 = 0x4300, where one unit is 1), minus 128 (exact), times s plus b, rounded once.
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t w, int shift, uint32_t s2,
-                                                 uint32_t b2) {
-  const uint32_t t = ((w >> shift) & 0x000F000Fu) | 0x43004300u;
+// One A-fragment register: a pair of consecutive elements of an 8-element code word, its two
+// codes at bits 0..3 and 16..19 of v (the word shifted right by 4 j for pair j), dequantised:
+// the bf16 pair (128 + e, 128 + e') (the code lands in the low mantissa bits of 128 = 0x4300,
+// where one unit is 1), minus 128 (exact), times s plus b, rounded once.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t v, uint32_t s2, uint32_t b2) {
+  const uint32_t t = (v & 0x000F000Fu) | 0x43004300u;
   const uint32_t q = bf16x2_fma(t, 0x3F803F80u, 0xC300C300u);
   return bf16x2_fma(q, s2, b2);
+}
+
+// The word's four pairs, in order (pair j = elements 2j, 2j + 1): constant shifts.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2,
+                                             uint32_t (&o)[4]) {
+  o[0] = dequant_pair(w, s2, b2);
+  o[1] = dequant_pair(w >> 4, s2, b2);
+  o[2] = dequant_pair(w >> 8, s2, b2);
+  o[3] = dequant_pair(w >> 12, s2, b2);
 }
 
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -117,7 +137,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (draft_step_idle(p)) return;  // before any setup: nothing in flight
   const int S = p.stages;              // slots of each warp's ring
   uint8_t* ring = smem;                // [16 warps][S][slot]; afterwards statistics and scratch
-  uint8_t* hs = smem + p.ring_bytes;   // H in B-fragment order: [d/32][8 rows][4 c][4 words]
+  uint8_t* hs = smem + p.ring_bytes;   // H: [d/32 groups][8 rows][32 bf16]
   uint64_t* full = reinterpret_cast<uint64_t*>(hs + p.hs_bytes);  // [8 warps][S]
   int* flags = reinterpret_cast<int*>(full + kQWarps * S);  // [0] abort, [1] last block
   float* s_temp = reinterpret_cast<float*>(flags + 4);
@@ -165,13 +185,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int it = 0; it < issued; ++it) issue(it);
   pdl_wait();
   {
-    // word ((G*8 + n)*4 + cc)*4 + q = the bf16 pair of H row n at elements 32 G + 8 q + 2 cc:
-    // thread (g, c) of a warp reads its B fragments of group G (n = g) in one 16-byte load;
-    // groups past d (the rest of a last half stage) are zero
-    // The 16 bytes of H row n at elements 8 j .. 8 j + 7 (group G = j / 4, q = j % 4) are the
-    // words cc = 0..3 of (G, n, q): one 16-byte load each, every load of a thread issued
-    // before its stores (word-by-word loads serialised into ~5 us here).
-    uint32_t* hw = reinterpret_cast<uint32_t*>(hs);
+    // 16-byte unit (G*8 + n)*4 + c = H row n at elements 32 G + 8 c .. 32 G + 8 c + 7: thread
+    // (g, c) of a warp reads its B fragments of group G (n = g) in one 16-byte load; groups
+    // past d (the rest of a last half stage) are zero. Every load of a thread is issued before
+    // its stores (word-by-word loads serialised into ~5 us here).
+    uint4* hu = reinterpret_cast<uint4*>(hs);
     const int nchunk = nks * kQGroups * 4;  // 16-byte chunks of a row, whole stages
     const int total = kMaxRows * nchunk;
     constexpr int kPer = 4;  // chunks a thread loads per round
@@ -188,13 +206,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int i = i0 + u * kQThreads, n = i / nchunk, j = i - n * nchunk;
-        if (i < total) {
-          uint32_t* o = hw + ((j >> 2) * 8 + n) * 16 + (j & 3);  // word cc at o[4 cc]
-          o[0] = v[u].x;
-          o[4] = v[u].y;
-          o[8] = v[u].z;
-          o[12] = v[u].w;
-        }
+        if (i < total) hu[((j >> 2) * 8 + n) * 4 + (j & 3)] = v[u];
       }
     }
   }
@@ -209,7 +221,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // Each warp streams its own 32-row box through its own ring of S slots: it waits for a slot,
   // computes, and refills the slot with its stage it + S, so no warp ever waits for another.
   // Thread (g, c) holds A-fragment rows g and g + 8 of the box's two 16-row tiles (box rows
-  // 16 mt + 8 h + g) and accumulates their logits for H rows 2c and 2c + 1.
+  // 16 mt + 8 h + g) and accumulates their logits for H rows 2c and 2c + 1. The MMA's k order
+  // within a group is permuted (A and B alike): thread c's fragment registers take the four
+  // pairs of code word c (elements 8c .. 8c + 7), so every shift is a constant and its B
+  // fragments are 16 contiguous bytes of the H row.
   float zv[kQMaxPasses][kQVals];  // each pass's logits, [mt][h][j]
 #pragma unroll
   for (int ps = 0; ps < kQMaxPasses; ++ps)
@@ -217,7 +232,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int v = 0; v < kQVals; ++v) zv[ps][v] = 0.f;
   {
     const uint32_t wring_s = smem_addr(wring), hs_s = smem_addr(hs);
-    const int shift = 4 * c;                 // pair c of a code word: elements 2c, 2c + 1
     // the swizzle of box rows 16 mt + 8 h + g: 16-byte unit u sits at u ^ (row & 7) (128-byte
     // rows) or u ^ ((row >> 1) & 3) (64-byte rows)
     const int swz = (kQCodeRow == 128 ? g : (g >> 1) & 3) << 4;
@@ -248,22 +262,22 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const uint4 hb = lds16(hk + gg * 512 + (g * 4 + c) * 16);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-          const uint32_t ra = st + (mt * 16 + g) * kQCodeRow + ((gg << 4) ^ swz);
-          const uint4 wa = lds16(ra);                   // row 16 mt + g
-          const uint4 wb = lds16(ra + 8 * kQCodeRow);   // row 16 mt + 8 + g (same swizzle)
+          // code word c of the group in rows 16 mt + g and 16 mt + 8 + g (the same swizzle)
+          const uint32_t ra = st + (mt * 16 + g) * kQCodeRow + ((gg << 4) ^ swz) + 4 * c;
+          const uint32_t wa = lds4(ra), wb = lds4(ra + 8 * kQCodeRow);
           const uint4 pa = pr[mt][0][gg >> 2], pb = pr[mt][1][gg >> 2];
           const int gq = gg & 3;
           const uint32_t sa = gq == 0 ? pa.x : gq == 1 ? pa.y : gq == 2 ? pa.z : pa.w;
           const uint32_t sb = gq == 0 ? pb.x : gq == 1 ? pb.y : gq == 2 ? pb.z : pb.w;
           const uint32_t sa2 = __byte_perm(sa, sa, 0x1010), ba2 = __byte_perm(sa, sa, 0x3232);
           const uint32_t sb2 = __byte_perm(sb, sb, 0x1010), bb2 = __byte_perm(sb, sb, 0x3232);
-          // k 0..15 of the group: words x (elements 0..7) and y (8..15); then z and w
-          mma_bf16_16816(acc[mt], dequant_pair(wa.x, shift, sa2, ba2),
-                         dequant_pair(wb.x, shift, sb2, bb2), dequant_pair(wa.y, shift, sa2, ba2),
-                         dequant_pair(wb.y, shift, sb2, bb2), hb.x, hb.y);
-          mma_bf16_16816(acc[mt], dequant_pair(wa.z, shift, sa2, ba2),
-                         dequant_pair(wb.z, shift, sb2, bb2), dequant_pair(wa.w, shift, sa2, ba2),
-                         dequant_pair(wb.w, shift, sb2, bb2), hb.z, hb.w);
+          uint32_t da[4], db[4];
+          dequant_word(wa, sa2, ba2, da);
+          dequant_word(wb, sb2, bb2, db);
+          // pairs 0, 1 of the word in the first k16 step (with H elements 8c .. 8c + 3), 2, 3
+          // in the second (8c + 4 .. 8c + 7)
+          mma_bf16_16816(acc[mt], da[0], db[0], da[1], db[1], hb.x, hb.y);
+          mma_bf16_16816(acc[mt], da[2], db[2], da[3], db[3], hb.z, hb.w);
         }
       }
       // every lane's reads of the slot are done: order them before the copy that refills it
@@ -431,7 +445,7 @@ int gemv_q4_stat_bytes() { return kQStatBytes; }
 int gemv_q4_code_box_bytes() { return kQCodeRow; }
 int gemv_q4_pair_box_bytes() { return kQPairRow; }
 int gemv_q4_box_rows() { return kQBoxRows; }
-// H in shared memory, in B-fragment order: 8 rows (rows past nrows zero) of d bf16 values,
+// H in shared memory, grouped by 32 elements: 8 rows (rows past nrows zero) of d bf16 values,
 // padded with zeros to whole stages
 size_t gemv_q4_h_bytes(int d) {
   return static_cast<size_t>((d + kQStageElems - 1) / kQStageElems) * kQStageElems * 16;
