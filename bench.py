@@ -610,10 +610,12 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     """Adaptive verify width on the k-sweep's greedy workload: the width of every cycle is
     chosen on the device (spec_adapt_width) from the per-depth acceptance and the request's
     cycle-cost fit (cycles timed on the device; a prior table from this run's measured verify
-    step and draft step until the fit is usable). One request: each cycle is a launch of the
-    width graph, whose select kernel picks the body of the chosen width (that many draft steps,
-    a verify of width + 1 rows, acceptance, next width); the cycle's inputs are copied into the
-    graph's input buffers first. Compared with every fixed width on the same inputs."""
+    step and draft step until the fit is usable). One request, two schedules:
+    host-scheduled widths (the headline: cycle n runs exactly the width chosen after cycle
+    n - 2, which the width update writes into pinned host memory; the host reads it once that
+    cycle has completed), and the width graph (each cycle a graph launch whose select kernel
+    picks the body of the chosen width, the cycle's inputs first copied into the graph's input
+    buffers). Compared with every fixed width on the same inputs."""
     import torch
 
     import mtp_speculative_decoding_spec_gb300 as spec
@@ -624,36 +626,45 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     Hp_d = torch.from_numpy(Hp.view(np.int16)).to(dev)
     Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
     cost = [(step_us + k * draft_us) / step_us for k in range(k_max + 1)]
-    eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
-                           cfg.eos_id, device=dev, adaptive_cost=cost, alpha=0.1)
-    eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])
-    for c in range(20):
-        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
-    torch.cuda.synchronize()
-    eng.counters.zero_()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for c in range(K):
-        eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
-    b.record()
-    torch.cuda.synchronize()
-    s = a.elapsed_time(b) / 1e3
-    cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
-    st = eng.width_state.cpu().numpy().view(spec.WIDTH_STATE_DTYPE)[0]
-    res = {"full_cycles_s": round(K / s, 1),
-           "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
-           "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
-           "mean_width": round(float(cnt["drafted"]) / K, 3),
-           "final_width": int(st["k"]),
-           "rates": [round(float(st["rate"][d]), 3) if (int(st["seen"]) >> d) & 1 else None
-                     for d in range(1, k_max + 1)],
-           "prior_cost": [round(x, 3) for x in cost],
-           "fitted_cost_ratio": round(float(st["rate"][0]), 4),
-           "fit_usable": bool(float(st["rate"][0]) > 0),
-           "mode": "width graph" if eng.width_graph else "k_max gated draft steps",
-           "workload": "k = 7 greedy sweep inputs (256 distinct cycles), k_max = 7"}
-    eng.close()
-    del eng
+
+    def run(lag):
+        eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
+                               cfg.eos_id, device=dev, adaptive_cost=cost, alpha=0.1,
+                               width_lag=lag)
+        eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])
+        for c in range(20):
+            eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
+        torch.cuda.synchronize()
+        eng.counters.zero_()
+        a.record()
+        for c in range(K):
+            eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
+        b.record()
+        torch.cuda.synchronize()
+        s = a.elapsed_time(b) / 1e3
+        cnt = eng.counters.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
+        st = eng.width_state.cpu().numpy().view(spec.WIDTH_STATE_DTYPE)[0]
+        out = {"full_cycles_s": round(K / s, 1),
+               "emitted_tok_s": round(float(cnt["emitted"]) / s, 1),
+               "tokens_per_cycle": round(float(cnt["emitted"]) / K, 3),
+               "mean_width": round(float(cnt["drafted"]) / K, 3),
+               "final_width": int(st["k"]),
+               "rates": [round(float(st["rate"][d]), 3) if (int(st["seen"]) >> d) & 1 else None
+                         for d in range(1, k_max + 1)],
+               "fitted_cost_ratio": round(float(st["rate"][0]), 4),
+               "fit_usable": bool(float(st["rate"][0]) > 0)}
+        eng.close()
+        del eng
+        return out
+
+    res = run(True)
+    res["mode"] = "host-scheduled widths, one cycle late"
+    res["prior_cost"] = [round(x, 3) for x in cost]
+    res["workload"] = "k = 7 greedy sweep inputs (256 distinct cycles), k_max = 7"
+    g = run(False)
+    res["width_graph"] = {key: g[key] for key in ("full_cycles_s", "emitted_tok_s",
+                                                  "tokens_per_cycle", "mean_width")}
     # every fixed width on the same inputs (the first k + 1 verify rows and k draft rows)
     fixed = {}
     for k in range(1, k_max + 1):
@@ -674,6 +685,9 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
         fixed[f"k{k}"] = round(float(cnt["emitted"]) / s, 1)
         del eng
     res["fixed_emitted_tok_s"] = fixed
+    best = max(fixed.values())
+    res["vs_best_fixed"] = round(res["emitted_tok_s"] / best, 4)
+    res["width_graph"]["vs_best_fixed"] = round(res["width_graph"]["emitted_tok_s"] / best, 4)
     return res
 
 

@@ -398,6 +398,21 @@ spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out *ou
                              spec_stream_t stream);
 
 /*
+ * spec_adapt_width_mirror -- spec_adapt_width that also writes each chosen width to
+ * k_mirror[b] (int32 [B], any memory the device can write: device memory, or the device alias
+ * of pinned host memory from spec_host_alias). No counterpart on the pages: it lets a host
+ * learn the widths without a copy on the stream, so that it can enqueue a later cycle at
+ * exactly the chosen width (no graph, no idle draft step). The mirror holds the values once
+ * the launch has completed (an event recorded after it). k_mirror NULL: SPEC_ERR_INVALID;
+ * other arguments and errors as for spec_adapt_width.
+ */
+spec_status spec_adapt_width_mirror(int32_t B, int32_t k_max, const spec_accept_out *out,
+                                    const int32_t *k_used, const float *cost,
+                                    const float *cycle_cost, float alpha,
+                                    spec_width_state *state, int32_t *k_next, int32_t *k_mirror,
+                                    spec_stream_t stream);
+
+/*
  * Adaptive-width cycles as one CUDA graph (no counterpart on the pages: it lets the width
  * chosen on the device decide how much work a cycle enqueues, with no host round trip and no
  * idle draft steps).

@@ -124,6 +124,14 @@ def spec_adapt_width(B, k_max, out, k_used, cost, cycle_cost, alpha, state, k_ne
         _ptr(state), _ptr(k_next), _stream(stream)))
 
 
+def spec_adapt_width_mirror(B, k_max, out, k_used, cost, cycle_cost, alpha, state, k_next,
+                            k_mirror, stream=None):
+    """k_mirror: a device-writable address (an int from spec_host_alias) or a tensor."""
+    _check("spec_adapt_width_mirror", _abi.lib().spec_adapt_width_mirror(
+        B, k_max, _ptr(out), _ptr(k_used), _ptr(cost), _ptr(cycle_cost), float(alpha),
+        _ptr(state), _ptr(k_next), _ptr(k_mirror), _stream(stream)))
+
+
 def spec_width_graph_create(n_bodies, k_next, B):
     """Returns (graph, [body graphs]) as integers (see include/spec.h)."""
     import ctypes

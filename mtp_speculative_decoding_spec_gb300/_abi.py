@@ -18,6 +18,7 @@ REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN,
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
 EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
            "spec_accept", "spec_accept_exact", "spec_accept_filtered", "spec_adapt_width",
+           "spec_adapt_width_mirror",
            "spec_draft_argmax_rows", "spec_accept_rows",
            "spec_commit_rollback",
            "spec_batched_supported", "spec_host_alias", "spec_copy_from_host",
@@ -113,6 +114,9 @@ def lib():
         L.spec_accept_rows.restype = i32
         L.spec_adapt_width.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.spec_adapt_width.restype = i32
+        L.spec_adapt_width_mirror.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                              vp, vp]
+        L.spec_adapt_width_mirror.restype = i32
         L.spec_commit_rollback.argtypes = [i32, ctypes.POINTER(spec_state_desc), vp, vp, i32, vp,
                                            vp]
         L.spec_commit_rollback.restype = i32

@@ -722,14 +722,15 @@ spec_status spec_accept(int32_t B, int32_t k_max, const int32_t* k, const int32_
                           workspace_bytes, stream, 0);
 }
 
-spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* out,
-                             const int32_t* k_used, const float* cost, const float* cycle_cost,
-                             float alpha, spec_width_state* state, int32_t* k_next,
-                             spec_stream_t stream) {
+namespace spec {
+spec_status run_adapt(int32_t B, int32_t k_max, const spec_accept_out* out,
+                      const int32_t* k_used, const float* cost, const float* cycle_cost,
+                      float alpha, spec_width_state* state, int32_t* k_next, int32_t* k_mirror,
+                      spec_stream_t stream) {
   if (B < 1 || k_max < 0 || k_max > kMaxRows - 1) return SPEC_ERR_INVALID;
   if (!out || !k_used || !cost || !state || !k_next) return SPEC_ERR_INVALID;
   if (!(alpha > 0.f && alpha <= 1.f)) return SPEC_ERR_INVALID;
-  spec::AdaptParams p;
+  AdaptParams p;
   p.B = B;
   p.k_max = k_max;
   p.out = out;
@@ -739,8 +740,28 @@ spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* ou
   p.alpha = alpha;
   p.state = state;
   p.k_next = k_next;
-  const cudaError_t e = spec::adapt_launch(p, reinterpret_cast<cudaStream_t>(stream));
+  p.k_mirror = k_mirror;
+  const cudaError_t e = adapt_launch(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+}  // namespace spec
+
+spec_status spec_adapt_width(int32_t B, int32_t k_max, const spec_accept_out* out,
+                             const int32_t* k_used, const float* cost, const float* cycle_cost,
+                             float alpha, spec_width_state* state, int32_t* k_next,
+                             spec_stream_t stream) {
+  return spec::run_adapt(B, k_max, out, k_used, cost, cycle_cost, alpha, state, k_next, nullptr,
+                         stream);
+}
+
+spec_status spec_adapt_width_mirror(int32_t B, int32_t k_max, const spec_accept_out* out,
+                                    const int32_t* k_used, const float* cost,
+                                    const float* cycle_cost, float alpha,
+                                    spec_width_state* state, int32_t* k_next, int32_t* k_mirror,
+                                    spec_stream_t stream) {
+  if (!k_mirror) return SPEC_ERR_INVALID;
+  return spec::run_adapt(B, k_max, out, k_used, cost, cycle_cost, alpha, state, k_next, k_mirror,
+                         stream);
 }
 
 spec_status spec_accept_exact(int32_t B, int32_t k_max, const int32_t* k, const int32_t* drafts,

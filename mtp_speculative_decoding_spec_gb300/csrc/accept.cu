@@ -1108,6 +1108,7 @@ __global__ void __launch_bounds__(128) adapt_width_kernel(const AdaptParams p) {
   s.k = kb;
   p.state[b] = s;
   p.k_next[b] = kb;
+  if (p.k_mirror) p.k_mirror[b] = kb;
 }
 
 // The select node of a width graph: the switch's value for this launch is the largest width

@@ -236,6 +236,7 @@ struct AdaptParams {
   float alpha;
   spec_width_state* state;
   int32_t* k_next;
+  int32_t* k_mirror;  // [B] or null: a second copy of the chosen widths (e.g. host-mapped)
 };
 cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream);
 const void* width_select_function();  // the select kernel of a width graph (see abi.cu)

@@ -134,6 +134,13 @@ def test_host_validation_of_the_later_entry_points(lib):
     assert lib.spec_adapt_width(1, 7, fake, fake, null, null, 0.1, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, null, 0.0, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, fake, 1.5, fake, fake, null) == 1
+    # the mirror entry point: the same checks, and the mirror is required
+    assert lib.spec_adapt_width_mirror(1, 7, fake, fake, fake, null, 0.1, fake, fake, null,
+                                       null) == 1
+    assert lib.spec_adapt_width_mirror(0, 7, fake, fake, fake, null, 0.1, fake, fake, fake,
+                                       null) == 1
+    assert lib.spec_adapt_width_mirror(1, 7, fake, fake, fake, null, 0.0, fake, fake, fake,
+                                       null) == 1
     # width graphs: 1..64 bodies, 1..128 requests, the widths and both outputs required
     import ctypes
     g, bodies = ctypes.c_void_p(), (ctypes.c_void_p * 8)()

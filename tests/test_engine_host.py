@@ -23,7 +23,7 @@ def calls(monkeypatch):
 
     for name in ("spec_draft_argmax", "spec_lmhead_verify", "spec_accept", "spec_accept_exact",
                  "spec_accept_filtered", "spec_commit_rollback", "spec_adapt_width",
-                 "spec_graph_capture_begin", "spec_graph_capture_end", "spec_graph_launch",
+                 "spec_adapt_width_mirror", "spec_graph_capture_begin", "spec_graph_capture_end", "spec_graph_launch",
                  "spec_graph_destroy"):
         monkeypatch.setattr(eng_mod, name, rec(name))
 
@@ -134,6 +134,44 @@ def test_adaptive_single_request_runs_a_width_graph(calls):
     assert _names(calls) == ["spec_graph_launch"]
     e.close()
     assert _names(calls)[-1] == "spec_graph_destroy"
+
+
+def test_adaptive_host_scheduled_widths_one_cycle_late(calls):
+    """width_lag: cycle n runs at the width the device wrote to host-visible slot n % 2 after
+    cycle n - 2 (the first two cycles at set_requests' k): exactly that many draft steps and no
+    gate, a verify and an acceptance of width + 1 rows, and a width update that reads and
+    writes device slot n % 2 and mirrors its choice into host slot n % 2."""
+    e = _engine(b=1, adaptive_cost=[1.0, 1.5, 2.0, 2.5], width_lag=True)
+    assert e.width_lag and not e.width_graph
+    e.set_requests(k=[2])
+    H, Hd = torch.ones((K_MAX + 1, d)), torch.ones((K_MAX, 1, d))
+    widths = []
+    for n in range(5):
+        if n >= 2:  # what the device chose after cycle n - 2
+            e.k_seen[n % 2, 0] = [3, 1, 2][n - 2]
+        calls.clear()
+        e.cycle(H, Hd, K_MAX)
+        w = e.last_width
+        widths.append(w)
+        assert _names(calls) == ["spec_draft_argmax"] * w + [
+            "spec_lmhead_verify", "spec_accept", "spec_adapt_width_mirror"]
+        for j in range(w):
+            assert calls[j][1][15] is None          # the cycle is its width: no gate
+            assert calls[j][1][9] == j              # draft j + 1
+        assert calls[w][1][6] == w + 1              # verify of w + 1 rows
+        assert calls[w][1][4].shape[0] == w + 1
+        acc = calls[w + 1][1]
+        slot = e.k_ring[n % 2].data_ptr()
+        assert acc[7] == w + 1 and acc[2].data_ptr() == slot
+        ad = calls[w + 2][1]
+        assert ad[3].data_ptr() == slot and ad[8].data_ptr() == slot
+        assert ad[9] == e.k_seen[n % 2].data_ptr()  # the host-visible copy of the choice
+        assert ad[4] is e.cost and ad[5] is None
+    assert widths == [2, 2, 3, 1, 2]
+    with pytest.raises(ValueError):
+        _engine(b=2, adaptive_cost=[1.0, 1.5, 2.0, 2.5], width_lag=True)  # one request only
+    with pytest.raises(ValueError):
+        _engine(b=1, width_lag=True)                # adaptive widths only
 
 
 def test_commit_only_with_attached_state(calls):

@@ -11,6 +11,9 @@ spec_draft_argmax, through the C ABI) against the oracle's ``adapt`` module.
 * The engine in adaptive mode at C0, as a width graph and as gated draft steps: identical
   results cycle for cycle, and widths equal to an oracle replay of those results; with no
   cost given, the graph's cycles are timed on the device.
+* Host-scheduled widths (one cycle late, spec_adapt_width_mirror): every cycle's result equals
+  a fixed-width cycle's at the width it ran, the width of cycle n + 2 is the oracle's choice
+  after cycle n, and the host-visible copy equals the device's widths.
 """
 
 import numpy as np
@@ -194,3 +197,58 @@ def test_engine_width_graph_times_its_cycles(c0):
     assert np.isfinite(st["fit"]).all() and st["fit"][2] > 0  # mean cycle cost > 0
     assert np.isfinite(st["rate"]).all()
     eng.close()
+
+
+def test_engine_host_scheduled_widths(c0):
+    """width_lag at C0, 40 cycles: each cycle's acceptance result is bitwise the one a
+    fixed-width engine gives at the width the cycle ran; the width of cycle n + 2 is the
+    oracle's choice from the results of cycles 0..n (no measured costs: the prior decides, a
+    nearly flat one so that deeper widths pay at C0's acceptance and the width moves); the
+    pinned copy the width update writes equals the device's widths."""
+    cfg, W, Wd = c0
+    k_max, alpha = cfg.k, 0.2
+    cost = [1.0 + 0.005 * k for k in range(k_max + 1)]
+    zero = torch.zeros(1, dtype=torch.float32, device=dev())
+    eng = SpecVerifyEngine(Wd, wdt_of(cfg), cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
+                           cfg.eos_id, device=dev(), adaptive_cost=cost, alpha=alpha,
+                           cycle_cost=zero, width_lag=True)
+    eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])  # widths grow from 1
+    fixed = {}
+
+    def fixed_out(w, H, Hd):
+        if w not in fixed:
+            f = SpecVerifyEngine(Wd, wdt_of(cfg), cfg.V, cfg.d, cfg.Vd, 1, w + 1, w, cfg.eos_id,
+                                 device=dev())
+            f.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[w])
+            fixed[w] = f
+        fixed[w].cycle(H[:w + 1], Hd[:w], w)
+        torch.cuda.synchronize()
+        return to_np(fixed[w].out, spec.ACCEPT_OUT_DTYPE)[0].copy()
+
+    ref = o_adapt.new_state(k_max)
+    chosen, widths, near = {}, [], 0
+    for n in range(40):
+        inp = gen.cycle_inputs(cfg, W, n, seed=23, k=k_max)
+        H, Hd = to_dev(inp["H"]), to_dev(inp["Hd"])[:, None, :]
+        eng.cycle(H, Hd, k_max)
+        torch.cuda.synchronize()
+        w = eng.last_width
+        widths.append(w)
+        o = to_np(eng.out, spec.ACCEPT_OUT_DTYPE)[0].copy()
+        assert o["status"] == 0 and o["n_accept"] <= w
+        assert o.tobytes() == fixed_out(w, H, Hd).tobytes(), n
+        if n >= 2 and chosen.get(n - 2) is not None:
+            assert w == chosen[n - 2], n
+        s = n % 2
+        assert eng.k_seen[s].tolist() == to_np(eng.k_ring[s]).tolist(), n
+        o_adapt.observe(ref, 0, int(o["n_accept"]), bool(o["eos_hit"]), w, alpha)
+        kb, vals = o_adapt.choose(ref, [float(x) for x in cost], k_max)
+        if _near_tie(vals, kb):
+            near += 1
+            chosen[n] = None
+        else:
+            chosen[n] = kb
+            assert int(eng.k_seen[s][0]) == kb, n
+    assert near < 10
+    assert len(set(widths)) > 1  # the width moved
+    print(f"\nC0 host-scheduled widths: {widths}")
