@@ -30,6 +30,13 @@ keeps exactly m rows**:
 
 A request whose acceptance status is non-zero commits m = 0 (state restored to slot 0).
 
+Index mode (this library's reading, not on the pages: a commit that moves no state). The live
+state of a request is one of its slots, live_slot; the verify forward reads it there and writes
+the state after verify row r into slot (live_slot + r + 1) mod n_slots, so the snapshot that
+snapshot commit would copy (slot m above) already sits in slot (live_slot + m) mod n_slots, and
+the commit makes that slot the live one. n_slots >= k + 2 keeps a cycle's k + 1 snapshots off
+its own live slot.
+
 The recurrent step is this project's synthetic stand-in for a gated linear-attention layer
 (the real GDN update needs trained weights): per layer and head, with per-row inputs a (scalar
 decay), b [dk], c [dv] and conv input x [W],
@@ -40,7 +47,9 @@ every operation rounded separately to float32 (numpy float32 arithmetic, no fuse
 multiply-add), so snapshot commit and replay must agree byte for byte.
 
 Pinned by: commit == the sequential no-draft run for every m and every EOS position, snapshot
-commit == replay, and closed forms of the step (a = 1, b = 0 keeps S; S = 0 gives b (x) c;
+commit == replay, index commit == snapshot commit for every live slot and m and over chained
+cycles (each cycle's snapshots written relative to the previous commit's live slot), and closed
+forms of the step (a = 1, b = 0 keeps S; S = 0 gives b (x) c;
 small-integer inputs against exact integer arithmetic).
 """
 
@@ -91,6 +100,18 @@ def kv_commit(kv, P, k, m):
 def commit_snapshot(slots_S, slots_conv, m):
     """Snapshot commit: live <- slot[m] (copies)."""
     return np.array(slots_S[m], copy=True), np.array(slots_conv[m], copy=True)
+
+
+def index_slot(live_slot, r, n_slots):
+    """Index mode: the slot holding snapshot r of a cycle (r = 0 the pre-cycle state, r + 1
+    the state after verify row r) whose live state is slot live_slot."""
+    return (int(live_slot) + int(r)) % int(n_slots)
+
+
+def commit_index(live_slot, m, n_slots):
+    """Index commit: no state moves; the slot holding the state after the m kept rows becomes
+    the live slot."""
+    return index_slot(live_slot, m, n_slots)
 
 
 def commit_replay(S0, conv0, a, b, c, x, m):

@@ -45,6 +45,65 @@ def test_commit_equals_sequential_no_draft_for_every_m(k):
         assert cv.tobytes() == cv_ref.tobytes() == cv2.tobytes()
 
 
+@pytest.mark.parametrize("k", [0, 3, 7])
+def test_index_commit_selects_the_snapshot(k):
+    """Index mode: with cycle snapshot r written to slot (L + r) mod n_slots (the live slot L
+    holding the pre-cycle state) and every other slot holding unrelated values, the slot the
+    index commit selects holds, for every L and m, the state ordinary decoding reaches."""
+    cfg = _cfg()
+    n_slots = 9
+    inp = gen.state_inputs(cfg, k, seed=4, n_slots=n_slots)
+    snaps_S, snaps_conv = state.verify_snapshots(inp["S0"], inp["conv0"], inp["a"], inp["b"],
+                                                 inp["c"], inp["x"], k + 1)
+    rng = np.random.default_rng(k)
+    for L in range(n_slots):
+        slots_S = rng.standard_normal((n_slots,) + snaps_S.shape[1:]).astype(np.float32)
+        slots_conv = rng.standard_normal((n_slots,) + snaps_conv.shape[1:]).astype(np.float32)
+        for r in range(k + 2):
+            j = state.index_slot(L, r, n_slots)
+            slots_S[j], slots_conv[j] = snaps_S[r], snaps_conv[r]
+        for m in range(0, k + 2):
+            L2 = state.commit_index(L, m, n_slots)
+            _, _, S_ref, cv_ref = state.sequential_no_draft(
+                inp["kv_pre"], inp["P"], inp["kv_rows"], inp["S0"], inp["conv0"], inp["a"],
+                inp["b"], inp["c"], inp["x"], m)
+            assert slots_S[L2].tobytes() == S_ref.tobytes(), (L, m)
+            assert slots_conv[L2].tobytes() == cv_ref.tobytes(), (L, m)
+            S_snap, cv_snap = state.commit_snapshot(snaps_S, snaps_conv, m)
+            assert slots_S[L2].tobytes() == S_snap.tobytes()
+    assert state.commit_index(5, 0, n_slots) == 5          # nothing kept: the live slot stays
+    assert state.commit_index(7, 4, n_slots) == 2          # wraps around
+
+
+def test_index_commit_over_chained_cycles():
+    """Three cycles in index mode, each verify forward reading the live slot the previous commit
+    chose and writing its snapshots after it: the live state after each commit equals ordinary
+    decoding of all rows kept so far, and no cycle overwrites its own live slot."""
+    cfg = _cfg()
+    n_slots = 9
+    inp0 = gen.state_inputs(cfg, 7, seed=6, n_slots=n_slots)
+    slots_S = np.zeros((n_slots,) + np.asarray(inp0["S0"]).shape, dtype=np.float32)
+    slots_conv = np.zeros((n_slots,) + np.asarray(inp0["conv0"]).shape, dtype=np.float32)
+    L = 3
+    slots_S[L], slots_conv[L] = inp0["S0"], inp0["conv0"]
+    S_seq, cv_seq = np.array(inp0["S0"]), np.array(inp0["conv0"])
+    for cyc, (k, m) in enumerate([(7, 5), (3, 0), (6, 7)]):
+        inp = gen.state_inputs(cfg, k, seed=10 + cyc, n_slots=n_slots)
+        S, cv = slots_S[L].copy(), slots_conv[L].copy()
+        for r in range(k + 1):  # the verify forward, from the live slot
+            S, cv = state.synthetic_step(S, cv, inp["a"][r], inp["b"][r], inp["c"][r],
+                                         inp["x"][r])
+            j = state.index_slot(L, r + 1, n_slots)
+            assert j != L
+            slots_S[j], slots_conv[j] = S, cv
+        for r in range(m):  # ordinary decoding of the kept rows
+            S_seq, cv_seq = state.synthetic_step(S_seq, cv_seq, inp["a"][r], inp["b"][r],
+                                                 inp["c"][r], inp["x"][r])
+        L = state.commit_index(L, m, n_slots)
+        assert slots_S[L].tobytes() == S_seq.tobytes(), cyc
+        assert slots_conv[L].tobytes() == cv_seq.tobytes(), cyc
+
+
 def test_eos_keeps_no_state_past_eos():
     """An accepted EOS at draft position i emits i tokens; the state keeps x_0, d_1..d_{i-1}."""
     cfg = _cfg()
