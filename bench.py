@@ -735,21 +735,23 @@ def c3_cycle(dev, W, Wd, hbm_peak, K=400):
                                    seeds, pos, i - 1, drafts_pool[c, i - 1:], 7, None, cfg.Vd,
                                    qs[(i - 1) * spec.ROWSTATS_BYTES:], None, ws)
 
-    def verify_cycle(c):
+    def verify_cycle(c, mode=spec.SPEC_COMMIT_SNAPSHOT):
         k = ks[c]
         spec.spec_lmhead_verify(Wd, spec.SPEC_BF16, cfg.V, cfg.d, Hp_d[c], 1, k + 1, temps, None,
                                 stats, ws)
         spec.spec_accept(1, 7, k_pool[c:c + 1], drafts_pool[c:c + 1], None, stats, cfg.V, k + 1,
                          None, None, cfg.Vd, cfg.Vd, temps, cfg.eos_id, seeds, pos, out, cnt, ws)
-        spec.spec_commit_rollback(1, st.desc, out, k_pool[c:c + 1], spec.SPEC_COMMIT_SNAPSHOT)
+        spec.spec_commit_rollback(1, st.desc, out, k_pool[c:c + 1], mode)
 
     for c in range(n_pool):
         drafts_of(c)
     res = {}
-    for name, with_drafts in (("verify_cycle", False), ("full_cycle", True)):
+    snap, index = spec.SPEC_COMMIT_SNAPSHOT, spec.SPEC_COMMIT_INDEX
+    for name, with_drafts, mode in (("verify_cycle", False, snap), ("full_cycle", True, snap),
+                                    ("verify_cycle_index", False, index)):
         st.kv_len.fill_(cfg.context)
         for c in range(5):
-            verify_cycle(c)
+            verify_cycle(c, mode)
         st.kv_len.fill_(cfg.context)
         cnt.zero_()
         torch.cuda.synchronize()
@@ -758,14 +760,14 @@ def c3_cycle(dev, W, Wd, hbm_peak, K=400):
         for c in range(K):
             if with_drafts:
                 drafts_of(c % n_pool)
-            verify_cycle(c % n_pool)
+            verify_cycle(c % n_pool, mode)
         b.record()
         torch.cuda.synchronize()
         s_ = a.elapsed_time(b) / 1e3
         cn = cnt.cpu().numpy().view(spec.COUNTERS_DTYPE)[0]
         rows = sum(ks[c % n_pool] + 1 for c in range(K))
         emitted = float(cn["emitted"])
-        commit_bytes = 2 * 4 * (st.rec_elems + st.conv_elems)
+        commit_bytes = 2 * 4 * (st.rec_elems + st.conv_elems) if mode == snap else 0
         zero_fill = (rows - emitted) * 2 * cfg.kv_layers * cfg.kv_row_bytes
         cyc_bytes = (K * (cfg.V * cfg.d * 2 + commit_bytes) + rows * (cfg.d * 2 + 16) +
                      zero_fill) / K
@@ -777,7 +779,8 @@ def c3_cycle(dev, W, Wd, hbm_peak, K=400):
                               "hbm_frac": round(cyc_bytes * K / s_ / 1e9 / hbm_peak, 4)})
     res["final_len"] = int(st.kv_len.cpu()[0])
     res["workload"] = ("k ~ U{1..7}, verify k+1 rows + greedy acceptance + snapshot commit of the "
-                       "64K-context state, P from 63,488")
+                       "64K-context state, P from 63,488; verify_cycle_index: the same with the "
+                       "index commit (the live state a slot, no state bytes moved)")
     del st
     return res
 
@@ -867,6 +870,7 @@ def commit_bench(dev, hbm_peak, reps=64, warm=8):
     c = torch.randn((ns - 1) * L * H * dv, device=dev)
     x = torch.randn((ns - 1) * L * cfg.conv_width, device=dev)
     descs = []
+    live_slot = torch.zeros(n_live, dtype=torch.int32, device=dev)  # index mode
     for j in range(n_live):
         d = spec.spec_state_desc()
         d.kv, d.kv_request_stride, d.kv_layers = kv.data_ptr(), kvb, cfg.kv_layers
@@ -879,6 +883,7 @@ def commit_bench(dev, hbm_peak, reps=64, warm=8):
         d.conv_slots, d.n_slots = cslots.data_ptr() + 4 * j * conv_elems, ns
         d.step_a, d.step_b, d.step_c, d.conv_in = (a.data_ptr(), b.data_ptr(), c.data_ptr(),
                                                    x.data_ptr())
+        d.live_slot = live_slot[j:].data_ptr()
         descs.append(d)
     accs = []
     for m in range(1, 9):  # n_emit = m: slot m is copied, KV rows [P+m, P+8) are cleared
@@ -888,9 +893,10 @@ def commit_bench(dev, hbm_peak, reps=64, warm=8):
     k_d = torch.tensor([7], dtype=torch.int32, device=dev)
     state_bytes = 2 * 4 * (rec_elems + conv_elems)
     out = {}
-    for mode, name in ((spec.SPEC_COMMIT_SNAPSHOT, "snapshot"), (spec.SPEC_COMMIT_REPLAY, "replay")):
+    for mode, name in ((spec.SPEC_COMMIT_SNAPSHOT, "snapshot"), (spec.SPEC_COMMIT_REPLAY, "replay"),
+                       (spec.SPEC_COMMIT_INDEX, "index")):
         def launch(i):
-            m_idx = (i // n_live) % 8 if mode == spec.SPEC_COMMIT_SNAPSHOT else 3
+            m_idx = (i // n_live) % 8 if mode != spec.SPEC_COMMIT_REPLAY else 3
             spec.spec_commit_rollback(1, descs[i % n_live], accs[m_idx], k_d, mode)
             return m_idx + 1
         kv_len.fill_(cfg.context)  # each commit keeps at most 8 rows: P stays below capacity
@@ -911,11 +917,12 @@ def commit_bench(dev, hbm_peak, reps=64, warm=8):
         t = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ts) / 1e3
         # KV rows cleared: [P+m, P+k+1) of both planes of every KV layer
         kv_bytes = statistics.mean(8 - m for m in kept) * cfg.kv_row_bytes * 2 * cfg.kv_layers
-        moved = state_bytes + kv_bytes
+        moved = (state_bytes if mode != spec.SPEC_COMMIT_INDEX else 0) + kv_bytes
         out[name] = {"us": round(t * 1e6, 2), "bytes": int(moved),
                      "gbs": round(moved / t / 1e9, 1), "frac": round(moved / t / 1e9 / hbm_peak, 4)}
     out["method"] = ("one request, 64 launches back to back between events; sources and "
-                     "destinations rotated over 302 MB so no commit hits L2 from an earlier one")
+                     "destinations rotated over 302 MB so no commit hits L2 from an earlier one; "
+                     "index: the live state a slot, only the index and the KV rows move")
     return out
 
 
@@ -1032,6 +1039,8 @@ class BatchedState:
         d.rec_live, d.rec_slots = self.live.data_ptr(), self.slots.data_ptr()
         d.conv_rows, d.conv_width = cfg.conv_rows, cfg.conv_width
         d.conv_live, d.conv_slots, d.n_slots = self.clive.data_ptr(), self.cslots.data_ptr(), ns
+        self.live_slot = torch.zeros(B, dtype=torch.int32, device=dev)  # index mode
+        d.live_slot = self.live_slot.data_ptr()
         self.desc = d
 
 

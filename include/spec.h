@@ -140,6 +140,10 @@ typedef struct {
  *             step_b [B][n_slots-1][rec_layers][rec_heads][rec_dk]
  *             step_c [B][n_slots-1][rec_layers][rec_heads][rec_dv]
  *             conv_in[B][n_slots-1][rec_layers][conv_width]         conv input of row r
+ *   index mode (SPEC_COMMIT_INDEX only): live_slot [B] int32, the slot of rec_slots (and of
+ *             conv_slots) that holds request b's live state; the cycle's verify forward read
+ *             it there and wrote the state after verify row r into slot
+ *             (live_slot[b] + r + 1) mod n_slots. rec_live and conv_live are not used.
  * n_slots >= k_max + 2. All float arrays 16-byte aligned; rec_dv, conv_width multiples of 4;
  * kv_row_bytes and kv_request_stride multiples of 16; one request's recurrent state
  * (rec_layers*rec_heads*rec_dk*rec_dv) and conv state (rec_layers*conv_rows*conv_width) each
@@ -162,9 +166,10 @@ typedef struct {
   const float *step_b;
   const float *step_c;
   const float *conv_in;
+  int32_t *live_slot;
 } spec_state_desc;
 
-enum { SPEC_COMMIT_SNAPSHOT = 0, SPEC_COMMIT_REPLAY = 1 };
+enum { SPEC_COMMIT_SNAPSHOT = 0, SPEC_COMMIT_REPLAY = 1, SPEC_COMMIT_INDEX = 2 };
 
 /* Workspace bytes needed by any call of this library on the current device for vocabularies
  * up to V rows and up to max_batch requests per call. */
@@ -450,7 +455,14 @@ spec_status spec_graph_destroy(void *graph, void *exec);
  *                         S = fl32(fl32(a*S) + fl32(b_i*c_j)) per layer and head, each
  *                         operation rounded separately; conv_live <- the last conv_rows rows
  *                         of (conv_slots[0] rows, conv_in rows 0..m-1).
- * Both modes produce identical bytes when the slots were captured with the same step.
+ *   SPEC_COMMIT_INDEX:    live_slot[b] <- (live_slot[b] + m) mod n_slots: the slot that holds
+ *                         the state snapshot commit would copy becomes the live one, and no
+ *                         state byte moves (this library's form, not the pages': it needs the
+ *                         forward pass to read and write the state through live_slot). A
+ *                         live_slot[b] outside [0, n_slots) is left as it is, with
+ *                         commit_status[b] = SPEC_REQ_BAD_K.
+ * The snapshot and replay modes produce identical bytes when the slots were captured with the
+ * same step; index mode selects those same bytes in place.
  *   k [B] the cycle's draft counts; commit_status [B] int32 or NULL (SPEC_REQ_KV_OVERFLOW).
  */
 spec_status spec_commit_rollback(int32_t B, const spec_state_desc *st,

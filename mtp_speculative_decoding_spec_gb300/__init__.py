@@ -11,7 +11,8 @@ from . import _abi
 from ._abi import (ACCEPT_OUT_DTYPE, COUNTERS_DTYPE, REQ_BAD_FILTER, REQ_BAD_K,  # noqa: F401
                    REQ_BAD_TOKEN,
                    REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_NONFINITE, REQ_OK, ROWSTATS_DTYPE,
-                   SPEC_BF16, SPEC_COMMIT_REPLAY, SPEC_COMMIT_SNAPSHOT, SPEC_F32, SPEC_Q4A32,
+                   SPEC_BF16, SPEC_COMMIT_INDEX, SPEC_COMMIT_REPLAY, SPEC_COMMIT_SNAPSHOT, SPEC_F32,
+                   SPEC_Q4A32,
                    WIDTH_STATE_DTYPE, spec_state_desc)
 
 ROWSTATS_BYTES = ROWSTATS_DTYPE.itemsize

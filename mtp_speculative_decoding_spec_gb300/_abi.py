@@ -11,7 +11,7 @@ LIB_PATH = os.path.join(HERE, "libspec.so")
 
 SPEC_OK, SPEC_ERR_INVALID, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
 SPEC_BF16, SPEC_F32, SPEC_Q4A32 = 0, 1, 2
-SPEC_COMMIT_SNAPSHOT, SPEC_COMMIT_REPLAY = 0, 1
+SPEC_COMMIT_SNAPSHOT, SPEC_COMMIT_REPLAY, SPEC_COMMIT_INDEX = 0, 1, 2
 REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN, \
     REQ_BAD_FILTER = range(7)
 
@@ -66,6 +66,7 @@ class spec_state_desc(ctypes.Structure):
         ("step_b", ctypes.c_void_p),
         ("step_c", ctypes.c_void_p),
         ("conv_in", ctypes.c_void_p),
+        ("live_slot", ctypes.c_void_p),
     ]
 
 

@@ -896,7 +896,8 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
                                  const spec_accept_out* acc, const int32_t* k, int32_t mode,
                                  int32_t* commit_status, spec_stream_t stream) {
   if (B < 1 || !st || !acc || !k) return SPEC_ERR_INVALID;
-  if (mode != SPEC_COMMIT_SNAPSHOT && mode != SPEC_COMMIT_REPLAY) return SPEC_ERR_INVALID;
+  if (mode != SPEC_COMMIT_SNAPSHOT && mode != SPEC_COMMIT_REPLAY && mode != SPEC_COMMIT_INDEX)
+    return SPEC_ERR_INVALID;
   if (st->n_slots < 2) return SPEC_ERR_INVALID;
   if (st->kv_layers < 0 || st->rec_layers < 0 || st->conv_rows < 0) return SPEC_ERR_INVALID;
   if (st->kv_layers > 0) {
@@ -907,7 +908,9 @@ spec_status spec_commit_rollback(int32_t B, const spec_state_desc* st,
         B > 1)
       return SPEC_ERR_INVALID;
   }
-  if (st->rec_layers > 0) {
+  if (st->rec_layers > 0 && mode == SPEC_COMMIT_INDEX) {
+    if (!st->live_slot) return SPEC_ERR_INVALID;  // the state itself is not touched
+  } else if (st->rec_layers > 0) {
     if (st->rec_heads < 1 || st->rec_dk < 1 || st->rec_dv < 4 || st->rec_dv % 4 != 0)
       return SPEC_ERR_INVALID;
     // the kernels index one request's state in 16-byte vectors with 32-bit integers

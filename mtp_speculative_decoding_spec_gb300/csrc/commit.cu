@@ -14,7 +14,9 @@
 // rows [P+m, P+k+1) and moves the length; all blocks stream the recurrent state with 16-byte
 // loads and stores. Two kernels, one per mode: the copy (snapshot mode: slot m) and the replay
 // (slot 0 advanced over rows 0..m-1 in registers, head by head, one pass over the state
-// whatever m is).
+// whatever m is). Index mode moves no state: the forward pass keeps the live state in a slot
+// (live_slot) and writes each verify row's snapshot into the slots after it, so the commit
+// only makes the kept prefix's slot the live one.
 #include "params.cuh"
 
 namespace spec {
@@ -101,6 +103,25 @@ __global__ void __launch_bounds__(256, 4) commit_snapshot_kernel(const __grid_co
                                                 (static_cast<size_t>(b) * ns + m) * celems),
                 static_cast<int>(celems / 4), gt, gs);
     }
+  }
+}
+
+// Index mode: one block per request trims the KV rows and moves live_slot[b] by the m kept rows
+// (mod n_slots): that slot holds the state snapshot mode would copy into rec_live and conv_live.
+__global__ void __launch_bounds__(256) commit_index_kernel(const __grid_constant__ CommitParams p) {
+  pdl_wait();
+  const int b = blockIdx.x;
+  int kk;
+  bool kvalid;
+  const int m = kept_rows(p, b, kk, kvalid);
+  kv_trim(p, b, m, kk, kvalid);  // every thread: it holds a block barrier
+  if (threadIdx.x == 0 && p.st.rec_layers > 0) {
+    const int ns = p.st.n_slots;
+    const int live = p.st.live_slot[b];
+    if (live >= 0 && live < ns)
+      p.st.live_slot[b] = (live + m) % ns;
+    else if (p.commit_status)
+      p.commit_status[b] = SPEC_REQ_BAD_K;
   }
 }
 
@@ -252,6 +273,8 @@ cudaError_t commit_launch(const CommitParams& prm, int B, int blocks_per_request
   if (prm.mode == SPEC_COMMIT_SNAPSHOT)
     return launch_pdl(commit_snapshot_kernel, dim3(blocks_per_request, B), dim3(256), 0, stream,
                       prm);
+  if (prm.mode == SPEC_COMMIT_INDEX)
+    return launch_pdl(commit_index_kernel, dim3(B), dim3(256), 0, stream, prm);
   // the replay: one block per (layer, head, chunk of the head's state), at least enough blocks
   // for the conv rows and the KV trim
   const spec_state_desc& st = prm.st;

@@ -112,6 +112,11 @@ def test_host_validation_without_gpu(lib):
     d.kv_layers = 0
     assert lib.spec_commit_rollback(1, ctypes.byref(d), fake, fake, 5, null, null) == 1
     assert lib.spec_commit_rollback(1, None, fake, fake, 0, null, null) == 1
+    # index mode: a recurrent state needs the live-slot array, and nothing else of the state
+    d.rec_layers, d.rec_heads, d.rec_dk, d.rec_dv = 2, 2, 4, 4
+    assert lib.spec_commit_rollback(1, ctypes.byref(d), fake, fake, spec.SPEC_COMMIT_INDEX,
+                                    null, null) == 1
+    assert lib.spec_commit_rollback(1, ctypes.byref(d), fake, fake, 3, null, null) == 1
 
 
 def test_host_validation_of_the_later_entry_points(lib):
@@ -220,7 +225,8 @@ def test_no_cpu_fallback_in_product_package():
 
 # threads per block of each kernel, as launched by abi.cu / gemv.cu
 _BLOCK_THREADS = {"gemv_rows_kernel": 16 * 32, "gemv_tc_kernel": 8 * 32, "gemv_q4_kernel": 16 * 32, "gemm_rows_tc_kernel": 10 * 32,
-                  "gemm_rows_combine_kernel": 256, "accept_kernel": 256, "commit_snapshot_kernel": 256,
+                  "gemm_rows_combine_kernel": 256, "accept_kernel": 256,
+                  "commit_index_kernel": 256, "commit_snapshot_kernel": 256,
                   "commit_replay_kernel": 128, "adapt_width_kernel": 128,
                   "width_select_kernel": 32, "copy_from_host_kernel": 256}
 

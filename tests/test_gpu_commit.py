@@ -3,7 +3,9 @@
 Rejected rows leave every cache and recurrent component identical to ordinary decoding, and
 capture-commit and replay agree (DS4Server issue #98, *Completion requirements*; lucebox-hub PR
 #15, *Exactness*). Checked for every m = 0..k+1, both modes, several requests in one call, a
-failed cycle, KV overflow, and the full-size state of a 64K-context workload.
+failed cycle, KV overflow, and the full-size state of a 64K-context workload. Index mode
+(the live state kept in a slot, the commit moving only the index): the selected slot holds the
+oracle's state, no state byte moves, and an invalid live slot is reported.
 """
 
 import numpy as np
@@ -168,4 +170,75 @@ def test_invalid_descriptors_rejected():
     with pytest.raises(spec.SpecError):
         spec.spec_commit_rollback(1, bad, acc, k, 0)
     with pytest.raises(spec.SpecError):
-        spec.spec_commit_rollback(1, ds.desc, acc, k, 2)
+        spec.spec_commit_rollback(1, ds.desc, acc, k, 3)  # no such mode
+    with pytest.raises(spec.SpecError):  # index mode without the live-slot array
+        spec.spec_commit_rollback(1, ds.desc, acc, k, spec.SPEC_COMMIT_INDEX)
+
+
+def _index_state(cfg, reqs, lives):
+    """DevState whose slots follow the index convention: request b's snapshot r in slot
+    (lives[b] + r) mod N_SLOTS, the live-slot array set to lives."""
+    rot = []
+    for r, L in zip(reqs, lives):
+        S = np.empty_like(r["slots_S"])
+        C = np.empty_like(r["slots_conv"])
+        for j in range(N_SLOTS):
+            S[o_st.index_slot(L, j, N_SLOTS)] = r["slots_S"][j]
+            C[o_st.index_slot(L, j, N_SLOTS)] = r["slots_conv"][j]
+        rot.append(dict(r, slots_S=S, slots_conv=C))
+    ds = DevState(cfg, rot)
+    ds.live = to_dev(np.array(lives, dtype=np.int32))
+    ds.desc.live_slot = ds.live.data_ptr()
+    return ds, rot
+
+
+@pytest.mark.parametrize("k", [0, 3, 7])
+def test_index_commit_c0(k):
+    """Several requests, each at its own live slot (wrapping included), every m = 0..k+1 and a
+    failed cycle: the new live slot is the oracle's, the KV trim is the oracle's, the selected
+    slot holds the state ordinary decoding reaches, and no state byte moved."""
+    ensure_built()
+    cfg = configs.get(0)
+    ms = list(range(0, k + 2)) + [k + 1]
+    statuses = [0] * (k + 2) + [1]
+    lives = [(3 * i + 5) % N_SLOTS for i in range(len(ms))]
+    reqs = [_request(cfg, k, seed=200 + 10 * k + i, P=20 + 40 * i) for i in range(len(ms))]
+    ds, rot = _index_state(cfg, reqs, lives)
+    slots_before = to_np(ds.rec_slots).tobytes(), to_np(ds.conv_slots).tobytes()
+    cs = torch.full((len(ms),), -9, dtype=torch.int32, device=dev())
+    spec.spec_commit_rollback(len(ms), ds.desc, _acc(statuses, ms),
+                              to_dev(np.array([k] * len(ms), np.int32)), spec.SPEC_COMMIT_INDEX,
+                              cs)
+    torch.cuda.synchronize()
+    live, kv, L = to_np(ds.live), to_np(ds.kv), to_np(ds.kv_len)
+    slots_S, slots_C = to_np(ds.rec_slots), to_np(ds.conv_slots)
+    assert (slots_S.tobytes(), slots_C.tobytes()) == slots_before  # nothing moved
+    assert (to_np(ds.rec_live) == -1.0).all() and (to_np(ds.conv_live) == -1.0).all()
+    for b, r in enumerate(reqs):
+        m = o_st.kept_rows(statuses[b], ms[b])
+        assert live[b] == o_st.commit_index(lives[b], m, N_SLOTS), b
+        kv_ref, len_ref = o_st.kv_commit(r["kv"], r["P"], r["k"], m)
+        assert L[b] == len_ref and kv[b].tobytes() == kv_ref.tobytes(), b
+        _, _, S_seq, c_seq = o_st.sequential_no_draft(
+            r["kv_pre"], r["P"], r["kv_rows"], r["S0"], r["conv0"], r["a"], r["b"], r["c"],
+            r["x"], m)
+        assert slots_S[b, live[b]].tobytes() == S_seq.tobytes(), b
+        assert slots_C[b, live[b]].tobytes() == c_seq.tobytes(), b
+    assert (to_np(cs) == 0).all()
+
+
+def test_index_commit_invalid_live_slot():
+    """A live slot outside [0, n_slots): left as it is, SPEC_REQ_BAD_K; the KV trim still runs
+    and the other requests commit."""
+    ensure_built()
+    cfg = configs.get(0)
+    reqs = [_request(cfg, 2, seed=300 + i, P=50 + 60 * i) for i in range(3)]
+    ds, _ = _index_state(cfg, reqs, [1, 4, 8])
+    ds.live.copy_(torch.tensor([1, N_SLOTS, -2], dtype=torch.int32))
+    cs = torch.full((3,), -9, dtype=torch.int32, device=dev())
+    spec.spec_commit_rollback(3, ds.desc, _acc([0, 0, 0], [2, 2, 2]),
+                              to_dev(np.array([2, 2, 2], np.int32)), spec.SPEC_COMMIT_INDEX, cs)
+    torch.cuda.synchronize()
+    assert list(to_np(ds.live)) == [3, N_SLOTS, -2]
+    assert list(to_np(cs)) == [0, spec.REQ_BAD_K, spec.REQ_BAD_K]
+    assert list(to_np(ds.kv_len)) == [r["P"] + 2 for r in reqs]
