@@ -864,7 +864,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
     // then the ratio test of the draft against p' (q one-hot), a residual draw at the first
     // rejection, or the bonus draw after row k
     __shared__ unsigned long long s_topr[kMaxRows][kMaxTopK];  // each row's top-k, descending
-    __shared__ int f_stop;
     __shared__ Decision F;
     const int K = p.top_k[b];
     const double tp = static_cast<double>(p.top_p[b]);
@@ -873,7 +872,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       F = D;
       F.need = 0;
       F.srow = -1;
-      f_stop = 0;
     }
     // every row's top-k set first: one warp per row, all rows at once (up to 256 slices);
     // the block tournament row by row above that
@@ -886,86 +884,110 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptPara
       }
     }
     __syncthreads();
-    for (int r = 0; r <= k; ++r) {
-      const unsigned long long* s_top = s_topr[r];
-      if (tid == 0) {
+    // Each row's target p' at once, one warp per row (lane j: the row's j-th key): the weights
+    // quantise(exp((z_j - z_top) / T)), their exact integer sum W, the top-p cut (key j is kept
+    // while the weight ahead of it, a warp prefix sum, is below top_p * W; the prefix only
+    // grows, so the kept keys are the leading ones), the kept mass Wk, and the draft's place in
+    // the kept set. Integer sums are exact in any order: the same values the row-by-row loop
+    // below once computed itself.
+    __shared__ unsigned long long f_w[kMaxRows][kMaxTopK], f_Wk[kMaxRows], f_wx[kMaxRows];
+    __shared__ int f_id[kMaxRows][kMaxTopK], f_n[kMaxRows], f_jx[kMaxRows];
+    if (warp <= k) {
+      const int r = warp;
+      const unsigned long long key = lane < K ? s_topr[r][lane] : 0ull;
+      const unsigned zero = __ballot_sync(0xffffffffu, key == 0ull);
+      const int nk = zero ? __ffs(zero) - 1 : 32;  // the leading non-empty keys
+      const float ztop = key_logit(s_topr[r][0]);
+      const int id = key_id(key);
+      const unsigned long long w =
+          lane < nk ? quantise(expf(__fmul_rn(__fsub_rn(key_logit(key), ztop), invT))) : 0ull;
+      unsigned long long incl = w;  // inclusive prefix sum over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned long long W = __shfl_sync(0xffffffffu, incl, 31);
+      const double cut = tp * static_cast<double>(W);
+      const bool kept = lane < nk && static_cast<double>(incl - w) < cut;
+      const unsigned keptm = __ballot_sync(0xffffffffu, kept);
+      unsigned long long wk = kept ? w : 0ull;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) wk += __shfl_xor_sync(0xffffffffu, wk, o);
+      const int x = r < k ? sx[r] : -1;
+      const unsigned hit = __ballot_sync(0xffffffffu, kept && id == x);
+      const int jx = hit ? 31 - __clz(hit) : -1;  // ids are distinct: at most one hit
+      f_w[r][lane] = w;
+      f_id[r][lane] = id;
+      if (lane == 0) {
+        f_n[r] = __popc(keptm);
+        f_Wk[r] = wk;
+        f_jx[r] = jx;
+      }
+      const unsigned long long wx = __shfl_sync(0xffffffffu, w, jx >= 0 ? jx : 0);
+      if (lane == 0) f_wx[r] = jx >= 0 ? wx : 0ull;
+    }
+    __syncthreads();
+    // the decisions, row after row: the ratio test of the draft against p' (q one-hot), a
+    // residual draw at the first rejection, or the bonus draw after row k
+    if (tid == 0) {
+      for (int r = 0; r <= k; ++r) {
+        const int n = f_n[r];
         int id[kMaxTopK];
         unsigned long long w[kMaxTopK];
-        int nk = 0;
-        float ztop = 0.f;
-        for (int j = 0; j < K; ++j) {
-          const unsigned long long key = s_top[j];
-          if (key == 0ull) break;
-          const float zj = key_logit(key);
-          if (j == 0) ztop = zj;
-          id[nk] = key_id(key);
-          w[nk] = quantise(expf(__fmul_rn(__fsub_rn(zj, ztop), invT)));
-          ++nk;
-        }
-        unsigned long long W = 0ull;
-        for (int j = 0; j < nk; ++j) W += w[j];
-        // top-p: keep while the mass ahead is below top_p of the top-k mass
-        int n = 0;
-        unsigned long long ahead = 0ull;
-        const double cut = tp * static_cast<double>(W);
-        while (n < nk && static_cast<double>(ahead) < cut) ahead += w[n++];
-        unsigned long long Wk = 0ull;
-        for (int j = 0; j < n; ++j) Wk += w[j];
         bool emitted_draw = false;
         int tok = -1;
         if (r < k) {
           const int x = sx[r];
-          int jx = -1;
-          for (int j = 0; j < n; ++j)
-            if (id[j] == x) jx = j;
-          const unsigned long long wx = (jx >= 0) ? w[jx] : 0ull;
+          const int jx = f_jx[r];
           const uint32_t ua = uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_ACCEPT);
-          if (wx > 0ull && u_le_ratio(ua, Wk, wx)) {
+          if (f_wx[r] > 0ull && u_le_ratio(ua, f_Wk[r], f_wx[r])) {
             F.tokens[F.ntok++] = x;
             F.n_accept++;
             if (p.eos >= 0 && x == p.eos) {
               F.eos_hit = 1;
-              f_stop = 1;
+              break;
             }
-          } else {  // residual: p' without the draft (p' itself if nothing else is left)
-            int m = 0;
-            for (int j = 0; j < n; ++j) {
-              if (j == jx) continue;
-              id[m] = id[j];
-              w[m] = w[j];
-              ++m;
-            }
-            unsigned long long rest = 0ull;
-            for (int j = 0; j < m; ++j) rest += w[j];
-            if (rest == 0ull) m = 0;
-            if (m == 0) {  // rebuild p' (the cut set) from the keys
-              for (int j = 0; j < n; ++j) {
-                const unsigned long long key = s_top[j];
-                id[j] = key_id(key);
-                w[j] = quantise(expf(__fmul_rn(__fsub_rn(key_logit(key), ztop), invT)));
-              }
-              m = n;
-            }
-            tok = small_draw(id, w, m,
-                             uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_RESIDUAL));
-            F.need = 1;
-            emitted_draw = true;
+            continue;
           }
+          // residual: p' without the draft (p' itself if nothing else is left)
+          int m = 0;
+          unsigned long long rest = 0ull;
+          for (int j = 0; j < n; ++j) {
+            if (j == jx) continue;
+            id[m] = f_id[r][j];
+            w[m] = f_w[r][j];
+            rest += w[m];
+            ++m;
+          }
+          if (rest == 0ull) {
+            for (int j = 0; j < n; ++j) {
+              id[j] = f_id[r][j];
+              w[j] = f_w[r][j];
+            }
+            m = n;
+          }
+          tok = small_draw(id, w, m,
+                           uniform_u24(p.seed[b], p.pos_base[b] + r, PURPOSE_RESIDUAL));
+          F.need = 1;
+          emitted_draw = true;
         } else {
+          for (int j = 0; j < n; ++j) {
+            id[j] = f_id[r][j];
+            w[j] = f_w[r][j];
+          }
           tok = small_draw(id, w, n, uniform_u24(p.seed[b], p.pos_base[b] + k, PURPOSE_BONUS));
           F.need = 2;
           emitted_draw = true;
         }
         if (emitted_draw) {
-          if (tok < 0) tok = id[0];  // unreachable: the cut set always has weight
+          if (tok < 0) tok = f_id[r][0];  // unreachable: the cut set always has weight
           F.srow = r;
           F.tokens[F.ntok++] = tok;
           if (p.eos >= 0 && tok == p.eos) F.eos_hit = 1;
-          f_stop = 1;
+          break;
         }
       }
-      __syncthreads();
-      if (f_stop) break;
     }
     if (tid == 0) {
       finalize(p, b, F, k);
@@ -1130,10 +1152,14 @@ cudaError_t adapt_launch(const AdaptParams& prm, cudaStream_t stream) {
 
 cudaError_t accept_launch(const AcceptParams& prm, cudaStream_t stream) {
   dim3 grid(prm.NS, prm.B);
-  if (prm.filtered)
-    return launch_pdl(accept_kernel<true>, grid, dim3(kAcceptThreads),
-                      kFilterStageKeys * static_cast<int>(sizeof(unsigned long long)), stream,
-                      prm);
+  if (prm.filtered) {
+    // the stage of candidate keys, dynamic, on top of the static arrays: past 48 KB together
+    constexpr int kStage = kFilterStageKeys * static_cast<int>(sizeof(unsigned long long));
+    static SmemAllowance allowed;
+    const cudaError_t e = allow_dynamic_smem(accept_kernel<true>, kStage, allowed);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(accept_kernel<true>, grid, dim3(kAcceptThreads), kStage, stream, prm);
+  }
   return launch_pdl(accept_kernel<false>, grid, dim3(kAcceptThreads), 0, stream, prm);
 }
 
