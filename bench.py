@@ -254,7 +254,7 @@ def run_ours(args, rank, local_rank, world):
     Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
 
     eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k, cfg.eos_id,
-                           device=dev, want_q_logits=False)
+                           device=dev, want_q_logits=False, fuse_greedy=True)
     eng.set_requests(temps=[0.0], seeds=[0], pos=[0], k=[k])
     # drafts of every pool entry, produced by the draft head on the GPU before timing
     drafts_pool = torch.zeros((n_pool, 1, k), dtype=torch.int32, device=dev)
@@ -264,7 +264,12 @@ def run_ours(args, rank, local_rank, world):
         drafts_pool[c].copy_(eng.drafts[:, :k])
     torch.cuda.synchronize()
 
-    def step(c):
+    def step(c):  # greedy verify + acceptance, fused into the LM-head kernel's last block
+        spec.spec_verify_accept_greedy(Wd, spec.SPEC_BF16, cfg.V, cfg.d, Hp_d[c], 1, k + 1,
+                                       eng.temps, eng.logits, eng.stats, k, eng.k,
+                                       drafts_pool[c], cfg.eos_id, eng.out, eng.counters, eng.ws)
+
+    def step_two_kernels(c):  # the same step as two launches: verify, then acceptance
         eng.verify(Hp_d[c])
         spec.spec_accept(1, k, eng.k, drafts_pool[c], eng.logits, eng.stats, cfg.V, k + 1,
                          None, None, cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id, eng.seeds, eng.pos,
@@ -307,12 +312,22 @@ def run_ours(args, rank, local_rank, world):
         "ms_per_step": round(elapsed_max / K * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"parallelism": f"replicas x{world}",
-                                        "step": "verify GEMV (2 rows) + acceptance"}),
+                                        "step": "verify GEMV (2 rows) + greedy acceptance, "
+                                                "fused into the GEMV's last block"}),
         "roofline": roof,
         "acceptance": round(float(cnt["accepted"]) / max(1.0, float(cnt["drafted"])), 4),
-        "gpu_launches": 2 * K,
+        "gpu_launches": K,
         "workspace_error": err,
     }
+    # the same step as two launches (verify, then the acceptance kernel), timed the same way
+    t_start.record(stream)
+    for c in range(K):
+        step_two_kernels(c % n_pool)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    e2k = max_over_ranks(t_start.elapsed_time(t_end) / 1e3)
+    res["step_two_kernels"] = {"value": round(whole_job_value(K, e2k, world), 2),
+                               "unit": "verify cycles/s", "ms_per_step": round(e2k / K * 1e3, 5)}
     cs = clocks.summary()
     res["clocks"] = cs
 
@@ -427,8 +442,8 @@ def full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, K, dev):
 def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
     """The headline step end to end through the C ABI from pinned host memory: each step moves
     its verify rows and drafts host -> device (one spec_copy_from_host of the cycle's packed
-    inputs), runs the verify and the acceptance, and the acceptance writes its result straight
-    into pinned host memory (spec_host_alias). Both transfers stay inside the chain of kernels,
+    inputs), runs the verify with the greedy acceptance fused into it, which writes its result
+    straight into pinned host memory (spec_host_alias). Both transfers stay inside the chain of kernels,
     so the next kernel still starts in the previous one's tail (a cudaMemcpyAsync between them
     would end that overlap)."""
     import torch
@@ -449,10 +464,9 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
 
     def one(c, j):
         spec.spec_copy_from_host(X_dev, X_host[c], xb)
-        eng.verify(H_dev)
-        spec.spec_accept(1, k, eng.k, D_dev, eng.logits, eng.stats, cfg.V, k + 1, None, None,
-                         cfg.Vd, cfg.Vd, eng.temps, cfg.eos_id, eng.seeds, eng.pos, out_alias[j],
-                         eng.counters, eng.ws)
+        spec.spec_verify_accept_greedy(eng.W, eng.wdt, cfg.V, cfg.d, H_dev, 1, k + 1, eng.temps,
+                                       eng.logits, eng.stats, k, eng.k, D_dev, cfg.eos_id,
+                                       out_alias[j], eng.counters, eng.ws)
 
     for c in range(10):
         one(c % n_pool, c)
@@ -464,8 +478,8 @@ def e2e(eng, cfg, Hp, drafts_pool, n_pool, k, K, dev, world, max_over_ranks):
     s = max_over_ranks(time.perf_counter() - t0)
     return {"value": round(whole_job_value(K, s, world), 2), "unit": "verify cycles/s",
             "h2d_bytes_per_step": int(hb + db), "d2h_bytes_per_step": spec.ACCEPT_OUT_BYTES,
-            "steps": K, "api": "spec_copy_from_host + SpecVerifyEngine.verify + spec_accept "
-                               "(result into pinned host memory)"}
+            "steps": K, "api": "spec_copy_from_host + spec_verify_accept_greedy (result into "
+                               "pinned host memory)"}
 
 
 def recipe_inputs(cfg, W, n_pool, k, T, rng_seed):
@@ -522,7 +536,7 @@ def sweep(dev, W, Wd, hbm_peak):
         Hdp_d = torch.from_numpy(Hdp.view(np.int16)).to(dev)
         eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
                                cfg.eos_id, device=dev, want_q_logits=True,
-                               acceptance=mode)
+                               acceptance=mode, fuse_greedy=True)
         eng.set_requests(temps=[T], seeds=[0], pos=[0], k=[k], top_k=[20], top_p=[0.95])
         # each cycle's drafts and draft rows (q), kept so that verify + acceptance can also be
         # timed on their own
@@ -564,11 +578,11 @@ def sweep(dev, W, Wd, hbm_peak):
                 ev[c][2].record()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        # pass 2: verify + acceptance back to back (the verify cycle, overlapped as in use)
+        # pass 2: verify + acceptance back to back (the verify cycle, overlapped as in use; one
+        # fused launch at T = 0)
         a.record()
         for c in range(K):
-            eng.verify(Hp_d[use(c)])
-            eng.accept()
+            eng.verify_accept(Hp_d[use(c)])
         b.record()
         torch.cuda.synchronize()
         va_s = a.elapsed_time(b) / 1e3
@@ -577,8 +591,7 @@ def sweep(dev, W, Wd, hbm_peak):
         a.record()
         for c in range(K):
             cc = drafts(c)
-            eng.verify(Hp_d[cc])
-            eng.accept()
+            eng.verify_accept(Hp_d[cc])
         b.record()
         torch.cuda.synchronize()
         s = a.elapsed_time(b) / 1e3

@@ -82,6 +82,14 @@ def spec_lmhead_verify(W, wdt, V, d, H, B, R, temperature, logits, stats, worksp
         _ptr(workspace), _nbytes(workspace), _stream(stream)))
 
 
+def spec_verify_accept_greedy(W, wdt, V, d, H, B, R, temperature, logits, stats, k_max, k,
+                              drafts, eos_id, out, counters, workspace, stream=None):
+    _check("spec_verify_accept_greedy", _abi.lib().spec_verify_accept_greedy(
+        _ptr(W), wdt, V, d, _ptr(H), B, R, _ptr(temperature), _ptr(logits), _ptr(stats), k_max,
+        _ptr(k), _ptr(drafts), eos_id, _ptr(out), _ptr(counters), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)))
+
+
 def spec_draft_argmax(W, wdt, V_draft, d, h, B, temperature, seed, pos, pos_offset, token_out,
                       token_stride, q_logits, q_stride, q_stats, k_active, workspace,
                       stream=None):

@@ -16,7 +16,8 @@ REQ_OK, REQ_NONFINITE, REQ_BAD_K, REQ_KV_OVERFLOW, REQ_NO_LOGITS, REQ_BAD_TOKEN,
     REQ_BAD_FILTER = range(7)
 
 # Exported symbols declared in include/spec.h (checked by the CPU test that loads the library).
-EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify", "spec_draft_argmax",
+EXPORTS = ("spec_workspace_bytes", "spec_status_str", "spec_lmhead_verify",
+           "spec_verify_accept_greedy", "spec_draft_argmax",
            "spec_accept", "spec_accept_exact", "spec_accept_filtered", "spec_adapt_width",
            "spec_adapt_width_mirror",
            "spec_draft_argmax_rows", "spec_accept_rows",
@@ -95,6 +96,9 @@ def lib():
         L.spec_copy_from_host.restype = i32
         L.spec_lmhead_verify.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, vp, sz, vp]
         L.spec_lmhead_verify.restype = i32
+        L.spec_verify_accept_greedy.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, i32,
+                                                vp, vp, i32, vp, vp, vp, sz, vp]
+        L.spec_verify_accept_greedy.restype = i32
         L.spec_draft_argmax.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp, i32, vp, i32, vp,
                                         i64, vp, vp, vp, sz, vp]
         L.spec_draft_argmax.restype = i32

@@ -134,7 +134,7 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
                         int32_t* token_out, int token_stride, const int32_t* kact,
                         void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
                         EncodeTiledFn encode, cudaStream_t stream, int64_t lo_rows,
-                        int64_t hi_row0, int64_t V_rows) {
+                        int64_t hi_row0, int64_t V_rows, const GreedyAcc* ga) {
   GemvTcLaunch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
@@ -207,6 +207,7 @@ spec_status run_gemv_tc(const void* W, int64_t V, int64_t d, const void* H, int 
   p.hi_row0 = hi_row0;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  set_greedy(p, ga);
   L.grid = grid;
   L.smem = static_cast<int>(smem_total);
   const cudaError_t e = gemv_tc_launch(L, stream);
@@ -222,7 +223,7 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
                         int32_t* token_out, int token_stride, const int32_t* kact,
                         void* workspace, const WsLayout& wl, int grid, const DevAttr& a,
                         EncodeTiledFn encode, cudaStream_t stream, int64_t lo_rows,
-                        int64_t hi_row0, int64_t V_rows) {
+                        int64_t hi_row0, int64_t V_rows, const GreedyAcc* ga) {
   GemvQ4Launch L;
   memset(&L, 0, sizeof(L));
   GemvParams& p = L.p;
@@ -296,6 +297,7 @@ spec_status run_gemv_q4(const void* W, int64_t V, int64_t d, const void* H, int 
   p.hi_row0 = hi_row0;
   p.hdr = static_cast<WsHeader*>(workspace);
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
+  set_greedy(p, ga);
   L.grid = grid;
   L.smem = static_cast<int>(smem_total);
   const cudaError_t e = gemv_q4_launch(L, stream);
@@ -310,7 +312,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
                      int32_t* token_out, int token_stride, const int32_t* kact, void* workspace,
                      size_t workspace_bytes, int32_t batch_for_ws, cudaStream_t stream,
                      int64_t lo_rows = -1, int64_t hi_row0 = -1, uint64_t ring_wait_ns = 0,
-                     int stall = 0) {
+                     int stall = 0, const GreedyAcc* ga = nullptr) {
   // rows [0, V) are weight rows [0, V), or [0, lo_rows) then hi_row0.. (a two-range draft set)
   if (lo_rows < 0 || lo_rows >= V) {
     lo_rows = V;
@@ -339,11 +341,11 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   if (wdt == SPEC_Q4A32)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_q4(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
-                       grid, a, encode, stream, lo_rows, hi_row0, V_rows);
+                       grid, a, encode, stream, lo_rows, hi_row0, V_rows, ga);
   if (wdt == SPEC_BF16)  // every entry point has checked that W and H are 16-byte aligned
     return run_gemv_tc(W, V, d, H, nrows, rows_per_req, temperature, logits, logits_stride, stats,
                        draft, seed, pos, pos_offset, token_out, token_stride, kact, workspace, wl,
-                       grid, a, encode, stream, lo_rows, hi_row0, V_rows);
+                       grid, a, encode, stream, lo_rows, hi_row0, V_rows, ga);
   if (lo_rows != V) return SPEC_ERR_UNSUPPORTED;  // the fp32 kernel's 60-row bands: [0, V) only
 
   GemvLaunch L;
@@ -415,6 +417,7 @@ spec_status run_gemv(const void* W, spec_dtype wdt, int64_t V, int64_t d, const 
   p.part = reinterpret_cast<GemvPartial*>(static_cast<uint8_t*>(workspace) + wl.part);
   p.ring_wait_ns = ring_wait_ns;
   p.stall = stall;
+  set_greedy(p, ga);
   L.grid = grid;
   L.threads = kGemvThreads;
   L.smem = static_cast<int>(smem_total);
@@ -650,6 +653,33 @@ spec_status spec_lmhead_verify(const void* W, spec_dtype wdt, int64_t V, int64_t
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
                   nullptr, 0, nullptr, 0, nullptr, workspace, workspace_bytes, B,
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+spec_status spec_verify_accept_greedy(const void* W, spec_dtype wdt, int64_t V, int64_t d,
+                                      const void* H, int32_t B, int32_t R,
+                                      const float* temperature, float* logits,
+                                      spec_rowstats* stats, int32_t k_max, const int32_t* k,
+                                      const int32_t* drafts, int32_t eos_id,
+                                      spec_accept_out* out, spec_counters* counters,
+                                      void* workspace, size_t workspace_bytes,
+                                      spec_stream_t stream) {
+  if (!W || !H || !temperature || !stats || !workspace || !k || !out) return SPEC_ERR_INVALID;
+  if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
+  if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
+    return SPEC_ERR_INVALID;
+  if (k_max < 0 || k_max > kMaxRows - 1 || (k_max > 0 && !drafts)) return SPEC_ERR_INVALID;
+  if (!aligned16(W) || !aligned16(H) || !aligned16(workspace)) return SPEC_ERR_INVALID;
+  if (static_cast<int64_t>(B) * R > kMaxRows) return SPEC_ERR_UNSUPPORTED;  // the GEMV path only
+  GreedyAcc ga;
+  ga.k = k;
+  ga.drafts = drafts;
+  ga.out = out;
+  ga.counters = counters;
+  ga.k_max = k_max;
+  ga.eos = eos_id;
+  return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
+                  nullptr, 0, nullptr, 0, nullptr, workspace, workspace_bytes, B,
+                  reinterpret_cast<cudaStream_t>(stream), -1, -1, 0, 0, &ga);
 }
 
 spec_status spec_draft_argmax(const void* W, spec_dtype wdt, int64_t V_draft, int64_t d,

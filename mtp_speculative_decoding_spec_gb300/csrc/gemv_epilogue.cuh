@@ -115,6 +115,112 @@ static __device__ __forceinline__ void gemv_block_partials(const GemvParams& p, 
   }
 }
 
+// Greedy acceptance of request b by one warp, from its verify rows' statistics st[b*R + r]:
+// the rule and status codes of spec_accept at T <= 0 (lucebox-hub PR #15, "Exactness": accept
+// d_i while it is the argmax of row i - 1, emit the argmax at the first mismatch or the bonus
+// argmax of row k after all k; EOS ends the block). Lane i holds draft i and row i.
+//
+// What it reads from global memory (k, the drafts, the 14 counter words, one a lane) is loaded
+// by greedy_prefetch when the last block starts its combine, so that those loads overlap it;
+// after the decision every lane stores its own counter word: no chain of round trips.
+struct GreedyPre {
+  int k, x_any;
+  unsigned long long cnt;  // counter word `lane` of the request (lane < 14)
+};
+static __device__ __forceinline__ GreedyPre greedy_prefetch(const GemvParams& p, int b,
+                                                            int lane) {
+  GreedyPre g;
+  g.k = p.acc_k[b];
+  g.x_any = (lane < p.acc_k_max) ? p.acc_drafts[static_cast<size_t>(b) * p.acc_k_max + lane]
+                                 : -1;
+  g.cnt = (p.acc_counters && lane < 14)
+              ? reinterpret_cast<const unsigned long long*>(p.acc_counters + b)[lane]
+              : 0ull;
+  return g;
+}
+static __device__ void greedy_accept_warp(const GemvParams& p, int b, int R,
+                                          const spec_rowstats* st_rows, int lane,
+                                          const GreedyPre& g) {
+  const int k = g.k;
+  const int kmax = p.acc_k_max;
+  int status = SPEC_REQ_OK;
+  const bool kbad = (k < 0 || k > kmax || k + 1 > R);
+  if (kbad) status = SPEC_REQ_BAD_K;
+  spec_rowstats st_any{0.f, 0.f, 0.f, -1};
+  if (lane < R) st_any = st_rows[b * R + lane];
+  int x = -1;
+  bool xbad = false;
+  if (!kbad && lane < k) {
+    x = g.x_any;
+    xbad = (x < 0 || static_cast<int64_t>(x) >= p.V);
+  }
+  if (status == SPEC_REQ_OK && __any_sync(0xffffffffu, xbad)) status = SPEC_REQ_BAD_TOKEN;
+  spec_rowstats st{0.f, 0.f, 0.f, -1};
+  bool nf = false;
+  if (status == SPEC_REQ_OK) {
+    if (lane <= k) {
+      st = st_any;
+      nf = isnan(st.max);
+    }
+    if (__any_sync(0xffffffffu, nf)) status = SPEC_REQ_NONFINITE;
+  }
+  const bool acc = status == SPEC_REQ_OK && lane < k && x == st.argmax;
+  const unsigned accmask = __ballot_sync(0xffffffffu, acc);
+  // the decision, worked out by every lane alike (status and k are the same in all lanes)
+  int ntok = 0, nacc = 0, eos_hit = 0, mytok = -1;  // mytok: the token at position `lane`
+  if (status == SPEC_REQ_OK) {
+    bool stop = false;
+    for (int i = 0; i < k && !stop; ++i) {
+      const int xi = __shfl_sync(0xffffffffu, x, i);
+      const int ai = __shfl_sync(0xffffffffu, st.argmax, i);
+      const int t = ((accmask >> i) & 1u) ? xi : ai;
+      if (lane == ntok) mytok = t;
+      ++ntok;
+      if ((accmask >> i) & 1u) {
+        ++nacc;
+        if (p.acc_eos >= 0 && xi == p.acc_eos) {
+          eos_hit = 1;
+          stop = true;
+        }
+      } else {
+        if (p.acc_eos >= 0 && ai == p.acc_eos) eos_hit = 1;
+        stop = true;
+      }
+    }
+    if (!stop) {
+      const int ak = __shfl_sync(0xffffffffu, st.argmax, k);
+      if (lane == ntok) mytok = ak;
+      ++ntok;
+      if (p.acc_eos >= 0 && ak == p.acc_eos) eos_hit = 1;
+    }
+  }
+  // the result record: lanes 0..7 its tokens, lane 8 the header fields
+  spec_accept_out* o = p.acc_out + b;
+  if (lane < 8) o->tokens[lane] = lane < ntok ? mytok : -1;
+  if (lane == 8) {
+    o->status = status;
+    o->n_accept = nacc;
+    o->n_emit = ntok;
+    o->eos_hit = eos_hit;
+    o->sample_kind = 0;
+    o->sample_row = -1;
+    o->reserved[0] = 0;
+    o->reserved[1] = 0;
+  }
+  if (p.acc_counters && lane < 14) {  // word `lane`: cycles, drafted, accepted, emitted, eos,
+    unsigned long long add = 0ull;    // errors, depth[0..7]
+    const bool ok = status == SPEC_REQ_OK;
+    if (lane == 0) add = 1ull;
+    else if (lane == 1 && ok) add = static_cast<unsigned long long>(k);
+    else if (lane == 2 && ok) add = static_cast<unsigned long long>(nacc);
+    else if (lane == 3 && ok) add = static_cast<unsigned long long>(ntok);
+    else if (lane == 4 && ok) add = static_cast<unsigned long long>(eos_hit);
+    else if (lane == 5 && !ok) add = 1ull;
+    else if (lane >= 6 && ok && lane - 6 == (nacc & 7)) add = 1ull;
+    reinterpret_cast<unsigned long long*>(p.acc_counters + b)[lane] = g.cnt + add;
+  }
+}
+
 // After every block has written its partials: the ticket, and in the last block the combine
 // of each row's partials into its statistics and, for the draft head, the token. All `nwarps`
 // (>= 8) warps call it; `scratch` (free shared memory, 8-byte aligned) needs
@@ -133,6 +239,11 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
   if (!flags[1]) return;
   __threadfence();
 
+  // the fused greedy acceptance's global reads, issued now so that they overlap the combine
+  GreedyPre gpre{0, -1, 0ull};
+  if (p.acc_out && warp < min(p.nrows, kMaxRows) / max(p.rows_per_req, 1))
+    gpre = greedy_prefetch(p, warp, lane);
+
   // ---------------- last block: combine the partials of every block ----------------
   // All threads first copy the partials of every (block, row) into shared memory in one round
   // of loads. Row q's region of the scratch holds blk_s (uint64 integer sums), blk_m (block
@@ -142,6 +253,8 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
   const int nr = min(p.nrows, kMaxRows);
   const size_t rstride = gemv_finish_row_bytes(GR);
   int* s_rbad = reinterpret_cast<int*>(scratch + kMaxRows * rstride);  // [8]
+  // [8]: the rows' statistics, for the fused greedy acceptance
+  spec_rowstats* s_st = reinterpret_cast<spec_rowstats*>(scratch + kMaxRows * rstride + 64);
   if (tid < kMaxRows) s_rbad[tid] = 0;
   __syncthreads();
   for (int i = tid; i < GR * nr; i += blockDim.x) {
@@ -200,6 +313,7 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
       st.argmax = t.idx < 0 ? t.idx : row_id(p, t.idx);
     }
     if (lane == 0 && p.stats) p.stats[q] = st;
+    if (lane == 0) s_st[q] = st;
 
     if (p.draft) {
       int32_t tok = -1;
@@ -310,6 +424,11 @@ static __device__ __forceinline__ void gemv_finish(const GemvParams& p, uint8_t*
       if (lane == 0)
         p.token_out[static_cast<size_t>(q) * p.token_stride] = tok < 0 ? tok : row_id(p, tok);
     }
+  }
+  if (p.acc_out) {  // the fused greedy acceptance, one warp per request
+    __syncthreads();
+    const int R = max(p.rows_per_req, 1);
+    if (warp < nr / R) greedy_accept_warp(p, warp, R, s_st, lane, gpre);  // B <= 8 <= nwarps
   }
   if (tid == 0) p.hdr->gemv_ticket = 0u;
 }

@@ -46,7 +46,34 @@ struct GemvParams {
   // producer issues no copy, and the consumers' waits for a stage give up after ring_wait_ns
   uint64_t ring_wait_ns;  // 0: the default limit
   int stall;
+  // greedy acceptance fused into the last block's finish (spec_verify_accept_greedy) when
+  // acc_out is set: drafts [B][acc_k_max], k [B], results and counters per request
+  const int32_t* acc_k;
+  const int32_t* acc_drafts;
+  spec_accept_out* acc_out;
+  spec_counters* acc_counters;
+  int acc_k_max;
+  int acc_eos;
 };
+
+// The greedy acceptance a GEMV launch may carry (see GemvParams::acc_out).
+struct GreedyAcc {
+  const int32_t* k;
+  const int32_t* drafts;
+  spec_accept_out* out;
+  spec_counters* counters;
+  int k_max;
+  int eos;
+};
+inline void set_greedy(GemvParams& p, const GreedyAcc* g) {
+  if (!g) return;
+  p.acc_k = g->k;
+  p.acc_drafts = g->drafts;
+  p.acc_out = g->out;
+  p.acc_counters = g->counters;
+  p.acc_k_max = g->k_max;
+  p.acc_eos = g->eos;
+}
 
 // Shared memory the last block's combine needs: per row, for each block, its integer sum (8
 // bytes), max / scale factor, runner-up / weight and argmax (4 bytes each), rounded up; then
@@ -55,7 +82,7 @@ __host__ __device__ constexpr size_t gemv_finish_row_bytes(int nblocks) {
   return 24 * static_cast<size_t>(nblocks);
 }
 __host__ __device__ constexpr size_t gemv_finish_scratch_bytes(int nblocks) {
-  return kMaxRows * gemv_finish_row_bytes(nblocks) + 64;
+  return kMaxRows * gemv_finish_row_bytes(nblocks) + 64 + kMaxRows * sizeof(spec_rowstats);
 }
 
 struct GemvLaunch {

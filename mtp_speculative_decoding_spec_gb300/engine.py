@@ -25,14 +25,14 @@ from . import (ACCEPT_OUT_BYTES, COUNTERS_BYTES, ROWSTATS_BYTES, SPEC_F32,
                spec_adapt_width, spec_adapt_width_mirror, spec_host_alias,
                spec_commit_rollback, spec_draft_argmax, spec_graph_capture_begin,
                spec_graph_capture_end, spec_graph_destroy, spec_graph_instantiate,
-               spec_graph_launch, spec_lmhead_verify, spec_width_graph_create,
-               spec_workspace_bytes)
+               spec_graph_launch, spec_lmhead_verify, spec_verify_accept_greedy,
+               spec_width_graph_create, spec_workspace_bytes)
 
 
 class SpecVerifyEngine:
     def __init__(self, W, wdt, V, d, Vd, B, R, k_max, eos_id=-1, device="cuda:0",
                  want_q_logits=True, acceptance="ratio", adaptive_cost=None, alpha=0.1,
-                 cycle_cost=None, width_graph=None, width_lag=False):
+                 cycle_cost=None, width_graph=None, width_lag=False, fuse_greedy=False):
         """acceptance: "ratio" (u*q <= p with residual correction; spec_accept), "exact"
         (a draft counts only if it is the trunk's own sample; spec_accept_exact) or "filtered"
         (the top-k / top-p filtered target of set_requests(top_k=..., top_p=...), argmax drafts
@@ -46,11 +46,16 @@ class SpecVerifyEngine:
         ``cycle`` enqueues k_max draft steps, of which those past every request's width return
         at once, and a verify of R rows.
         width_lag: run adaptive cycles of one request at host-scheduled widths, one cycle late
-        (see the module doc); replaces the width graph."""
+        (see the module doc); replaces the width graph.
+        fuse_greedy: while every request is greedy (set_requests' temperatures <= 0) and the
+        rule is the ratio rule, run a cycle's verify and acceptance as one launch
+        (spec_verify_accept_greedy: the acceptance taken in the LM-head kernel's last block)."""
         if acceptance not in ("ratio", "exact", "filtered"):
             raise ValueError(
                 f"acceptance must be 'ratio', 'exact' or 'filtered', not {acceptance!r}")
         self.acceptance = acceptance
+        self.fuse_greedy = bool(fuse_greedy)
+        self.all_greedy = False  # set_requests' temperatures, as the host gave them
         self.W, self.wdt, self.V, self.d, self.Vd = W, wdt, V, d, Vd
         self.B, self.R, self.k_max, self.eos_id = B, R, k_max, eos_id
         dev = torch.device(device)
@@ -113,6 +118,8 @@ class SpecVerifyEngine:
 
     # ---------------------------------------------------------------- configuration
     def set_requests(self, temps=None, seeds=None, pos=None, k=None, top_k=None, top_p=None):
+        if temps is not None:
+            self.all_greedy = bool((torch.as_tensor(temps, dtype=torch.float32) <= 0).all())
         for dst, src in ((self.temps, temps), (self.seeds, seeds), (self.pos, pos),
                          (self.k, k), (self.top_k, top_k), (self.top_p, top_p)):
             if src is not None:
@@ -162,6 +169,18 @@ class SpecVerifyEngine:
                     R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
                     self.eos_id, self.seeds, self.pos, self.out, self.counters, self.ws)
 
+    def verify_accept(self, H, R=None, k=None):
+        """Verify rows H and acceptance: one fused launch when greedy (see fuse_greedy)."""
+        R = R or self.R
+        if self.fuse_greedy and self.all_greedy and self.acceptance == "ratio":
+            spec_verify_accept_greedy(self.W, self.wdt, self.V, self.d, H, self.B, R, self.temps,
+                                      self.logits, self.stats, self.k_max,
+                                      self.k if k is None else k, self.drafts, self.eos_id,
+                                      self.out, self.counters, self.ws)
+            return
+        self.verify(H, R=R)
+        self.accept(R=R, k=k)
+
     def commit(self, k=None):
         if self.state is not None:
             spec_commit_rollback(self.B, self.state, self.out, self.k if k is None else k,
@@ -175,8 +194,7 @@ class SpecVerifyEngine:
     def verify_cycle(self, H):
         """Verify + accept (+ commit, + the next width when adaptive): one verify cycle on
         device-resident inputs."""
-        self.verify(H)
-        self.accept()
+        self.verify_accept(H)
         self.commit()
         self.adapt()
 
@@ -190,8 +208,7 @@ class SpecVerifyEngine:
         k_dev = self.k_ring[s]
         for i in range(1, w + 1):
             self.draft_step(i, Hd[i - 1], gate=False)
-        self.verify(H[:w + 1], R=w + 1)
-        self.accept(R=w + 1, k=k_dev)
+        self.verify_accept(H[:w + 1], R=w + 1, k=k_dev)
         self.commit(k=k_dev)
         # the choice after this cycle is cycle n + 2's width: slot s again, on both sides
         spec_adapt_width_mirror(self.B, self.k_max, self.out, k_dev, self.cost, self.cycle_cost,
@@ -207,8 +224,7 @@ class SpecVerifyEngine:
         w = max(w, 1)
         for i in range(1, w + 1):
             self.draft_step(i, self.Hd_in[i - 1], gate=False)
-        self.verify(self.H_in[:w + 1], R=w + 1)
-        self.accept(R=w + 1)
+        self.verify_accept(self.H_in[:w + 1], R=w + 1)
         self.commit()
         self.adapt()
 

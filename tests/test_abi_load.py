@@ -139,6 +139,15 @@ def test_host_validation_of_the_later_entry_points(lib):
     assert lib.spec_adapt_width(1, 7, fake, fake, null, null, 0.1, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, null, 0.0, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, fake, 1.5, fake, fake, null) == 1
+    # the fused greedy verify + acceptance: the verify's checks, k_max <= 7, k and out required
+    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 8,
+                                         fake, fake, -1, fake, null, fake, 1 << 20, null) == 1
+    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 1,
+                                         null, fake, -1, fake, null, fake, 1 << 20, null) == 1
+    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 1,
+                                         fake, fake, -1, null, null, fake, 1 << 20, null) == 1
+    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 2, 8, fake, null, fake, 1,
+                                         fake, fake, -1, fake, null, fake, 1 << 20, null) == 2
     # the mirror entry point: the same checks, and the mirror is required
     assert lib.spec_adapt_width_mirror(1, 7, fake, fake, fake, null, 0.1, fake, fake, null,
                                        null) == 1

@@ -23,7 +23,8 @@ def calls(monkeypatch):
 
     for name in ("spec_draft_argmax", "spec_lmhead_verify", "spec_accept", "spec_accept_exact",
                  "spec_accept_filtered", "spec_commit_rollback", "spec_adapt_width",
-                 "spec_adapt_width_mirror", "spec_graph_capture_begin", "spec_graph_capture_end", "spec_graph_launch",
+                 "spec_adapt_width_mirror", "spec_verify_accept_greedy",
+                 "spec_graph_capture_begin", "spec_graph_capture_end", "spec_graph_launch",
                  "spec_graph_destroy"):
         monkeypatch.setattr(eng_mod, name, rec(name))
 
@@ -172,6 +173,31 @@ def test_adaptive_host_scheduled_widths_one_cycle_late(calls):
         _engine(b=2, adaptive_cost=[1.0, 1.5, 2.0, 2.5], width_lag=True)  # one request only
     with pytest.raises(ValueError):
         _engine(b=1, width_lag=True)                # adaptive widths only
+
+
+def test_fused_greedy_verify_and_acceptance(calls):
+    """fuse_greedy: while every request is greedy a cycle's verify and acceptance are one call
+    (spec_verify_accept_greedy, with the engine's widths, drafts, results and counters); a
+    request at T > 0, or another acceptance rule, brings back the two calls."""
+    e = _engine(fuse_greedy=True)
+    e.set_requests(temps=[0.0, 0.0])
+    H, Hd = torch.zeros((B * R, d)), torch.zeros((K_MAX, B, d))
+    e.cycle(H, Hd, 2)
+    assert _names(calls) == ["spec_draft_argmax", "spec_draft_argmax",
+                             "spec_verify_accept_greedy"]
+    a = calls[-1][1]
+    assert a[4] is H and a[5] == B and a[6] == R and a[10] == K_MAX
+    assert a[11] is e.k and a[12] is e.drafts and a[13] == 2
+    assert a[14] is e.out and a[15] is e.counters and a[16] is e.ws
+    calls.clear()
+    e.set_requests(temps=[0.0, 1.0])
+    e.verify_cycle(H)
+    assert _names(calls) == ["spec_lmhead_verify", "spec_accept"]
+    calls.clear()
+    f = _engine(fuse_greedy=True, acceptance="exact")
+    f.set_requests(temps=[0.0, 0.0])
+    f.verify_cycle(H)
+    assert _names(calls) == ["spec_lmhead_verify", "spec_accept_exact"]
 
 
 def test_commit_only_with_attached_state(calls):
