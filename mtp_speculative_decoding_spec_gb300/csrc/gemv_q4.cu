@@ -109,6 +109,15 @@ __device__ __forceinline__ uint4 lds16(uint32_t a) {
   return v;
 }
 
+// (s, s) and (b, b) from a (scale, bias) pair, by unpacking the two bf16 halves and packing
+// each twice. Measured against a byte permute per splat: 76.4 -> 71.9 us for the 2-row verify.
+__device__ __forceinline__ void splat_pair(uint32_t sb, uint32_t& s2, uint32_t& b2) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tmov.b32 %0, {lo, lo};\n\t"
+      "mov.b32 %1, {hi, hi};\n\t}"
+      : "=r"(s2), "=r"(b2)
+      : "r"(sb));
+}
+
 // One A-fragment register: a pair of consecutive elements of an 8-element code word, its two
 // codes at bits 0..3 and 16..19 of v (the word shifted right by 4 j for pair j), dequantised:
 // the bf16 pair (128 + e, 128 + e') (the code lands in the low mantissa bits of 128 = 0x4300,
@@ -269,8 +278,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const int gq = gg & 3;
           const uint32_t sa = gq == 0 ? pa.x : gq == 1 ? pa.y : gq == 2 ? pa.z : pa.w;
           const uint32_t sb = gq == 0 ? pb.x : gq == 1 ? pb.y : gq == 2 ? pb.z : pb.w;
-          const uint32_t sa2 = __byte_perm(sa, sa, 0x1010), ba2 = __byte_perm(sa, sa, 0x3232);
-          const uint32_t sb2 = __byte_perm(sb, sb, 0x1010), bb2 = __byte_perm(sb, sb, 0x3232);
+          uint32_t sa2, ba2, sb2, bb2;
+          splat_pair(sa, sa2, ba2);
+          splat_pair(sb, sb2, bb2);
           uint32_t da[4], db[4];
           dequant_word(wa, sa2, ba2, da);
           dequant_word(wb, sb2, bb2, db);
