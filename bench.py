@@ -647,7 +647,8 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     step and draft step until the fit is usable). One request, two schedules:
     host-scheduled widths (the headline: cycle n runs exactly the width chosen after cycle
     n - 2, which the width update writes into pinned host memory; the host reads it once that
-    cycle has completed), and the width graph (each cycle a graph launch whose select kernel
+    cycle has completed; acceptance and width update run in the verify kernel's last block),
+    and the width graph (each cycle a graph launch whose select kernel
     picks the body of the chosen width, the cycle's inputs first copied into the graph's input
     buffers). Compared with every fixed width on the same inputs."""
     import torch
@@ -665,7 +666,7 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     def run(lag):
         eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
                                cfg.eos_id, device=dev, adaptive_cost=cost, alpha=0.1,
-                               width_lag=lag)
+                               width_lag=lag, fuse_greedy=True)
         eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])
         for c in range(20):
             eng.cycle(Hp_d[c % n_pool], Hdp_d[c % n_pool, :, None, :], k_max)
@@ -703,7 +704,7 @@ def adaptive_bench(dev, W, Wd, step_us, draft_us, K=512):
     fixed = {}
     for k in range(1, k_max + 1):
         eng = SpecVerifyEngine(Wd, spec.SPEC_BF16, cfg.V, cfg.d, cfg.Vd, 1, k + 1, k,
-                               cfg.eos_id, device=dev)
+                               cfg.eos_id, device=dev, fuse_greedy=True)
         eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[k])
         for c in range(5):
             eng.cycle(Hp_d[c, :k + 1], Hdp_d[c, :k, None, :], k)

@@ -204,28 +204,6 @@ spec_status spec_lmhead_verify(const void *W, spec_dtype wdt, int64_t V, int64_t
                                size_t workspace_bytes, spec_stream_t stream);
 
 /*
- * spec_verify_accept_greedy -- spec_lmhead_verify followed by the greedy acceptance of
- * spec_accept (lucebox-hub PR #15, "Exactness": a draft is kept while it is the verify row's
- * argmax), fused: the LM-head kernel's last block, which combines every row's statistics,
- * also takes each request's decision from them, so the cycle runs one kernel instead of two.
- * Every request is decided by the greedy rule whatever its temperature (the temperature still
- * sets its statistics and logits as in spec_lmhead_verify; use spec_accept for sampled
- * acceptance). out[b], counters[b] (nullable) and the status codes are exactly those
- * spec_accept writes at temperature <= 0 for the same k, drafts [B, k_max] and eos_id; the
- * stats (and logits) are those of spec_lmhead_verify. B*R <= 8 (the GEMV path) and
- * k_max <= 7; otherwise SPEC_ERR_UNSUPPORTED / SPEC_ERR_INVALID. Other arguments as for
- * spec_lmhead_verify and spec_accept.
- */
-spec_status spec_verify_accept_greedy(const void *W, spec_dtype wdt, int64_t V, int64_t d,
-                                      const void *H, int32_t B, int32_t R,
-                                      const float *temperature, float *logits,
-                                      spec_rowstats *stats, int32_t k_max, const int32_t *k,
-                                      const int32_t *drafts, int32_t eos_id,
-                                      spec_accept_out *out, spec_counters *counters,
-                                      void *workspace, size_t workspace_bytes,
-                                      spec_stream_t stream);
-
-/*
  * spec_draft_argmax -- draft-head projection over the first V_draft rows of the same LM head
  * with the token choice fused in; the token stays in device memory for the next draft
  * (lucebox-hub PR #15, "What": the draft head spans the first 64,000 vocabulary rows, chooses
@@ -438,6 +416,35 @@ spec_status spec_adapt_width_mirror(int32_t B, int32_t k_max, const spec_accept_
                                     const float *cycle_cost, float alpha,
                                     spec_width_state *state, int32_t *k_next, int32_t *k_mirror,
                                     spec_stream_t stream);
+
+/*
+ * spec_verify_accept_greedy -- spec_lmhead_verify followed by the greedy acceptance of
+ * spec_accept (lucebox-hub PR #15, "Exactness": a draft is kept while it is the verify row's
+ * argmax), fused: the LM-head kernel's last block, which combines every row's statistics,
+ * also takes each request's decision from them, so the cycle runs one kernel instead of two.
+ * Every request is decided by the greedy rule whatever its temperature (the temperature still
+ * sets its statistics and logits as in spec_lmhead_verify; use spec_accept for sampled
+ * acceptance). out[b], counters[b] (nullable) and the status codes are exactly those
+ * spec_accept writes at temperature <= 0 for the same k, drafts [B, k_max] and eos_id; the
+ * stats (and logits) are those of spec_lmhead_verify. B*R <= 8 (the GEMV path) and
+ * k_max <= 7; otherwise SPEC_ERR_UNSUPPORTED / SPEC_ERR_INVALID. Other arguments as for
+ * spec_lmhead_verify and spec_accept.
+ * With state non-NULL the width update of spec_adapt_width_mirror follows in the same block,
+ * with k_used = k and the arguments cost, cycle_cost, alpha, state, k_next and k_mirror
+ * (nullable) as there: state, k_next and k_mirror get the bytes that call writes (a cycle
+ * timed on the device, cycle_cost NULL, is timed to this kernel's last block instead of to the
+ * width kernel). state NULL: no width update (cost ... k_mirror ignored).
+ */
+spec_status spec_verify_accept_greedy(const void *W, spec_dtype wdt, int64_t V, int64_t d,
+                                      const void *H, int32_t B, int32_t R,
+                                      const float *temperature, float *logits,
+                                      spec_rowstats *stats, int32_t k_max, const int32_t *k,
+                                      const int32_t *drafts, int32_t eos_id,
+                                      spec_accept_out *out, spec_counters *counters,
+                                      const float *cost, const float *cycle_cost, float alpha,
+                                      spec_width_state *state, int32_t *k_next,
+                                      int32_t *k_mirror, void *workspace,
+                                      size_t workspace_bytes, spec_stream_t stream);
 
 /*
  * Adaptive-width cycles as one CUDA graph (no counterpart on the pages: it lets the width

@@ -83,10 +83,15 @@ def spec_lmhead_verify(W, wdt, V, d, H, B, R, temperature, logits, stats, worksp
 
 
 def spec_verify_accept_greedy(W, wdt, V, d, H, B, R, temperature, logits, stats, k_max, k,
-                              drafts, eos_id, out, counters, workspace, stream=None):
+                              drafts, eos_id, out, counters, workspace, stream=None, cost=None,
+                              cycle_cost=None, alpha=0.1, state=None, k_next=None,
+                              k_mirror=None):
+    """Verify + greedy acceptance in one launch; with `state` also the width update of
+    spec_adapt_width_mirror (k_mirror: a device-writable address or a tensor)."""
     _check("spec_verify_accept_greedy", _abi.lib().spec_verify_accept_greedy(
         _ptr(W), wdt, V, d, _ptr(H), B, R, _ptr(temperature), _ptr(logits), _ptr(stats), k_max,
-        _ptr(k), _ptr(drafts), eos_id, _ptr(out), _ptr(counters), _ptr(workspace),
+        _ptr(k), _ptr(drafts), eos_id, _ptr(out), _ptr(counters), _ptr(cost), _ptr(cycle_cost),
+        float(alpha), _ptr(state), _ptr(k_next), _ptr(k_mirror), _ptr(workspace),
         _nbytes(workspace), _stream(stream)))
 
 

@@ -97,7 +97,8 @@ def lib():
         L.spec_lmhead_verify.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, vp, sz, vp]
         L.spec_lmhead_verify.restype = i32
         L.spec_verify_accept_greedy.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, vp, vp, i32,
-                                                vp, vp, i32, vp, vp, vp, sz, vp]
+                                                vp, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp,
+                                                vp, vp, vp, sz, vp]
         L.spec_verify_accept_greedy.restype = i32
         L.spec_draft_argmax.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp, i32, vp, i32, vp,
                                         i64, vp, vp, vp, sz, vp]

@@ -661,9 +661,12 @@ spec_status spec_verify_accept_greedy(const void* W, spec_dtype wdt, int64_t V, 
                                       spec_rowstats* stats, int32_t k_max, const int32_t* k,
                                       const int32_t* drafts, int32_t eos_id,
                                       spec_accept_out* out, spec_counters* counters,
-                                      void* workspace, size_t workspace_bytes,
-                                      spec_stream_t stream) {
+                                      const float* cost, const float* cycle_cost, float alpha,
+                                      spec_width_state* state, int32_t* k_next,
+                                      int32_t* k_mirror, void* workspace,
+                                      size_t workspace_bytes, spec_stream_t stream) {
   if (!W || !H || !temperature || !stats || !workspace || !k || !out) return SPEC_ERR_INVALID;
+  if (state && (!cost || !k_next || !(alpha > 0.f && alpha <= 1.f))) return SPEC_ERR_INVALID;
   if (!known_wdt(wdt)) return SPEC_ERR_INVALID;
   if (V < 1 || V >= (int64_t(1) << 24) || d < 1 || B < 1 || R < 1 || R > kMaxRows)
     return SPEC_ERR_INVALID;
@@ -677,6 +680,12 @@ spec_status spec_verify_accept_greedy(const void* W, spec_dtype wdt, int64_t V, 
   ga.counters = counters;
   ga.k_max = k_max;
   ga.eos = eos_id;
+  ga.cost = cost;
+  ga.cycle_cost = cycle_cost;
+  ga.alpha = alpha;
+  ga.state = state;
+  ga.k_next = k_next;
+  ga.k_mirror = k_mirror;
   return run_gemv(W, wdt, V, d, H, B * R, R, temperature, logits, V, stats, 0, nullptr,
                   nullptr, 0, nullptr, 0, nullptr, workspace, workspace_bytes, B,
                   reinterpret_cast<cudaStream_t>(stream), -1, -1, 0, 0, &ga);

@@ -6,6 +6,7 @@
 
 #include <math.h>
 
+#include "adapt_core.cuh"
 #include "params.cuh"
 
 namespace spec {
@@ -218,6 +219,25 @@ static __device__ void greedy_accept_warp(const GemvParams& p, int b, int R,
     else if (lane == 5 && !ok) add = 1ull;
     else if (lane >= 6 && ok && lane - 6 == (nacc & 7)) add = 1ull;
     reinterpret_cast<unsigned long long*>(p.acc_counters + b)[lane] = g.cnt + add;
+  }
+  if (p.ad_state && lane == 0) {  // the width update of spec_adapt_width_mirror, fused
+    AdaptParams ap;
+    ap.B = 0;  // unused by the update of one request
+    ap.k_max = p.acc_k_max;
+    ap.out = p.acc_out;
+    ap.k_used = p.acc_k;
+    ap.cost = p.ad_cost;
+    ap.cycle_cost = p.ad_cycle_cost;
+    ap.alpha = p.ad_alpha;
+    ap.state = p.ad_state;
+    ap.k_next = p.ad_k_next;
+    ap.k_mirror = p.ad_k_mirror;
+    spec_accept_out r;  // the fields of this cycle's record the update reads
+    r.status = status;
+    r.n_accept = nacc;
+    r.n_emit = ntok;
+    r.eos_hit = eos_hit;
+    adapt_request(ap, b, r);
   }
 }
 

@@ -54,9 +54,17 @@ struct GemvParams {
   spec_counters* acc_counters;
   int acc_k_max;
   int acc_eos;
+  // and after it, when ad_state is set, the width update of spec_adapt_width_mirror (k_used =
+  // acc_k; ad_k_mirror nullable)
+  const float* ad_cost;
+  const float* ad_cycle_cost;
+  float ad_alpha;
+  spec_width_state* ad_state;
+  int32_t* ad_k_next;
+  int32_t* ad_k_mirror;
 };
 
-// The greedy acceptance a GEMV launch may carry (see GemvParams::acc_out).
+// The greedy acceptance (and width update) a GEMV launch may carry (see GemvParams::acc_out).
 struct GreedyAcc {
   const int32_t* k;
   const int32_t* drafts;
@@ -64,6 +72,12 @@ struct GreedyAcc {
   spec_counters* counters;
   int k_max;
   int eos;
+  const float* cost;
+  const float* cycle_cost;
+  float alpha;
+  spec_width_state* state;  // null: no width update
+  int32_t* k_next;
+  int32_t* k_mirror;
 };
 inline void set_greedy(GemvParams& p, const GreedyAcc* g) {
   if (!g) return;
@@ -73,6 +87,12 @@ inline void set_greedy(GemvParams& p, const GreedyAcc* g) {
   p.acc_counters = g->counters;
   p.acc_k_max = g->k_max;
   p.acc_eos = g->eos;
+  p.ad_cost = g->cost;
+  p.ad_cycle_cost = g->cycle_cost;
+  p.ad_alpha = g->alpha;
+  p.ad_state = g->state;
+  p.ad_k_next = g->k_next;
+  p.ad_k_mirror = g->k_mirror;
 }
 
 // Shared memory the last block's combine needs: per row, for each block, its integer sum (8

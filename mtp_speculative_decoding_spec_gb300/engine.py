@@ -169,17 +169,27 @@ class SpecVerifyEngine:
                     R, q, self.qs if q is not None else None, self.Vd, self.Vd, self.temps,
                     self.eos_id, self.seeds, self.pos, self.out, self.counters, self.ws)
 
-    def verify_accept(self, H, R=None, k=None):
-        """Verify rows H and acceptance: one fused launch when greedy (see fuse_greedy)."""
+    def verify_accept(self, H, R=None, k=None, k_mirror=None):
+        """Verify rows H and acceptance: one fused launch when greedy (see fuse_greedy). With
+        k_mirror (adaptive, host-scheduled widths) the fused launch also takes the width update,
+        into k and k_mirror; returns whether it did."""
         R = R or self.R
+        k = self.k if k is None else k
         if self.fuse_greedy and self.all_greedy and self.acceptance == "ratio":
+            adapt = k_mirror is not None and self.adaptive
             spec_verify_accept_greedy(self.W, self.wdt, self.V, self.d, H, self.B, R, self.temps,
-                                      self.logits, self.stats, self.k_max,
-                                      self.k if k is None else k, self.drafts, self.eos_id,
-                                      self.out, self.counters, self.ws)
-            return
+                                      self.logits, self.stats, self.k_max, k, self.drafts,
+                                      self.eos_id, self.out, self.counters, self.ws,
+                                      cost=self.cost if adapt else None,
+                                      cycle_cost=self.cycle_cost if adapt else None,
+                                      alpha=self.alpha if adapt else 0.1,
+                                      state=self.width_state if adapt else None,
+                                      k_next=k if adapt else None,
+                                      k_mirror=k_mirror if adapt else None)
+            return adapt
         self.verify(H, R=R)
         self.accept(R=R, k=k)
+        return False
 
     def commit(self, k=None):
         if self.state is not None:
@@ -208,11 +218,19 @@ class SpecVerifyEngine:
         k_dev = self.k_ring[s]
         for i in range(1, w + 1):
             self.draft_step(i, Hd[i - 1], gate=False)
-        self.verify_accept(H[:w + 1], R=w + 1, k=k_dev)
-        self.commit(k=k_dev)
         # the choice after this cycle is cycle n + 2's width: slot s again, on both sides
-        spec_adapt_width_mirror(self.B, self.k_max, self.out, k_dev, self.cost, self.cycle_cost,
-                                self.alpha, self.width_state, k_dev, self.k_seen_dev[s])
+        if self.state is None:
+            # nothing to commit: the width update can share the fused verify's launch
+            fused = self.verify_accept(H[:w + 1], R=w + 1, k=k_dev, k_mirror=self.k_seen_dev[s])
+        else:
+            # the commit reads this cycle's widths, which the update overwrites: it goes first
+            self.verify_accept(H[:w + 1], R=w + 1, k=k_dev)
+            self.commit(k=k_dev)
+            fused = False
+        if not fused:
+            spec_adapt_width_mirror(self.B, self.k_max, self.out, k_dev, self.cost,
+                                    self.cycle_cost, self.alpha, self.width_state, k_dev,
+                                    self.k_seen_dev[s])
         if self.lag_events is not None:
             self.lag_events[s].record()
         self.n_cycles = n + 1

@@ -139,15 +139,18 @@ def test_host_validation_of_the_later_entry_points(lib):
     assert lib.spec_adapt_width(1, 7, fake, fake, null, null, 0.1, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, null, 0.0, fake, fake, null) == 1
     assert lib.spec_adapt_width(1, 7, fake, fake, fake, fake, 1.5, fake, fake, null) == 1
-    # the fused greedy verify + acceptance: the verify's checks, k_max <= 7, k and out required
-    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 8,
-                                         fake, fake, -1, fake, null, fake, 1 << 20, null) == 1
-    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 1,
-                                         null, fake, -1, fake, null, fake, 1 << 20, null) == 1
-    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 1, 2, fake, null, fake, 1,
-                                         fake, fake, -1, null, null, fake, 1 << 20, null) == 1
-    assert lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, 2, 8, fake, null, fake, 1,
-                                         fake, fake, -1, fake, null, fake, 1 << 20, null) == 2
+    # the fused greedy verify + acceptance: the verify's checks, k_max <= 7, k and out required;
+    # a width update (state set) needs cost, k_next and alpha in (0, 1]
+    def vag(B, R, k_max, k, out, state=null, cost=null, k_next=null, alpha=0.1):
+        return lib.spec_verify_accept_greedy(fake, 0, 10, 128, fake, B, R, fake, null, fake,
+                                             k_max, k, fake, -1, out, null, cost, null, alpha,
+                                             state, k_next, null, fake, 1 << 20, null)
+    assert vag(1, 2, 8, fake, fake) == 1
+    assert vag(1, 2, 1, null, fake) == 1
+    assert vag(1, 2, 1, fake, null) == 1
+    assert vag(2, 8, 1, fake, fake) == 2
+    assert vag(1, 2, 1, fake, fake, state=fake) == 1                      # no cost, no k_next
+    assert vag(1, 2, 1, fake, fake, state=fake, cost=fake, k_next=fake, alpha=0.0) == 1
     # the mirror entry point: the same checks, and the mirror is required
     assert lib.spec_adapt_width_mirror(1, 7, fake, fake, fake, null, 0.1, fake, fake, null,
                                        null) == 1

@@ -200,6 +200,35 @@ def test_fused_greedy_verify_and_acceptance(calls):
     assert _names(calls) == ["spec_lmhead_verify", "spec_accept_exact"]
 
 
+def test_host_scheduled_widths_with_the_update_fused(calls, monkeypatch):
+    """width_lag with fuse_greedy, greedy requests, no state: a cycle is its draft steps and one
+    fused launch that also takes the width update (k_used = k_next = the device slot, the
+    host-visible slot as mirror); with a state attached the commit reads the widths before the
+    update overwrites them, so the update stays a launch of its own after the commit."""
+    kws = []
+
+    def fused(*args, **kw):
+        calls.append(("spec_verify_accept_greedy", args))
+        kws.append(kw)
+    monkeypatch.setattr(eng_mod, "spec_verify_accept_greedy", fused)
+    e = _engine(b=1, adaptive_cost=[1.0, 1.5, 2.0, 2.5], width_lag=True, fuse_greedy=True)
+    e.set_requests(temps=[0.0], k=[2])
+    H, Hd = torch.ones((K_MAX + 1, d)), torch.ones((K_MAX, 1, d))
+    e.cycle(H, Hd, K_MAX)
+    assert _names(calls) == ["spec_draft_argmax"] * 2 + ["spec_verify_accept_greedy"]
+    kw = kws[-1]
+    slot = e.k_ring[0].data_ptr()
+    assert calls[-1][1][11].data_ptr() == slot and kw["k_next"].data_ptr() == slot
+    assert kw["state"] is e.width_state and kw["cost"] is e.cost
+    assert kw["k_mirror"] == e.k_seen[0].data_ptr() and kw["alpha"] == e.alpha
+    calls.clear()
+    e.attach_state(object(), 0)
+    e.cycle(H, Hd, K_MAX)
+    assert _names(calls) == ["spec_draft_argmax"] * 2 + [
+        "spec_verify_accept_greedy", "spec_commit_rollback", "spec_adapt_width_mirror"]
+    assert kws[-1]["state"] is None  # no update inside the fused launch
+
+
 def test_commit_only_with_attached_state(calls):
     e = _engine()
     e.verify_cycle(torch.zeros((B * R, d)))

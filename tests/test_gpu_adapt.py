@@ -199,19 +199,21 @@ def test_engine_width_graph_times_its_cycles(c0):
     eng.close()
 
 
-def test_engine_host_scheduled_widths(c0):
+@pytest.mark.parametrize("fused", [False, True])
+def test_engine_host_scheduled_widths(c0, fused):
     """width_lag at C0, 40 cycles: each cycle's acceptance result is bitwise the one a
     fixed-width engine gives at the width the cycle ran; the width of cycle n + 2 is the
     oracle's choice from the results of cycles 0..n (no measured costs: the prior decides, a
     nearly flat one so that deeper widths pay at C0's acceptance and the width moves); the
-    pinned copy the width update writes equals the device's widths."""
+    pinned copy the width update writes equals the device's widths. Run with the width
+    update as its own launch and fused into the verify's last block (fuse_greedy)."""
     cfg, W, Wd = c0
     k_max, alpha = cfg.k, 0.2
     cost = [1.0 + 0.005 * k for k in range(k_max + 1)]
     zero = torch.zeros(1, dtype=torch.float32, device=dev())
     eng = SpecVerifyEngine(Wd, wdt_of(cfg), cfg.V, cfg.d, cfg.Vd, 1, k_max + 1, k_max,
                            cfg.eos_id, device=dev(), adaptive_cost=cost, alpha=alpha,
-                           cycle_cost=zero, width_lag=True)
+                           cycle_cost=zero, width_lag=True, fuse_greedy=fused)
     eng.set_requests(temps=[0.0], seeds=[1], pos=[0], k=[1])  # widths grow from 1
     fixed = {}
 

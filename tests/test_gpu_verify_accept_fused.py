@@ -8,7 +8,8 @@ argmax of row k; an emitted or accepted EOS ends the block (DS4Server issue #98,
 *Implementation*). Cases: every acceptance depth, EOS accepted and EOS emitted, a bad k, a
 draft outside the vocabulary, a non-finite row, several requests per call, each weight format
 (fp32 at the tiny configuration, bf16 and 4-bit at full size), and the headline 2-row and the
-8-row shapes.
+8-row shapes. With the width update fused too, its state, next widths and mirror against
+spec_adapt_width_mirror over 30 cycles.
 """
 
 import numpy as np
@@ -158,3 +159,54 @@ def test_fused_greedy_full_size_q4(full):
                                       "bf16").view(np.int16)).to(dev()) for _ in range(2)]
     temps = [torch.zeros(B, dtype=torch.float32, device=dev())]
     assert _check_cases(Wq, spec.SPEC_Q4A32, cfg.V, cfg.d, Hs, B, R, R - 1, rng, temps) > 0
+
+
+def test_fused_width_update_matches_the_width_kernel():
+    """30 cycles at the tiny configuration, one request of 4 rows: the fused launch with the
+    width update (state set) against the fused launch without it followed by
+    spec_adapt_width_mirror, each path with its own buffers. Records, counters, width state,
+    next widths and the mirror bitwise equal after every cycle; the widths each path runs come
+    from its own updates; cycle costs given (the cost fit in use), so both are deterministic."""
+    ensure_built()
+    cfg = configs.get(0)
+    W = to_dev(gen.lm_weights(cfg))
+    rng = np.random.default_rng(41)
+    B, k_max = 1, 3
+    R = k_max + 1
+    cost = torch.tensor([1.0 + 0.3 * i for i in range(k_max + 1)], dtype=torch.float32,
+                        device=dev())
+    temps = torch.zeros(B, dtype=torch.float32, device=dev())
+    paths = []
+    for _ in range(2):
+        paths.append(dict(
+            ws=workspace(cfg.V, B),
+            stats=torch.zeros(B * R * spec.ROWSTATS_BYTES, dtype=torch.uint8, device=dev()),
+            out=torch.zeros(B * spec.ACCEPT_OUT_BYTES, dtype=torch.uint8, device=dev()),
+            cnt=torch.zeros(B * spec.COUNTERS_BYTES, dtype=torch.uint8, device=dev()),
+            state=torch.zeros(B * spec.WIDTH_STATE_BYTES, dtype=torch.uint8, device=dev()),
+            k=torch.full((B,), 1, dtype=torch.int32, device=dev()),
+            mirror=torch.full((B,), -5, dtype=torch.int32, device=dev())))
+    for c in range(30):
+        H = to_dev(gen.encode(rng.standard_normal((R, cfg.d), dtype=np.float32), "f32"))
+        am = _argmax(W, spec.SPEC_F32, cfg.V, cfg.d, H, B, R, temps)
+        depth = int(rng.integers(0, R))
+        drafts = to_dev(np.array([[am[0, i] if i < depth else (am[0, i] + 7) % cfg.V
+                                   for i in range(k_max)]], dtype=np.int32))
+        cyc = torch.tensor([100.0 + 40.0 * int(to_np(paths[0]["k"])[0]) + float(c % 5)],
+                           dtype=torch.float32, device=dev())
+        for fused_update, q in zip((False, True), paths):
+            spec.spec_verify_accept_greedy(
+                W, spec.SPEC_F32, cfg.V, cfg.d, H, B, R, temps, None, q["stats"], k_max, q["k"],
+                drafts, -1, q["out"], q["cnt"], q["ws"], cost=cost if fused_update else None,
+                cycle_cost=cyc if fused_update else None, alpha=0.2,
+                state=q["state"] if fused_update else None,
+                k_next=q["k"] if fused_update else None,
+                k_mirror=q["mirror"] if fused_update else None)
+            if not fused_update:
+                spec.spec_adapt_width_mirror(B, k_max, q["out"], q["k"], cost, cyc, 0.2,
+                                             q["state"], q["k"], q["mirror"])
+        torch.cuda.synchronize()
+        for key in ("out", "cnt", "state", "k", "mirror"):
+            assert to_np(paths[0][key]).tobytes() == to_np(paths[1][key]).tobytes(), (c, key)
+    st = to_np(paths[1]["state"]).view(spec.WIDTH_STATE_DTYPE)[0]
+    assert int(st["cycles"]) == 30 and float(st["rate"][0]) > 0  # the fit in use
