@@ -355,8 +355,10 @@ def run_ours(args, rank, local_rank, world):
     if args.profile:
         profile_extras(dev, W, Wd)
     if not args.profile:
-        res["full_cycle"] = full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, min(K, 2000), dev)
-        res["e2e"] = e2e(eng, cfg, Hp, drafts_pool, n_pool, k, min(K, 2000), dev, world,
+        # secondary figures: at least 500 cycles whatever --steps is (each reports its count)
+        n_sec = min(max(K, 500), 2000)
+        res["full_cycle"] = full_cycle(eng, cfg, Hp_d, Hdp_d, n_pool, k, n_sec, dev)
+        res["e2e"] = e2e(eng, cfg, Hp, drafts_pool, n_pool, k, n_sec, dev, world,
                          max_over_ranks)
         if not args.no_sweep:
             res["sweep"] = sweep(dev, W, Wd, hbm_peak)
