@@ -8,7 +8,8 @@
 // 5..8 rows the FMA pipe, not HBM, sets the pace; here the multiply-adds go to the tensor cores
 // and the kernel is left with streaming alone:
 //   * one persistent CTA per SM owns a contiguous run of 32-row bands of the vocabulary and
-//     walks it in tiles of 128 rows (the last one partial);
+//     walks it in tiles of 128 rows (the last one partial: its stages carry more k-blocks, so
+//     that it takes fewer of them);
 //   * a producer warp loads, per stage, 512 contiguous bytes of each of the tile's weight rows
 //     (four 64-wide k-blocks as 2-D TMA boxes of 32 rows, 128-byte swizzle; only the boxes the
 //     tile needs) and the matching 16-row H blocks (rows past the live ones read as zero) into
@@ -47,6 +48,24 @@ constexpr int kSkBoxBytes = kSkBoxRows * kSkKBlock * 2;  // 4 KB
 constexpr int kSkWBytes = kSkTileRows * kSkKBlock * 2;   // 16 KB per k-block
 constexpr int kSkHBytes = kSkN * kSkKBlock * 2;          // 2 KB per k-block
 constexpr int kSkStageBytes = kSkKB * (kSkWBytes + kSkHBytes);  // 72 KB, a multiple of 1024
+
+// k-blocks per stage of a tile that holds nbox of the four boxes. A stage's round trip costs
+// about the same whatever it carries (a block's last tile of one box took ~10 us over its ten
+// stages, against ~12-14 us for a full tile), so a partial tile packs more k-blocks into each
+// stage: 12, 7 and 5 for one, two and three boxes, and runs in 4, 6 or 8 stages instead of 10.
+// In a stage the k-blocks' weight boxes sit back to back (nbox * 4 KB each), then their H
+// blocks; the MMA still reads a 128-row operand at each k-block's start, so the largest start
+// plus 16 KB must stay inside the stage (the rows past the tile's boxes are other k-blocks'
+// bytes, in lanes nobody reads). The MMAs keep their k order, so the results do not change.
+__host__ __device__ constexpr int tile_kblocks(int nbox) {
+  return (kSkStageBytes / (nbox * kSkBoxBytes + kSkHBytes)) <
+                 ((kSkStageBytes - kSkWBytes) / (nbox * kSkBoxBytes) + 1)
+             ? kSkStageBytes / (nbox * kSkBoxBytes + kSkHBytes)
+             : (kSkStageBytes - kSkWBytes) / (nbox * kSkBoxBytes) + 1;
+}
+static_assert(tile_kblocks(4) == kSkKB, "a full tile keeps the 4-k-block stage");
+static_assert(tile_kblocks(1) == 12 && tile_kblocks(2) == 7 && tile_kblocks(3) == 5,
+              "the packed stages of a partial tile");
 constexpr int kSkThreads = 8 * 32;  // producer, MMA issuer, two idle warps, four drain warps
 constexpr int kSkDrainWarp0 = 4;    // warps 4..7: TMEM lane quadrants 0..3
 constexpr int kSkMaxTiles = 16;     // tiles per block: 16 x 16 = 256 TMEM columns at most
@@ -59,6 +78,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   if (draft_step_idle(p)) return;  // before any setup: nothing allocated, nothing in flight
+  if (threadIdx.x == 0) {  // the tensor maps' descriptors, ahead of the first copies
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&hmap) : "memory");
+  }
   const int S = p.stages;
   // the ring of stages; once streaming is over it holds the block's statistics and then the
   // combine's scratch
@@ -78,15 +101,40 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int nt = static_cast<int>(v1 - v0);
   const int ntile = (nt + kSkTileRows - 1) / kSkTileRows;
   const int nkb = (p.d + kSkKBlock - 1) / kSkKBlock;  // k-blocks per row
-  const int nks = (nkb + kSkKB - 1) / kSkKB;           // stages per tile
+  const int nks = (nkb + kSkKB - 1) / kSkKB;           // stages per full tile
   const int nr = min(p.nrows, kMaxRows);
   // one 16-column accumulator per tile of the block, all resident until the end
   const int ntile_cap = (p.tile_cap + kSkTileRows - 1) / kSkTileRows;
   uint32_t tcols = 32;
   while (tcols < static_cast<uint32_t>(ntile_cap * kSkN)) tcols <<= 1;
 
-  // The stage schedule: iteration it covers tile it / nks, stage ks = it % nks of that tile.
-  const int total_it = ntile * nks;
+  // The stage schedule: iterations [0, full_it) cover the full tiles, tile it / nks and stage
+  // it % nks; the rest cover the last tile, whose nbox_last boxes take kpb_last k-blocks a
+  // stage (four boxes: the same stages as any other tile).
+  const int nbox_last =
+      ntile > 0 ? (nt - (ntile - 1) * kSkTileRows + kSkBoxRows - 1) / kSkBoxRows : 0;
+  const int kpb_last = ntile > 0 ? tile_kblocks(nbox_last) : kSkKB;
+  const int full_it = ntile > 0 ? (ntile - 1) * nks : 0;
+  const int total_it = ntile > 0 ? full_it + (nkb + kpb_last - 1) / kpb_last : 0;
+  struct StageMap {
+    int t, ks, nbox, kpb, nk;  // tile, its stage, boxes, k-blocks a stage, k-blocks in this one
+  };
+  auto stage_of = [&](int it) {
+    StageMap m;
+    if (it < full_it) {
+      m.t = it / nks;
+      m.ks = it - m.t * nks;
+      m.nbox = kSkTileRows / kSkBoxRows;
+      m.kpb = kSkKB;
+    } else {
+      m.t = ntile - 1;
+      m.ks = it - full_it;
+      m.nbox = nbox_last;
+      m.kpb = kpb_last;
+    }
+    m.nk = min(m.kpb, nkb - m.ks * m.kpb);
+    return m;
+  };
   // weight rows of a tile's four 32-row boxes, worked out once per stage in 32-bit arithmetic
   // (V < 2^24): the producer's issue loop sets this kernel's pace, and mapping every box there
   // measured ~5% slower
@@ -101,51 +149,46 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
   };
   auto issue_w = [&](int it, int s) {  // the weight boxes of iteration it into stage s
-    const int t = it / nks, ks = it - t * nks;
-    const int rows = min(kSkTileRows, nt - t * kSkTileRows);
-    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
-    const int y = static_cast<int>(v0) + t * kSkTileRows;
-    const int nk = min(kSkKB, nkb - ks * kSkKB);  // k-blocks in this stage
+    const StageMap m = stage_of(it);
+    const int y = static_cast<int>(v0) + m.t * kSkTileRows;
     uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
     int yb[kSkTileRows / kSkBoxRows];
     box_rows(y, yb);
-    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
-    for (int kk = 0; kk < nk; ++kk)
+    mbar_arrive_expect_tx(&full[s],
+                          static_cast<uint32_t>(m.nk * (m.nbox * kSkBoxBytes + kSkHBytes)));
+    for (int kk = 0; kk < m.nk; ++kk)
 #pragma unroll
       for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
-        if (b < nbox)
-          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap,
-                              (ks * kSkKB + kk) * kSkKBlock, yb[b], &full[s], wpol);
+        if (b < m.nbox)
+          tc_tma_load_2d_hint(st + (kk * m.nbox + b) * kSkBoxBytes, &wmap,
+                              (m.ks * m.kpb + kk) * kSkKBlock, yb[b], &full[s], wpol);
   };
   auto issue_h = [&](int it, int s) {  // the H blocks of iteration it into stage s
-    const int t = it / nks, ks = it - t * nks;
-    const int nk = min(kSkKB, nkb - ks * kSkKB);
-    uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
-    for (int kk = 0; kk < nk; ++kk)
-      tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, (ks * kSkKB + kk) * kSkKBlock,
-                     0, &full[s]);
+    const StageMap m = stage_of(it);
+    uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes + m.kpb * m.nbox * kSkBoxBytes;
+    for (int kk = 0; kk < m.nk; ++kk)
+      tc_tma_load_2d(st + kk * kSkHBytes, &hmap, (m.ks * m.kpb + kk) * kSkKBlock, 0, &full[s]);
   };
-  // Steady state: per k-block its four weight boxes, then its H block. This order (k-block outer,
+  // Steady state: per k-block its weight boxes, then its H block. This order (k-block outer,
   // 32-row boxes inner, H between k-blocks) streamed measurably faster than issuing all weight
   // boxes first or walking each row band's 512 bytes first.
   auto issue_all = [&](int it, int s) {
-    const int t = it / nks, ks = it - t * nks;
-    const int rows = min(kSkTileRows, nt - t * kSkTileRows);
-    const int nbox = (rows + kSkBoxRows - 1) / kSkBoxRows;
-    const int y = static_cast<int>(v0) + t * kSkTileRows;
-    const int nk = min(kSkKB, nkb - ks * kSkKB);
+    const StageMap m = stage_of(it);
+    const int y = static_cast<int>(v0) + m.t * kSkTileRows;
     uint8_t* st = ring + static_cast<size_t>(s) * kSkStageBytes;
+    uint8_t* sh = st + m.kpb * m.nbox * kSkBoxBytes;
     int yb[kSkTileRows / kSkBoxRows];
     box_rows(y, yb);
-    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nk * (nbox * kSkBoxBytes + kSkHBytes)));
-    for (int kk = 0; kk < nk; ++kk) {
-      const int x = (ks * kSkKB + kk) * kSkKBlock;
+    mbar_arrive_expect_tx(&full[s],
+                          static_cast<uint32_t>(m.nk * (m.nbox * kSkBoxBytes + kSkHBytes)));
+    for (int kk = 0; kk < m.nk; ++kk) {
+      const int x = (m.ks * m.kpb + kk) * kSkKBlock;
 #pragma unroll
       for (int b = 0; b < kSkTileRows / kSkBoxRows; ++b)
-        if (b < nbox)
-          tc_tma_load_2d_hint(st + kk * kSkWBytes + b * kSkBoxBytes, &wmap, x, yb[b], &full[s],
+        if (b < m.nbox)
+          tc_tma_load_2d_hint(st + (kk * m.nbox + b) * kSkBoxBytes, &wmap, x, yb[b], &full[s],
                               wpol);
-      tc_tma_load_2d(st + kSkKB * kSkWBytes + kk * kSkHBytes, &hmap, x, 0, &full[s]);
+      tc_tma_load_2d(sh + kk * kSkHBytes, &hmap, x, 0, &full[s]);
     }
   };
   // The weights are never written by the path: the first stages stream in before the wait for
@@ -221,7 +264,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       for (int t = 0; t < ntile; ++t) {
         const uint32_t dacc = tmem_base + static_cast<uint32_t>(t * kSkN);
         bool ok = true;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int it_end = (t + 1 < ntile) ? it + nks : total_it;  // this tile's stages
+        for (; it < it_end; ++it) {
           if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((it / S) & 1))) {
             atomicOr(&p.hdr->error, ERR_TC_WAIT);
             atomicExch(&flags[0], 1);
@@ -229,16 +273,17 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             break;
           }
           tc_fence_after();
+          const StageMap m = stage_of(it);
           const uint64_t st = desc_advance(ring_desc, static_cast<uint32_t>(s * kSkStageBytes));
-          const int nk = min(kSkKB, nkb - ks * kSkKB);
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t a = desc_advance(st, static_cast<uint32_t>(kk * kSkWBytes));
-            const uint64_t b =
-                desc_advance(st, static_cast<uint32_t>(kSkKB * kSkWBytes + kk * kSkHBytes));
+          const uint32_t wstep = static_cast<uint32_t>(m.nbox * kSkBoxBytes);  // per k-block
+          const uint32_t hbase = static_cast<uint32_t>(m.kpb) * wstep;
+          for (int kk = 0; kk < m.nk; ++kk) {
+            const uint64_t a = desc_advance(st, static_cast<uint32_t>(kk) * wstep);
+            const uint64_t b = desc_advance(st, hbase + static_cast<uint32_t>(kk * kSkHBytes));
 #pragma unroll
             for (int k16 = 0; k16 < kSkKBlock / 16; ++k16)
               tc_mma(dacc, desc_advance(a, k16 * 32), desc_advance(b, k16 * 32), idesc,
-                     (ks > 0 || kk > 0 || k16 > 0) ? 1u : 0u);
+                     (m.ks > 0 || kk > 0 || k16 > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
           if (++s == S) s = 0;
