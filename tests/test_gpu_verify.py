@@ -99,6 +99,25 @@ def test_verify_c0_ragged_vocab_and_odd_shapes():
         _verify_case(cfg, W, to_dev(W), H, 1, 3, [1.0], f"V={V} d={d}")
 
 
+@pytest.mark.parametrize("bands,extra", [(5, 0), (6, 0), (7, 0), (8, 0), (13, 17)])
+def test_verify_partial_last_tile_shapes(bands, extra):
+    """d = 2560 (40 k-blocks of 64) and V = SMs x 32 x bands + extra: every block's last
+    128-row tile holds 1, 2, 3 or 4 boxes of 32 rows (its stages packed with 12, 7, 5 or 4
+    k-blocks), and with 17 extra rows a few blocks own one band more and the last band is
+    ragged. Logits and statistics against the oracle, one sampled and one greedy request."""
+    ensure_built()
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    V = sms * 32 * bands + extra
+    cfg = configs.Config(name="tiles", d=2560, V=V, Vd=V, wdtype="bf16", k=3, k_mode="fixed",
+                         batch=2, rows_per_request=2, temps=(1.0,), cycles=1, seeds=(0,),
+                         plant_scale=0.0, pi_draft=0.0, draft_noise=0.5)
+    W = gen.lm_weights(cfg, seed=bands, cache=False)
+    rng = np.random.default_rng(bands)
+    H = gen.encode(rng.standard_normal((4, cfg.d), dtype=np.float32), "bf16")
+    near = _verify_case(cfg, W, to_dev(W), H, 2, 2, [1.0, 0.0], f"bands={bands} V={V}")
+    assert near <= 1
+
+
 @pytest.mark.parametrize("V,d", [(300_000, 1024), (400_000, 512)])
 def test_verify_large_vocabulary_sixteen_tiles_per_block(V, d):
     """V = 300,000 at 152 SMs gives each block up to 62 bands of 32 rows, about 16 tiles of 128
